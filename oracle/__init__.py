@@ -1,0 +1,146 @@
+"""The oracle: a plain CPU statement of block-quantized packing and the batch-1
+dequant + GEMV, in C with fp64 accumulation (``bq_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the benchmark's CPU-baseline / reference leg may import this package.  The
+GPU library neither imports it nor shares code with it.
+
+Every function takes and returns numpy arrays.  ``Oracle(lib_path)`` loads a
+given build of the C source, which lets the tests run their pins against
+deliberately broken copies of the source (mutants) as well as the real one.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+Q4_0 = 2
+Q8_0 = 8
+BLOCK_BYTES = {Q8_0: 34, Q4_0: 18}
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+
+
+def _ptr(a, ct):
+    return a.ctypes.data_as(ctypes.POINTER(ct)) if a is not None else None
+
+
+class Oracle:
+    def __init__(self, lib_path=None):
+        if lib_path is None:
+            lib_path = _build.compile_oracle()
+        self.path = lib_path
+        lib = ctypes.CDLL(lib_path)
+        i64, i32 = ctypes.c_int64, ctypes.c_int
+        lib.bqo_f32_to_f16_bits.restype = ctypes.c_uint16
+        lib.bqo_f32_to_f16_bits.argtypes = [ctypes.c_float]
+        lib.bqo_f16_bits_to_f64.restype = ctypes.c_double
+        lib.bqo_f16_bits_to_f64.argtypes = [ctypes.c_uint16]
+        lib.bqo_f32_to_f16_array.restype = None
+        lib.bqo_f32_to_f16_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, i64]
+        lib.bqo_packed_bytes.restype = i64
+        lib.bqo_packed_bytes.argtypes = [i32, i64, i64]
+        lib.bqo_quantize_pack.restype = i32
+        lib.bqo_quantize_pack.argtypes = [i32, ctypes.c_void_p, i64, i64, ctypes.c_void_p]
+        lib.bqo_dequant.restype = i32
+        lib.bqo_dequant.argtypes = [i32, ctypes.c_void_p, i64, i64, ctypes.c_void_p]
+        lib.bqo_gemv.restype = i32
+        lib.bqo_gemv.argtypes = [i32, ctypes.c_void_p, i64, i64, ctypes.c_void_p,
+                                 ctypes.c_void_p, ctypes.c_void_p]
+        lib.bqo_rmsnorm.restype = i32
+        lib.bqo_rmsnorm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, i64, ctypes.c_double,
+                                    ctypes.c_void_p]
+        lib.bqo_silu.restype = ctypes.c_double
+        lib.bqo_silu.argtypes = [ctypes.c_double]
+        lib.bqo_gate_up_silu.restype = i32
+        lib.bqo_gate_up_silu.argtypes = [i32, ctypes.c_void_p, ctypes.c_void_p, i64, i64,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        self.lib = lib
+
+    # -- fp16 ---------------------------------------------------------------
+    def f32_to_f16_bits(self, a):
+        a = np.ascontiguousarray(a, dtype=np.float32)
+        out = np.empty(a.shape, dtype=np.uint16)
+        self.lib.bqo_f32_to_f16_array(a.ctypes.data, out.ctypes.data, a.size)
+        return out
+
+    def f16_bits_to_f64(self, h):
+        return self.lib.bqo_f16_bits_to_f64(int(h))
+
+    # -- formats --------------------------------------------------------------
+    def packed_bytes(self, qtype, M, K):
+        return int(self.lib.bqo_packed_bytes(qtype, M, K))
+
+    def quantize_pack(self, qtype, W):
+        """fp32 [M, K] -> uint8 [M, (K/32)*block_bytes]."""
+        W = np.ascontiguousarray(W, dtype=np.float32)
+        M, K = W.shape
+        out = np.empty((M, (K // 32) * BLOCK_BYTES[qtype]), dtype=np.uint8)
+        rc = self.lib.bqo_quantize_pack(qtype, W.ctypes.data, M, K, out.ctypes.data)
+        if rc:
+            raise ValueError(f"oracle quantize_pack rejected qtype={qtype} shape={W.shape}")
+        return out
+
+    def dequant(self, qtype, Wq, M, K):
+        Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+        out = np.empty((M, K), dtype=np.float64)
+        if self.lib.bqo_dequant(qtype, Wq.ctypes.data, M, K, out.ctypes.data):
+            raise ValueError("oracle dequant: bad arguments")
+        return out
+
+    def gemv(self, qtype, Wq, M, K, x):
+        """Returns (y, S): fp64 y = W x and S = sum_k |w_mk x_k|."""
+        Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        assert x.shape == (K,)
+        y = np.empty(M, dtype=np.float64)
+        S = np.empty(M, dtype=np.float64)
+        if self.lib.bqo_gemv(qtype, Wq.ctypes.data, M, K, x.ctypes.data, y.ctypes.data,
+                             S.ctypes.data):
+            raise ValueError("oracle gemv: bad arguments")
+        return y, S
+
+    def gemv_y_only(self, qtype, Wq, M, K, x, y):
+        """The same product without S, into a caller-owned fp64 ``y``."""
+        return self.lib.bqo_gemv(qtype, Wq.ctypes.data, M, K, x.ctypes.data, y.ctypes.data,
+                                 None)
+
+    def rmsnorm(self, x, gamma, eps):
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float64)
+        xn = np.empty_like(x)
+        if self.lib.bqo_rmsnorm(x.ctypes.data, None if g is None else g.ctypes.data, x.size,
+                                eps, xn.ctypes.data):
+            raise ValueError("oracle rmsnorm: bad arguments")
+        return xn
+
+    def silu(self, z):
+        return self.lib.bqo_silu(float(z))
+
+    def gate_up_silu(self, qtype, Wg, Wu, M, K, xn):
+        """Returns dict of fp64 arrays y, g, u, Sg, Su for y = silu(Wg xn) * (Wu xn)."""
+        Wg = np.ascontiguousarray(Wg, dtype=np.uint8)
+        Wu = np.ascontiguousarray(Wu, dtype=np.uint8)
+        xn = np.ascontiguousarray(xn, dtype=np.float64)
+        r = {k: np.empty(M, dtype=np.float64) for k in ("y", "g", "u", "Sg", "Su")}
+        if self.lib.bqo_gate_up_silu(qtype, Wg.ctypes.data, Wu.ctypes.data, M, K,
+                                     xn.ctypes.data, r["y"].ctypes.data, r["g"].ctypes.data,
+                                     r["u"].ctypes.data, r["Sg"].ctypes.data,
+                                     r["Su"].ctypes.data):
+            raise ValueError("oracle gate_up_silu: bad arguments")
+        return r
+
+
+_default = None
+
+
+def get():
+    """The oracle built from ``oracle/bq_oracle.c`` (built on first use)."""
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default
