@@ -1,0 +1,163 @@
+"""Block-quantized weight dequant + batch-1 GEMV for GB300 (sm_103a).
+
+A thin Python binding over libbqgemv.so (include/bqgemv.h).  Every function
+here only marshals arguments: it checks tensor dtypes/devices, allocates
+outputs with PyTorch when the caller passes none, and calls the C ABI on the
+current CUDA stream.  All arithmetic runs in this package's CUDA kernels.
+
+Packed weights are uint8 tensors of shape [M, (K/32) * block_bytes]
+(34 bytes per 32 weights for Q8_0, 18 for Q4_0), so M and K are read from
+the packed tensor's shape.
+"""
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import BQ_Q4_0, BQ_Q8_0, BQ_VERIFY_MAX_ROWS, BQError, lib  # noqa: F401
+
+Q8_0 = BQ_Q8_0
+Q4_0 = BQ_Q4_0
+BLOCK_BYTES = {Q8_0: 34, Q4_0: 18}
+QTYPES = {"q8_0": Q8_0, "q4_0": Q4_0}
+
+__all__ = ["Q8_0", "Q4_0", "BLOCK_BYTES", "BQError", "packed_bytes", "quantize_pack",
+           "gemv", "gemv_q8_0", "gemv_q4_0", "gemv_gate_up_silu", "gemv_verify",
+           "device_status", "tree_lanes", "version"]
+
+
+def _qt(qtype):
+    return QTYPES[qtype] if isinstance(qtype, str) else int(qtype)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _need(t, dtype, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (this package has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _packed_shape(Wq, qtype):
+    if Wq.dim() != 2:
+        raise ValueError("packed weights must be 2-D [M, (K/32)*block_bytes]")
+    bb = BLOCK_BYTES[qtype]
+    M, rb = Wq.shape
+    if rb % bb:
+        raise ValueError(f"packed row of {rb} bytes is not whole {bb}-byte blocks")
+    return M, (rb // bb) * 32
+
+
+def version():
+    return lib.bq_version()
+
+
+def tree_lanes(K):
+    """Lanes G of the fixed summation tree of a row of K weights."""
+    return lib.bq_tree_lanes(int(K))
+
+
+def packed_bytes(qtype, M, K):
+    n = lib.bq_packed_bytes(_qt(qtype), int(M), int(K))
+    if n < 0:
+        raise ValueError(f"no packed size for qtype={qtype} M={M} K={K}")
+    return n
+
+
+def quantize_pack(W, qtype, out=None):
+    """fp32 CUDA [M, K] -> packed uint8 [M, (K/32)*block_bytes]."""
+    qt = _qt(qtype)
+    _need(W, torch.float32, "W")
+    if W.dim() != 2:
+        raise ValueError("W must be 2-D [M, K]")
+    M, K = W.shape
+    if out is None:
+        out = torch.empty((M, (K // 32) * BLOCK_BYTES[qt]), dtype=torch.uint8, device=W.device)
+    _need(out, torch.uint8, "out")
+    _lib.check(lib.bq_quantize_pack(qt, _ptr(W), M, K, _ptr(out), _stream(W)), "quantize_pack")
+    return out
+
+
+def gemv(qtype, Wq, x, y=None):
+    """y = W x for packed weights Wq and fp32 x [K]."""
+    qt = _qt(qtype)
+    _need(Wq, torch.uint8, "Wq")
+    _need(x, torch.float32, "x")
+    M, K = _packed_shape(Wq, qt)
+    if x.numel() != K:
+        raise ValueError(f"x has {x.numel()} elements, weights have K={K}")
+    if y is None:
+        y = torch.empty(M, dtype=torch.float32, device=Wq.device)
+    _need(y, torch.float32, "y")
+    fn = lib.bq_gemv_q8_0 if qt == Q8_0 else lib.bq_gemv_q4_0
+    _lib.check(fn(_ptr(Wq), _ptr(x), _ptr(y), M, K, _stream(Wq)), "gemv")
+    return y
+
+
+def gemv_q8_0(Wq, x, y=None):
+    return gemv(Q8_0, Wq, x, y)
+
+
+def gemv_q4_0(Wq, x, y=None):
+    return gemv(Q4_0, Wq, x, y)
+
+
+def gemv_gate_up_silu(qtype, Wg, Wu, x, gamma=None, eps=1e-6, y=None):
+    """y = silu(Wg xn) * (Wu xn), xn = x * gamma / sqrt(mean(x^2) + eps)
+    (xn = x when gamma is None)."""
+    qt = _qt(qtype)
+    _need(Wg, torch.uint8, "Wg")
+    _need(Wu, torch.uint8, "Wu")
+    _need(x, torch.float32, "x")
+    if gamma is not None:
+        _need(gamma, torch.float32, "gamma")
+    M, K = _packed_shape(Wg, qt)
+    if tuple(Wu.shape) != tuple(Wg.shape):
+        raise ValueError("Wg and Wu must have the same shape")
+    if x.numel() != K or (gamma is not None and gamma.numel() != K):
+        raise ValueError("x and gamma must have K elements")
+    if y is None:
+        y = torch.empty(M, dtype=torch.float32, device=Wg.device)
+    _need(y, torch.float32, "y")
+    _lib.check(lib.bq_gemv_gate_up_silu(qt, _ptr(Wg), _ptr(Wu), _ptr(x), _ptr(gamma),
+                                        float(eps), _ptr(y), M, K, _stream(Wg)),
+               "gemv_gate_up_silu")
+    return y
+
+
+def gemv_verify(qtype, Wq, X, Y=None):
+    """Y [R, M] = X [R, K] @ W^T with the weights streamed once; row r is
+    bit-identical to gemv(qtype, Wq, X[r])."""
+    qt = _qt(qtype)
+    _need(Wq, torch.uint8, "Wq")
+    _need(X, torch.float32, "X")
+    M, K = _packed_shape(Wq, qt)
+    if X.dim() != 2 or X.shape[1] != K:
+        raise ValueError(f"X must be [R, {K}]")
+    R = X.shape[0]
+    if Y is None:
+        Y = torch.empty((R, M), dtype=torch.float32, device=Wq.device)
+    _need(Y, torch.float32, "Y")
+    _lib.check(lib.bq_gemv_verify(qt, _ptr(Wq), _ptr(X), _ptr(Y), R, M, K, _stream(Wq)),
+               "gemv_verify")
+    return Y
+
+
+def device_status(clear=True):
+    """Device-side error word (0 = healthy); synchronises the device."""
+    flags = ctypes.c_uint(0)
+    st = lib.bq_device_status(ctypes.byref(flags), int(clear))
+    if st not in (_lib.BQ_OK, _lib.BQ_ERR_DEVICE):
+        raise BQError(st, "device_status")
+    return flags.value

@@ -1,0 +1,285 @@
+// bq_api.cu -- the extern "C" entry points of libbqgemv.so (include/bqgemv.h):
+// argument validation, launch planning and dispatch to the per-format
+// kernels.  Validation runs entirely on the host before any CUDA call, so a
+// rejected call touches no device state.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "../../include/bqgemv.h"
+#include "bq_dot.cuh"
+#include "bq_internal.h"
+
+namespace bq {
+
+namespace {
+
+constexpr long long K_MAX = 1LL << 18;
+constexpr long long M_MAX = (1LL << 31) - 1;
+
+// launch-geometry defaults; BQ_PLAN="nwc=4,stage=32768,inflight=98304,ns=4"
+// overrides them for tuning sweeps (read once)
+struct Tunables {
+    int max_nwc = 8;
+    int stage_target = 32 * 1024;
+    int stage_max = 64 * 1024;
+    int inflight = 96 * 1024;
+    int ns_force = 0;
+    int xres_max = 100 * 1024;
+};
+
+const Tunables &tunables() {
+    static Tunables t = [] {
+        Tunables v;
+        const char *s = std::getenv("BQ_PLAN");
+        if (!s) return v;
+        char buf[256];
+        std::strncpy(buf, s, sizeof buf - 1);
+        buf[sizeof buf - 1] = 0;
+        for (char *tok = std::strtok(buf, ","); tok; tok = std::strtok(nullptr, ",")) {
+            char *eq = std::strchr(tok, '=');
+            if (!eq) continue;
+            *eq = 0;
+            const int val = std::atoi(eq + 1);
+            if (!std::strcmp(tok, "nwc") && val >= 1 && val <= 8) v.max_nwc = val;
+            else if (!std::strcmp(tok, "stage") && val >= 4096) v.stage_target = val;
+            else if (!std::strcmp(tok, "stagemax") && val >= 4096) v.stage_max = val;
+            else if (!std::strcmp(tok, "inflight") && val >= 8192) v.inflight = val;
+            else if (!std::strcmp(tok, "ns") && val >= 2 && val <= 8) v.ns_force = val;
+            else if (!std::strcmp(tok, "xres") && val >= 0) v.xres_max = val;
+        }
+        return v;
+    }();
+    return t;
+}
+
+int num_sms_current() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int n = cache[dev].load();
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev].store(n);
+    }
+    return n;
+}
+
+int max_smem_optin() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int n = cache[dev].load();
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return 0;
+        cache[dev].store(n);
+    }
+    return n;
+}
+
+int block_bytes(int qtype) { return qtype == BQ_Q8_0 ? 34 : qtype == BQ_Q4_0 ? 18 : -1; }
+
+}  // namespace
+
+int tree_lanes_for_units(long long nsc) {
+    for (int G = 32; G > 1; G >>= 1) {
+        const long long slots = G * ((nsc + G - 1) / G);
+        if ((slots - nsc) * 8 <= slots) return G;
+    }
+    return 1;
+}
+
+bool plan_gemv(const GemvCall &c, LaunchPlan *p) {
+    const Tunables &t = tunables();
+    std::memset(p, 0, sizeof *p);
+    const int bb = block_bytes(c.qtype);
+    const int ub = 8 * bb;
+    const long long nb = c.K / 32;
+    p->nsc = (int)((nb + 7) / 8);
+    p->G = tree_lanes_for_units(p->nsc);
+    p->rb = nb * bb;
+    p->num_sms = num_sms_current();
+    if (p->num_sms <= 0) return false;
+    const int rpw = 32 / p->G;
+    if (c.K % 256 != 0) {
+        p->kind = PLAN_GENERIC;
+        return true;
+    }
+    p->kind = PLAN_STREAM;
+    const int nmat = c.mode == MODE_GATE_UP ? 2 : 1;
+    const int smem_cap = max_smem_optin();
+    const int xpad = x_padded_floats((int)c.K);
+    p->xres = (long long)c.R * xpad * 4 <= t.xres_max;
+    const int x_bytes = p->xres ? c.R * xpad * 4 : 0;
+    int nwc = t.max_nwc;
+    while (nwc > 1 && (c.M + (long long)nwc * rpw - 1) / ((long long)nwc * rpw) < p->num_sms)
+        nwc >>= 1;
+    for (;; nwc >>= 1) {
+        const int TR = nwc * rpw;
+        int KCU;
+        if ((long long)TR * p->rb * nmat <= t.stage_target) {
+            KCU = p->nsc;
+        } else {
+            const long long per = (long long)TR * p->G * ub * nmat;
+            const long long k = t.stage_target / per;
+            KCU = p->G * (int)(k > 1 ? k : 1);
+            if (KCU > p->nsc) KCU = p->nsc;
+        }
+        const bool single = KCU == p->nsc && (p->G >= 8 || (p->rb / 16) % 8 == p->G % 8);
+        int stride;
+        if (single) {
+            stride = (int)p->rb;
+        } else {
+            int s16 = KCU * ub / 16;
+            if (p->G < 8)
+                while (s16 % 8 != p->G % 8) ++s16;
+            stride = s16 * 16;
+        }
+        const long long stage = (long long)TR * stride * nmat;
+        const long long room = (long long)smem_cap - HDR_BYTES - x_bytes;
+        if ((stage > t.stage_max || 2 * stage > room) && nwc > 1) continue;
+        if (2 * stage > room) return false;
+        int NS = t.ns_force ? t.ns_force : (int)(t.inflight / stage);
+        if (NS < 2) NS = 2;
+        if (NS > 8) NS = 8;
+        while (NS > 2 && NS * stage > room) --NS;
+        p->NWC = nwc;
+        p->TR = TR;
+        p->KCU = KCU;
+        p->NS = NS;
+        p->nchunks = (p->nsc + KCU - 1) / KCU;
+        p->ntiles = (int)((c.M + TR - 1) / TR);
+        p->single_copy = single;
+        p->row_stride = stride;
+        p->mat_stride = TR * stride;
+        p->stage_bytes = (int)stage;
+        p->x_off = HDR_BYTES;
+        p->x_rstride = xpad;
+        p->stage_off = (HDR_BYTES + x_bytes + 127) / 128 * 128;
+        p->smem = (size_t)p->stage_off + (size_t)NS * stage;
+        return true;
+    }
+}
+
+}  // namespace bq
+
+using bq::GemvCall;
+using bq::LaunchPlan;
+
+namespace {
+
+bool aligned_ok(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bq_status from_cuda(int e) { return e == 0 ? BQ_OK : BQ_ERR_CUDA; }
+
+bq_status check_shape(long long M, long long K) {
+    if (M < 0 || M > bq::M_MAX) return BQ_ERR_SHAPE;
+    if (K < 32 || K > bq::K_MAX || K % 32) return BQ_ERR_SHAPE;
+    return BQ_OK;
+}
+
+bq_status run_gemv(const GemvCall &c) {
+    LaunchPlan p;
+    if (!bq::plan_gemv(c, &p)) return BQ_ERR_CUDA;
+    const int e = c.qtype == BQ_Q8_0 ? bq_internal_launch_q8_0(c, p) : bq_internal_launch_q4_0(c, p);
+    return from_cuda(e);
+}
+
+bq_status gemv_common(int qtype, const void *Wq, const float *x, float *y, int R, int64_t M,
+                      int64_t K, void *stream) {
+    if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0) return BQ_ERR_QTYPE;
+    if (R < 1 || R > BQ_VERIFY_MAX_ROWS) return BQ_ERR_SHAPE;
+    bq_status s = check_shape(M, K);
+    if (s != BQ_OK) return s;
+    if (!Wq || !x || !y) return BQ_ERR_NULL;
+    if (!aligned_ok(Wq, 16) || !aligned_ok(x, 16) || !aligned_ok(y, 4)) return BQ_ERR_ALIGN;
+    if (M == 0) return BQ_OK;
+    GemvCall c{qtype, bq::MODE_PLAIN, R, Wq, nullptr, x, nullptr, 0.0f, y, M, K, stream};
+    return run_gemv(c);
+}
+
+}  // namespace
+
+extern "C" {
+
+int bq_version(void) { return 100; }
+
+const char *bq_status_str(int status) {
+    switch (status) {
+        case BQ_OK: return "ok";
+        case BQ_ERR_NULL: return "a required pointer is NULL";
+        case BQ_ERR_SHAPE: return "shape outside the supported range (M >= 0, K % 32 == 0, 32 <= K <= 2^18, 1 <= R <= 6)";
+        case BQ_ERR_ALIGN: return "pointer misaligned (packed weights and fp32 inputs need 16 bytes, outputs 4)";
+        case BQ_ERR_QTYPE: return "unknown quantization type (BQ_Q8_0 = 8, BQ_Q4_0 = 2)";
+        case BQ_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+        case BQ_ERR_DEVICE: return "a kernel recorded a device-side error (bounded wait ran out)";
+        default: return "unknown status";
+    }
+}
+
+int64_t bq_packed_bytes(int qtype, int64_t M, int64_t K) {
+    const int bb = bq::block_bytes(qtype);
+    if (bb < 0 || M < 0 || K < 0 || K % 32) return -1;
+    return M * (K / 32) * bb;
+}
+
+int bq_tree_lanes(int64_t K) {
+    if (K <= 0 || K % 32) return -1;
+    return bq::tree_lanes_for_units((K / 32 + 7) / 8);
+}
+
+bq_status bq_quantize_pack(int qtype, const float *W, int64_t M, int64_t K, void *Wq, void *stream) {
+    if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0) return BQ_ERR_QTYPE;
+    bq_status s = check_shape(M, K);
+    if (s != BQ_OK) return s;
+    if (!W || !Wq) return BQ_ERR_NULL;
+    if (!aligned_ok(W, 4) || !aligned_ok(Wq, 16)) return BQ_ERR_ALIGN;
+    if (M == 0) return BQ_OK;
+    return from_cuda(bq_internal_pack(qtype, W, M, K, Wq, stream));
+}
+
+bq_status bq_gemv_q8_0(const void *Wq, const float *x, float *y, int64_t M, int64_t K, void *stream) {
+    return gemv_common(BQ_Q8_0, Wq, x, y, 1, M, K, stream);
+}
+
+bq_status bq_gemv_q4_0(const void *Wq, const float *x, float *y, int64_t M, int64_t K, void *stream) {
+    return gemv_common(BQ_Q4_0, Wq, x, y, 1, M, K, stream);
+}
+
+bq_status bq_gemv_verify(int qtype, const void *Wq, const float *X, float *Y, int R, int64_t M,
+                         int64_t K, void *stream) {
+    return gemv_common(qtype, Wq, X, Y, R, M, K, stream);
+}
+
+bq_status bq_gemv_gate_up_silu(int qtype, const void *Wg, const void *Wu, const float *x,
+                               const float *gamma, float eps, float *y, int64_t M, int64_t K,
+                               void *stream) {
+    if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0) return BQ_ERR_QTYPE;
+    bq_status s = check_shape(M, K);
+    if (s != BQ_OK) return s;
+    if (!Wg || !Wu || !x || !y) return BQ_ERR_NULL;
+    if (!aligned_ok(Wg, 16) || !aligned_ok(Wu, 16) || !aligned_ok(x, 16) || !aligned_ok(y, 4) ||
+        (gamma && !aligned_ok(gamma, 16)))
+        return BQ_ERR_ALIGN;
+    if (gamma && !(std::isfinite(eps) && eps >= 0.0f)) return BQ_ERR_SHAPE;
+    if (M == 0) return BQ_OK;
+    GemvCall c{qtype, bq::MODE_GATE_UP, 1, Wg, Wu, x, gamma, eps, y, M, K, stream};
+    return run_gemv(c);
+}
+
+bq_status bq_device_status(unsigned int *flags, int clear) {
+    if (!flags) return BQ_ERR_NULL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return BQ_ERR_CUDA;
+    unsigned int a = 0, b = 0;
+    if (bq_internal_status_q8_0(&a, clear) != 0) return BQ_ERR_CUDA;
+    if (bq_internal_status_q4_0(&b, clear) != 0) return BQ_ERR_CUDA;
+    *flags = a | b;
+    return *flags ? BQ_ERR_DEVICE : BQ_OK;
+}
+
+}  // extern "C"

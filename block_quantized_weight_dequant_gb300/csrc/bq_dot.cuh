@@ -1,0 +1,249 @@
+// bq_dot.cuh -- the fixed-order arithmetic of one row of a block-quantized
+// GEMV: on-the-fly dequant of 8-block units and their dot products with x.
+//
+// Every GEMV kernel in this library (single-row, gate+up, multi-row verify,
+// streaming or generic) reaches each output through these functions, so the
+// rounding of a row depends only on (qtype, K).  That is what makes a verify
+// row memcmp-equal to the single-row result ("We Wrote Our Own Inference
+// Engine", "Correctness first": verify is checked against decode with memcmp,
+// because kernels with different summation orders drift).
+//
+// The tree, for one row:
+//   unit     = 8 consecutive blocks (256 weights; 272 B in Q8_0, 144 B in Q4_0)
+//   block b  : a_i = sum over t = 0..7 of q[4t+i] * x[4t+i]  (fma chain, i = 0..3)
+//              s_b = (a_0 + a_1) + (a_2 + a_3)
+//   unit     : c = sum over b of d_b * s_b                    (fma chain, b = 0..7)
+//   lane l   : p_l = c_l + c_{l+G} + c_{l+2G} + ...           (in order, G lanes)
+//   row      : p folded pairwise by xor-butterfly over the G lanes
+// All steps use explicit _rn intrinsics, so the compiler cannot contract or
+// reassociate them differently in different kernels.  Every code is converted
+// to fp32 exactly (q and n-8 are small integers), so dequantisation itself
+// adds no rounding; the per-block scale multiplies the block's partial sum
+// once, as w = d*q factors out of the block's dot product.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cstdint>
+
+namespace bq {
+
+constexpr int QT_Q4_0 = 2;
+constexpr int QT_Q8_0 = 8;
+
+template <int QT> struct Fmt;
+template <> struct Fmt<QT_Q8_0> {
+    static constexpr int block_bytes = 34;
+    static constexpr int unit_bytes = 272;  // 8 blocks = 17 x 16 B
+    static constexpr int unit_words = 68;
+};
+template <> struct Fmt<QT_Q4_0> {
+    static constexpr int block_bytes = 18;
+    static constexpr int unit_bytes = 144;  // 8 blocks = 9 x 16 B
+    static constexpr int unit_words = 36;
+};
+
+// ---------------------------------------------------------------------------
+// exact code -> fp32 conversion
+// ---------------------------------------------------------------------------
+// Q8_0: flip the sign bit of every byte (q + 128 as an unsigned byte), place
+// that byte in the low mantissa of 2^23 and subtract 2^23 + 128.
+__device__ __forceinline__ float q8_code(uint32_t word, int pos) {
+    const uint32_t flipped = word ^ 0x80808080u;
+    const uint32_t bits = __byte_perm(flipped, 0x4B000000u, 0x7540u | (uint32_t)pos);
+    return __fsub_rn(__uint_as_float(bits), 8388736.0f);
+}
+// Q4_0: the nibble at bit `shift`, placed in the mantissa of 2^23, minus 2^23 + 8.
+__device__ __forceinline__ float q4_code(uint32_t word, int shift) {
+    const uint32_t bits = ((word >> shift) & 0xFu) | 0x4B000000u;
+    return __fsub_rn(__uint_as_float(bits), 8388616.0f);
+}
+
+__device__ __forceinline__ float scale_at(const uint32_t *w, int byte_off) {
+    const uint32_t h = (w[byte_off >> 2] >> (8 * (byte_off & 3))) & 0xFFFFu;
+    return __half2float(__ushort_as_half((unsigned short)h));
+}
+
+// ---------------------------------------------------------------------------
+// x sources: element e (a multiple of 4) of input row r, as a float4
+// ---------------------------------------------------------------------------
+// x staged in shared memory with 4 floats of padding after every 256, so that
+// lanes reading different units hit different banks
+struct XSmem {
+    const float *base;
+    int rstride;  // floats between rows
+    __device__ __forceinline__ float4 get(int r, int e) const {
+        return *reinterpret_cast<const float4 *>(base + r * rstride + e + ((e >> 8) << 2));
+    }
+};
+__host__ __device__ constexpr int x_padded_floats(int K) { return K + (K >> 6) + 4; }
+
+// x read from global memory (through L1)
+struct XGlobal {
+    const float *x;
+    int K;
+    __device__ __forceinline__ float4 get(int r, int e) const {
+        return __ldg(reinterpret_cast<const float4 *>(x + (size_t)r * K + e));
+    }
+};
+
+// RMSNorm applied while reading: xn = (x * rs) * gamma, rs from rms_scale()
+struct XGlobalNorm {
+    const float *x;
+    const float *gamma;
+    float rs;
+    __device__ __forceinline__ float4 get(int, int e) const {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(x + e));
+        const float4 g = __ldg(reinterpret_cast<const float4 *>(gamma + e));
+        return make_float4(__fmul_rn(__fmul_rn(v.x, rs), g.x), __fmul_rn(__fmul_rn(v.y, rs), g.y),
+                           __fmul_rn(__fmul_rn(v.z, rs), g.z), __fmul_rn(__fmul_rn(v.w, rs), g.w));
+    }
+};
+
+__device__ __forceinline__ float f4(const float4 &v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// ---------------------------------------------------------------------------
+// one block of NW weight sets against R input rows:
+//   c[v][r] = fma(d_b(v), s_b(v, r), c[v][r])
+// NW = 1 serves the single-row GEMV (R = 1) and verify (R > 1); NW = 2 serves
+// gate+up (two matrices, one x).  Each (v, r) pair sees exactly the operation
+// sequence of the NW = 1, R = 1 case, so results do not depend on NW or R.
+// ---------------------------------------------------------------------------
+template <int QT>
+__device__ __forceinline__ float code_at(const uint32_t *w, int B, int j) {
+    constexpr int bb = Fmt<QT>::block_bytes;
+    if constexpr (QT == QT_Q8_0) {
+        const int byte = bb * B + 2 + j;
+        return q8_code(w[byte >> 2], byte & 3);
+    } else {
+        const int byte = bb * B + 2 + (j & 15);
+        return q4_code(w[byte >> 2], 8 * (byte & 3) + (j >= 16 ? 4 : 0));
+    }
+}
+
+template <int QT, int NW, int R, int B, class XS>
+__device__ __forceinline__ void block_dot(const uint32_t *const (&w)[NW], const XS &xs, int e0,
+                                          float (&c)[NW][R]) {
+    constexpr int bb = Fmt<QT>::block_bytes;
+    float a[NW][R][4];
+#pragma unroll
+    for (int v = 0; v < NW; ++v)
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[v][r][i] = -0.0f;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        float4 xv[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) xv[r] = xs.get(r, e0 + 32 * B + 4 * t);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int v = 0; v < NW; ++v) {
+                const float q = code_at<QT>(w[v], B, 4 * t + i);
+#pragma unroll
+                for (int r = 0; r < R; ++r) a[v][r][i] = __fmaf_rn(q, f4(xv[r], i), a[v][r][i]);
+            }
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < NW; ++v) {
+        const float d = scale_at(w[v], bb * B);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float s =
+                __fadd_rn(__fadd_rn(a[v][r][0], a[v][r][1]), __fadd_rn(a[v][r][2], a[v][r][3]));
+            c[v][r] = __fmaf_rn(d, s, c[v][r]);
+        }
+    }
+}
+
+// One unit (nbk <= 8 blocks; w[v] holds the unit's bytes little-endian from
+// its start) against x elements from e0.  c[v][r] receives the unit partials.
+template <int QT, int NW, int R, class XS>
+__device__ __forceinline__ void unit_dot(const uint32_t *const (&w)[NW], int nbk, const XS &xs,
+                                         int e0, float (&c)[NW][R]) {
+#pragma unroll
+    for (int v = 0; v < NW; ++v)
+#pragma unroll
+        for (int r = 0; r < R; ++r) c[v][r] = -0.0f;
+    block_dot<QT, NW, R, 0>(w, xs, e0, c);
+    if (nbk > 1) block_dot<QT, NW, R, 1>(w, xs, e0, c);
+    if (nbk > 2) block_dot<QT, NW, R, 2>(w, xs, e0, c);
+    if (nbk > 3) block_dot<QT, NW, R, 3>(w, xs, e0, c);
+    if (nbk > 4) block_dot<QT, NW, R, 4>(w, xs, e0, c);
+    if (nbk > 5) block_dot<QT, NW, R, 5>(w, xs, e0, c);
+    if (nbk > 6) block_dot<QT, NW, R, 6>(w, xs, e0, c);
+    if (nbk > 7) block_dot<QT, NW, R, 7>(w, xs, e0, c);
+}
+
+// load a full unit from shared memory (16-byte aligned)
+template <int QT>
+__device__ __forceinline__ void load_unit_smem(uint32_t *w, const uint8_t *p) {
+    constexpr int n16 = Fmt<QT>::unit_bytes / 16;
+#pragma unroll
+    for (int i = 0; i < n16; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(p + 16 * i);
+        w[4 * i + 0] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+    }
+}
+
+// load nbk blocks of a unit from global memory (2-byte aligned); bytes past
+// the unit's blocks are zero
+template <int QT>
+__device__ __forceinline__ void load_unit_global(uint32_t *w, const uint8_t *p, int nbk) {
+    constexpr int nw = Fmt<QT>::unit_words;
+    const int nhalf = nbk * Fmt<QT>::block_bytes / 2;
+    const unsigned short *h = reinterpret_cast<const unsigned short *>(p);
+#pragma unroll
+    for (int i = 0; i < nw; ++i) {
+        const uint32_t lo = (2 * i < nhalf) ? (uint32_t)__ldg(h + 2 * i) : 0u;
+        const uint32_t hi = (2 * i + 1 < nhalf) ? (uint32_t)__ldg(h + 2 * i + 1) : 0u;
+        w[i] = lo | (hi << 16);
+    }
+}
+
+// fold lane partials of a G-lane group (G a power of two <= 32)
+__device__ __forceinline__ float fold_lanes(float v, int G) {
+    for (int o = G >> 1; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// silu(g) * u in fp32
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    const float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+    return __fmul_rn(s, u);
+}
+
+// RMSNorm scale 1/sqrt(mean(x^2) + eps) with a summation order that does not
+// depend on the number of threads: 256 virtual lanes v each sum x[v],
+// x[v+256], ... in order; the 256 lane sums are folded by a fixed tree.
+// Called by `nthr` threads (thread index tid) sharing `red` (>= 257 floats);
+// `sync` is a barrier over exactly those threads.
+template <class Sync>
+__device__ float rms_scale(const float *x, int K, float eps, float *red, int tid, int nthr,
+                           Sync sync) {
+    for (int v = tid; v < 256; v += nthr) {
+        float s = 0.0f;
+        for (int k = v; k < K; k += 256) s = __fmaf_rn(x[k], x[k], s);
+        red[v] = s;
+    }
+    sync();
+    if (tid < 32) {
+        const float *q = red + 8 * tid;
+        float v = __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
+                            __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
+        for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (tid == 0) red[256] = v;
+    }
+    sync();
+    const float ms = __fdiv_rn(red[256], (float)K);
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+}  // namespace bq

@@ -1,0 +1,66 @@
+// bq_internal.h -- host-side types shared by the C-ABI layer (bq_api.cu) and
+// the per-format kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace bq {
+
+constexpr int MODE_PLAIN = 0;    // y = W x  (R input rows: R = 1 decode, R > 1 verify)
+constexpr int MODE_GATE_UP = 1;  // y = silu(Wg xn) * (Wu xn)
+
+constexpr int PLAN_STREAM = 0;   // TMA-staged streaming kernel (K % 256 == 0)
+constexpr int PLAN_GENERIC = 1;  // direct global loads (any K % 32 == 0)
+
+// shared-memory header of the streaming kernel: mbarriers, flags, reduction scratch
+constexpr int HDR_BYTES = 2048;
+
+struct GemvCall {
+    int qtype, mode, R;
+    const void *W0, *W1;
+    const float *x, *gamma;
+    float eps;
+    float *y;
+    long long M, K;
+    void *stream;
+};
+
+// Launch geometry.  Only G affects results (it fixes the row's summation
+// tree); everything else is free to tune.
+struct LaunchPlan {
+    int kind;
+    int G;           // lanes per row
+    int nsc;         // 8-block units per row
+    long long rb;    // packed bytes per row
+    int NWC;         // consumer warps per CTA
+    int TR;          // rows per tile
+    int KCU;         // units per row per stage
+    int NS;          // stages in the ring
+    int nchunks;     // stages per tile
+    int ntiles;
+    int row_stride;  // shared-memory bytes per row in a stage
+    int mat_stride;  // shared-memory bytes per matrix in a stage
+    int stage_bytes;
+    int single_copy; // one bulk copy per stage (rows contiguous, no padding)
+    int xres;        // x resident in shared memory
+    int x_off, x_rstride, stage_off;
+    size_t smem;
+    int num_sms;
+};
+
+// lanes per row for a row of nsc units: the largest power of two G <= 32 whose
+// padding to a multiple of G wastes at most 1/8 of the lane slots
+int tree_lanes_for_units(long long nsc);
+
+// plan a GEMV call on the current device; returns false if it cannot be planned
+bool plan_gemv(const GemvCall &c, LaunchPlan *p);
+
+}  // namespace bq
+
+// per-format launchers (one translation unit each) and their device status words
+int bq_internal_launch_q8_0(const bq::GemvCall &c, const bq::LaunchPlan &p);
+int bq_internal_launch_q4_0(const bq::GemvCall &c, const bq::LaunchPlan &p);
+int bq_internal_status_q8_0(unsigned int *flags, int clear);
+int bq_internal_status_q4_0(unsigned int *flags, int clear);
+int bq_internal_pack(int qtype, const float *W, long long M, long long K, void *Wq, void *stream);

@@ -1,0 +1,151 @@
+/*
+ * bqgemv.h -- block-quantized weight dequant + batch-1 GEMV for GB300 (sm_103a).
+ *
+ * The C ABI of libbqgemv.so.  Plain C: pointers, sizes and an opaque stream
+ * handle; no CUDA or PyTorch types.
+ *
+ * What is computed (sources are the four pages this library restates):
+ *  - The batch-1 decode step of a quantized LLM is a bandwidth-bound
+ *    matrix-vector product over quantized weights, dequantized on the fly
+ *    inside the dot product with no fp32 weight buffer ("We Wrote Our Own
+ *    Inference Engine", "What actually moved it" #2; EdgeRunner blog post,
+ *    "What worked" #2; RunIT README, optimisation table "Fused Q8_0 GEMV" /
+ *    "Fused Q4_0 GEMV").
+ *  - Block formats (GGUF-style, 32 weights per block; the RunIT README's
+ *    "Quantization" table gives 1.06 B/elem for Q8_0 and 0.56 B/elem for Q4_0):
+ *      Q8_0, 34 bytes: fp16 scale d (little-endian) then 32 int8 codes q;
+ *            w = d * q.
+ *      Q4_0, 18 bytes: fp16 scale d then 16 bytes qs; element j < 16 is the
+ *            low nibble of qs[j], element j + 16 the high nibble; w = d*(n-8).
+ *  - A packed matrix with M rows and K columns is M rows of K/32 blocks, rows
+ *    contiguous with no padding: row m starts at byte m * (K/32) * {34, 18}.
+ *
+ * Conventions for every call below:
+ *  - All data pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA memory)
+ *    owned by the caller; the library allocates nothing and keeps no state
+ *    except a per-device record of kernel attributes it has set.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Every call only enqueues work and returns; results are ready
+ *    when the stream reaches that point.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns an error status and enqueues nothing.  Launch failures
+ *    return BQ_ERR_CUDA.  Faults inside a kernel surface at the caller's next
+ *    synchronisation, as with any CUDA library.  No call aborts or throws.
+ *  - Outputs are overwritten, never accumulated into.  Inputs and outputs
+ *    must not overlap.
+ *  - Shapes: M >= 0 (M == 0 is a no-op), K a multiple of 32, 32 <= K <= 2^18,
+ *    M <= 2^31 - 1.  The fast streaming kernels need K % 256 == 0 (whole
+ *    8-block units per row); other multiples of 32 take a slower kernel with
+ *    the same results.
+ *  - Alignment: packed weights and fp32 vectors/matrices 16-byte aligned;
+ *    fp32 outputs 4-byte aligned.
+ *  - Determinism: every output element is computed in a fixed order that
+ *    depends only on (qtype, K).  The same call on the same inputs gives the
+ *    same bits on every run, and bq_gemv_verify row r is bit-identical to the
+ *    single-row GEMV on X[r].
+ */
+#ifndef BQGEMV_H
+#define BQGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BQ_OK = 0,
+    BQ_ERR_NULL = 1,   /* a required pointer is NULL */
+    BQ_ERR_SHAPE = 2,  /* M, K or R outside the documented range */
+    BQ_ERR_ALIGN = 3,  /* a pointer is not aligned as documented */
+    BQ_ERR_QTYPE = 4,  /* unknown quantization type */
+    BQ_ERR_CUDA = 5,   /* a CUDA runtime call or kernel launch failed */
+    BQ_ERR_DEVICE = 6  /* a kernel recorded a device-side error (see bq_device_status) */
+} bq_status;
+
+typedef enum { BQ_Q4_0 = 2, BQ_Q8_0 = 8 } bq_qtype;
+
+/* Largest R accepted by bq_gemv_verify (the multi-row verify pass of
+ * speculative decoding runs 3-6 rows; "We Wrote Our Own Inference Engine",
+ * Update). */
+#define BQ_VERIFY_MAX_ROWS 6
+
+/* Library version, major*10000 + minor*100 + patch. */
+int bq_version(void);
+
+/* Human-readable text for a bq_status value (never NULL). */
+const char *bq_status_str(int status);
+
+/* Bytes of a packed M x K matrix: M * (K/32) * {34 for Q8_0, 18 for Q4_0}.
+ * Returns -1 for an unknown qtype, a negative size or K % 32 != 0.
+ * (RunIT README, "Quantization" table: 1.06 / 0.56 bytes per element.) */
+int64_t bq_packed_bytes(int qtype, int64_t M, int64_t K);
+
+/* Quantize fp32 weights W [M, K] (row-major) into packed blocks Wq
+ * (bq_packed_bytes(qtype, M, K) bytes).  Per block of 32 weights:
+ *   Q8_0: d = fp16_rne(max|w| / 127);  q = clamp(round(w / d), -127, 127)
+ *   Q4_0: d = fp16_rne(max|w| / 8);    n = clamp(round(w / d) + 8, 0, 15)
+ * with fp32 IEEE divisions by the stored scale, round = half away from zero,
+ * and d == 0 giving q = 0 / n = 8.  The output bytes are a pure function of
+ * the input bits.  This is the load-time conversion the pages do in their
+ * converters ("We Wrote Our Own Inference Engine", "The recipe rule"), not
+ * part of the per-token path.
+ * W: 4-byte aligned; Wq: 16-byte aligned.  NaN/Inf weights are outside the
+ * contract. */
+bq_status bq_quantize_pack(int qtype, const float *W, int64_t M, int64_t K, void *Wq,
+                           void *stream);
+
+/* y[m] = sum_k w[m,k] * x[k] for packed Q8_0 weights Wq (M x K), fp32 x[K],
+ * fp32 y[M]; dequantized on the fly, fp32 accumulation in a fixed order.
+ * (RunIT README kernel table, gemv_q8_0_f32in_f32out; EdgeRunner blog post,
+ * "What worked" #2.) */
+bq_status bq_gemv_q8_0(const void *Wq, const float *x, float *y, int64_t M, int64_t K,
+                       void *stream);
+
+/* The same for packed Q4_0 weights.  (RunIT README kernel table,
+ * gemv_q4_0_f32in_f32out; "We Wrote Our Own Inference Engine", "What actually
+ * moved it" #2, the dedicated 4-bit GEMV.) */
+bq_status bq_gemv_q4_0(const void *Wq, const float *x, float *y, int64_t M, int64_t K,
+                       void *stream);
+
+/* Fused feed-forward input stage:
+ *   xn = gamma == NULL ? x : x * gamma / sqrt(mean(x^2) + eps)
+ *   y[m] = silu(g[m]) * u[m],  g = Wg xn,  u = Wu xn,  silu(z) = z / (1 + e^-z)
+ * Wg and Wu are packed M x K matrices of the same qtype; x, gamma: fp32[K];
+ * y: fp32[M].  eps must be finite and >= 0 (with gamma != NULL).
+ * (RunIT README kernel table, fused_ffn_q4_0_f32 "gate+up+silu fused" and
+ * rms_norm_f32_f32_f32g; EdgeRunner blog post, "The progression", the
+ * RMSNorm+GEMV fusion stage.) */
+bq_status bq_gemv_gate_up_silu(int qtype, const void *Wg, const void *Wu, const float *x,
+                               const float *gamma, float eps, float *y, int64_t M, int64_t K,
+                               void *stream);
+
+/* Multi-row verify GEMV: Y[r, m] = sum_k w[m,k] * X[r, k] for r < R,
+ * 1 <= R <= BQ_VERIFY_MAX_ROWS, with the weights streamed once for all R rows.
+ * X: fp32 [R, K] row-major; Y: fp32 [R, M] row-major.  Row r of Y is
+ * bit-identical (memcmp-equal) to bq_gemv_q8_0 / bq_gemv_q4_0 on X[r].
+ * ("We Wrote Our Own Inference Engine": the one-stream 3-6-row verify kernel
+ * of the Update, and "Correctness first", verify checked against decode with
+ * memcmp.) */
+bq_status bq_gemv_verify(int qtype, const void *Wq, const float *X, float *Y, int R,
+                         int64_t M, int64_t K, void *stream);
+
+/* Device-side error word of the current device.  The kernels bound every
+ * wait on their shared-memory pipeline; a wait that runs out sets a bit here
+ * and the kernel returns early.  *flags receives the word (0 = no error);
+ * clear != 0 resets it.  Synchronises the device.  Returns BQ_ERR_DEVICE if
+ * the word is non-zero, else BQ_OK (or BQ_ERR_CUDA). */
+bq_status bq_device_status(unsigned int *flags, int clear);
+
+/* The fixed summation tree of a row: each row of K/256 units (8 blocks) is
+ * split over bq_tree_lanes(K) lanes, lane l summing units l, l+G, l+2G, ...
+ * in order, and the lane sums are folded pairwise.  Exposed so callers and
+ * tests can reason about determinism; -1 if K is not a positive multiple of 32. */
+int bq_tree_lanes(int64_t K);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BQGEMV_H */

@@ -1,0 +1,186 @@
+"""GPU parity: the CUDA library (through its C ABI) against the oracle.
+
+- packing: bit-exact bytes;
+- GEMV, Q8_0 and Q4_0: |y - y_ref| <= 1e-5 * sum|w x| per row, and exactly
+  equal wherever every partial sum is an exact dyadic (power-of-two scales
+  with small-integer x, one-hot x, the worked examples);
+- gate+up+SiLU: the propagated bound of tests/tolerance.py;
+- verify: every row memcmp-equal to the single-row GEMV, and within the bound.
+Shapes span several tiles with ragged tails, both kernels (K % 256 == 0 and
+not), and the edge cases M = 0, M = 1, K = 32.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_quantized_weight_dequant_gb300 as bq
+from block_quantized_weight_dequant_gb300 import workloads as wl
+
+import oracle
+import oracle_checks as oc
+from tolerance import assert_gate_up_close, assert_gemv_close
+
+pytestmark = pytest.mark.gpu
+
+QT = {"q8_0": oracle.Q8_0, "q4_0": oracle.Q4_0}
+DEV = "cuda"
+
+# (M, K): stream kernel (K % 256 == 0) with several tiles and ragged tails,
+# and the generic kernel (K % 256 != 0)
+SHAPES = [(1, 256), (7, 256), (33, 512), (64, 1024), (97, 1280), (300, 1024), (130, 2048),
+          (40, 3072), (19, 3584), (9, 5120), (37, 17408), (5, 18944),
+          (1, 32), (3, 96), (17, 288), (65, 544), (31, 1056), (2, 18976)]
+
+
+def ora():
+    return oracle.get()
+
+
+def weights(M, K, seed, spread=True):
+    """N(0, 0.02) weights; with `spread`, blocks scaled by 2^-30..2^7 (down to
+    fp16-subnormal and zero scales), and one all-zero block."""
+    w = wl.normal_np((M, K), wl.W_STD, seed=seed, stream=wl.stream_id("parity", M, K))
+    if spread:
+        rng = np.random.default_rng([seed, M, K])
+        s = (2.0 ** rng.integers(-30, 8, size=(M, K // 32, 1))).astype(np.float32)
+        w = (w.reshape(M, K // 32, 32) * s).reshape(M, K)
+        w[0, :32] = 0.0
+    return np.ascontiguousarray(w)
+
+
+def xvec(K, seed, R=None):
+    shape = (K,) if R is None else (R, K)
+    return wl.normal_np(shape, wl.X_STD, seed=seed, stream=wl.stream_id("x", K, R))
+
+
+def cuda(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def gpu_pack(qt, W):
+    return bq.quantize_pack(cuda(W), qt)
+
+
+# ---------------------------------------------------------------------------
+# packing
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("M,K", SHAPES)
+def test_pack_bit_exact(qt, M, K):
+    W = weights(M, K, seed=1)
+    got = gpu_pack(qt, W).cpu().numpy()
+    want = ora().quantize_pack(QT[qt], W)
+    assert got.shape == want.shape
+    bad = np.flatnonzero((got != want).any(axis=1))
+    assert bad.size == 0, f"rows {bad[:5]} differ"
+
+
+@pytest.mark.parametrize("name", oc.GOLDEN_FILES)
+def test_pack_and_gemv_golden(name):
+    g = oc.load_golden(name)
+    qt = "q8_0" if g["qtype"] == oracle.Q8_0 else "q4_0"
+    P = gpu_pack(qt, g["w"])
+    assert np.array_equal(P.cpu().numpy(), g["packed"])
+    y = bq.gemv(qt, P, torch.ones(g["K"], device=DEV)).cpu().numpy()
+    assert y.tolist() == g["x_ones_y"]
+
+
+# ---------------------------------------------------------------------------
+# GEMV
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("M,K", SHAPES)
+def test_gemv_within_bound(qt, M, K):
+    W = weights(M, K, seed=2)
+    x = xvec(K, seed=2)
+    P = gpu_pack(qt, W)
+    y = torch.full((M,), float("nan"), device=DEV)  # every element must be written
+    bq.gemv(qt, P, cuda(x), y)
+    y_ref, S = ora().gemv(QT[qt], P.cpu().numpy(), M, K, x.astype(np.float64))
+    assert_gemv_close(y.cpu().numpy(), y_ref, S, f"{qt} {M}x{K}")
+
+
+@pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("M,K", [(33, 256), (9, 288), (70, 1024), (5, 1056), (11, 2048)])
+def test_gemv_exact_on_dyadic_inputs(qt, M, K):
+    rng = np.random.default_rng([7, M, K])
+    raw, dsel = oc._direct_blocks(rng, QT[qt], M, K)
+    x = rng.integers(-2, 3, size=K).astype(np.float32)
+    y = bq.gemv(qt, cuda(raw), cuda(x)).cpu().numpy().astype(np.float64)
+    y_ref, _ = ora().gemv(QT[qt], raw, M, K, x.astype(np.float64))
+    assert np.array_equal(y, y_ref)
+
+
+@pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("K", [256, 1024, 1056])
+def test_gemv_one_hot_gives_exact_columns(qt, K):
+    M = 50
+    P = gpu_pack(qt, weights(M, K, seed=3))
+    deq = oc.dequant_independent(QT[qt], P.cpu().numpy(), M, K)
+    for k in (0, 1, 33, K // 2 + 5, K - 1):
+        x = torch.zeros(K, device=DEV)
+        x[k] = 1.0
+        y = bq.gemv(qt, P, x).cpu().numpy().astype(np.float64)
+        assert np.array_equal(y, deq[:, k]), f"column {k}"
+
+
+def test_gemv_empty_rows_is_noop():
+    P = torch.zeros((0, 34 * 8), dtype=torch.uint8, device=DEV)
+    y = torch.full((4,), 7.0, device=DEV)
+    bq.gemv_q8_0(P, torch.ones(256, device=DEV), y[:0])
+    torch.cuda.synchronize()
+    assert y.tolist() == [7.0] * 4
+
+
+# ---------------------------------------------------------------------------
+# gate + up + SiLU
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("use_gamma", [True, False])
+@pytest.mark.parametrize("M,K", [(3072, 1024), (77, 256), (130, 2048), (33, 3584), (13, 288),
+                                 (5, 1056)])
+def test_gate_up_silu_within_bound(qt, use_gamma, M, K):
+    Wg, Wu = weights(M, K, seed=4, spread=False), weights(M, K, seed=5, spread=False)
+    x = xvec(K, seed=4)
+    gamma = wl.normal_np(K, 0.1, seed=4, stream=wl.stream_id("gamma", K), mean=1.0)
+    Pg, Pu = gpu_pack(qt, Wg), gpu_pack(qt, Wu)
+    y = bq.gemv_gate_up_silu(qt, Pg, Pu, cuda(x), cuda(gamma) if use_gamma else None,
+                             1e-6).cpu().numpy()
+    o = ora()
+    xn = o.rmsnorm(x, gamma, 1e-6) if use_gamma else x.astype(np.float64)
+    r = o.gate_up_silu(QT[qt], Pg.cpu().numpy(), Pu.cpu().numpy(), M, K, xn)
+    assert_gate_up_close(y, r, f"{qt} {M}x{K} gamma={use_gamma}")
+
+
+def test_gate_up_without_gamma_matches_plain_gemv_bits():
+    """With no RMSNorm the gate/up operands are the plain GEMV's, bit for bit."""
+    M, K = 200, 1024
+    Pg, Pu = gpu_pack("q8_0", weights(M, K, 8)), gpu_pack("q8_0", weights(M, K, 9))
+    x = cuda(xvec(K, 8))
+    y = bq.gemv_gate_up_silu("q8_0", Pg, Pu, x, None).cpu().numpy()
+    g = bq.gemv_q8_0(Pg, x).cpu().numpy()
+    u = bq.gemv_q8_0(Pu, x).cpu().numpy()
+    want = (torch.from_numpy(g) / (1 + torch.exp(-torch.from_numpy(g))) * torch.from_numpy(u))
+    assert np.allclose(y, want.numpy(), rtol=2e-6, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# multi-row verify
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("qt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("M,K", [(300, 1024), (97, 5120), (40, 17408), (17, 288), (9, 1056)])
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 5, 6])
+def test_verify_rows_memcmp_equal_to_decode(qt, M, K, R):
+    P = gpu_pack(qt, weights(M, K, seed=6))
+    X = xvec(K, seed=6, R=R)
+    Y = bq.gemv_verify(qt, P, cuda(X)).cpu().numpy()
+    Pn = P.cpu().numpy()
+    for r in range(R):
+        y1 = bq.gemv(qt, P, cuda(X[r])).cpu().numpy()
+        assert Y[r].tobytes() == y1.tobytes(), f"row {r} differs from decode"
+        y_ref, S = ora().gemv(QT[qt], Pn, M, K, X[r].astype(np.float64))
+        assert_gemv_close(Y[r], y_ref, S, f"verify {qt} {M}x{K} R={R} row {r}")
+
+
+def test_no_device_errors_recorded():
+    assert bq.device_status(clear=True) == 0
