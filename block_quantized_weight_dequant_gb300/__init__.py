@@ -23,7 +23,7 @@ QTYPES = {"q8_0": Q8_0, "q4_0": Q4_0}
 
 __all__ = ["Q8_0", "Q4_0", "BLOCK_BYTES", "BQError", "packed_bytes", "quantize_pack",
            "gemv", "gemv_q8_0", "gemv_q4_0", "gemv_gate_up_silu", "gemv_verify",
-           "device_status", "tree_lanes", "version"]
+           "device_status", "tree_lanes", "version", "StreamOp", "StreamPlan"]
 
 
 def _qt(qtype):
@@ -161,3 +161,73 @@ def device_status(clear=True):
     if st not in (_lib.BQ_OK, _lib.BQ_ERR_DEVICE):
         raise BQError(st, "device_status")
     return flags.value
+
+
+class StreamOp:
+    """One op of a per-token stream: a GEMV (``W`` only) or a fused
+    RMSNorm+gate+up+SiLU (``W`` = gate, ``W_up`` = up, optional ``gamma``).
+    ``stage`` orders the ops: ops of one stage run concurrently, and an op may
+    read the output ``y`` of an op of an earlier stage as its ``x``."""
+
+    def __init__(self, stage, W, x, y, W_up=None, gamma=None, eps=1e-6):
+        self.stage, self.W, self.x, self.y = int(stage), W, x, y
+        self.W_up, self.gamma, self.eps = W_up, gamma, float(eps)
+
+
+class StreamPlan:
+    """A whole list of StreamOps run by ONE cooperative launch per call
+    (bq_stream_plan_* of include/bqgemv.h).  The descriptor workspace is a
+    torch tensor this object owns; keep the op tensors alive as long as the
+    plan.  ``launch()`` enqueues on the current stream and can be captured in
+    a CUDA graph; creating the plan synchronises, so do it before capture."""
+
+    def __init__(self, qtype, ops):
+        qt = _qt(qtype)
+        if not ops:
+            raise ValueError("empty op list")
+        arr = (_lib.BqOp * len(ops))()
+        for i, op in enumerate(ops):
+            _need(op.W, torch.uint8, "W")
+            _need(op.x, torch.float32, "x")
+            _need(op.y, torch.float32, "y")
+            M, K = _packed_shape(op.W, qt)
+            if op.x.numel() != K or op.y.numel() != M:
+                raise ValueError(f"op {i}: x must have K={K} and y M={M} elements")
+            a = arr[i]
+            a.stage, a.M, a.K = op.stage, M, K
+            a.W, a.x, a.y = op.W.data_ptr(), op.x.data_ptr(), op.y.data_ptr()
+            if op.W_up is not None:
+                _need(op.W_up, torch.uint8, "W_up")
+                if tuple(op.W_up.shape) != tuple(op.W.shape):
+                    raise ValueError(f"op {i}: W_up must match W")
+                a.kind, a.W_up, a.eps = _lib.BQ_OP_GATE_UP_SILU, op.W_up.data_ptr(), op.eps
+                if op.gamma is not None:
+                    _need(op.gamma, torch.float32, "gamma")
+                    a.gamma = op.gamma.data_ptr()
+            else:
+                a.kind = _lib.BQ_OP_GEMV
+        nstages = len({op.stage for op in ops})
+        nbytes = lib.bq_stream_workspace_bytes(len(ops), nstages)
+        if nbytes < 0:
+            raise ValueError("bad op/stage counts")
+        dev = ops[0].W.device
+        self.workspace = torch.empty(nbytes + 256, dtype=torch.uint8, device=dev)
+        base = self.workspace.data_ptr()
+        ws = ctypes.c_void_p((base + 255) // 256 * 256)
+        self._ops = ops  # keep the tensors alive
+        self._handle = ctypes.c_void_p()
+        self.n_ops, self.n_stages = len(ops), nstages
+        with torch.cuda.device(dev):
+            _lib.check(lib.bq_stream_plan_create(qt, arr, len(ops), ws, nbytes,
+                                                 ctypes.byref(self._handle)), "stream_plan_create")
+        self.device = dev
+
+    def launch(self):
+        _lib.check(lib.bq_stream_plan_launch(self._handle, _stream(self._ops[0].W)),
+                   "stream_plan_launch")
+
+    def __del__(self):
+        h = getattr(self, "_handle", None)
+        if h is not None and h.value:
+            lib.bq_stream_plan_destroy(h)
+            self._handle = None

@@ -14,10 +14,21 @@ BQ_OK, BQ_ERR_NULL, BQ_ERR_SHAPE, BQ_ERR_ALIGN, BQ_ERR_QTYPE, BQ_ERR_CUDA, BQ_ER
 BQ_Q4_0, BQ_Q8_0 = 2, 8
 BQ_VERIFY_MAX_ROWS = 6
 
+BQ_OP_GEMV, BQ_OP_GATE_UP_SILU = 0, 1
+
 # every extern "C" symbol of include/bqgemv.h
 EXPORTS = ("bq_version", "bq_status_str", "bq_packed_bytes", "bq_quantize_pack", "bq_gemv_q8_0",
            "bq_gemv_q4_0", "bq_gemv_gate_up_silu", "bq_gemv_verify", "bq_device_status",
-           "bq_tree_lanes")
+           "bq_tree_lanes", "bq_stream_workspace_bytes", "bq_stream_plan_create",
+           "bq_stream_plan_launch", "bq_stream_plan_destroy")
+
+
+class BqOp(ctypes.Structure):
+    """struct bq_op of include/bqgemv.h"""
+    _fields_ = [("kind", ctypes.c_int32), ("stage", ctypes.c_int32), ("M", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("W", ctypes.c_void_p), ("W_up", ctypes.c_void_p),
+                ("x", ctypes.c_void_p), ("gamma", ctypes.c_void_p), ("eps", ctypes.c_float),
+                ("y", ctypes.c_void_p)]
 
 
 class BQError(RuntimeError):
@@ -39,6 +50,11 @@ def _declare(lib):
         "bq_gemv_verify": (i32, [i32, vp, vp, vp, i32, i64, i64, vp]),
         "bq_device_status": (i32, [ctypes.POINTER(ctypes.c_uint), i32]),
         "bq_tree_lanes": (i32, [i64]),
+        "bq_stream_workspace_bytes": (i64, [i32, i32]),
+        "bq_stream_plan_create": (i32, [i32, ctypes.POINTER(BqOp), i32, vp, i64,
+                                        ctypes.POINTER(vp)]),
+        "bq_stream_plan_launch": (i32, [vp, vp]),
+        "bq_stream_plan_destroy": (i32, [vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

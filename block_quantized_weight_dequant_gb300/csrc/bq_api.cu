@@ -9,9 +9,13 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <new>
+#include <algorithm>
+#include <vector>
 
 #include "../../include/bqgemv.h"
 #include "bq_dot.cuh"
+#include "bq_exec.cuh"
 #include "bq_internal.h"
 
 namespace bq {
@@ -30,6 +34,9 @@ struct Tunables {
     int inflight = 96 * 1024;
     int ns_force = 0;
     int xres_max = 100 * 1024;
+    int exec_slot = 9216;  // stream executor: bytes per ring slot
+    int exec_nsw = 0;      // stream executor: slots per warp (0 = as many as fit, <= 4)
+    int exec_warps = 8;    // stream executor: warps per CTA
 };
 
 const Tunables &tunables() {
@@ -51,6 +58,9 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "inflight") && val >= 8192) v.inflight = val;
             else if (!std::strcmp(tok, "ns") && val >= 2 && val <= 8) v.ns_force = val;
             else if (!std::strcmp(tok, "xres") && val >= 0) v.xres_max = val;
+            else if (!std::strcmp(tok, "slot") && val >= 4096) v.exec_slot = val;
+            else if (!std::strcmp(tok, "nsw") && val >= 2 && val <= 8) v.exec_nsw = val;
+            else if (!std::strcmp(tok, "ewarps") && val >= 1 && val <= 8) v.exec_warps = val;
         }
         return v;
     }();
@@ -166,7 +176,25 @@ bool plan_gemv(const GemvCall &c, LaunchPlan *p) {
     }
 }
 
+// padded shared-memory row stride for `bytes` of units: conflict-free LDS.128
+// when fewer than 8 lanes share a row (see the bank analysis in bq_kernels.cuh)
+int padded_stride(int bytes, int G) {
+    int s16 = bytes / 16;
+    if (G < 8)
+        while (s16 % 8 != G % 8) ++s16;
+    return s16 * 16;
+}
+
 }  // namespace bq
+
+// the opaque plan handle of include/bqgemv.h
+struct bq_stream_plan {
+    int qtype, n_ops, n_stages, device;
+    int grid, threads;
+    size_t smem;
+    bq::ExecArgs args;
+    unsigned int *counters;
+};
 
 using bq::GemvCall;
 using bq::LaunchPlan;
@@ -196,9 +224,9 @@ bq_status gemv_common(int qtype, const void *Wq, const float *x, float *y, int R
     if (R < 1 || R > BQ_VERIFY_MAX_ROWS) return BQ_ERR_SHAPE;
     bq_status s = check_shape(M, K);
     if (s != BQ_OK) return s;
+    if (M == 0) return BQ_OK;  // empty product: nothing is read or written
     if (!Wq || !x || !y) return BQ_ERR_NULL;
     if (!aligned_ok(Wq, 16) || !aligned_ok(x, 16) || !aligned_ok(y, 4)) return BQ_ERR_ALIGN;
-    if (M == 0) return BQ_OK;
     GemvCall c{qtype, bq::MODE_PLAIN, R, Wq, nullptr, x, nullptr, 0.0f, y, M, K, stream};
     return run_gemv(c);
 }
@@ -237,9 +265,9 @@ bq_status bq_quantize_pack(int qtype, const float *W, int64_t M, int64_t K, void
     if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0) return BQ_ERR_QTYPE;
     bq_status s = check_shape(M, K);
     if (s != BQ_OK) return s;
+    if (M == 0) return BQ_OK;
     if (!W || !Wq) return BQ_ERR_NULL;
     if (!aligned_ok(W, 4) || !aligned_ok(Wq, 16)) return BQ_ERR_ALIGN;
-    if (M == 0) return BQ_OK;
     return from_cuda(bq_internal_pack(qtype, W, M, K, Wq, stream));
 }
 
@@ -262,14 +290,153 @@ bq_status bq_gemv_gate_up_silu(int qtype, const void *Wg, const void *Wu, const 
     if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0) return BQ_ERR_QTYPE;
     bq_status s = check_shape(M, K);
     if (s != BQ_OK) return s;
+    if (gamma && !(std::isfinite(eps) && eps >= 0.0f)) return BQ_ERR_SHAPE;
+    if (M == 0) return BQ_OK;
     if (!Wg || !Wu || !x || !y) return BQ_ERR_NULL;
     if (!aligned_ok(Wg, 16) || !aligned_ok(Wu, 16) || !aligned_ok(x, 16) || !aligned_ok(y, 4) ||
         (gamma && !aligned_ok(gamma, 16)))
         return BQ_ERR_ALIGN;
-    if (gamma && !(std::isfinite(eps) && eps >= 0.0f)) return BQ_ERR_SHAPE;
-    if (M == 0) return BQ_OK;
     GemvCall c{qtype, bq::MODE_GATE_UP, 1, Wg, Wu, x, gamma, eps, y, M, K, stream};
     return run_gemv(c);
+}
+
+static int64_t align256(int64_t v) { return (v + 255) / 256 * 256; }
+
+int64_t bq_stream_workspace_bytes(int n_ops, int n_stages) {
+    if (n_ops < 1 || n_stages < 1 || n_stages > n_ops) return -1;
+    return align256((int64_t)n_ops * sizeof(bq::ExecOp)) +
+           align256((int64_t)n_stages * sizeof(bq::ExecStage)) + align256((int64_t)n_stages * 4);
+}
+
+bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *workspace,
+                                int64_t workspace_bytes, bq_stream_plan **plan) {
+    if (!plan) return BQ_ERR_NULL;
+    *plan = nullptr;
+    if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0) return BQ_ERR_QTYPE;
+    if (!ops || !workspace) return BQ_ERR_NULL;
+    if (n_ops < 1) return BQ_ERR_SHAPE;
+    if (!aligned_ok(workspace, 256)) return BQ_ERR_ALIGN;
+    const bq::Tunables &t = bq::tunables();
+    const int bb = bq::block_bytes(qtype), ub = 8 * bb;
+    // a slot holds at least one warp tile of one unit per lane (32 units; the
+    // row stride of KCU = G units needs no bank padding, as 17 and 9 are 1 mod 8)
+    const int slot = (std::max(t.exec_slot, 32 * ub) + 127) / 128 * 128;
+    std::vector<bq::ExecOp> eo((size_t)n_ops);
+    std::vector<bq::ExecStage> es;
+    for (int i = 0; i < n_ops; ++i) {
+        const bq_op &o = ops[i];
+        if (o.kind != BQ_OP_GEMV && o.kind != BQ_OP_GATE_UP_SILU) return BQ_ERR_SHAPE;
+        if (i == 0 ? o.stage != 0 : (o.stage != ops[i - 1].stage && o.stage != ops[i - 1].stage + 1))
+            return BQ_ERR_SHAPE;
+        if (o.M < 1 || o.M > bq::M_MAX || o.K < 256 || o.K > bq::K_MAX || o.K % 256) return BQ_ERR_SHAPE;
+        const bool gu = o.kind == BQ_OP_GATE_UP_SILU;
+        if (!o.W || !o.x || !o.y || (gu && !o.W_up)) return BQ_ERR_NULL;
+        if (!aligned_ok(o.W, 16) || !aligned_ok(o.x, 16) || !aligned_ok(o.y, 4) ||
+            (gu && !aligned_ok(o.W_up, 16)) || (gu && o.gamma && !aligned_ok(o.gamma, 16)))
+            return BQ_ERR_ALIGN;
+        if (gu && o.gamma && !(std::isfinite(o.eps) && o.eps >= 0.0f)) return BQ_ERR_SHAPE;
+        bq::ExecOp &e = eo[(size_t)i];
+        e.W[0] = static_cast<const uint8_t *>(o.W);
+        e.W[1] = gu ? static_cast<const uint8_t *>(o.W_up) : nullptr;
+        e.x = o.x;
+        e.gamma = gu ? o.gamma : nullptr;
+        e.eps = o.eps;
+        e.y = o.y;
+        e.mode = gu ? bq::MODE_GATE_UP : bq::MODE_PLAIN;
+        e.nmat = gu ? 2 : 1;
+        e.M = (int)o.M;
+        e.K = (int)o.K;
+        e.nsc = (int)(o.K / 256);
+        e.G = bq::tree_lanes_for_units(e.nsc);
+        e.rpw = 32 / e.G;
+        e.rb = (long long)e.nsc * ub;
+        // whole rows per slot when they fit, else chunks of a multiple of G units
+        int KCU = e.nsc, stride = 0, single = 0;
+        if ((long long)e.rpw * e.rb <= slot) {
+            single = e.G >= 8 || (e.rb / 16) % 8 == e.G % 8;
+            stride = single ? (int)e.rb : bq::padded_stride((int)e.rb, e.G);
+            if ((long long)e.rpw * stride > slot) single = 0, stride = 0;
+        }
+        if (!stride) {
+            single = 0;
+            for (int m = (e.nsc + e.G - 1) / e.G; m >= 1; --m) {
+                KCU = std::min(e.nsc, e.G * m);
+                stride = bq::padded_stride(KCU * ub, e.G);
+                if ((long long)e.rpw * stride <= slot) break;
+            }
+        }
+        e.KCU = KCU;
+        e.row_stride = stride;
+        e.single = single;
+        e.nchunks = (e.nsc + KCU - 1) / KCU;
+        e.ntiles = (e.M + e.rpw - 1) / e.rpw;
+        if (i == 0 || o.stage != ops[i - 1].stage) es.push_back(bq::ExecStage{i, i + 1, 0, 0});
+        bq::ExecStage &st = es.back();
+        st.op_end = i + 1;
+        e.tile_base = st.tiles;
+        st.tiles += e.ntiles;
+    }
+    const int n_stages = (int)es.size();
+    const int64_t need = bq_stream_workspace_bytes(n_ops, n_stages);
+    if (workspace_bytes < need) return BQ_ERR_SHAPE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int64_t off_st = align256((int64_t)n_ops * sizeof(bq::ExecOp));
+    const int64_t off_cnt = off_st + align256((int64_t)n_stages * sizeof(bq::ExecStage));
+    if (cudaMemcpy(ws, eo.data(), eo.size() * sizeof(bq::ExecOp), cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
+        cudaMemcpy(ws + off_st, es.data(), es.size() * sizeof(bq::ExecStage),
+                   cudaMemcpyHostToDevice) != cudaSuccess)
+        return BQ_ERR_CUDA;
+    // launch geometry: as many ring slots per warp as fit (2..4), one CTA per SM
+    const int warps = t.exec_warps, threads = 32 * warps;
+    const int cap = bq::max_smem_optin();
+    auto ring_offset = [warps](int nsw) { return (64 + 8 * warps * nsw + 4 * 260 * warps + 127) / 128 * 128; };
+    int nsw = t.exec_nsw ? t.exec_nsw : 4;
+    while (nsw > 2 && ring_offset(nsw) + warps * nsw * slot > cap) --nsw;
+    const int ring_off = ring_offset(nsw);
+    const size_t smem = (size_t)ring_off + (size_t)warps * nsw * slot;
+    if ((int)smem > cap) return BQ_ERR_SHAPE;
+    int occ = 0;
+    const int e = qtype == BQ_Q8_0 ? bq_internal_exec_occupancy_q8_0(threads, smem, &occ)
+                                   : bq_internal_exec_occupancy_q4_0(threads, smem, &occ);
+    if (e != 0 || occ < 1) return BQ_ERR_CUDA;
+    auto *p = new (std::nothrow) bq_stream_plan;
+    if (!p) return BQ_ERR_CUDA;
+    p->qtype = qtype;
+    p->n_ops = n_ops;
+    p->n_stages = n_stages;
+    cudaGetDevice(&p->device);
+    p->grid = bq::num_sms_current() * occ;
+    p->threads = threads;
+    p->smem = smem;
+    p->args.ops = reinterpret_cast<const bq::ExecOp *>(ws);
+    p->args.stages = reinterpret_cast<const bq::ExecStage *>(ws + off_st);
+    p->counters = reinterpret_cast<unsigned int *>(ws + off_cnt);
+    p->args.counters = p->counters;
+    p->args.nstages = n_stages;
+    p->args.NSW = nsw;
+    p->args.slot_bytes = slot;
+    p->args.ring_off = ring_off;
+    *plan = p;
+    return BQ_OK;
+}
+
+bq_status bq_stream_plan_launch(const bq_stream_plan *plan, void *stream) {
+    if (!plan) return BQ_ERR_NULL;
+    auto s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(plan->counters, 0, (size_t)plan->n_stages * 4, s) != cudaSuccess)
+        return BQ_ERR_CUDA;
+    const int e = plan->qtype == BQ_Q8_0
+                      ? bq_internal_exec_launch_q8_0(plan->args, plan->grid, plan->threads,
+                                                     plan->smem, stream)
+                      : bq_internal_exec_launch_q4_0(plan->args, plan->grid, plan->threads,
+                                                     plan->smem, stream);
+    return from_cuda(e);
+}
+
+bq_status bq_stream_plan_destroy(bq_stream_plan *plan) {
+    delete plan;
+    return BQ_OK;
 }
 
 bq_status bq_device_status(unsigned int *flags, int clear) {

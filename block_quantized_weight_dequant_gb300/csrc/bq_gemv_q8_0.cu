@@ -1,26 +1,62 @@
 // bq_gemv_q8_0.cu -- the Q8_0 instantiations of the GEMV kernels (one
 // translation unit per format so the two compile in parallel) and this
 // unit's device-side error word.
+#include "bq_exec.cuh"
 #include "bq_kernels.cuh"
 
 namespace {
 __device__ unsigned int g_status_q8_0 = 0;
 }
 
-int bq_internal_launch_q8_0(const bq::GemvCall &c, const bq::LaunchPlan &p) {
-    // the status word's device address, looked up once per device
-    static unsigned int *addr[64] = {};
+namespace {
+// the status word's device address, looked up once per device
+cudaError_t status_addr(unsigned int **out) {
+    static std::atomic<unsigned int *> addr[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return (int)e;
-    if (dev < 0 || dev >= 64) return (int)cudaErrorInvalidDevice;
-    unsigned int *status = addr[dev];
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    unsigned int *status = addr[dev].load();
     if (!status) {
         e = cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status_q8_0);
-        if (e != cudaSuccess) return (int)e;
-        addr[dev] = status;
+        if (e != cudaSuccess) return e;
+        addr[dev].store(status);
     }
+    *out = status;
+    return cudaSuccess;
+}
+}  // namespace
+
+int bq_internal_launch_q8_0(const bq::GemvCall &c, const bq::LaunchPlan &p) {
+    unsigned int *status = nullptr;
+    cudaError_t e = status_addr(&status);
+    if (e != cudaSuccess) return (int)e;
     return (int)bq::launch_gemv<bq::QT_Q8_0>(c, p, status);
+}
+
+int bq_internal_exec_occupancy_q8_0(int threads, size_t smem, int *occ) {
+    auto kern = bq::exec_kernel<bq::QT_Q8_0>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kern, threads, smem);
+}
+
+int bq_internal_exec_launch_q8_0(const bq::ExecArgs &a, int grid, int threads, size_t smem,
+                               void *stream) {
+    unsigned int *status = nullptr;
+    cudaError_t e = status_addr(&status);
+    if (e != cudaSuccess) return (int)e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return (int)cudaLaunchKernelEx(&cfg, bq::exec_kernel<bq::QT_Q8_0>, a, status);
 }
 
 int bq_internal_status_q8_0(unsigned int *flags, int clear) {

@@ -64,3 +64,14 @@ int bq_internal_launch_q4_0(const bq::GemvCall &c, const bq::LaunchPlan &p);
 int bq_internal_status_q8_0(unsigned int *flags, int clear);
 int bq_internal_status_q4_0(unsigned int *flags, int clear);
 int bq_internal_pack(int qtype, const float *W, long long M, long long K, void *Wq, void *stream);
+
+namespace bq {
+struct ExecArgs;
+}
+// persistent per-token stream executor (bq_exec.cuh), one instantiation per format
+int bq_internal_exec_occupancy_q8_0(int threads, size_t smem, int *occ);
+int bq_internal_exec_occupancy_q4_0(int threads, size_t smem, int *occ);
+int bq_internal_exec_launch_q8_0(const bq::ExecArgs &a, int grid, int threads, size_t smem,
+                                 void *stream);
+int bq_internal_exec_launch_q4_0(const bq::ExecArgs &a, int grid, int threads, size_t smem,
+                                 void *stream);

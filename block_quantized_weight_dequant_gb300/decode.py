@@ -1,0 +1,96 @@
+"""The GEMV weight stream of one batch-1 decode step.
+
+A decoder layer's weight stream, in model order (RunIT README, data-flow
+diagram: RMSNorm -> Q/K/V projections -> attention -> FFN gate/up -> SiLU ->
+down -> ... -> lm_head):
+
+    stage 4l+0: q, k, v        x = the layer input h
+    stage 4l+1: o              x = q's output (stand-in for the attention
+                               output, which has q's width)
+    stage 4l+2: gate+up+SiLU   x = o's output, RMSNorm-ed with the layer gain
+    stage 4l+3: down           x = the gate+up output; its output is the next
+                               layer's input h
+    last stage: LM head        x = the last layer's output
+
+Attention itself, residual adds and the other norms are outside this stream
+(they are not weight streaming).  Every op reads the previous stage's output,
+so the stages are truly dependent, as in decode.  ``run_plan()`` runs the
+whole stream in one cooperative launch (bq_stream_plan_*); ``run_per_op()``
+launches one kernel per op in stage order; the two give identical bits.
+"""
+import torch
+
+from . import StreamOp, StreamPlan, gemv, gemv_gate_up_silu
+
+
+class DecodeStream:
+    def __init__(self, qtype, layers, lm_head, eps=1e-6):
+        """layers: list of dicts with packed q, k, v, o, gate, up, down
+        (uint8 [M, row bytes]) and gamma (fp32 [hidden]); lm_head: packed."""
+        from . import _packed_shape, _qt
+        self.qtype = _qt(qtype)
+        self.eps = eps
+        dev = lm_head.device
+        self.layers = layers
+        self.lm_head = lm_head
+        f32 = dict(dtype=torch.float32, device=dev)
+
+        def rows(P):
+            return _packed_shape(P, self.qtype)
+
+        hidden = rows(layers[0]["q"])[1]
+        self.x0 = torch.zeros(hidden, **f32)
+        self.ops = []
+        self.buffers = []
+        h = self.x0
+        st = 0
+        for L in layers:
+            bufs = {n: torch.empty(rows(L[n])[0], **f32) for n in ("q", "k", "v", "o", "down")}
+            bufs["ffn"] = torch.empty(rows(L["gate"])[0], **f32)
+            self.buffers.append(bufs)
+            for n in ("q", "k", "v"):
+                self.ops.append(StreamOp(st, L[n], h, bufs[n]))
+            self.ops.append(StreamOp(st + 1, L["o"], bufs["q"], bufs["o"]))
+            self.ops.append(StreamOp(st + 2, L["gate"], bufs["o"], bufs["ffn"], W_up=L["up"],
+                                     gamma=L["gamma"], eps=eps))
+            self.ops.append(StreamOp(st + 3, L["down"], bufs["ffn"], bufs["down"]))
+            h = bufs["down"]
+            st += 4
+        self.logits = torch.empty(rows(lm_head)[0], **f32)
+        self.ops.append(StreamOp(st, lm_head, h, self.logits))
+        self._plan = None
+
+    @property
+    def n_stages(self):
+        return self.ops[-1].stage + 1
+
+    def weight_bytes(self):
+        n = 0
+        for op in self.ops:
+            n += op.W.numel() + (op.W_up.numel() if op.W_up is not None else 0)
+        return n
+
+    def activation_bytes(self):
+        """Algorithmic activation traffic: every op reads x (and gamma) and
+        writes y once."""
+        n = 0
+        for op in self.ops:
+            n += 4 * (op.x.numel() + op.y.numel())
+            if op.gamma is not None:
+                n += 4 * op.gamma.numel()
+        return n
+
+    def plan(self):
+        if self._plan is None:
+            self._plan = StreamPlan(self.qtype, self.ops)
+        return self._plan
+
+    def run_plan(self):
+        self.plan().launch()
+
+    def run_per_op(self):
+        for op in self.ops:
+            if op.W_up is None:
+                gemv(self.qtype, op.W, op.x, op.y)
+            else:
+                gemv_gate_up_silu(self.qtype, op.W, op.W_up, op.x, op.gamma, op.eps, op.y)

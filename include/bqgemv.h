@@ -33,10 +33,12 @@
  *    synchronisation, as with any CUDA library.  No call aborts or throws.
  *  - Outputs are overwritten, never accumulated into.  Inputs and outputs
  *    must not overlap.
- *  - Shapes: M >= 0 (M == 0 is a no-op), K a multiple of 32, 32 <= K <= 2^18,
- *    M <= 2^31 - 1.  The fast streaming kernels need K % 256 == 0 (whole
- *    8-block units per row); other multiples of 32 take a slower kernel with
- *    the same results.
+ *  - Shapes: 0 <= M <= 2^31 - 1, K a multiple of 32, 32 <= K <= 2^18.
+ *    M == 0 is an empty product: after the qtype and shape checks the call
+ *    returns BQ_OK without reading or writing anything, so its pointers may
+ *    be NULL (an empty PyTorch tensor has a NULL data pointer).  The fast
+ *    streaming kernels need K % 256 == 0 (whole 8-block units per row); other
+ *    multiples of 32 take a slower kernel with the same results.
  *  - Alignment: packed weights and fp32 vectors/matrices 16-byte aligned;
  *    fp32 outputs 4-byte aligned.
  *  - Determinism: every output element is computed in a fixed order that
@@ -143,6 +145,61 @@ bq_status bq_device_status(unsigned int *flags, int clear);
  * in order, and the lane sums are folded pairwise.  Exposed so callers and
  * tests can reason about determinism; -1 if K is not a positive multiple of 32. */
 int bq_tree_lanes(int64_t K);
+
+/* ------------------------------------------------------------------------
+ * Per-token stream executor.
+ *
+ * A decode step is a chain of dependent GEMV stages (per layer q|k|v, o,
+ * gate+up, down, then the LM head).  The pages run it as one command buffer
+ * per token because dispatch cost dominates small GEMVs (EdgeRunner blog
+ * post, "What worked" #1; "We Wrote Our Own Inference Engine", 770 dispatches
+ * per token).  A plan runs a whole list of GEMV ops in ONE cooperative
+ * launch: ops of one stage run concurrently; a grid-wide barrier separates
+ * stages, so an op may read an output written by an earlier stage.  Weights
+ * never depend on earlier stages, so each warp streams the next stage's
+ * weights into shared memory while it waits at the barrier.  Every output is
+ * bit-identical to the single-op call (bq_gemv_q8_0 / _q4_0 /
+ * bq_gemv_gate_up_silu) on the same inputs.
+ * ------------------------------------------------------------------------ */
+typedef enum { BQ_OP_GEMV = 0, BQ_OP_GATE_UP_SILU = 1 } bq_op_kind;
+
+typedef struct {
+    int32_t kind;        /* bq_op_kind */
+    int32_t stage;       /* 0 for the first op; then equal to, or one more than,
+                            the previous op's stage */
+    int64_t M, K;        /* M >= 1; K % 256 == 0, 256 <= K <= 2^18 */
+    const void *W;       /* packed weights (the gate matrix for GATE_UP_SILU) */
+    const void *W_up;    /* packed up matrix (GATE_UP_SILU), else ignored */
+    const float *x;      /* fp32[K]; may be the output of an earlier stage */
+    const float *gamma;  /* GATE_UP_SILU: RMSNorm gain fp32[K] or NULL */
+    float eps;           /* GATE_UP_SILU with gamma: finite, >= 0 */
+    float *y;            /* fp32[M]; must not overlap any input of its own stage */
+} bq_op;
+
+typedef struct bq_stream_plan bq_stream_plan;
+
+/* Device workspace a plan of n_ops ops in n_stages stages needs (descriptor
+ * table and one barrier counter per stage); -1 for bad counts. */
+int64_t bq_stream_workspace_bytes(int n_ops, int n_stages);
+
+/* Validate the ops (all of one qtype), plan their launch geometry and upload
+ * the descriptor table into `workspace` (caller-owned device memory of at
+ * least bq_stream_workspace_bytes bytes, 256-byte aligned, kept alive and
+ * untouched until the plan is destroyed).  Synchronous (it copies host to
+ * device): create plans before capturing a CUDA graph.  *plan is a small
+ * host object owned by the caller until bq_stream_plan_destroy.  The device
+ * that is current at creation runs the plan. */
+bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *workspace,
+                                int64_t workspace_bytes, bq_stream_plan **plan);
+
+/* Enqueue one run of the plan on `stream`: a memset of the stage counters and
+ * one cooperative kernel launch; no host synchronisation, capturable in a
+ * CUDA graph.  Two runs of one plan must not overlap on the GPU (they share
+ * the counters). */
+bq_status bq_stream_plan_launch(const bq_stream_plan *plan, void *stream);
+
+/* Free the host object (the workspace stays the caller's). */
+bq_status bq_stream_plan_destroy(bq_stream_plan *plan);
 
 #ifdef __cplusplus
 }

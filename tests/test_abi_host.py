@@ -89,8 +89,10 @@ def test_gemv_argument_validation(lib):
         assert fn(MIS, FAKE, FAKE, 8, 256, None) == _lib.BQ_ERR_ALIGN
         assert fn(FAKE, MIS, FAKE, 8, 256, None) == _lib.BQ_ERR_ALIGN
         assert fn(FAKE, FAKE, ctypes.c_void_p(0x10002), 8, 256, None) == _lib.BQ_ERR_ALIGN
-        # M == 0 is an empty product: accepted, nothing launched
+        # M == 0 is an empty product: accepted, nothing launched, NULL allowed
         assert fn(FAKE, FAKE, FAKE, 0, 256, None) == _lib.BQ_OK
+        assert fn(None, None, None, 0, 256, None) == _lib.BQ_OK
+        assert fn(None, None, None, 0, 48, None) == _lib.BQ_ERR_SHAPE
 
 
 def test_verify_and_gate_up_validation(lib):

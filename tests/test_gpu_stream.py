@@ -1,0 +1,108 @@
+"""The per-token stream executor (one cooperative launch) against the
+launch-per-op path: every output of every stage bit-identical, on chained
+decode streams where each stage reads the previous stage's output; plus the
+oracle bound on the final outputs and repeat-run determinism."""
+import numpy as np
+import pytest
+import torch
+
+import block_quantized_weight_dequant_gb300 as bq
+from block_quantized_weight_dequant_gb300 import workloads as wl
+from block_quantized_weight_dequant_gb300.decode import DecodeStream
+
+import oracle
+from tolerance import assert_gemv_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab, seed=0):
+    def packed(M, K, *tag):
+        W = wl.normal_torch((M, K), wl.W_STD, seed=seed, stream=wl.stream_id(*tag), device=DEV)
+        return bq.quantize_pack(W, qt)
+
+    layers = []
+    for l in range(n_layers):
+        layers.append(dict(
+            q=packed(q_dim, hidden, l, "q"), k=packed(kv_dim, hidden, l, "k"),
+            v=packed(kv_dim, hidden, l, "v"), o=packed(hidden, q_dim, l, "o"),
+            gate=packed(inter, hidden, l, "g"), up=packed(inter, hidden, l, "u"),
+            down=packed(hidden, inter, l, "d"),
+            gamma=wl.normal_torch(hidden, 0.1, seed=seed, stream=wl.stream_id(l, "gm"),
+                                  device=DEV, mean=1.0)))
+    ds = DecodeStream(qt, layers, packed(vocab, hidden, "lm"))
+    ds.x0.copy_(wl.normal_torch(hidden, 1.0, seed=seed, stream=7, device=DEV))
+    return ds
+
+
+def snapshot(ds):
+    return [op.y.clone() for op in ds.ops]
+
+
+STREAMS = [
+    ("q8_0", 3, 512, 512, 128, 1024, 3000),      # G = 4 and 8, whole rows per slot
+    ("q8_0", 2, 1024, 2048, 512, 3072, 20000),   # Qwen3-0.6B layer shapes, chunked down
+    ("q4_0", 2, 3584, 3584, 512, 18944, 4096),   # 7B layer shapes, G = 16, chunked down
+    ("q4_0", 2, 256, 768, 256, 1280, 999),       # odd unit counts, ragged tiles
+]
+
+
+@pytest.mark.parametrize("qt,n_layers,hidden,q_dim,kv_dim,inter,vocab", STREAMS)
+def test_plan_matches_launch_per_op_bitwise(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab):
+    ds = make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab)
+    ds.run_per_op()
+    want = snapshot(ds)
+    for op in ds.ops:
+        op.y.fill_(float("nan"))
+    ds.run_plan()
+    got = snapshot(ds)
+    for i, (g, w) in enumerate(zip(got, want)):
+        assert torch.equal(g.view(torch.int32), w.view(torch.int32)), f"op {i} differs"
+    # run again: the counters are reset per launch and the result repeats
+    ds.run_plan()
+    again = snapshot(ds)
+    for g, w in zip(again, want):
+        assert torch.equal(g.view(torch.int32), w.view(torch.int32))
+    assert bq.device_status(clear=True) == 0
+
+
+def test_plan_final_output_within_oracle_bound():
+    qt = "q8_0"
+    ds = make_stream(qt, 1, 512, 512, 128, 1024, 700)
+    ds.run_plan()
+    lm = ds.ops[-1]
+    x = lm.x.cpu().numpy().astype(np.float64)
+    y_ref, S = oracle.get().gemv(oracle.Q8_0, lm.W.cpu().numpy(), lm.W.shape[0], x.size, x)
+    assert_gemv_close(lm.y.cpu().numpy(), y_ref, S, "plan lm_head")
+
+
+def test_plan_in_cuda_graph():
+    ds = make_stream("q8_0", 2, 512, 512, 128, 1024, 2000)
+    ds.run_per_op()
+    want = snapshot(ds)
+    ds.plan()  # created before capture (it synchronises)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ds.run_plan()
+    for op in ds.ops:
+        op.y.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for g_, w in zip(snapshot(ds), want):
+        assert torch.equal(g_.view(torch.int32), w.view(torch.int32))
+
+
+def test_plan_rejects_bad_ops():
+    P = bq.quantize_pack(torch.zeros(64, 512, device=DEV), "q8_0")
+    x = torch.zeros(512, device=DEV)
+    y = torch.zeros(64, device=DEV)
+    with pytest.raises(bq.BQError):  # first stage must be 0
+        bq.StreamPlan("q8_0", [bq.StreamOp(1, P, x, y)])
+    with pytest.raises(bq.BQError):  # stages may not skip
+        bq.StreamPlan("q8_0", [bq.StreamOp(0, P, x, y), bq.StreamOp(2, P, x, y)])
+    P2 = bq.quantize_pack(torch.zeros(64, 288, device=DEV), "q8_0")
+    with pytest.raises(bq.BQError):  # K % 256 != 0 is not streamed
+        bq.StreamPlan("q8_0", [bq.StreamOp(0, P2, torch.zeros(288, device=DEV), y)])
