@@ -34,7 +34,7 @@ struct Tunables {
     int inflight = 96 * 1024;
     int ns_force = 0;
     int xres_max = 100 * 1024;
-    int exec_slot = 9216;  // stream executor: bytes per ring slot
+    int exec_slot = 0;     // stream executor: bytes per ring slot (0 = one warp tile of 32 units)
     int exec_nsw = 0;      // stream executor: slots per warp (0 = as many as fit, <= 4)
     int exec_warps = 8;    // stream executor: warps per CTA
 };
@@ -305,6 +305,7 @@ static int64_t align256(int64_t v) { return (v + 255) / 256 * 256; }
 int64_t bq_stream_workspace_bytes(int n_ops, int n_stages) {
     if (n_ops < 1 || n_stages < 1 || n_stages > n_ops) return -1;
     return align256((int64_t)n_ops * sizeof(bq::ExecOp)) +
+           align256((int64_t)n_ops * sizeof(bq::ExecX)) +
            align256((int64_t)n_stages * sizeof(bq::ExecStage)) + align256((int64_t)n_stages * 4);
 }
 
@@ -323,6 +324,8 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
     const int slot = (std::max(t.exec_slot, 32 * ub) + 127) / 128 * 128;
     std::vector<bq::ExecOp> eo((size_t)n_ops);
     std::vector<bq::ExecStage> es;
+    std::vector<bq::ExecX> ex;
+    int x_area = 0, stage_x = 0;  // floats: largest stage, current stage
     for (int i = 0; i < n_ops; ++i) {
         const bq_op &o = ops[i];
         if (o.kind != BQ_OP_GEMV && o.kind != BQ_OP_GATE_UP_SILU) return BQ_ERR_SHAPE;
@@ -338,9 +341,6 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
         bq::ExecOp &e = eo[(size_t)i];
         e.W[0] = static_cast<const uint8_t *>(o.W);
         e.W[1] = gu ? static_cast<const uint8_t *>(o.W_up) : nullptr;
-        e.x = o.x;
-        e.gamma = gu ? o.gamma : nullptr;
-        e.eps = o.eps;
         e.y = o.y;
         e.mode = gu ? bq::MODE_GATE_UP : bq::MODE_PLAIN;
         e.nmat = gu ? 2 : 1;
@@ -370,31 +370,53 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
         e.single = single;
         e.nchunks = (e.nsc + KCU - 1) / KCU;
         e.ntiles = (e.M + e.rpw - 1) / e.rpw;
-        if (i == 0 || o.stage != ops[i - 1].stage) es.push_back(bq::ExecStage{i, i + 1, 0, 0});
+        if (i == 0 || o.stage != ops[i - 1].stage) {
+            es.push_back(bq::ExecStage{i, i + 1, 0, (int)ex.size(), (int)ex.size()});
+            stage_x = 0;
+        }
         bq::ExecStage &st = es.back();
         st.op_end = i + 1;
         e.tile_base = st.tiles;
         st.tiles += e.ntiles;
+        // the stage's distinct inputs: ops sharing x (and its norm) share one copy
+        const float *g = gu ? o.gamma : nullptr;
+        const float eps = g ? o.eps : 0.0f;
+        int found = -1;
+        for (int j = st.x_begin; j < st.x_end; ++j)
+            if (ex[j].x == o.x && ex[j].gamma == g && ex[j].eps == eps && ex[j].K == e.K) found = j;
+        if (found < 0) {
+            ex.push_back(bq::ExecX{o.x, g, eps, e.K, stage_x});
+            stage_x += bq::x_padded_floats(e.K);
+            found = st.x_end++;
+        }
+        e.xoff = ex[found].off;
+        x_area = std::max(x_area, stage_x);
     }
     const int n_stages = (int)es.size();
     const int64_t need = bq_stream_workspace_bytes(n_ops, n_stages);
     if (workspace_bytes < need) return BQ_ERR_SHAPE;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const int64_t off_st = align256((int64_t)n_ops * sizeof(bq::ExecOp));
+    const int64_t off_x = align256((int64_t)n_ops * sizeof(bq::ExecOp));
+    const int64_t off_st = off_x + align256((int64_t)n_ops * sizeof(bq::ExecX));
     const int64_t off_cnt = off_st + align256((int64_t)n_stages * sizeof(bq::ExecStage));
     if (cudaMemcpy(ws, eo.data(), eo.size() * sizeof(bq::ExecOp), cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
+        cudaMemcpy(ws + off_x, ex.data(), ex.size() * sizeof(bq::ExecX), cudaMemcpyHostToDevice) !=
             cudaSuccess ||
         cudaMemcpy(ws + off_st, es.data(), es.size() * sizeof(bq::ExecStage),
                    cudaMemcpyHostToDevice) != cudaSuccess)
         return BQ_ERR_CUDA;
-    // launch geometry: as many ring slots per warp as fit (2..4), one CTA per SM
+    // shared memory: flag + reduction scratch + mbarriers | stage x area | rings
+    // (as many slots per warp as fit, 2..4; one CTA per SM)
     const int warps = t.exec_warps, threads = 32 * warps;
     const int cap = bq::max_smem_optin();
-    auto ring_offset = [warps](int nsw) { return (64 + 8 * warps * nsw + 4 * 260 * warps + 127) / 128 * 128; };
+    auto x_offset = [warps](int nsw) { return (64 + 4 * 264 + 8 * warps * nsw + 127) / 128 * 128; };
     int nsw = t.exec_nsw ? t.exec_nsw : 4;
-    while (nsw > 2 && ring_offset(nsw) + warps * nsw * slot > cap) --nsw;
-    const int ring_off = ring_offset(nsw);
-    const size_t smem = (size_t)ring_off + (size_t)warps * nsw * slot;
+    auto total = [&](int n) { return (size_t)x_offset(n) + ((size_t)x_area * 4 + 127) / 128 * 128 + (size_t)warps * n * slot; };
+    while (nsw > 2 && total(nsw) > (size_t)cap) --nsw;
+    const int x_off = x_offset(nsw);
+    const int ring_off = x_off + (x_area * 4 + 127) / 128 * 128;
+    const size_t smem = total(nsw);
     if ((int)smem > cap) return BQ_ERR_SHAPE;
     int occ = 0;
     const int e = qtype == BQ_Q8_0 ? bq_internal_exec_occupancy_q8_0(threads, smem, &occ)
@@ -410,7 +432,9 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
     p->threads = threads;
     p->smem = smem;
     p->args.ops = reinterpret_cast<const bq::ExecOp *>(ws);
+    p->args.xs = reinterpret_cast<const bq::ExecX *>(ws + off_x);
     p->args.stages = reinterpret_cast<const bq::ExecStage *>(ws + off_st);
+    p->args.x_off = x_off;
     p->counters = reinterpret_cast<unsigned int *>(ws + off_cnt);
     p->args.counters = p->counters;
     p->args.nstages = n_stages;

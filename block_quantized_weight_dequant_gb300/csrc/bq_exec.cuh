@@ -13,10 +13,12 @@
 //    tiles (32/G rows x a chunk of units) of packed weights into them with
 //    1-D bulk copies (TMA), running ahead of its compute -- across stage
 //    boundaries too, because weights never depend on earlier stages;
-//  - only x depends on the previous stage, so a warp reads x after a
-//    grid-wide stage barrier: each CTA's thread 0 adds one release-arrival
-//    per stage and waits (bounded) for all CTAs with acquire loads; x is then
-//    read with plain coherent loads, never the read-only path;
+//  - only x depends on the previous stage, so x is read after a grid-wide
+//    stage barrier: each CTA's thread 0 adds one release-arrival per stage
+//    and waits (bounded) for all CTAs with acquire loads; the CTA then loads
+//    the stage's distinct x vectors into shared memory at once with plain
+//    coherent loads (never the read-only path), applies RMSNorm there, and
+//    every warp reads x from shared memory;
 //  - arithmetic is bq_dot.cuh's fixed tree, so every output is bit-identical
 //    to the standalone single-row kernels on the same inputs.
 // The barrier is an explicit, ordered, device-scope handoff between CTAs of a
@@ -37,32 +39,42 @@ namespace bq {
 
 struct ExecOp {
     const uint8_t *W[2];
-    const float *x;
-    const float *gamma;
     float *y;
     long long rb;
-    float eps;
     int mode, M, K, nsc, G, rpw;
     int KCU, nchunks, ntiles, row_stride, single, nmat;
     int tile_base;  // first tile of this op within its stage
+    int xoff;       // float offset of this op's (normalised) x in the stage's x area
+};
+
+// one distinct input vector of a stage, staged into shared memory after the
+// stage barrier (and RMSNorm-ed there when gamma is set)
+struct ExecX {
+    const float *x;
+    const float *gamma;
+    float eps;
+    int K, off;  // off: float offset in the x area
 };
 
 struct ExecStage {
-    int op_begin, op_end, tiles, pad;
+    int op_begin, op_end, tiles;
+    int x_begin, x_end;  // range in the ExecX table
 };
 
 struct ExecArgs {
     const ExecOp *ops;
     const ExecStage *stages;
+    const ExecX *xs;
     unsigned int *counters;  // one per stage, zero at launch
     int nstages;
     int NSW;         // ring slots per warp
     int slot_bytes;  // bytes per slot (a multiple of 128)
-    int ring_off;    // shared-memory offset of the rings (header: flag, mbarriers, scratch)
+    int x_off;       // shared-memory offset of the stage's x area
+    int ring_off;    // shared-memory offset of the rings
 };
 
-// x read with plain (coherent, L1-allowed) loads: x may have been written by
-// another CTA before the stage barrier, so the read-only path is not allowed
+// x read with plain (coherent) loads: x may have been written by another CTA
+// before the stage barrier, so the read-only path is not allowed
 __device__ __forceinline__ float4 ld_coherent4(const float *p) {
     float4 v;
     asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -70,46 +82,56 @@ __device__ __forceinline__ float4 ld_coherent4(const float *p) {
                  : "l"(p));
     return v;
 }
-__device__ __forceinline__ float ld_coherent(const float *p) {
-    float v;
-    asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
-    return v;
-}
 
-struct XCoherent {
-    const float *x;
-    __device__ __forceinline__ float4 get(int, int e) const { return ld_coherent4(x + e); }
-};
-struct XCoherentNorm {
-    const float *x;
-    const float *gamma;
-    float rs;
-    __device__ __forceinline__ float4 get(int, int e) const {
-        const float4 v = ld_coherent4(x + e);
-        const float4 g = ld_coherent4(gamma + e);
-        return make_float4(__fmul_rn(__fmul_rn(v.x, rs), g.x), __fmul_rn(__fmul_rn(v.y, rs), g.y),
-                           __fmul_rn(__fmul_rn(v.z, rs), g.z), __fmul_rn(__fmul_rn(v.w, rs), g.w));
+// Stage the x vectors of stage s into shared memory (padded layout of XSmem),
+// RMSNorm-ing those with a gain: every thread of the CTA takes part; ends with
+// the x area complete and visible to all warps.  The RMS scale uses the same
+// fixed tree as rms_scale(), so xn matches the single-op kernels bit for bit.
+__device__ __forceinline__ void exec_stage_x(const ExecArgs &a, int s, float *xa, float *red) {
+    const ExecStage st = a.stages[s];
+    const int nthr = blockDim.x;
+    auto sync = [nthr]() { named_bar_sync(1, nthr); };
+    bool any_norm = false;
+    for (int j = st.x_begin; j < st.x_end; ++j) {
+        const ExecX xd = a.xs[j];
+        for (int e = 4 * threadIdx.x; e < xd.K; e += 4 * nthr)
+            *reinterpret_cast<float4 *>(xa + xd.off + e + ((e >> 8) << 2)) = ld_coherent4(xd.x + e);
+        any_norm |= xd.gamma != nullptr;
     }
-};
-
-// RMSNorm scale computed by one warp with the same fixed tree as rms_scale()
-__device__ __forceinline__ float rms_scale_warp(const float *x, int K, float eps, float *red, int lane) {
-    for (int v = lane; v < 256; v += 32) {
-        float s = 0.0f;
-        for (int k = v; k < K; k += 256) {
-            const float xv = ld_coherent(x + k);
-            s = __fmaf_rn(xv, xv, s);
+    sync();
+    if (!any_norm) return;
+    for (int j = st.x_begin; j < st.x_end; ++j) {
+        const ExecX xd = a.xs[j];
+        if (!xd.gamma) continue;
+        float *xv = xa + xd.off;
+        for (int v = threadIdx.x; v < 256; v += nthr) {
+            float acc = 0.0f;
+            for (int k = v; k < xd.K; k += 256) {
+                const float t = xv[k + ((k >> 8) << 2)];
+                acc = __fmaf_rn(t, t, acc);
+            }
+            red[v] = acc;
         }
-        red[v] = s;
+        sync();
+        if (threadIdx.x < 32) {
+            const float *q = red + 8 * threadIdx.x;
+            float v = __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
+                                __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
+            for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (threadIdx.x == 0) red[256] = v;
+        }
+        sync();
+        const float ms = __fdiv_rn(red[256], (float)xd.K);
+        const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, xd.eps)));
+        for (int e = 4 * threadIdx.x; e < xd.K; e += 4 * nthr) {
+            float4 *p = reinterpret_cast<float4 *>(xv + e + ((e >> 8) << 2));
+            const float4 v = *p;
+            const float4 g = __ldg(reinterpret_cast<const float4 *>(xd.gamma + e));
+            *p = make_float4(__fmul_rn(__fmul_rn(v.x, rs), g.x), __fmul_rn(__fmul_rn(v.y, rs), g.y),
+                             __fmul_rn(__fmul_rn(v.z, rs), g.z), __fmul_rn(__fmul_rn(v.w, rs), g.w));
+        }
+        sync();  // also protects red[] before the next gain's reduction
     }
-    __syncwarp();
-    const float *q = red + 8 * lane;
-    float v = __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
-                        __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
-    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-    __syncwarp();
-    const float ms = __fdiv_rn(v, (float)K);
-    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
 }
 
 // position of a warp in the item sequence: stage, tile index in the stage
@@ -194,11 +216,11 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
     const int nwarps = nw * gridDim.x;
     const int gw = warp * gridDim.x + blockIdx.x;  // warp-major: consecutive tiles on different SMs
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem);
-    uint64_t *fulls = reinterpret_cast<uint64_t *>(smem + 64);                 // nw * NSW
-    float *red = reinterpret_cast<float *>(smem + 64 + 8 * nw * a.NSW);       // nw * 260
+    float *red = reinterpret_cast<float *>(smem + 64);                         // 260 floats
+    uint64_t *fulls = reinterpret_cast<uint64_t *>(smem + 64 + 4 * 264);      // nw * NSW
+    float *xa = reinterpret_cast<float *>(smem + a.x_off);
     uint8_t *ring = smem + a.ring_off + (size_t)warp * a.NSW * a.slot_bytes;
     uint64_t *full = fulls + warp * a.NSW;
-    float *wred = red + warp * 260;
 
     if (threadIdx.x == 0) *abort_flag = 0;
     if (lane == 0)
@@ -252,11 +274,12 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
             named_bar_sync(1, blockDim.x);
         }
         if (*abort_flag) continue;  // keep every barrier's arrival, skip the work
+        exec_stage_x(a, s, xa, red);
 
         ExecItem it;
         exec_first_in_stage(a, it, s, gw);
         if (it.op < 0) continue;
-        float p0 = -0.0f, p1 = -0.0f, rs = 1.0f;
+        float p0 = -0.0f, p1 = -0.0f;
         for (;;) {
             const ExecOp &op = a.ops[it.op];
             const int slot = consumed % a.NSW;
@@ -275,13 +298,12 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
             const int rows = min(op.rpw, op.M - row0);
             const int u0 = it.chunk * op.KCU;
             const int cnt = min(op.KCU, op.nsc - u0);
-            const bool norm = op.mode == MODE_GATE_UP && op.gamma != nullptr;
             if (it.mat == 0 && it.chunk == 0) {
                 p0 = -0.0f;
                 p1 = -0.0f;
-                if (norm) rs = rms_scale_warp(op.x, op.K, op.eps, wred, lane);
             }
             const uint8_t *st = ring + (size_t)slot * a.slot_bytes + rho * op.row_stride;
+            const XSmem xs{xa + op.xoff, 0};
             float acc = it.mat == 0 ? p0 : p1;
             if (rho < rows) {
                 for (int ul = l; ul < cnt; ul += G) {
@@ -289,10 +311,7 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
                     load_unit_smem<QT>(w, st + ul * UB);
                     const uint32_t *const ws[1] = {w};
                     float cc[1][1];
-                    if (norm)
-                        unit_dot<QT, 1, 1>(ws, 8, XCoherentNorm{op.x, op.gamma, rs}, (u0 + ul) * 256, cc);
-                    else
-                        unit_dot<QT, 1, 1>(ws, 8, XCoherent{op.x}, (u0 + ul) * 256, cc);
+                    unit_dot<QT, 1, 1>(ws, 8, xs, (u0 + ul) * 256, cc);
                     acc = __fadd_rn(acc, cc[0][0]);
                 }
             }

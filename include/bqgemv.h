@@ -179,7 +179,11 @@ typedef struct {
 typedef struct bq_stream_plan bq_stream_plan;
 
 /* Device workspace a plan of n_ops ops in n_stages stages needs (descriptor
- * table and one barrier counter per stage); -1 for bad counts. */
+ * tables and one barrier counter per stage); -1 for bad counts.  Besides the
+ * shape rules of bq_op, the distinct inputs of one stage (ops sharing an x and
+ * its norm count once) must fit the executor's shared-memory x area together
+ * with two ring slots per warp: about 150 KB of fp32 x per stage;
+ * bq_stream_plan_create returns BQ_ERR_SHAPE otherwise. */
 int64_t bq_stream_workspace_bytes(int n_ops, int n_stages);
 
 /* Validate the ops (all of one qtype), plan their launch geometry and upload
