@@ -185,6 +185,112 @@ int padded_stride(int bytes, int G) {
     return s16 * 16;
 }
 
+bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, ExecX *ex,
+                           ExecStage *es, ExecGeometry *geo) {
+    const Tunables &t = tunables();
+    const int bb = block_bytes(qtype), ub = 8 * bb;
+    if (bb < 0) return BQ_ERR_QTYPE;
+    // a slot holds at least one warp tile of one unit per lane (32 units; the
+    // row stride of KCU = G units needs no bank padding, as 17 and 9 are 1 mod 8)
+    const int slot = (std::max(t.exec_slot, 32 * ub) + 127) / 128 * 128;
+    int n_stages = 0, n_x = 0;
+    int x_area = 0, stage_x = 0;  // floats: largest stage, current stage
+    for (int i = 0; i < n_ops; ++i) {
+        const bq_op &o = ops[i];
+        if (o.kind != BQ_OP_GEMV && o.kind != BQ_OP_GATE_UP_SILU) return BQ_ERR_SHAPE;
+        if (i == 0 ? o.stage != 0 : (o.stage != ops[i - 1].stage && o.stage != ops[i - 1].stage + 1))
+            return BQ_ERR_SHAPE;
+        if (o.M < 1 || o.M > M_MAX || o.K < 256 || o.K > K_MAX || o.K % 256) return BQ_ERR_SHAPE;
+        const bool gu = o.kind == BQ_OP_GATE_UP_SILU;
+        if (!o.W || !o.x || !o.y || (gu && !o.W_up)) return BQ_ERR_NULL;
+        auto al = [](const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+        if (!al(o.W, 16) || !al(o.x, 16) || !al(o.y, 4) || (gu && !al(o.W_up, 16)) ||
+            (gu && o.gamma && !al(o.gamma, 16)))
+            return BQ_ERR_ALIGN;
+        if (gu && o.gamma && !(std::isfinite(o.eps) && o.eps >= 0.0f)) return BQ_ERR_SHAPE;
+        ExecOp &e = eo[i];
+        e.W[0] = static_cast<const uint8_t *>(o.W);
+        e.W[1] = gu ? static_cast<const uint8_t *>(o.W_up) : nullptr;
+        e.y = o.y;
+        e.mode = gu ? MODE_GATE_UP : MODE_PLAIN;
+        e.nmat = gu ? 2 : 1;
+        e.M = (int)o.M;
+        e.K = (int)o.K;
+        e.nsc = (int)(o.K / 256);
+        e.G = tree_lanes_for_units(e.nsc);
+        e.rpw = 32 / e.G;
+        e.rb = (long long)e.nsc * ub;
+        // whole rows per slot when they fit, else chunks of a multiple of G units
+        int KCU = e.nsc, stride = 0, single = 0;
+        if ((long long)e.rpw * e.rb <= slot) {
+            single = e.G >= 8 || (e.rb / 16) % 8 == e.G % 8;
+            stride = single ? (int)e.rb : padded_stride((int)e.rb, e.G);
+            if ((long long)e.rpw * stride > slot) single = 0, stride = 0;
+        }
+        if (!stride) {
+            single = 0;
+            for (int m = (e.nsc + e.G - 1) / e.G; m >= 1; --m) {
+                KCU = std::min(e.nsc, e.G * m);
+                stride = padded_stride(KCU * ub, e.G);
+                if ((long long)e.rpw * stride <= slot) break;
+            }
+        }
+        e.KCU = KCU;
+        e.row_stride = stride;
+        e.single = single;
+        e.nchunks = (e.nsc + KCU - 1) / KCU;
+        e.ntiles = (e.M + e.rpw - 1) / e.rpw;
+        if (i == 0 || o.stage != ops[i - 1].stage) {
+            es[n_stages++] = ExecStage{i, i + 1, 0, n_x, n_x};
+            stage_x = 0;
+        }
+        ExecStage &st = es[n_stages - 1];
+        st.op_end = i + 1;
+        e.tile_base = st.tiles;
+        st.tiles += e.ntiles;
+        // the stage's distinct inputs: ops sharing x (and its norm) share one copy
+        const float *g = gu ? o.gamma : nullptr;
+        const float eps = g ? o.eps : 0.0f;
+        int found = -1;
+        for (int j = st.x_begin; j < st.x_end; ++j)
+            if (ex[j].x == o.x && ex[j].gamma == g && ex[j].eps == eps && ex[j].K == e.K) found = j;
+        if (found < 0) {
+            ex[n_x] = ExecX{o.x, g, eps, e.K, stage_x};
+            stage_x += x_padded_floats(e.K);
+            found = n_x++;
+            st.x_end = n_x;
+        }
+        e.xoff = ex[found].off;
+        x_area = std::max(x_area, stage_x);
+    }
+    // shared memory: flag + reduction scratch + mbarriers | stage x area | rings
+    // (as many slots per warp as fit, 2..4; one CTA per SM)
+    const int warps = t.exec_warps, threads = 32 * warps;
+    const int cap = max_smem_optin();
+    auto x_offset = [warps](int nsw) { return (64 + 4 * 264 + 8 * warps * nsw + 127) / 128 * 128; };
+    int nsw = t.exec_nsw ? t.exec_nsw : 4;
+    auto total = [&](int n) {
+        return (size_t)x_offset(n) + ((size_t)x_area * 4 + 127) / 128 * 128 + (size_t)warps * n * slot;
+    };
+    while (nsw > 2 && total(nsw) > (size_t)cap) --nsw;
+    const size_t smem = total(nsw);
+    if ((int)smem > cap) return BQ_ERR_SHAPE;
+    int occ = 0;
+    const int err = qtype == BQ_Q8_0 ? bq_internal_exec_occupancy_q8_0(threads, smem, &occ)
+                                     : bq_internal_exec_occupancy_q4_0(threads, smem, &occ);
+    if (err != 0 || occ < 1) return BQ_ERR_CUDA;
+    geo->n_stages = n_stages;
+    geo->n_x = n_x;
+    geo->slot = slot;
+    geo->nsw = nsw;
+    geo->x_off = x_offset(nsw);
+    geo->ring_off = geo->x_off + (x_area * 4 + 127) / 128 * 128;
+    geo->threads = threads;
+    geo->smem = smem;
+    geo->grid = num_sms_current() * occ;
+    return BQ_OK;
+}
+
 }  // namespace bq
 
 // the opaque plan handle of include/bqgemv.h
@@ -317,130 +423,45 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
     if (!ops || !workspace) return BQ_ERR_NULL;
     if (n_ops < 1) return BQ_ERR_SHAPE;
     if (!aligned_ok(workspace, 256)) return BQ_ERR_ALIGN;
-    const bq::Tunables &t = bq::tunables();
-    const int bb = bq::block_bytes(qtype), ub = 8 * bb;
-    // a slot holds at least one warp tile of one unit per lane (32 units; the
-    // row stride of KCU = G units needs no bank padding, as 17 and 9 are 1 mod 8)
-    const int slot = (std::max(t.exec_slot, 32 * ub) + 127) / 128 * 128;
     std::vector<bq::ExecOp> eo((size_t)n_ops);
-    std::vector<bq::ExecStage> es;
-    std::vector<bq::ExecX> ex;
-    int x_area = 0, stage_x = 0;  // floats: largest stage, current stage
-    for (int i = 0; i < n_ops; ++i) {
-        const bq_op &o = ops[i];
-        if (o.kind != BQ_OP_GEMV && o.kind != BQ_OP_GATE_UP_SILU) return BQ_ERR_SHAPE;
-        if (i == 0 ? o.stage != 0 : (o.stage != ops[i - 1].stage && o.stage != ops[i - 1].stage + 1))
-            return BQ_ERR_SHAPE;
-        if (o.M < 1 || o.M > bq::M_MAX || o.K < 256 || o.K > bq::K_MAX || o.K % 256) return BQ_ERR_SHAPE;
-        const bool gu = o.kind == BQ_OP_GATE_UP_SILU;
-        if (!o.W || !o.x || !o.y || (gu && !o.W_up)) return BQ_ERR_NULL;
-        if (!aligned_ok(o.W, 16) || !aligned_ok(o.x, 16) || !aligned_ok(o.y, 4) ||
-            (gu && !aligned_ok(o.W_up, 16)) || (gu && o.gamma && !aligned_ok(o.gamma, 16)))
-            return BQ_ERR_ALIGN;
-        if (gu && o.gamma && !(std::isfinite(o.eps) && o.eps >= 0.0f)) return BQ_ERR_SHAPE;
-        bq::ExecOp &e = eo[(size_t)i];
-        e.W[0] = static_cast<const uint8_t *>(o.W);
-        e.W[1] = gu ? static_cast<const uint8_t *>(o.W_up) : nullptr;
-        e.y = o.y;
-        e.mode = gu ? bq::MODE_GATE_UP : bq::MODE_PLAIN;
-        e.nmat = gu ? 2 : 1;
-        e.M = (int)o.M;
-        e.K = (int)o.K;
-        e.nsc = (int)(o.K / 256);
-        e.G = bq::tree_lanes_for_units(e.nsc);
-        e.rpw = 32 / e.G;
-        e.rb = (long long)e.nsc * ub;
-        // whole rows per slot when they fit, else chunks of a multiple of G units
-        int KCU = e.nsc, stride = 0, single = 0;
-        if ((long long)e.rpw * e.rb <= slot) {
-            single = e.G >= 8 || (e.rb / 16) % 8 == e.G % 8;
-            stride = single ? (int)e.rb : bq::padded_stride((int)e.rb, e.G);
-            if ((long long)e.rpw * stride > slot) single = 0, stride = 0;
-        }
-        if (!stride) {
-            single = 0;
-            for (int m = (e.nsc + e.G - 1) / e.G; m >= 1; --m) {
-                KCU = std::min(e.nsc, e.G * m);
-                stride = bq::padded_stride(KCU * ub, e.G);
-                if ((long long)e.rpw * stride <= slot) break;
-            }
-        }
-        e.KCU = KCU;
-        e.row_stride = stride;
-        e.single = single;
-        e.nchunks = (e.nsc + KCU - 1) / KCU;
-        e.ntiles = (e.M + e.rpw - 1) / e.rpw;
-        if (i == 0 || o.stage != ops[i - 1].stage) {
-            es.push_back(bq::ExecStage{i, i + 1, 0, (int)ex.size(), (int)ex.size()});
-            stage_x = 0;
-        }
-        bq::ExecStage &st = es.back();
-        st.op_end = i + 1;
-        e.tile_base = st.tiles;
-        st.tiles += e.ntiles;
-        // the stage's distinct inputs: ops sharing x (and its norm) share one copy
-        const float *g = gu ? o.gamma : nullptr;
-        const float eps = g ? o.eps : 0.0f;
-        int found = -1;
-        for (int j = st.x_begin; j < st.x_end; ++j)
-            if (ex[j].x == o.x && ex[j].gamma == g && ex[j].eps == eps && ex[j].K == e.K) found = j;
-        if (found < 0) {
-            ex.push_back(bq::ExecX{o.x, g, eps, e.K, stage_x});
-            stage_x += bq::x_padded_floats(e.K);
-            found = st.x_end++;
-        }
-        e.xoff = ex[found].off;
-        x_area = std::max(x_area, stage_x);
-    }
-    const int n_stages = (int)es.size();
+    std::vector<bq::ExecX> ex((size_t)n_ops);
+    std::vector<bq::ExecStage> es((size_t)n_ops);
+    bq::ExecGeometry geo;
+    const bq_status st = bq::plan_exec_tables(qtype, ops, n_ops, eo.data(), ex.data(), es.data(), &geo);
+    if (st != BQ_OK) return st;
+    const int n_stages = geo.n_stages;
     const int64_t need = bq_stream_workspace_bytes(n_ops, n_stages);
     if (workspace_bytes < need) return BQ_ERR_SHAPE;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const int64_t off_x = align256((int64_t)n_ops * sizeof(bq::ExecOp));
     const int64_t off_st = off_x + align256((int64_t)n_ops * sizeof(bq::ExecX));
     const int64_t off_cnt = off_st + align256((int64_t)n_stages * sizeof(bq::ExecStage));
-    if (cudaMemcpy(ws, eo.data(), eo.size() * sizeof(bq::ExecOp), cudaMemcpyHostToDevice) !=
+    if (cudaMemcpy(ws, eo.data(), (size_t)n_ops * sizeof(bq::ExecOp), cudaMemcpyHostToDevice) !=
             cudaSuccess ||
-        cudaMemcpy(ws + off_x, ex.data(), ex.size() * sizeof(bq::ExecX), cudaMemcpyHostToDevice) !=
-            cudaSuccess ||
-        cudaMemcpy(ws + off_st, es.data(), es.size() * sizeof(bq::ExecStage),
+        cudaMemcpy(ws + off_x, ex.data(), (size_t)geo.n_x * sizeof(bq::ExecX),
+                   cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(ws + off_st, es.data(), (size_t)n_stages * sizeof(bq::ExecStage),
                    cudaMemcpyHostToDevice) != cudaSuccess)
         return BQ_ERR_CUDA;
-    // shared memory: flag + reduction scratch + mbarriers | stage x area | rings
-    // (as many slots per warp as fit, 2..4; one CTA per SM)
-    const int warps = t.exec_warps, threads = 32 * warps;
-    const int cap = bq::max_smem_optin();
-    auto x_offset = [warps](int nsw) { return (64 + 4 * 264 + 8 * warps * nsw + 127) / 128 * 128; };
-    int nsw = t.exec_nsw ? t.exec_nsw : 4;
-    auto total = [&](int n) { return (size_t)x_offset(n) + ((size_t)x_area * 4 + 127) / 128 * 128 + (size_t)warps * n * slot; };
-    while (nsw > 2 && total(nsw) > (size_t)cap) --nsw;
-    const int x_off = x_offset(nsw);
-    const int ring_off = x_off + (x_area * 4 + 127) / 128 * 128;
-    const size_t smem = total(nsw);
-    if ((int)smem > cap) return BQ_ERR_SHAPE;
-    int occ = 0;
-    const int e = qtype == BQ_Q8_0 ? bq_internal_exec_occupancy_q8_0(threads, smem, &occ)
-                                   : bq_internal_exec_occupancy_q4_0(threads, smem, &occ);
-    if (e != 0 || occ < 1) return BQ_ERR_CUDA;
     auto *p = new (std::nothrow) bq_stream_plan;
     if (!p) return BQ_ERR_CUDA;
     p->qtype = qtype;
     p->n_ops = n_ops;
     p->n_stages = n_stages;
     cudaGetDevice(&p->device);
-    p->grid = bq::num_sms_current() * occ;
-    p->threads = threads;
-    p->smem = smem;
+    p->grid = geo.grid;
+    p->threads = geo.threads;
+    p->smem = geo.smem;
     p->args.ops = reinterpret_cast<const bq::ExecOp *>(ws);
     p->args.xs = reinterpret_cast<const bq::ExecX *>(ws + off_x);
     p->args.stages = reinterpret_cast<const bq::ExecStage *>(ws + off_st);
-    p->args.x_off = x_off;
+    p->args.x_off = geo.x_off;
     p->counters = reinterpret_cast<unsigned int *>(ws + off_cnt);
     p->args.counters = p->counters;
     p->args.nstages = n_stages;
-    p->args.NSW = nsw;
-    p->args.slot_bytes = slot;
-    p->args.ring_off = ring_off;
+    p->args.NSW = geo.nsw;
+    p->args.slot_bytes = geo.slot;
+    p->args.ring_off = geo.ring_off;
     *plan = p;
     return BQ_OK;
 }

@@ -73,6 +73,12 @@ struct ExecArgs {
     int ring_off;    // shared-memory offset of the rings
 };
 
+// launch geometry of a planned executor run (host side)
+struct ExecGeometry {
+    int n_stages, n_x, slot, nsw, x_off, ring_off, threads, grid;
+    size_t smem;
+};
+
 // x read with plain (coherent) loads: x may have been written by another CTA
 // before the stage barrier, so the read-only path is not allowed
 __device__ __forceinline__ float4 ld_coherent4(const float *p) {

@@ -65,8 +65,19 @@ int bq_internal_status_q8_0(unsigned int *flags, int clear);
 int bq_internal_status_q4_0(unsigned int *flags, int clear);
 int bq_internal_pack(int qtype, const float *W, long long M, long long K, void *Wq, void *stream);
 
+#include "../../include/bqgemv.h"
+
 namespace bq {
 struct ExecArgs;
+struct ExecOp;
+struct ExecX;
+struct ExecStage;
+struct ExecGeometry;
+// Validate a stream executor op list and plan it into caller-provided tables
+// (each with room for n_ops entries) and a launch geometry for the current
+// device.  Touches no device memory.
+bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, ExecX *ex,
+                           ExecStage *es, ExecGeometry *geo);
 }
 // persistent per-token stream executor (bq_exec.cuh), one instantiation per format
 int bq_internal_exec_occupancy_q8_0(int threads, size_t smem, int *occ);

@@ -1,0 +1,99 @@
+// bq_noalloc.cu -- the per-token stream executor for callers that cannot
+// allocate device memory (bq_stream_run_noalloc in include/bqgemv.h).
+//
+// The regular executor keeps its descriptor tables and stage-barrier counters
+// in a workspace the caller allocates.  This entry point keeps them instead in
+// one file-scope device array of fixed size, which every GPU that loads the
+// library holds until the process exits.  Nothing is allocated per call: the
+// host side plans into static arrays, copies the tables into the device array
+// on the caller's stream, clears the counters, and launches the same kernel
+// the workspace path launches.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "bq_exec.cuh"
+#include "bq_internal.h"
+
+namespace {
+
+constexpr size_t al256(size_t v) { return (v + 255) / 256 * 256; }
+
+constexpr int MAX_OPS = BQ_NOALLOC_MAX_OPS;  // also the most stages and inputs
+constexpr size_t OFF_X = al256((size_t)MAX_OPS * sizeof(bq::ExecOp));
+constexpr size_t OFF_ST = OFF_X + al256((size_t)MAX_OPS * sizeof(bq::ExecX));
+constexpr size_t OFF_CNT = OFF_ST + al256((size_t)MAX_OPS * sizeof(bq::ExecStage));
+constexpr size_t SCRATCH_BYTES = OFF_CNT + al256((size_t)MAX_OPS * sizeof(unsigned int));
+
+// The scratch: descriptor tables, then one barrier counter per stage.  In host
+// code this name is only a stand-in for the symbol; the kernel gets the
+// device address fetched by scratch_address().
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SCRATCH_BYTES];
+
+std::atomic<unsigned char *> g_scratch_addr[64];
+
+// Device address of the scratch on the current device, looked up on the
+// device's first call (that first call must come before any stream capture).
+cudaError_t scratch_address(unsigned char **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    unsigned char *p = g_scratch_addr[dev].load();
+    if (!p) {
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev].store(p);
+    }
+    *out = p;
+    return cudaSuccess;
+}
+
+// host staging for the tables: static storage, one call at a time
+std::mutex g_host_mutex;
+bq::ExecOp g_eo[MAX_OPS];
+bq::ExecX g_ex[MAX_OPS];
+bq::ExecStage g_es[MAX_OPS];
+
+}  // namespace
+
+extern "C" bq_status bq_stream_run_noalloc(int qtype, const bq_op *ops, int n_ops, void *stream) {
+    if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0) return BQ_ERR_QTYPE;
+    if (!ops) return BQ_ERR_NULL;
+    if (n_ops < 1 || n_ops > MAX_OPS) return BQ_ERR_SHAPE;
+    unsigned char *scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess) return BQ_ERR_CUDA;
+    auto s = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_host_mutex);
+    bq::ExecGeometry geo;
+    const bq_status st = bq::plan_exec_tables(qtype, ops, n_ops, g_eo, g_ex, g_es, &geo);
+    if (st != BQ_OK) return st;
+    // the copies read the host tables before returning (pageable source), so
+    // the static arrays are free again once the lock is released
+    if (cudaMemcpyAsync(scratch, g_eo, (size_t)n_ops * sizeof(bq::ExecOp), cudaMemcpyHostToDevice,
+                        s) != cudaSuccess ||
+        cudaMemcpyAsync(scratch + OFF_X, g_ex, (size_t)geo.n_x * sizeof(bq::ExecX),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(scratch + OFF_ST, g_es, (size_t)geo.n_stages * sizeof(bq::ExecStage),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return BQ_ERR_CUDA;
+    // the counters keep the previous call's values: clear them
+    if (cudaMemsetAsync(scratch + OFF_CNT, 0, (size_t)geo.n_stages * sizeof(unsigned int), s) !=
+        cudaSuccess)
+        return BQ_ERR_CUDA;
+    bq::ExecArgs a;
+    a.ops = reinterpret_cast<const bq::ExecOp *>(scratch);
+    a.xs = reinterpret_cast<const bq::ExecX *>(scratch + OFF_X);
+    a.stages = reinterpret_cast<const bq::ExecStage *>(scratch + OFF_ST);
+    a.counters = reinterpret_cast<unsigned int *>(scratch + OFF_CNT);
+    a.nstages = geo.n_stages;
+    a.NSW = geo.nsw;
+    a.slot_bytes = geo.slot;
+    a.x_off = geo.x_off;
+    a.ring_off = geo.ring_off;
+    const int e = qtype == BQ_Q8_0
+                      ? bq_internal_exec_launch_q8_0(a, geo.grid, geo.threads, geo.smem, stream)
+                      : bq_internal_exec_launch_q4_0(a, geo.grid, geo.threads, geo.smem, stream);
+    return e == 0 ? BQ_OK : BQ_ERR_CUDA;
+}

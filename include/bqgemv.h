@@ -205,6 +205,37 @@ bq_status bq_stream_plan_launch(const bq_stream_plan *plan, void *stream);
 /* Free the host object (the workspace stays the caller's). */
 bq_status bq_stream_plan_destroy(bq_stream_plan *plan);
 
+/* Allocation-free run of the stream executor.  (The pages have no
+ * counterpart: this entry point exists for callers of this library, not for
+ * the method.)
+ *
+ * Some callers cannot allocate device memory for the workspace above: a
+ * serving process that has already handed all free HBM to its weight and
+ * KV-cache pools, where a new cudaMalloc fails or fragments them; a host
+ * framework that owns device memory through its own caching allocator and
+ * forbids raw cudaMalloc beside it; or a latency-critical path that cannot
+ * afford cudaMalloc/cudaFree, which can synchronise the device.  For them
+ * this call runs the same ops as bq_stream_plan_create + bq_stream_plan_launch
+ * (same validation, same kernel, bit-identical outputs) with the descriptor
+ * tables and stage counters kept in one fixed device array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits (72 KiB).  The caller still passes the inputs and outputs (in
+ * the ops).  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *  - At most BQ_NOALLOC_MAX_OPS ops (and as many stages); more returns
+ *    BQ_ERR_SHAPE without touching the device.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make
+ *    that first call before any stream capture.
+ *  - Each call copies the tables from host memory into the array on `stream`
+ *    and clears the counters there, then launches.  All calls share the one
+ *    array, which keeps the last call's contents: calls that overlap on the
+ *    GPU (on different streams, or from different host threads without
+ *    ordering) race on it and must be serialised by the caller.  Host-side
+ *    staging is serialised internally. */
+#define BQ_NOALLOC_MAX_OPS 512
+bq_status bq_stream_run_noalloc(int qtype, const bq_op *ops, int n_ops, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

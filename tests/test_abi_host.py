@@ -130,3 +130,12 @@ def test_python_binding_refuses_cpu_tensors():
         bq.quantize_pack(W, "q8_0")
     with pytest.raises(TypeError):
         bq.gemv_q8_0(torch.zeros(4, 68, dtype=torch.int8), torch.zeros(64))
+
+
+def test_noalloc_entry_rejects_before_touching_the_device(lib):
+    ops = (_lib.BqOp * 2)()
+    assert lib.bq_stream_run_noalloc(bq.Q8_0, ops, 0, None) == _lib.BQ_ERR_SHAPE
+    assert lib.bq_stream_run_noalloc(bq.Q8_0, None, 1, None) == _lib.BQ_ERR_NULL
+    assert lib.bq_stream_run_noalloc(3, ops, 1, None) == _lib.BQ_ERR_QTYPE
+    big = (_lib.BqOp * (_lib.BQ_NOALLOC_MAX_OPS + 1))()
+    assert lib.bq_stream_run_noalloc(bq.Q4_0, big, len(big), None) == _lib.BQ_ERR_SHAPE
