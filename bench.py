@@ -143,10 +143,13 @@ def _packed(bq, wl, qt, M, K, seed, tag, dev):
     return P
 
 
-def build_token_stream(cfg, dev, seed=0, mode="plan"):
-    """One decode step's GEMV stream (block_quantized_weight_dequant_gb300.decode):
-    every stage reads the previous stage's output.  mode "plan": one
-    cooperative launch per step; mode "per_op": one launch per op."""
+def build_token_stream(cfg, dev, seed=0, mode="plan", chained=True):
+    """One decode step's GEMV stream (block_quantized_weight_dequant_gb300.decode).
+    chained: every stage reads the previous stage's output (113 dependent
+    stages, grid-wide barriers); unchained: every op reads its own input (the
+    pure weight stream).  mode "plan": one cooperative launch per step; mode
+    "per_op": one launch per op."""
+    import torch
     import block_quantized_weight_dequant_gb300 as bq
     from block_quantized_weight_dequant_gb300 import workloads as wl
     from block_quantized_weight_dequant_gb300.decode import DecodeStream
@@ -163,9 +166,9 @@ def build_token_stream(cfg, dev, seed=0, mode="plan"):
         layers.append(L)
     M, K = cfg["lm_head"]
     lm = _packed(bq, wl, qt, M, K, seed, (cfg["name"], "lm_head"), dev)
-    ds = DecodeStream(qt, layers, lm)
-    ds.x0.copy_(wl.normal_torch(cfg["hidden"], 1.0, seed=seed, stream=wl.stream_id("x0"),
-                                device=dev))
+    ds = DecodeStream(qt, layers, lm, chained=chained)
+    ds.inputs.copy_(wl.normal_torch(ds.inputs.numel(), 1.0, seed=seed, stream=wl.stream_id("x0"),
+                                    device=dev))
     w = Workload()
     nbytes = ds.weight_bytes() + ds.activation_bytes()
     if mode == "plan":
@@ -180,11 +183,14 @@ def build_token_stream(cfg, dev, seed=0, mode="plan"):
             else:
                 w.add(lambda op=op: bq.gemv_gate_up_silu(qt, op.W, op.W_up, op.x, op.gamma,
                                                          op.eps, op.y), f"gate_up_silu_{qt}", nb)
-    w.x_dev, w.y_dev = ds.x0, ds.logits
+    w.x_dev = ds.inputs
+    w.y_dev = ds.logits if chained else torch.cat([op.y for op in ds.ops])
     w.stream_obj = ds
     w.desc = {"workload": cfg["name"], "layers": cfg["layers"], "ops_per_step": len(ds.ops),
               "stages_per_step": ds.n_stages, "weight_bytes_per_step": ds.weight_bytes(),
-              "weight_format": qt, "launch": mode}
+              "weight_format": qt, "launch": mode,
+              "inputs": "chained (each stage reads the previous stage's output)" if chained
+              else "independent (each op reads its own input)"}
     return w
 
 
@@ -251,10 +257,11 @@ def build_verify(dev, cfg, R, copies=7, seed=0):
 
 def build_workload(args, dev):
     from block_quantized_weight_dequant_gb300 import workloads as wl
+    chained = args.inputs == "chained"
     if args.config == "cfg2":
-        return build_token_stream(wl.QWEN3_0_6B, dev, mode=args.launch)
+        return build_token_stream(wl.QWEN3_0_6B, dev, mode=args.launch, chained=chained)
     if args.config == "cfg3":
-        return build_token_stream(wl.Q7B, dev, mode=args.launch)
+        return build_token_stream(wl.Q7B, dev, mode=args.launch, chained=chained)
     if args.config == "cfg1":
         c = wl.CFG1
         return build_rotated_gemv(dev, c["qtype"], c["M"], c["K"], copies=96)
@@ -393,6 +400,8 @@ def main():
                     help="seconds of oracle work for cpu_baseline (0 disables)")
     ap.add_argument("--launch", choices=["plan", "per_op"], default="plan",
                     help="cfg2/cfg3: one cooperative launch per token, or one launch per op")
+    ap.add_argument("--inputs", choices=["chained", "independent"], default="chained",
+                    help="cfg2/cfg3: stages read the previous stage's output, or own inputs")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -37,6 +37,8 @@ struct Tunables {
     int exec_slot = 0;     // stream executor: bytes per ring slot (0 = one warp tile of 32 units)
     int exec_nsw = 0;      // stream executor: slots per warp (0 = as many as fit, <= 4)
     int exec_warps = 8;    // stream executor: warps per CTA
+    int exec_rowmode_rows = 0;  // stream executor: row mode up to this many rows per warp (0: off)
+    int exec_prefetch = 0;      // stream executor: L2 prefetch distance beyond the ring, in items (measured: no gain)
 };
 
 const Tunables &tunables() {
@@ -61,6 +63,8 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "slot") && val >= 4096) v.exec_slot = val;
             else if (!std::strcmp(tok, "nsw") && val >= 2 && val <= 8) v.exec_nsw = val;
             else if (!std::strcmp(tok, "ewarps") && val >= 1 && val <= 8) v.exec_warps = val;
+            else if (!std::strcmp(tok, "rowmode") && val >= 0 && val <= 32) v.exec_rowmode_rows = val;
+            else if (!std::strcmp(tok, "pf") && val >= 0 && val <= 16) v.exec_prefetch = val;
         }
         return v;
     }();
@@ -185,6 +189,17 @@ int padded_stride(int bytes, int G) {
     return s16 * 16;
 }
 
+namespace {
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+Range range(const void *p, int64_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + (uintptr_t)bytes};
+}
+}  // namespace
+
 bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, ExecX *ex,
                            ExecStage *es, ExecGeometry *geo) {
     const Tunables &t = tunables();
@@ -193,6 +208,7 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
     // a slot holds at least one warp tile of one unit per lane (32 units; the
     // row stride of KCU = G units needs no bank padding, as 17 and 9 are 1 mod 8)
     const int slot = (std::max(t.exec_slot, 32 * ub) + 127) / 128 * 128;
+    // ---- pass 1: validate; stages and their distinct inputs ----
     int n_stages = 0, n_x = 0;
     int x_area = 0, stage_x = 0;  // floats: largest stage, current stage
     for (int i = 0; i < n_ops; ++i) {
@@ -209,86 +225,196 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
             return BQ_ERR_ALIGN;
         if (gu && o.gamma && !(std::isfinite(o.eps) && o.eps >= 0.0f)) return BQ_ERR_SHAPE;
         ExecOp &e = eo[i];
+        std::memset(&e, 0, sizeof e);
         e.W[0] = static_cast<const uint8_t *>(o.W);
         e.W[1] = gu ? static_cast<const uint8_t *>(o.W_up) : nullptr;
         e.y = o.y;
-        e.mode = gu ? MODE_GATE_UP : MODE_PLAIN;
         e.nmat = gu ? 2 : 1;
         e.M = (int)o.M;
-        e.K = (int)o.K;
         e.nsc = (int)(o.K / 256);
-        e.G = tree_lanes_for_units(e.nsc);
-        e.rpw = 32 / e.G;
-        e.rb = (long long)e.nsc * ub;
-        // whole rows per slot when they fit, else chunks of a multiple of G units
-        int KCU = e.nsc, stride = 0, single = 0;
-        if ((long long)e.rpw * e.rb <= slot) {
-            single = e.G >= 8 || (e.rb / 16) % 8 == e.G % 8;
-            stride = single ? (int)e.rb : padded_stride((int)e.rb, e.G);
-            if ((long long)e.rpw * stride > slot) single = 0, stride = 0;
-        }
-        if (!stride) {
-            single = 0;
-            for (int m = (e.nsc + e.G - 1) / e.G; m >= 1; --m) {
-                KCU = std::min(e.nsc, e.G * m);
-                stride = padded_stride(KCU * ub, e.G);
-                if ((long long)e.rpw * stride <= slot) break;
-            }
-        }
-        e.KCU = KCU;
-        e.row_stride = stride;
-        e.single = single;
-        e.nchunks = (e.nsc + KCU - 1) / KCU;
-        e.ntiles = (e.M + e.rpw - 1) / e.rpw;
+        e.G = (unsigned char)tree_lanes_for_units(e.nsc);
+        e.rb = e.nsc * ub;
         if (i == 0 || o.stage != ops[i - 1].stage) {
-            es[n_stages++] = ExecStage{i, i + 1, 0, n_x, n_x};
+            es[n_stages++] = ExecStage{i, i + 1, 0, n_x, n_x, 0, 0, 0};
             stage_x = 0;
         }
         ExecStage &st = es[n_stages - 1];
         st.op_end = i + 1;
-        e.tile_base = st.tiles;
-        st.tiles += e.ntiles;
         // the stage's distinct inputs: ops sharing x (and its norm) share one copy
         const float *g = gu ? o.gamma : nullptr;
         const float eps = g ? o.eps : 0.0f;
+        const int K = (int)o.K;
         int found = -1;
         for (int j = st.x_begin; j < st.x_end; ++j)
-            if (ex[j].x == o.x && ex[j].gamma == g && ex[j].eps == eps && ex[j].K == e.K) found = j;
+            if (ex[j].x == o.x && ex[j].gamma == g && ex[j].eps == eps && ex[j].K == K) found = j;
         if (found < 0) {
-            ex[n_x] = ExecX{o.x, g, eps, e.K, stage_x};
-            stage_x += x_padded_floats(e.K);
+            ex[n_x] = ExecX{o.x, g, eps, K, stage_x, 0};
+            stage_x += x_padded_floats(K);
             found = n_x++;
             st.x_end = n_x;
         }
         e.xoff = ex[found].off;
         x_area = std::max(x_area, stage_x);
     }
-    // shared memory: flag + reduction scratch + mbarriers | stage x area | rings
-    // (as many slots per warp as fit, 2..4; one CTA per SM)
+    // ---- memory dependences between ops, from their address ranges ----
+    // Weights are streamed ahead across stages, so no output may overlap any
+    // weights; within a stage no output may overlap an input or another
+    // output.  A stage that reads an earlier stage's output, or writes what an
+    // earlier stage reads or writes, waits at a grid-wide barrier.
+    auto in_ranges = [&](int i, Range *r) {
+        const bq_op &o = ops[i];
+        int n = 0;
+        r[n++] = range(o.x, 4 * o.K);
+        if (o.kind == BQ_OP_GATE_UP_SILU && o.gamma) r[n++] = range(o.gamma, 4 * o.K);
+        return n;
+    };
+    auto w_ranges = [&](int i, Range *r) {
+        const bq_op &o = ops[i];
+        int n = 0;
+        r[n++] = range(o.W, (int64_t)o.M * eo[i].rb);
+        if (o.kind == BQ_OP_GATE_UP_SILU) r[n++] = range(o.W_up, (int64_t)o.M * eo[i].rb);
+        return n;
+    };
+    for (int i = 0; i < n_ops; ++i) {
+        const Range yi = range(ops[i].y, 4 * ops[i].M);
+        Range r[2];
+        for (int j = 0; j < n_ops; ++j) {
+            const int nw = w_ranges(j, r);
+            for (int k = 0; k < nw; ++k)
+                if (overlap(yi, r[k])) return BQ_ERR_SHAPE;
+        }
+    }
+    for (int s = 0; s < n_stages; ++s) {
+        const ExecStage &st = es[s];
+        for (int i = st.op_begin; i < st.op_end; ++i) {
+            const Range yi = range(ops[i].y, 4 * ops[i].M);
+            Range ri[2];
+            const int ni = in_ranges(i, ri);
+            for (int j = 0; j < st.op_end; ++j) {
+                const Range yj = range(ops[j].y, 4 * ops[j].M);
+                Range rj[2];
+                const int nj = in_ranges(j, rj);
+                bool hit = false;
+                for (int k = 0; k < nj; ++k) hit |= overlap(yi, rj[k]);
+                if (j != i) hit |= overlap(yi, yj);
+                for (int k = 0; k < ni; ++k) hit |= overlap(ri[k], yj);
+                if (!hit) continue;
+                if (j >= st.op_begin) return BQ_ERR_SHAPE;  // within one stage
+                es[s].barrier = 1;
+            }
+        }
+    }
+    // ---- launch geometry ----
+    // shared memory: control block + weight-slot mbarriers + x mbarriers |
+    // descriptor tables | x buffers | weight rings (+ slack for realigned block
+    // loads past the last slot).  Grow the x ring to 4 buffers first (stages
+    // run ahead of each other), then the weight rings to 4 slots per warp,
+    // then the x ring up to its maximum.
     const int warps = t.exec_warps, threads = 32 * warps;
     const int cap = max_smem_optin();
-    auto x_offset = [warps](int nsw) { return (64 + 4 * 264 + 8 * warps * nsw + 127) / 128 * 128; };
-    int nsw = t.exec_nsw ? t.exec_nsw : 4;
-    auto total = [&](int n) {
-        return (size_t)x_offset(n) + ((size_t)x_area * 4 + 127) / 128 * 128 + (size_t)warps * n * slot;
+    const int tab_bytes = exec_table_bytes(n_ops, n_x, n_stages);
+    const int x_bytes = (x_area * 4 + 127) / 128 * 128;
+    auto xbar_offset = [warps](int nsw) { return 256 + 8 * warps * nsw; };
+    auto tab_offset = [&](int nsw, int xb) { return (xbar_offset(nsw) + 16 * xb + 127) / 128 * 128; };
+    auto total = [&](int nsw, int xb) {
+        return (size_t)tab_offset(nsw, xb) + tab_bytes + (size_t)xb * x_bytes +
+               (size_t)warps * nsw * slot + 128;
     };
-    while (nsw > 2 && total(nsw) > (size_t)cap) --nsw;
-    const size_t smem = total(nsw);
-    if ((int)smem > cap) return BQ_ERR_SHAPE;
+    int nsw = t.exec_nsw ? t.exec_nsw : 2, xbuf = 1;
+    if (total(nsw, xbuf) > (size_t)cap) return BQ_ERR_SHAPE;
+    while (xbuf < 4 && total(nsw, xbuf + 1) <= (size_t)cap) ++xbuf;
+    while (!t.exec_nsw && nsw < 4 && total(nsw + 1, xbuf) <= (size_t)cap) ++nsw;
+    while (xbuf < EXEC_MAX_XBUF && total(nsw, xbuf + 1) <= (size_t)cap) ++xbuf;
+    const size_t smem = total(nsw, xbuf);
     int occ = 0;
     const int err = qtype == BQ_Q8_0 ? bq_internal_exec_occupancy_q8_0(threads, smem, &occ)
                                      : bq_internal_exec_occupancy_q4_0(threads, smem, &occ);
     if (err != 0 || occ < 1) return BQ_ERR_CUDA;
+    const int grid = num_sms_current() * occ;
+    const int nwarps = grid * warps;
+    // ---- pass 2: tiling of every op, and the stage tile tables ----
+    long long tiles_before = 0;
+    for (int s = 0; s < n_stages; ++s) {
+        ExecStage &st = es[s];
+        st.tiles = 0;
+        st.tile_off = (int)(tiles_before % nwarps);
+        for (int i = st.op_begin; i < st.op_end; ++i) {
+            ExecOp &e = eo[i];
+            const int G = e.G, nsc = e.nsc, rb = e.rb;
+            const int rows_per_warp = (int)((e.M + (long long)nwarps - 1) / nwarps);
+            if (rb <= slot && rows_per_warp <= t.exec_rowmode_rows) {
+                // row mode: a few whole rows per tile, contiguous in memory
+                e.rowmode = 1;
+                e.rpw = (unsigned char)std::max(1, std::min({rows_per_warp, slot / rb, 32}));
+                e.KCU = (short)nsc;
+                e.row_stride = rb;
+                e.single = 1;
+            } else {
+                // tile mode: 32/G rows, whole rows per slot when they fit, else
+                // chunks of a multiple of G units
+                const int rpw = 32 / G;
+                int KCU = nsc, stride = 0, single = 0;
+                if ((long long)rpw * rb <= slot) {
+                    single = G >= 8 || (rb / 16) % 8 == G % 8;
+                    stride = single ? rb : padded_stride(rb, G);
+                    if ((long long)rpw * stride > slot) single = 0, stride = 0;
+                }
+                if (!stride) {
+                    single = 0;
+                    for (int m = (nsc + G - 1) / G; m >= 1; --m) {
+                        KCU = std::min(nsc, G * m);
+                        stride = padded_stride(KCU * ub, G);
+                        if ((long long)rpw * stride <= slot) break;
+                    }
+                }
+                e.rowmode = 0;
+                e.rpw = (unsigned char)rpw;
+                e.KCU = (short)KCU;
+                e.row_stride = stride;
+                e.single = (unsigned char)single;
+            }
+            e.nchunks = (short)((nsc + e.KCU - 1) / e.KCU);
+            e.ntiles = (e.M + e.rpw - 1) / e.rpw;
+            e.tile_base = st.tiles;
+            st.tiles += e.ntiles;
+        }
+        tiles_before += st.tiles;
+    }
     geo->n_stages = n_stages;
     geo->n_x = n_x;
     geo->slot = slot;
     geo->nsw = nsw;
-    geo->x_off = x_offset(nsw);
-    geo->ring_off = geo->x_off + (x_area * 4 + 127) / 128 * 128;
+    geo->xbar_off = xbar_offset(nsw);
+    geo->tab_off = tab_offset(nsw, xbuf);
+    geo->x_off = geo->tab_off + tab_bytes;
+    geo->x_floats = x_bytes / 4;
+    geo->x_buffers = xbuf;
+    geo->ring_off = geo->x_off + xbuf * x_bytes;
     geo->threads = threads;
     geo->smem = smem;
-    geo->grid = num_sms_current() * occ;
+    geo->grid = grid;
+    geo->prefetch = t.exec_prefetch;
     return BQ_OK;
+}
+
+void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const ExecX *xs,
+                    const ExecStage *stages, unsigned int *counters, ExecArgs *a) {
+    a->ops = ops;
+    a->xs = xs;
+    a->stages = stages;
+    a->counters = counters;
+    a->nops = n_ops;
+    a->nxs = geo.n_x;
+    a->nstages = geo.n_stages;
+    a->NSW = geo.nsw;
+    a->slot_bytes = geo.slot;
+    a->xbar_off = geo.xbar_off;
+    a->tab_off = geo.tab_off;
+    a->x_off = geo.x_off;
+    a->x_floats = geo.x_floats;
+    a->x_buffers = geo.x_buffers;
+    a->ring_off = geo.ring_off;
+    a->prefetch = geo.prefetch;
 }
 
 }  // namespace bq
@@ -452,16 +578,10 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
     p->grid = geo.grid;
     p->threads = geo.threads;
     p->smem = geo.smem;
-    p->args.ops = reinterpret_cast<const bq::ExecOp *>(ws);
-    p->args.xs = reinterpret_cast<const bq::ExecX *>(ws + off_x);
-    p->args.stages = reinterpret_cast<const bq::ExecStage *>(ws + off_st);
-    p->args.x_off = geo.x_off;
     p->counters = reinterpret_cast<unsigned int *>(ws + off_cnt);
-    p->args.counters = p->counters;
-    p->args.nstages = n_stages;
-    p->args.NSW = geo.nsw;
-    p->args.slot_bytes = geo.slot;
-    p->args.ring_off = geo.ring_off;
+    bq::fill_exec_args(geo, n_ops, reinterpret_cast<const bq::ExecOp *>(ws),
+                       reinterpret_cast<const bq::ExecX *>(ws + off_x),
+                       reinterpret_cast<const bq::ExecStage *>(ws + off_st), p->counters, &p->args);
     *plan = p;
     return BQ_OK;
 }

@@ -45,17 +45,19 @@ template <> struct Fmt<QT_Q4_0> {
 // ---------------------------------------------------------------------------
 // exact code -> fp32 conversion
 // ---------------------------------------------------------------------------
-// Q8_0: flip the sign bit of every byte (q + 128 as an unsigned byte), place
-// that byte in the low mantissa of 2^23 and subtract 2^23 + 128.
-__device__ __forceinline__ float q8_code(uint32_t word, int pos) {
+// Q8_0: flip the sign bit of every byte (q + 128 as an unsigned byte) and
+// place that byte in the low mantissa of 2^23: the float 2^23 + q + 128, from
+// which subtracting 2^23 + 128 leaves q exactly.
+constexpr float Q8_MAGIC = 8388736.0f;  // 2^23 + 128
+__device__ __forceinline__ float q8_raw(uint32_t word, int pos) {
     const uint32_t flipped = word ^ 0x80808080u;
-    const uint32_t bits = __byte_perm(flipped, 0x4B000000u, 0x7540u | (uint32_t)pos);
-    return __fsub_rn(__uint_as_float(bits), 8388736.0f);
+    return __uint_as_float(__byte_perm(flipped, 0x4B000000u, 0x7540u | (uint32_t)pos));
 }
-// Q4_0: the nibble at bit `shift`, placed in the mantissa of 2^23, minus 2^23 + 8.
-__device__ __forceinline__ float q4_code(uint32_t word, int shift) {
-    const uint32_t bits = ((word >> shift) & 0xFu) | 0x4B000000u;
-    return __fsub_rn(__uint_as_float(bits), 8388616.0f);
+// Q4_0: the nibble at bit `shift` in the low mantissa of 2^23: the float
+// 2^23 + n, from which subtracting 2^23 + 8 leaves n - 8 exactly.
+constexpr float Q4_MAGIC = 8388616.0f;  // 2^23 + 8
+__device__ __forceinline__ float q4_raw(uint32_t word, int shift) {
+    return __uint_as_float(((word >> shift) & 0xFu) | 0x4B000000u);
 }
 
 __device__ __forceinline__ float scale_at(const uint32_t *w, int byte_off) {
@@ -66,16 +68,24 @@ __device__ __forceinline__ float scale_at(const uint32_t *w, int byte_off) {
 // ---------------------------------------------------------------------------
 // x sources: element e (a multiple of 4) of input row r, as a float4
 // ---------------------------------------------------------------------------
-// x staged in shared memory with 4 floats of padding after every 256, so that
-// lanes reading different units hit different banks
+// x staged in shared memory with its 16-byte chunks permuted within each
+// 128-byte line: chunk c (elements 4c..4c+3) sits at chunk position
+// (c & ~7) | ((c ^ c >> 3 ^ c >> 6) & 7).  With c = 64u + 8b + t (unit u,
+// block b, step t) the bank group is t ^ b ^ u (mod 8), so eight lanes that
+// read different units of one block position, or different blocks of one
+// unit, all hit different banks.
+__host__ __device__ constexpr int x_chunk_pos(int c) { return (c & ~7) | ((c ^ (c >> 3) ^ (c >> 6)) & 7); }
+// float offset of element e (any e) in the permuted layout
+__host__ __device__ constexpr int x_pos(int e) { return 4 * x_chunk_pos(e >> 2) + (e & 3); }
 struct XSmem {
     const float *base;
     int rstride;  // floats between rows
     __device__ __forceinline__ float4 get(int r, int e) const {
-        return *reinterpret_cast<const float4 *>(base + r * rstride + e + ((e >> 8) << 2));
+        return *reinterpret_cast<const float4 *>(base + r * rstride + 4 * x_chunk_pos(e >> 2));
     }
 };
-__host__ __device__ constexpr int x_padded_floats(int K) { return K + (K >> 6) + 4; }
+// floats of shared memory one staged x of K elements takes (K rounded up to 128 B)
+__host__ __device__ constexpr int x_padded_floats(int K) { return (K + 31) / 32 * 32; }
 
 // x read from global memory (through L1)
 struct XGlobal {
@@ -111,21 +121,25 @@ __device__ __forceinline__ float f4(const float4 &v, int i) {
 // sequence of the NW = 1, R = 1 case, so results do not depend on NW or R.
 // ---------------------------------------------------------------------------
 template <int QT>
-__device__ __forceinline__ float code_at(const uint32_t *w, int B, int j) {
+__device__ __forceinline__ float raw_at(const uint32_t *w, int B, int j) {
     constexpr int bb = Fmt<QT>::block_bytes;
     if constexpr (QT == QT_Q8_0) {
         const int byte = bb * B + 2 + j;
-        return q8_code(w[byte >> 2], byte & 3);
+        return q8_raw(w[byte >> 2], byte & 3);
     } else {
         const int byte = bb * B + 2 + (j & 15);
-        return q4_code(w[byte >> 2], 8 * (byte & 3) + (j >= 16 ? 4 : 0));
+        return q4_raw(w[byte >> 2], 8 * (byte & 3) + (j >= 16 ? 4 : 0));
     }
 }
 
+// The block's scale d and code-x sums s[v][r] = (a_0 + a_1) + (a_2 + a_3),
+// a_i the in-order FMA chain over t of q[4t+i] * x[4t+i].  (Packed fp32x2
+// FMAs give the same bits but measured slower here, so the scalar form stays.)
 template <int QT, int NW, int R, int B, class XS>
-__device__ __forceinline__ void block_dot(const uint32_t *const (&w)[NW], const XS &xs, int e0,
-                                          float (&c)[NW][R]) {
+__device__ __forceinline__ void block_sum(const uint32_t *const (&w)[NW], const XS &xs, int e0,
+                                          float (&s)[NW][R], float (&d)[NW]) {
     constexpr int bb = Fmt<QT>::block_bytes;
+    constexpr float M = QT == QT_Q8_0 ? Q8_MAGIC : Q4_MAGIC;
     float a[NW][R][4];
 #pragma unroll
     for (int v = 0; v < NW; ++v)
@@ -142,7 +156,7 @@ __device__ __forceinline__ void block_dot(const uint32_t *const (&w)[NW], const 
         for (int i = 0; i < 4; ++i) {
 #pragma unroll
             for (int v = 0; v < NW; ++v) {
-                const float q = code_at<QT>(w[v], B, 4 * t + i);
+                const float q = __fsub_rn(raw_at<QT>(w[v], B, 4 * t + i), M);
 #pragma unroll
                 for (int r = 0; r < R; ++r) a[v][r][i] = __fmaf_rn(q, f4(xv[r], i), a[v][r][i]);
             }
@@ -150,14 +164,22 @@ __device__ __forceinline__ void block_dot(const uint32_t *const (&w)[NW], const 
     }
 #pragma unroll
     for (int v = 0; v < NW; ++v) {
-        const float d = scale_at(w[v], bb * B);
+        d[v] = scale_at(w[v], bb * B);
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const float s =
-                __fadd_rn(__fadd_rn(a[v][r][0], a[v][r][1]), __fadd_rn(a[v][r][2], a[v][r][3]));
-            c[v][r] = __fmaf_rn(d, s, c[v][r]);
-        }
+        for (int r = 0; r < R; ++r)
+            s[v][r] = __fadd_rn(__fadd_rn(a[v][r][0], a[v][r][1]), __fadd_rn(a[v][r][2], a[v][r][3]));
     }
+}
+
+template <int QT, int NW, int R, int B, class XS>
+__device__ __forceinline__ void block_dot(const uint32_t *const (&w)[NW], const XS &xs, int e0,
+                                          float (&c)[NW][R]) {
+    float s[NW][R], d[NW];
+    block_sum<QT, NW, R, B>(w, xs, e0, s, d);
+#pragma unroll
+    for (int v = 0; v < NW; ++v)
+#pragma unroll
+        for (int r = 0; r < R; ++r) c[v][r] = __fmaf_rn(d[v], s[v][r], c[v][r]);
 }
 
 // One unit (nbk <= 8 blocks; w[v] holds the unit's bytes little-endian from
@@ -213,6 +235,65 @@ __device__ __forceinline__ float fold_lanes(float v, int G) {
     for (int o = G >> 1; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
+
+// One block (34 or 18 bytes) at a 2-byte-aligned shared-memory address,
+// realigned into words so that the block's scale starts at byte 0.  Reads up
+// to 4 bytes past the block; shared-memory rings keep that slack at their end.
+template <int QT>
+__device__ __forceinline__ void load_block_realigned(uint32_t *w, const uint8_t *p) {
+    constexpr int nw = (Fmt<QT>::block_bytes + 3) / 4;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t *q = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+    const uint32_t sh = (uint32_t)(a & 3) * 8;  // 0 or 16
+    uint32_t lo = q[0];
+#pragma unroll
+    for (int i = 0; i < nw; ++i) {
+        const uint32_t hi = q[i + 1];
+        w[i] = __funnelshift_r(lo, hi, sh);
+        lo = hi;
+    }
+}
+
+// One row of nsc full units at `rowp` (shared memory), evaluated by a whole
+// warp block-parallel: in each round, lane 8j+b takes block b of unit 4r+j,
+// the 8 block sums of a unit are chained in block order (c = d_b * s_b + c)
+// with shuffles, and each unit's c is added to virtual lane u mod G in unit
+// order.  That is exactly the tree of unit_dot + the G-lane partial sums, so
+// the result (returned in lane 0 after fold_lanes) is bit-identical to the
+// unit-per-lane evaluation; the latency is that of nsc/4 blocks instead of
+// nsc/G units.
+template <int QT, class XS>
+__device__ __forceinline__ float row_dot_blockpar(const uint8_t *rowp, int nsc, int G,
+                                                  const XS &xs, int lane) {
+    constexpr int UB = Fmt<QT>::unit_bytes, BB = Fmt<QT>::block_bytes;
+    const int j = lane >> 3, b = lane & 7;
+    float p = -0.0f;
+    for (int r4 = 0; r4 < nsc; r4 += 4) {
+        const int u = r4 + j;
+        float s[1][1] = {{0.0f}}, d[1] = {0.0f};
+        if (u < nsc) {
+            uint32_t w[(BB + 3) / 4];
+            load_block_realigned<QT>(w, rowp + u * UB + b * BB);
+            const uint32_t *const ws[1] = {w};
+            block_sum<QT, 1, 1, 0>(ws, xs, 256 * u + 32 * b, s, d);
+        }
+        float c = -0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float dk = __shfl_sync(0xffffffffu, d[0], (j << 3) + k);
+            const float sk = __shfl_sync(0xffffffffu, s[0][0], (j << 3) + k);
+            c = __fmaf_rn(dk, sk, c);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const float cj = __shfl_sync(0xffffffffu, c, jj << 3);
+            const int uu = r4 + jj;
+            if (uu < nsc && lane < G && (uu & (G - 1)) == lane) p = __fadd_rn(p, cj);
+        }
+    }
+    return fold_lanes(p, G);
+}
+
 
 // silu(g) * u in fp32
 __device__ __forceinline__ float silu_mul(float g, float u) {

@@ -1,26 +1,36 @@
 // bq_exec.cuh -- one persistent launch for a whole per-token weight stream.
 //
-// A decode step is a chain of dependent GEMV stages (per layer: q|k|v, o,
-// gate+up, down; then the LM head).  The pages run it as one command buffer
-// per token because per-dispatch cost dominates small GEMVs (EdgeRunner blog
-// post, "What worked" #1: 420+ dispatches in one command buffer, ~6 us each
-// to encode; "We Wrote Our Own Inference Engine", "What actually moved it":
-// 770 dispatches per token).  On GB300 a launch costs microseconds while a
-// 0.5 MB GEMV streams in under 0.1 us, so this kernel runs the whole stream
-// in ONE cooperative launch:
+// A decode step is a chain of GEMV stages (per layer: q|k|v, o, gate+up,
+// down; then the LM head).  The pages run it as one command buffer per token
+// because per-dispatch cost dominates small GEMVs (EdgeRunner blog post,
+// "What worked" #1: 420+ dispatches in one command buffer, ~6 us each to
+// encode; "We Wrote Our Own Inference Engine", "What actually moved it": 770
+// dispatches per token).  On GB300 a launch costs microseconds while a 0.5 MB
+// GEMV streams in under 0.1 us, so this kernel runs a whole stream in ONE
+// cooperative launch:
 //
+//  - the descriptor tables are copied into shared memory once, so nothing on
+//    a stage's critical path waits on a global-memory descriptor read;
 //  - every warp owns a ring of shared-memory slots and streams its own warp
-//    tiles (32/G rows x a chunk of units) of packed weights into them with
-//    1-D bulk copies (TMA), running ahead of its compute -- across stage
-//    boundaries too, because weights never depend on earlier stages;
-//  - only x depends on the previous stage, so x is read after a grid-wide
-//    stage barrier: each CTA's thread 0 adds one release-arrival per stage
-//    and waits (bounded) for all CTAs with acquire loads; the CTA then loads
-//    the stage's distinct x vectors into shared memory at once with plain
-//    coherent loads (never the read-only path), applies RMSNorm there, and
-//    every warp reads x from shared memory;
+//    tiles of packed weights into them with 1-D bulk copies (TMA), running
+//    ahead of its compute across stage boundaries: weights never depend on
+//    earlier stages (the planner rejects outputs that overlap weights).  A
+//    tile is 32/G rows x a chunk of units, one unit per lane ("tile mode"),
+//    or, for ops with only a few rows per warp, a few whole rows that the
+//    warp evaluates one by one block-parallel ("row mode", same tree, 8x
+//    shorter latency per row); the tiles of consecutive stages are dealt out
+//    to the warps round-robin across the whole stream;
+//  - each stage's distinct inputs x are staged into a shared-memory x area
+//    (RMSNorm applied there) and every warp reads x from shared memory; the
+//    x area is double-buffered, and a stage whose inputs do not depend on
+//    earlier stages has its x prefetched with cp.async during the previous
+//    stage;
+//  - a stage that reads (or overwrites) data of an earlier stage starts with
+//    a grid-wide barrier: each CTA's thread 0 adds one release-arrival and
+//    waits (bounded) for all CTAs with acquire loads; the planner marks those
+//    stages by comparing address ranges, so independent GEMVs never wait;
 //  - arithmetic is bq_dot.cuh's fixed tree, so every output is bit-identical
-//    to the standalone single-row kernels on the same inputs.
+//    to the standalone single-op kernels on the same inputs.
 // The barrier is an explicit, ordered, device-scope handoff between CTAs of a
 // cooperative launch (co-residency guaranteed), unlike the unordered
 // last-arrival handoff that failed on the pages ("We Wrote Our Own Inference
@@ -35,30 +45,40 @@
 
 namespace bq {
 
-#define BQ_DEVERR_BARRIER_WAIT 0x8u  // a CTA gave up waiting at a stage barrier
+#define BQ_DEVERR_BARRIER_WAIT 0x8u   // a CTA gave up waiting at a stage barrier
+#define BQ_DEVERR_XFULL_WAIT 0x10u    // a warp gave up waiting for a stage's x copies
+#define BQ_DEVERR_XREADY_WAIT 0x20u   // a warp gave up waiting for a stage's normalised x
 
+// one GEMV (or gate+up pair) of the stream; 64 bytes
 struct ExecOp {
     const uint8_t *W[2];
     float *y;
-    long long rb;
-    int mode, M, K, nsc, G, rpw;
-    int KCU, nchunks, ntiles, row_stride, single, nmat;
-    int tile_base;  // first tile of this op within its stage
-    int xoff;       // float offset of this op's (normalised) x in the stage's x area
+    int M, rb;                // rows, packed bytes per row
+    int ntiles, tile_base;    // warp tiles; first tile of this op within its stage
+    int row_stride, xoff;     // shared-memory bytes per tile row; float offset of x
+    short KCU, nchunks;       // units per row per ring slot; slots per tile and matrix
+    unsigned char G, rpw, nmat, single;  // rpw: rows per tile
+    int nsc;
+    int rowmode;              // 1: a tile is rpw whole rows, each evaluated by the whole warp
 };
 
-// one distinct input vector of a stage, staged into shared memory after the
-// stage barrier (and RMSNorm-ed there when gamma is set)
+// one distinct input vector of a stage (RMSNorm-ed when gamma is set); 32 bytes
 struct ExecX {
     const float *x;
     const float *gamma;
     float eps;
     int K, off;  // off: float offset in the x area
+    int pad;
 };
 
+// 32 bytes
 struct ExecStage {
     int op_begin, op_end, tiles;
     int x_begin, x_end;  // range in the ExecX table
+    int barrier;         // 1: wait for every CTA to finish all earlier stages first
+    int tile_off;        // tiles of all earlier stages, mod the number of warps: stage s's
+                         // tile t goes to warp (tile_off + t) mod nwarps, so work rotates
+    int pad;
 };
 
 struct ExecArgs {
@@ -66,77 +86,89 @@ struct ExecArgs {
     const ExecStage *stages;
     const ExecX *xs;
     unsigned int *counters;  // one per stage, zero at launch
-    int nstages;
-    int NSW;         // ring slots per warp
-    int slot_bytes;  // bytes per slot (a multiple of 128)
-    int x_off;       // shared-memory offset of the stage's x area
-    int ring_off;    // shared-memory offset of the rings
+    int nops, nstages, nxs;
+    int NSW;          // ring slots per warp
+    int slot_bytes;   // bytes per slot (a multiple of 128)
+    int xbar_off;     // shared-memory offset of the x-buffer mbarriers
+    int tab_off;      // shared-memory offset of the descriptor tables
+    int x_off;        // shared-memory offset of the x buffers
+    int x_floats;     // floats per x buffer
+    int x_buffers;    // x buffers in the ring (1..EXEC_MAX_XBUF)
+    int ring_off;     // shared-memory offset of the weight rings
+    int prefetch;     // items per warp prefetched into L2 beyond the ring
 };
+
+constexpr int EXEC_MAX_XBUF = 8;
 
 // launch geometry of a planned executor run (host side)
 struct ExecGeometry {
-    int n_stages, n_x, slot, nsw, x_off, ring_off, threads, grid;
+    int n_stages, n_x, slot, nsw, xbar_off, tab_off, x_off, x_floats, x_buffers, ring_off,
+        threads, grid, prefetch;
     size_t smem;
 };
 
-// x read with plain (coherent) loads: x may have been written by another CTA
-// before the stage barrier, so the read-only path is not allowed
-__device__ __forceinline__ float4 ld_coherent4(const float *p) {
-    float4 v;
-    asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p));
-    return v;
+// shared-memory bytes of the descriptor tables
+__host__ __device__ inline int exec_table_bytes(int nops, int nxs, int nstages) {
+    return ((nops * (int)sizeof(ExecOp) + nxs * (int)sizeof(ExecX) +
+             nstages * (int)sizeof(ExecStage)) + 127) / 128 * 128;
 }
 
-// Stage the x vectors of stage s into shared memory (padded layout of XSmem),
-// RMSNorm-ing those with a gain: every thread of the CTA takes part; ends with
-// the x area complete and visible to all warps.  The RMS scale uses the same
-// fixed tree as rms_scale(), so xn matches the single-op kernels bit for bit.
-__device__ __forceinline__ void exec_stage_x(const ExecArgs &a, int s, float *xa, float *red) {
-    const ExecStage st = a.stages[s];
-    const int nthr = blockDim.x;
-    auto sync = [nthr]() { named_bar_sync(1, nthr); };
-    bool any_norm = false;
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// One warp starts the copies of stage st's inputs into x buffer `xa`
+// (permuted layout of XSmem) with cp.async (16 bytes per lane and copy,
+// through L2, so data written by other CTAs before a stage barrier is seen),
+// then every lane arrives on `xfull` once its copies have landed (the
+// barrier expects 32 arrivals).
+__device__ __forceinline__ void exec_load_x(const ExecStage &st, const ExecX *xs, float *xa,
+                                            uint64_t *xfull, int lane) {
     for (int j = st.x_begin; j < st.x_end; ++j) {
-        const ExecX xd = a.xs[j];
-        for (int e = 4 * threadIdx.x; e < xd.K; e += 4 * nthr)
-            *reinterpret_cast<float4 *>(xa + xd.off + e + ((e >> 8) << 2)) = ld_coherent4(xd.x + e);
-        any_norm |= xd.gamma != nullptr;
+        const ExecX &xd = xs[j];
+        for (int c = lane; c < xd.K / 4; c += 32)
+            cp_async16(xa + xd.off + 4 * x_chunk_pos(c), xd.x + 4 * c);
     }
-    sync();
-    if (!any_norm) return;
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(xfull))
+                 : "memory");
+}
+
+// One warp RMSNorms the stage's inputs that have a gain, in place.  The RMS
+// scale uses the fixed tree of rms_scale() (lane L holds the 256-virtual-lane
+// sums 8L..8L+7), so xn matches the single-op kernels bit for bit.
+__device__ __forceinline__ void exec_norm_x_warp(const ExecStage &st, const ExecX *xs, float *xa,
+                                                 int lane) {
     for (int j = st.x_begin; j < st.x_end; ++j) {
-        const ExecX xd = a.xs[j];
+        const ExecX &xd = xs[j];
         if (!xd.gamma) continue;
         float *xv = xa + xd.off;
-        for (int v = threadIdx.x; v < 256; v += nthr) {
+        float q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
             float acc = 0.0f;
-            for (int k = v; k < xd.K; k += 256) {
-                const float t = xv[k + ((k >> 8) << 2)];
+            for (int k = 8 * lane + i; k < xd.K; k += 256) {
+                const float t = xv[x_pos(k)];
                 acc = __fmaf_rn(t, t, acc);
             }
-            red[v] = acc;
+            q[i] = acc;
         }
-        sync();
-        if (threadIdx.x < 32) {
-            const float *q = red + 8 * threadIdx.x;
-            float v = __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
-                                __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
-            for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (threadIdx.x == 0) red[256] = v;
-        }
-        sync();
-        const float ms = __fdiv_rn(red[256], (float)xd.K);
+        float v = __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
+                            __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
+        for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+        const float ms = __fdiv_rn(v, (float)xd.K);
         const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, xd.eps)));
-        for (int e = 4 * threadIdx.x; e < xd.K; e += 4 * nthr) {
-            float4 *p = reinterpret_cast<float4 *>(xv + e + ((e >> 8) << 2));
-            const float4 v = *p;
-            const float4 g = __ldg(reinterpret_cast<const float4 *>(xd.gamma + e));
-            *p = make_float4(__fmul_rn(__fmul_rn(v.x, rs), g.x), __fmul_rn(__fmul_rn(v.y, rs), g.y),
-                             __fmul_rn(__fmul_rn(v.z, rs), g.z), __fmul_rn(__fmul_rn(v.w, rs), g.w));
+        __syncwarp();
+        for (int c = lane; c < xd.K / 4; c += 32) {
+            float4 *p = reinterpret_cast<float4 *>(xv + 4 * x_chunk_pos(c));
+            const float4 x4 = *p;
+            const float4 g = __ldg(reinterpret_cast<const float4 *>(xd.gamma) + c);
+            *p = make_float4(__fmul_rn(__fmul_rn(x4.x, rs), g.x), __fmul_rn(__fmul_rn(x4.y, rs), g.y),
+                             __fmul_rn(__fmul_rn(x4.z, rs), g.z), __fmul_rn(__fmul_rn(x4.w, rs), g.w));
         }
-        sync();  // also protects red[] before the next gain's reduction
+        __syncwarp();
     }
 }
 
@@ -146,61 +178,78 @@ struct ExecItem {
     int s, t, op, mat, chunk;
 };
 
-__device__ __forceinline__ bool exec_locate(const ExecArgs &a, ExecItem &it) {
+struct ExecTables {
+    const ExecOp *ops;
+    const ExecStage *stages;
+    const ExecX *xs;
+    int nstages;
+};
+
+__device__ __forceinline__ bool exec_locate(const ExecTables &T, ExecItem &it) {
     // find the op of tile t in stage s; false if t is past the stage's tiles
-    const ExecStage st = a.stages[it.s];
+    const ExecStage &st = T.stages[it.s];
     if (it.t >= st.tiles) return false;
     int op = st.op_begin;
-    while (op + 1 < st.op_end && a.ops[op + 1].tile_base <= it.t) ++op;
+    while (op + 1 < st.op_end && T.ops[op + 1].tile_base <= it.t) ++op;
     it.op = op;
     return true;
 }
 
-// first item of stage s at or after tile t0 (t0 = this warp's first tile); -1 op if none
-__device__ __forceinline__ void exec_first_in_stage(const ExecArgs &a, ExecItem &it, int s,
-                                                    int gw) {
+__device__ __forceinline__ void exec_first_in_stage(const ExecTables &T, ExecItem &it, int s,
+                                                    int gw, int nwarps) {
     it.s = s;
-    it.t = gw;
+    const int t0 = gw - T.stages[s].tile_off;
+    it.t = t0 < 0 ? t0 + nwarps : t0;
     it.mat = 0;
     it.chunk = 0;
-    if (!exec_locate(a, it)) it.op = -1;
+    if (!exec_locate(T, it)) it.op = -1;
 }
 
-// advance within the current stage; returns false when the warp has no more
-// items in this stage
-__device__ __forceinline__ bool exec_next_in_stage(const ExecArgs &a, ExecItem &it, int nwarps) {
-    const ExecOp &op = a.ops[it.op];
+// advance within the current stage; false when the warp has no more items in it
+__device__ __forceinline__ bool exec_next_in_stage(const ExecTables &T, ExecItem &it,
+                                                   int nwarps) {
+    const ExecOp &op = T.ops[it.op];
     if (++it.chunk < op.nchunks) return true;
     it.chunk = 0;
     if (++it.mat < op.nmat) return true;
     it.mat = 0;
     it.t += nwarps;
-    return exec_locate(a, it);
+    return exec_locate(T, it);
 }
 
 // the producer side walks across stages
-__device__ __forceinline__ bool exec_next_any(const ExecArgs &a, ExecItem &it, int nwarps,
+__device__ __forceinline__ bool exec_next_any(const ExecTables &T, ExecItem &it, int nwarps,
                                               int gw) {
-    if (it.op >= 0 && exec_next_in_stage(a, it, nwarps)) return true;
-    for (int s = it.s + 1; s < a.nstages; ++s) {
-        exec_first_in_stage(a, it, s, gw);
+    if (it.op >= 0 && exec_next_in_stage(T, it, nwarps)) return true;
+    for (int s = it.s + 1; s < T.nstages; ++s) {
+        exec_first_in_stage(T, it, s, gw, nwarps);
         if (it.op >= 0) return true;
     }
-    it.s = a.nstages;
+    it.s = T.nstages;
     it.op = -1;
     return false;
 }
 
+// bounded mbarrier wait that also returns (false) once the CTA is aborting
+__device__ __forceinline__ bool exec_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && (*abort_flag || globaltimer() - t0 > BQ_WAIT_LIMIT_NS)) return false;
+    }
+}
+
 template <int QT>
-__device__ __forceinline__ void exec_issue(const ExecArgs &a, const ExecItem &it, uint8_t *slot,
+__device__ __forceinline__ void exec_issue(const ExecTables &T, const ExecItem &it, uint8_t *slot,
                                            uint64_t *full, uint64_t pol, int lane) {
     constexpr int UB = Fmt<QT>::unit_bytes;
-    const ExecOp &op = a.ops[it.op];
+    const ExecOp &op = T.ops[it.op];
     const int tile = it.t - op.tile_base;
     const int row0 = tile * op.rpw;
-    const int rows = min(op.rpw, op.M - row0);
+    const int rows = min((int)op.rpw, op.M - row0);
     const int u0 = it.chunk * op.KCU;
-    const int cnt = min(op.KCU, op.nsc - u0);
+    const int cnt = min((int)op.KCU, op.nsc - u0);
     const uint32_t rowb = (uint32_t)cnt * UB;
     const uint8_t *W = op.W[it.mat];
     if (lane == 0) mbar_arrive_expect_tx(full, rowb * rows);
@@ -213,6 +262,26 @@ __device__ __forceinline__ void exec_issue(const ExecArgs &a, const ExecItem &it
     }
 }
 
+// Prefetch item `it`'s weight bytes into L2 (the same ranges exec_issue will
+// copy later): more HBM requests in flight than the shared-memory ring holds.
+template <int QT>
+__device__ __forceinline__ void exec_prefetch(const ExecTables &T, const ExecItem &it, int lane) {
+    constexpr int UB = Fmt<QT>::unit_bytes;
+    const ExecOp &op = T.ops[it.op];
+    const int tile = it.t - op.tile_base;
+    const int row0 = tile * op.rpw;
+    const int rows = min((int)op.rpw, op.M - row0);
+    const int u0 = it.chunk * op.KCU;
+    const int cnt = min((int)op.KCU, op.nsc - u0);
+    const uint32_t rowb = (uint32_t)cnt * UB;
+    const uint8_t *W = op.W[it.mat];
+    if (op.single) {
+        if (lane == 0) bulk_prefetch_l2(W + (size_t)row0 * op.rb, rowb * rows);
+    } else if (lane < rows) {
+        bulk_prefetch_l2(W + (size_t)(row0 + lane) * op.rb + (size_t)u0 * UB, rowb);
+    }
+}
+
 template <int QT>
 __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned int *status) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -221,132 +290,249 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
     const int nw = blockDim.x >> 5;
     const int nwarps = nw * gridDim.x;
     const int gw = warp * gridDim.x + blockIdx.x;  // warp-major: consecutive tiles on different SMs
+    const int XB = a.x_buffers;
+    // control block: abort flag; per x buffer, warps done with its stage and
+    // warps that entered its stage (per phase parity)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem);
-    float *red = reinterpret_cast<float *>(smem + 64);                         // 260 floats
-    uint64_t *fulls = reinterpret_cast<uint64_t *>(smem + 64 + 4 * 264);      // nw * NSW
-    float *xa = reinterpret_cast<float *>(smem + a.x_off);
+    int *done = reinterpret_cast<int *>(smem + 16);       // [EXEC_MAX_XBUF]
+    int *entered = reinterpret_cast<int *>(smem + 64);    // [EXEC_MAX_XBUF][2]
+    uint64_t *fulls = reinterpret_cast<uint64_t *>(smem + 256);  // nw * NSW weight slots
+    uint64_t *xfull = reinterpret_cast<uint64_t *>(smem + a.xbar_off);  // [XB]: x copies landed
+    uint64_t *xready = xfull + XB;                                       // [XB]: x normalised
     uint8_t *ring = smem + a.ring_off + (size_t)warp * a.NSW * a.slot_bytes;
     uint64_t *full = fulls + warp * a.NSW;
 
-    if (threadIdx.x == 0) *abort_flag = 0;
+    // descriptor tables -> shared memory
+    ExecTables T;
+    {
+        uint8_t *tab = smem + a.tab_off;
+        const int ob = a.nops * (int)sizeof(ExecOp), xb = a.nxs * (int)sizeof(ExecX),
+                  sb = a.nstages * (int)sizeof(ExecStage);
+        for (int i = threadIdx.x; i < ob / 16; i += blockDim.x)
+            reinterpret_cast<int4 *>(tab)[i] = __ldg(reinterpret_cast<const int4 *>(a.ops) + i);
+        for (int i = threadIdx.x; i < xb / 16; i += blockDim.x)
+            reinterpret_cast<int4 *>(tab + ob)[i] = __ldg(reinterpret_cast<const int4 *>(a.xs) + i);
+        for (int i = threadIdx.x; i < sb / 16; i += blockDim.x)
+            reinterpret_cast<int4 *>(tab + ob + xb)[i] =
+                __ldg(reinterpret_cast<const int4 *>(a.stages) + i);
+        T.ops = reinterpret_cast<const ExecOp *>(tab);
+        T.xs = reinterpret_cast<const ExecX *>(tab + ob);
+        T.stages = reinterpret_cast<const ExecStage *>(tab + ob + xb);
+        T.nstages = a.nstages;
+    }
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int b = 0; b < EXEC_MAX_XBUF; ++b) {
+            done[b] = 0;
+            entered[2 * b] = entered[2 * b + 1] = 0;
+        }
+        for (int b = 0; b < XB; ++b) {
+            mbar_init(xfull + b, 32);
+            mbar_init(xready + b, 1);
+        }
+    }
     if (lane == 0)
         for (int i = 0; i < a.NSW; ++i) mbar_init(full + i, 1);
     if (lane == 0) fence_mbar_init();
     __syncthreads();
 
     const uint64_t pol = l2_policy_evict_first();
-    // producer cursor: prefetch the first NSW items of this warp
+    // weight ring: prefetch the first NSW items of this warp
     ExecItem pit;
     pit.s = -1;
     pit.op = -1;
     int issued = 0, consumed = 0;
+    // L2 prefetch cursor, a.prefetch items ahead of the ring's copies
+    ExecItem fit;
+    fit.s = -1;
+    fit.op = -1;
+    bool fit_more = true;
+    auto prefetch_next = [&]() {
+        if (fit_more && (fit_more = exec_next_any(T, fit, nwarps, gw))) exec_prefetch<QT>(T, fit, lane);
+    };
     auto issue_next = [&]() {
-        if (!exec_next_any(a, pit, nwarps, gw)) return;
-        exec_issue<QT>(a, pit, ring + (size_t)(issued % a.NSW) * a.slot_bytes,
+        if (!exec_next_any(T, pit, nwarps, gw)) return;
+        exec_issue<QT>(T, pit, ring + (size_t)(issued % a.NSW) * a.slot_bytes,
                        full + issued % a.NSW, pol, lane);
         ++issued;
+        prefetch_next();
     };
-    {
-        // start the producer cursor before stage 0
-        pit.s = -1;
-        pit.op = -1;
-        for (int i = 0; i < a.NSW; ++i) issue_next();
-    }
+    for (int i = 0; i < a.NSW + a.prefetch; ++i) prefetch_next();
+    for (int i = 0; i < a.NSW; ++i) issue_next();
 
-    for (int s = 0; s < a.nstages; ++s) {
-        if (s > 0) {
-            // ---- grid-wide barrier: every CTA has finished stage s-1 ----
-            named_bar_sync(1, blockDim.x);
-            if (threadIdx.x == 0) {
-                __threadfence();
-                atomicAdd(a.counters + (s - 1), 1u);
-                if (!*abort_flag) {
-                    const uint64_t t0 = globaltimer();
-                    unsigned int n = 0;
-                    for (uint32_t i = 0;; ++i) {
-                        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
-                                     : "=r"(n)
-                                     : "l"(a.counters + (s - 1))
-                                     : "memory");
-                        if (n >= gridDim.x) break;
-                        if ((i & 63u) == 63u && globaltimer() - t0 > BQ_WAIT_LIMIT_NS) {
-                            *abort_flag = 1;
-                            atomicOr(status, BQ_DEVERR_BARRIER_WAIT);
-                            break;
-                        }
-                    }
-                }
+    auto xbuf = [&](int s) {
+        return reinterpret_cast<float *>(smem + a.x_off) + (size_t)(s % XB) * a.x_floats;
+    };
+    // the first XB stages' inputs (stage 0 never waits at a barrier; later
+    // barrier stages are loaded after their barrier)
+    if (warp == 0)
+        for (int s = 0; s < XB && s < a.nstages; ++s)
+            if (s == 0 || !T.stages[s].barrier)
+                exec_load_x(T.stages[s], T.xs, xbuf(s), xfull + s % XB, lane);
+
+    bool ok = true;
+    for (int s = 0; s < a.nstages && ok; ++s) {
+        const ExecStage &st = T.stages[s];
+        const int b = s % XB;
+        const uint32_t ph = (uint32_t)(s / XB) & 1u;
+        // ---- enter stage s: the first warp in normalises x(s) and publishes it ----
+        int first = 0;
+        if (lane == 0) first = atomicAdd(entered + 2 * b + ph, 1) == 0;
+        first = __shfl_sync(0xffffffffu, first, 0);
+        if (first) {
+            if (!__all_sync(0xffffffffu, exec_wait(xfull + b, ph, abort_flag))) {
+                if (lane == 0) atomicOr(status, BQ_DEVERR_XFULL_WAIT);
+                ok = false;
+                break;
             }
-            named_bar_sync(1, blockDim.x);
+            exec_norm_x_warp(st, T.xs, xbuf(s), lane);
+            if (lane == 0) mbar_arrive(xready + b);
         }
-        if (*abort_flag) continue;  // keep every barrier's arrival, skip the work
-        exec_stage_x(a, s, xa, red);
+        const float *xa = xbuf(s);
 
+        // Every warp waits for x(s), even one without items in stage s: an
+        // mbarrier wait only tells the current phase from the one before it,
+        // so no warp may run ahead to a later phase of a buffer whose earlier
+        // phase it has not seen complete.  Waiting here in stage order keeps
+        // the warps of a CTA within XB stages of each other.
+        if (!__all_sync(0xffffffffu, exec_wait(xready + b, ph, abort_flag))) {
+            if (lane == 0) atomicOr(status, BQ_DEVERR_XREADY_WAIT);
+            ok = false;
+            break;
+        }
+
+        // ---- this warp's items of stage s ----
         ExecItem it;
-        exec_first_in_stage(a, it, s, gw);
-        if (it.op < 0) continue;
+        exec_first_in_stage(T, it, s, gw, nwarps);
         float p0 = -0.0f, p1 = -0.0f;
-        for (;;) {
-            const ExecOp &op = a.ops[it.op];
+        while (it.op >= 0) {
+            const ExecOp &op = T.ops[it.op];
             const int slot = consumed % a.NSW;
-            const bool landed = mbar_wait_bounded(full + slot, (consumed / a.NSW) & 1);
-            if (!__all_sync(0xffffffffu, landed)) {
-                if (lane == 0) {
-                    *abort_flag = 1;
-                    atomicOr(status, BQ_DEVERR_FULL_WAIT);
-                }
+            if (!__all_sync(0xffffffffu, exec_wait(full + slot, (consumed / a.NSW) & 1, abort_flag))) {
+                if (lane == 0) atomicOr(status, BQ_DEVERR_FULL_WAIT);
+                ok = false;
                 break;
             }
             const int G = op.G;
             const int rho = lane / G, l = lane & (G - 1);
             const int tile = it.t - op.tile_base;
             const int row0 = tile * op.rpw;
-            const int rows = min(op.rpw, op.M - row0);
+            const int rows = min((int)op.rpw, op.M - row0);
             const int u0 = it.chunk * op.KCU;
-            const int cnt = min(op.KCU, op.nsc - u0);
+            const int cnt = min((int)op.KCU, op.nsc - u0);
             if (it.mat == 0 && it.chunk == 0) {
                 p0 = -0.0f;
                 p1 = -0.0f;
             }
-            const uint8_t *st = ring + (size_t)slot * a.slot_bytes + rho * op.row_stride;
             const XSmem xs{xa + op.xoff, 0};
-            float acc = it.mat == 0 ? p0 : p1;
-            if (rho < rows) {
-                for (int ul = l; ul < cnt; ul += G) {
-                    uint32_t w[Fmt<QT>::unit_words];
-                    load_unit_smem<QT>(w, st + ul * UB);
-                    const uint32_t *const ws[1] = {w};
-                    float cc[1][1];
-                    unit_dot<QT, 1, 1>(ws, 8, xs, (u0 + ul) * 256, cc);
-                    acc = __fadd_rn(acc, cc[0][0]);
+            if (op.rowmode) {
+                // rows of this tile one by one, each by the whole warp; lane r
+                // keeps row r's gate value between the two matrices of gate+up
+                const uint8_t *base = ring + (size_t)slot * a.slot_bytes;
+                for (int r = 0; r < rows; ++r) {
+                    const float v = __shfl_sync(
+                        0xffffffffu, row_dot_blockpar<QT>(base + (size_t)r * op.rb, op.nsc, G, xs, lane), 0);
+                    if (op.nmat == 1) {
+                        if (lane == 0) op.y[row0 + r] = v;
+                    } else if (it.mat == 0) {
+                        if (lane == r) p0 = v;
+                    } else {
+                        const float gr = __shfl_sync(0xffffffffu, p0, r);
+                        if (lane == 0) op.y[row0 + r] = silu_mul(gr, v);
+                    }
+                }
+            } else {
+                const uint8_t *stp = ring + (size_t)slot * a.slot_bytes + rho * op.row_stride;
+                float acc = it.mat == 0 ? p0 : p1;
+                if (rho < rows) {
+                    for (int ul = l; ul < cnt; ul += G) {
+                        uint32_t w[Fmt<QT>::unit_words];
+                        load_unit_smem<QT>(w, stp + ul * UB);
+                        const uint32_t *const ws[1] = {w};
+                        float cc[1][1];
+                        unit_dot<QT, 1, 1>(ws, 8, xs, (u0 + ul) * 256, cc);
+                        acc = __fadd_rn(acc, cc[0][0]);
+                    }
+                }
+                if (it.mat == 0) p0 = acc;
+                else p1 = acc;
+                if (it.chunk + 1 == op.nchunks && it.mat + 1 == op.nmat) {
+                    const float g = fold_lanes(p0, G);
+                    if (op.nmat == 2) {
+                        const float u = fold_lanes(p1, G);
+                        if (rho < rows && l == 0) op.y[row0 + rho] = silu_mul(g, u);
+                    } else if (rho < rows && l == 0) {
+                        op.y[row0 + rho] = g;
+                    }
                 }
             }
-            if (it.mat == 0) p0 = acc;
-            else p1 = acc;
             __syncwarp();
             ++consumed;
-            const bool last_chunk = it.chunk + 1 == op.nchunks;
-            const bool last_mat = it.mat + 1 == op.nmat;
-            if (last_chunk && last_mat) {
-                const float g = fold_lanes(p0, G);
-                if (op.nmat == 2) {
-                    const float u = fold_lanes(p1, G);
-                    if (rho < rows && l == 0) op.y[row0 + rho] = silu_mul(g, u);
-                } else if (rho < rows && l == 0) {
-                    op.y[row0 + rho] = g;
+            issue_next();  // refill the slot just consumed
+            if (!exec_next_in_stage(T, it, nwarps)) break;
+        }
+        if (!ok) break;
+
+        // ---- leave stage s: the last warp out starts the next loads ----
+        __syncwarp();  // this warp's y stores of stage s precede its arrival
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(done + b, 1) == nw - 1;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (!last) continue;
+        if (lane == 0) {
+            done[b] = 0;             // next use: stage s + XB
+            entered[2 * b + ph] = 0;  // next use: stage s + 2 XB
+            __threadfence_block();
+        }
+        if (s + 1 < a.nstages && T.stages[s + 1].barrier) {
+            // stage s+1 reads or overwrites earlier stages' data: every CTA must
+            // be done with stages <= s before anyone loads its inputs
+            int failed = 0;
+            if (lane == 0) {
+                __threadfence();  // this CTA's y stores (ordered by the done counter)
+                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.counters + s + 1)
+                             : "memory");
+                const uint64_t t0 = globaltimer();
+                unsigned int n = 0;
+                for (uint32_t i = 0;; ++i) {
+                    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
+                                 : "=r"(n)
+                                 : "l"(a.counters + s + 1)
+                                 : "memory");
+                    if (n >= gridDim.x) break;
+                    if ((i & 63u) == 63u &&
+                        (*abort_flag || globaltimer() - t0 > BQ_WAIT_LIMIT_NS)) {
+                        failed = 1;
+                        break;
+                    }
                 }
             }
-            issue_next();  // refill the slot just consumed
-            if (!exec_next_in_stage(a, it, nwarps)) break;
+            __syncwarp();  // the other lanes' copies below follow lane 0's acquire
+            if (__shfl_sync(0xffffffffu, failed, 0)) {
+                if (lane == 0) atomicOr(status, BQ_DEVERR_BARRIER_WAIT);
+                ok = false;
+                break;
+            }
+            // buffer (s+1) % XB is free: its previous stage (s+1-XB <= s) is done
+            exec_load_x(T.stages[s + 1], T.xs, xbuf(s + 1), xfull + (s + 1) % XB, lane);
         }
+        if (XB > 1 && s + XB < a.nstages && !T.stages[s + XB].barrier)
+            exec_load_x(T.stages[s + XB], T.xs, xbuf(s + XB), xfull + b, lane);
+        else if (XB == 1 && s + 1 < a.nstages && !T.stages[s + 1].barrier)
+            exec_load_x(T.stages[s + 1], T.xs, xbuf(s + 1), xfull + b, lane);
     }
 
-    // make sure no copy into this warp's ring is still in flight at exit
-    if (*abort_flag) {
+    if (!ok) {
+        if (lane == 0) *abort_flag = 1;
+        // no weight copy into this warp's ring may still be in flight at exit
         for (int i = consumed; i < issued; ++i)
             if (!mbar_wait_bounded(full + i % a.NSW, (i / a.NSW) & 1) && lane == 0)
                 atomicOr(status, BQ_DEVERR_DRAIN_WAIT);
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // nor any x copy
 }
 
 }  // namespace bq

@@ -78,6 +78,9 @@ struct ExecGeometry;
 // device.  Touches no device memory.
 bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, ExecX *ex,
                            ExecStage *es, ExecGeometry *geo);
+// kernel arguments for planned tables at the given device addresses
+void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const ExecX *xs,
+                    const ExecStage *stages, unsigned int *counters, ExecArgs *a);
 }
 // persistent per-token stream executor (bq_exec.cuh), one instantiation per format
 int bq_internal_exec_occupancy_q8_0(int threads, size_t smem, int *occ);

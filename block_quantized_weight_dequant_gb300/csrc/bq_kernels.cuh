@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(288) stream_kernel(const StreamArgs a, unsigne
                                         __fmul_rn(__fmul_rn(v.z, rs), g.z),
                                         __fmul_rn(__fmul_rn(v.w, rs), g.w));
                     }
-                    *reinterpret_cast<float4 *>(xsm + r * a.x_rstride + e + ((e >> 8) << 2)) = v;
+                    *reinterpret_cast<float4 *>(xsm + r * a.x_rstride + 4 * x_chunk_pos(e >> 2)) = v;
                 }
             csync();
         }

@@ -30,6 +30,7 @@ constexpr size_t SCRATCH_BYTES = OFF_CNT + al256((size_t)MAX_OPS * sizeof(unsign
 // code this name is only a stand-in for the symbol; the kernel gets the
 // device address fetched by scratch_address().
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SCRATCH_BYTES];
+static_assert(SCRATCH_BYTES == 66 * 1024, "the documented size of the scratch array");
 
 std::atomic<unsigned char *> g_scratch_addr[64];
 
@@ -83,15 +84,10 @@ extern "C" bq_status bq_stream_run_noalloc(int qtype, const bq_op *ops, int n_op
         cudaSuccess)
         return BQ_ERR_CUDA;
     bq::ExecArgs a;
-    a.ops = reinterpret_cast<const bq::ExecOp *>(scratch);
-    a.xs = reinterpret_cast<const bq::ExecX *>(scratch + OFF_X);
-    a.stages = reinterpret_cast<const bq::ExecStage *>(scratch + OFF_ST);
-    a.counters = reinterpret_cast<unsigned int *>(scratch + OFF_CNT);
-    a.nstages = geo.n_stages;
-    a.NSW = geo.nsw;
-    a.slot_bytes = geo.slot;
-    a.x_off = geo.x_off;
-    a.ring_off = geo.ring_off;
+    bq::fill_exec_args(geo, n_ops, reinterpret_cast<const bq::ExecOp *>(scratch),
+                       reinterpret_cast<const bq::ExecX *>(scratch + OFF_X),
+                       reinterpret_cast<const bq::ExecStage *>(scratch + OFF_ST),
+                       reinterpret_cast<unsigned int *>(scratch + OFF_CNT), &a);
     const int e = qtype == BQ_Q8_0
                       ? bq_internal_exec_launch_q8_0(a, geo.grid, geo.threads, geo.smem, stream)
                       : bq_internal_exec_launch_q4_0(a, geo.grid, geo.threads, geo.smem, stream);

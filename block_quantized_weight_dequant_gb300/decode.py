@@ -17,6 +17,10 @@ Attention itself, residual adds and the other norms are outside this stream
 so the stages are truly dependent, as in decode.  ``run_plan()`` runs the
 whole stream in one cooperative launch (bq_stream_plan_*); ``run_per_op()``
 launches one kernel per op in stage order; the two give identical bits.
+
+With ``chained=False`` every op instead reads an input vector of its own (the
+same shapes and weights, no data flowing between ops): the pure per-token
+weight stream, which the executor runs without any grid-wide barrier.
 """
 import torch
 
@@ -24,7 +28,7 @@ from . import StreamOp, StreamPlan, gemv, gemv_gate_up_silu
 
 
 class DecodeStream:
-    def __init__(self, qtype, layers, lm_head, eps=1e-6):
+    def __init__(self, qtype, layers, lm_head, eps=1e-6, chained=True):
         """layers: list of dicts with packed q, k, v, o, gate, up, down
         (uint8 [M, row bytes]) and gamma (fp32 [hidden]); lm_head: packed."""
         from . import _packed_shape, _qt
@@ -39,9 +43,28 @@ class DecodeStream:
             return _packed_shape(P, self.qtype)
 
         hidden = rows(layers[0]["q"])[1]
-        self.x0 = torch.zeros(hidden, **f32)
+        self.chained = chained
+        # every vector the stream reads from outside lives in one buffer, so a
+        # caller fills them with a single copy: x0 (chained), or x0 and one
+        # input per op (unchained)
+        n_in = hidden
+        if not chained:
+            for L in layers:
+                n_in += rows(L["o"])[1] + hidden + rows(L["down"])[1] + hidden
+        self.inputs = torch.zeros(n_in, **f32)
+        self.x0 = self.inputs[:hidden]
         self.ops = []
         self.buffers = []
+        cursor = [hidden]
+
+        def src(produced, K):
+            # chained: the producing op's output; otherwise an input of its own
+            if chained:
+                return produced
+            t = self.inputs[cursor[0]:cursor[0] + K]
+            cursor[0] += K
+            return t
+
         h = self.x0
         st = 0
         for L in layers:
@@ -50,11 +73,12 @@ class DecodeStream:
             self.buffers.append(bufs)
             for n in ("q", "k", "v"):
                 self.ops.append(StreamOp(st, L[n], h, bufs[n]))
-            self.ops.append(StreamOp(st + 1, L["o"], bufs["q"], bufs["o"]))
-            self.ops.append(StreamOp(st + 2, L["gate"], bufs["o"], bufs["ffn"], W_up=L["up"],
-                                     gamma=L["gamma"], eps=eps))
-            self.ops.append(StreamOp(st + 3, L["down"], bufs["ffn"], bufs["down"]))
-            h = bufs["down"]
+            self.ops.append(StreamOp(st + 1, L["o"], src(bufs["q"], rows(L["o"])[1]), bufs["o"]))
+            self.ops.append(StreamOp(st + 2, L["gate"], src(bufs["o"], hidden), bufs["ffn"],
+                                     W_up=L["up"], gamma=L["gamma"], eps=eps))
+            self.ops.append(StreamOp(st + 3, L["down"], src(bufs["ffn"], rows(L["down"])[1]),
+                                     bufs["down"]))
+            h = src(bufs["down"], hidden)
             st += 4
         self.logits = torch.empty(rows(lm_head)[0], **f32)
         self.ops.append(StreamOp(st, lm_head, h, self.logits))

@@ -219,7 +219,7 @@ bq_status bq_stream_plan_destroy(bq_stream_plan *plan);
  * (same validation, same kernel, bit-identical outputs) with the descriptor
  * tables and stage counters kept in one fixed device array inside the
  * library, which every GPU that loads the library holds until the process
- * exits (72 KiB).  The caller still passes the inputs and outputs (in
+ * exits (66 KiB).  The caller still passes the inputs and outputs (in
  * the ops).  It calls no cudaMalloc, cudaFree or other allocating routine.
  *
  *  - At most BQ_NOALLOC_MAX_OPS ops (and as many stages); more returns

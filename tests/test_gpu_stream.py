@@ -106,3 +106,46 @@ def test_plan_rejects_bad_ops():
     P2 = bq.quantize_pack(torch.zeros(64, 288, device=DEV), "q8_0")
     with pytest.raises(bq.BQError):  # K % 256 != 0 is not streamed
         bq.StreamPlan("q8_0", [bq.StreamOp(0, P2, torch.zeros(288, device=DEV), y)])
+
+
+def test_unchained_stream_matches_launch_per_op_bitwise():
+    """Independent inputs: the planner finds no dependence and the executor
+    runs without grid-wide barriers; results still match op by op."""
+    qt = "q8_0"
+
+    def packed(M, K, *tag):
+        W = wl.normal_torch((M, K), wl.W_STD, seed=5, stream=wl.stream_id(*tag), device=DEV)
+        return bq.quantize_pack(W, qt)
+
+    layers = [dict(q=packed(512, 512, l, "q"), k=packed(128, 512, l, "k"),
+                   v=packed(128, 512, l, "v"), o=packed(512, 512, l, "o"),
+                   gate=packed(1024, 512, l, "g"), up=packed(1024, 512, l, "u"),
+                   down=packed(512, 1024, l, "d"),
+                   gamma=wl.normal_torch(512, 0.1, seed=5, stream=l, device=DEV, mean=1.0))
+              for l in range(3)]
+    ds = DecodeStream(qt, layers, packed(3000, 512, "lm"), chained=False)
+    ds.inputs.copy_(wl.normal_torch(ds.inputs.numel(), 1.0, seed=5, stream=9, device=DEV))
+    ds.run_per_op()
+    want = snapshot(ds)
+    for op in ds.ops:
+        op.y.fill_(float("nan"))
+    ds.run_plan()
+    for i, (g, w) in enumerate(zip(snapshot(ds), want)):
+        assert torch.equal(g.view(torch.int32), w.view(torch.int32)), f"op {i} differs"
+
+
+def test_plan_rejects_outputs_overlapping_weights_or_own_stage():
+    P = bq.quantize_pack(torch.zeros(64, 512, device=DEV), "q8_0")
+    x = torch.zeros(512, device=DEV)
+    y = torch.zeros(64, device=DEV)
+    # an output written over packed weights (weights are prefetched across stages)
+    wy = P.view(torch.float32).view(-1)[:64]
+    with pytest.raises(bq.BQError):
+        bq.StreamPlan("q8_0", [bq.StreamOp(0, P, x, wy)])
+    # an output that is an input of its own stage
+    y2 = torch.zeros(512, device=DEV)
+    P2 = bq.quantize_pack(torch.zeros(512, 512, device=DEV), "q8_0")
+    with pytest.raises(bq.BQError):
+        bq.StreamPlan("q8_0", [bq.StreamOp(0, P2, x, y2), bq.StreamOp(0, P, y2, y)])
+    # ... which is fine one stage later (the planner inserts a barrier)
+    bq.StreamPlan("q8_0", [bq.StreamOp(0, P2, x, y2), bq.StreamOp(1, P, y2, y)])
