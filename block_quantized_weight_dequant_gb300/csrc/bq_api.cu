@@ -16,6 +16,7 @@
 #include "../../include/bqgemv.h"
 #include "bq_dot.cuh"
 #include "bq_exec.cuh"
+#include "bq_multi.cuh"
 #include "bq_internal.h"
 
 namespace bq {
@@ -39,6 +40,9 @@ struct Tunables {
     int exec_warps = 8;    // stream executor: warps per CTA
     int exec_rowmode_rows = 0;  // stream executor: row mode up to this many rows per warp (0: off)
     int exec_prefetch = 0;      // stream executor: L2 prefetch distance beyond the ring, in items (measured: no gain)
+    int multi = 1;              // independent op lists: multi-op streaming kernel (0: executor)
+    int multi_ng = 2;           // multi-op kernel: consumer groups
+    int multi_stage = 36 * 1024;  // multi-op kernel: bytes per stage
 };
 
 const Tunables &tunables() {
@@ -65,6 +69,9 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "ewarps") && val >= 1 && val <= 8) v.exec_warps = val;
             else if (!std::strcmp(tok, "rowmode") && val >= 0 && val <= 32) v.exec_rowmode_rows = val;
             else if (!std::strcmp(tok, "pf") && val >= 0 && val <= 16) v.exec_prefetch = val;
+            else if (!std::strcmp(tok, "multi") && val >= 0 && val <= 1) v.multi = val;
+            else if (!std::strcmp(tok, "ng") && val >= 1 && val <= 16) v.multi_ng = val;
+            else if (!std::strcmp(tok, "mstage") && val >= 8192) v.multi_stage = val;
         }
         return v;
     }();
@@ -397,6 +404,112 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
     return BQ_OK;
 }
 
+bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo, int *cta_tiles,
+                            MultiGeometry *geo) {
+    const Tunables &t = tunables();
+    const int bb = block_bytes(qtype), ub = 8 * bb;
+    const int NG = (MULTI_NWC % t.multi_ng == 0 && t.multi_ng <= 8) ? t.multi_ng : 1,
+              NWG = MULTI_NWC / NG;
+    const int stage_cap = t.multi_stage;
+    int stage_bytes = 0, maxK = 0;
+    long long tiles = 0;
+    for (int i = 0; i < n_ops; ++i) {
+        const bq_op &o = ops[i];
+        MultiOp &m = mo[i];
+        std::memset(&m, 0, sizeof m);
+        const bool gu = o.kind == BQ_OP_GATE_UP_SILU;
+        m.W[0] = static_cast<const uint8_t *>(o.W);
+        m.W[1] = gu ? static_cast<const uint8_t *>(o.W_up) : nullptr;
+        m.x = o.x;
+        m.gamma = gu ? o.gamma : nullptr;
+        m.eps = o.eps;
+        m.y = o.y;
+        m.nmat = gu ? 2 : 1;
+        m.M = (int)o.M;
+        m.K = (int)o.K;
+        m.nsc = m.K / 256;
+        m.G = tree_lanes_for_units(m.nsc);
+        m.rpw = 32 / m.G;
+        m.TR = NWG * m.rpw;
+        m.rb = m.nsc * ub;
+        // whole rows per stage when they fit, else chunks of a multiple of G units
+        int KCU = m.nsc, stride = 0, single = 0;
+        if ((long long)m.TR * m.rb <= stage_cap) {
+            single = m.G >= 8 || (m.rb / 16) % 8 == m.G % 8;
+            stride = single ? m.rb : padded_stride(m.rb, m.G);
+            if ((long long)m.TR * stride > stage_cap) single = 0, stride = 0;
+        }
+        if (!stride) {
+            for (int k = (m.nsc + m.G - 1) / m.G; k >= 1; --k) {
+                KCU = std::min(m.nsc, m.G * k);
+                stride = padded_stride(KCU * ub, m.G);
+                if ((long long)m.TR * stride <= stage_cap) break;
+            }
+        }
+        m.KCU = KCU;
+        m.row_stride = stride;
+        m.single = single;
+        m.nchunks = (m.nsc + KCU - 1) / KCU;
+        m.ntiles = (m.M + m.TR - 1) / m.TR;
+        m.tile_base = (int)tiles;
+        tiles += m.ntiles;
+        stage_bytes = std::max(stage_bytes, m.TR * stride);
+        maxK = std::max(maxK, m.K);
+    }
+    if (tiles > (1LL << 30)) return BQ_ERR_SHAPE;
+    // shared memory: mbarriers, flags, reduction scratch | x (one op's) | stages
+    const int cap = max_smem_optin();
+    const int x_off = 2048;
+    const int stage_off = (x_off + maxK * 4 + 127) / 128 * 128;
+    // slots: a multiple of NG, at least 2 per group, at most 16
+    const int NS = std::min(16, (cap - stage_off) / std::max(stage_bytes, 1)) / NG * NG;
+    if (NS < 2 * NG) return BQ_ERR_SHAPE;
+    const size_t smem = (size_t)stage_off + (size_t)NS * stage_bytes;
+    const int threads = (MULTI_NWC + 1) * 32;
+    int occ = 0;
+    const int err = qtype == BQ_Q8_0 ? bq_internal_multi_occupancy_q8_0(threads, smem, &occ)
+                                     : bq_internal_multi_occupancy_q4_0(threads, smem, &occ);
+    if (err != 0 || occ < 1) return BQ_ERR_CUDA;
+    const int grid = std::min(MULTI_MAX_CTAS, num_sms_current() * occ);
+    // byte-balanced contiguous tile ranges
+    long long total = 0;
+    for (int i = 0; i < n_ops; ++i)
+        for (int k = 0; k < mo[i].ntiles; ++k)
+            total += (long long)std::min(mo[i].TR, mo[i].M - k * mo[i].TR) * mo[i].rb * mo[i].nmat;
+    cta_tiles[0] = 0;
+    int c = 1;
+    long long acc = 0;
+    for (int i = 0; i < n_ops && c < grid; ++i)
+        for (int k = 0; k < mo[i].ntiles && c < grid; ++k) {
+            acc += (long long)std::min(mo[i].TR, mo[i].M - k * mo[i].TR) * mo[i].rb * mo[i].nmat;
+            while (c < grid && acc * grid >= total * c) cta_tiles[c++] = mo[i].tile_base + k + 1;
+        }
+    while (c <= grid) cta_tiles[c++] = (int)tiles;
+    geo->grid = grid;
+    geo->threads = threads;
+    geo->NS = NS;
+    geo->stage_bytes = stage_bytes;
+    geo->NG = NG;
+    geo->x_off = x_off;
+    geo->stage_off = stage_off;
+    geo->smem = smem;
+    return BQ_OK;
+}
+
+bool tunables_multi() { return tunables().multi != 0; }
+
+void fill_multi_args(const MultiGeometry &geo, int n_ops, const MultiOp *ops,
+                     const int *cta_tiles, MultiArgs *a) {
+    a->ops = ops;
+    a->cta_tiles = cta_tiles;
+    a->nops = n_ops;
+    a->NS = geo.NS;
+    a->stage_bytes = geo.stage_bytes;
+    a->NG = geo.NG;
+    a->x_off = geo.x_off;
+    a->stage_off = geo.stage_off;
+}
+
 void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const ExecX *xs,
                     const ExecStage *stages, unsigned int *counters, ExecArgs *a) {
     a->ops = ops;
@@ -422,9 +535,11 @@ void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const
 // the opaque plan handle of include/bqgemv.h
 struct bq_stream_plan {
     int qtype, n_ops, n_stages, device;
+    int multi;  // 1: independent ops, multi-op streaming kernel; 0: stream executor
     int grid, threads;
     size_t smem;
     bq::ExecArgs args;
+    bq::MultiArgs margs;
     unsigned int *counters;
 };
 
@@ -536,9 +651,13 @@ static int64_t align256(int64_t v) { return (v + 255) / 256 * 256; }
 
 int64_t bq_stream_workspace_bytes(int n_ops, int n_stages) {
     if (n_ops < 1 || n_stages < 1 || n_stages > n_ops) return -1;
-    return align256((int64_t)n_ops * sizeof(bq::ExecOp)) +
-           align256((int64_t)n_ops * sizeof(bq::ExecX)) +
-           align256((int64_t)n_stages * sizeof(bq::ExecStage)) + align256((int64_t)n_stages * 4);
+    const int64_t exec = align256((int64_t)n_ops * sizeof(bq::ExecOp)) +
+                         align256((int64_t)n_ops * sizeof(bq::ExecX)) +
+                         align256((int64_t)n_stages * sizeof(bq::ExecStage)) +
+                         align256((int64_t)n_stages * 4);
+    const int64_t multi = align256((int64_t)n_ops * sizeof(bq::MultiOp)) +
+                          align256((int64_t)(bq::MULTI_MAX_CTAS + 1) * 4);
+    return std::max(exec, multi);
 }
 
 bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *workspace,
@@ -559,6 +678,38 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
     const int64_t need = bq_stream_workspace_bytes(n_ops, n_stages);
     if (workspace_bytes < need) return BQ_ERR_SHAPE;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    bool independent = bq::tunables().multi != 0;
+    for (int s = 0; s < n_stages; ++s) independent &= !es[(size_t)s].barrier;
+    if (independent) {
+        std::vector<bq::MultiOp> mo((size_t)n_ops);
+        std::vector<int> ct(bq::MULTI_MAX_CTAS + 1);
+        bq::MultiGeometry mg;
+        const bq_status ms = bq::plan_multi_tables(qtype, ops, n_ops, mo.data(), ct.data(), &mg);
+        if (ms == BQ_OK) {
+            const int64_t off_ct = align256((int64_t)n_ops * sizeof(bq::MultiOp));
+            if (cudaMemcpy(ws, mo.data(), (size_t)n_ops * sizeof(bq::MultiOp),
+                           cudaMemcpyHostToDevice) != cudaSuccess ||
+                cudaMemcpy(ws + off_ct, ct.data(), (size_t)(mg.grid + 1) * sizeof(int),
+                           cudaMemcpyHostToDevice) != cudaSuccess)
+                return BQ_ERR_CUDA;
+            auto *p = new (std::nothrow) bq_stream_plan;
+            if (!p) return BQ_ERR_CUDA;
+            std::memset(p, 0, sizeof *p);
+            p->qtype = qtype;
+            p->n_ops = n_ops;
+            p->n_stages = n_stages;
+            p->multi = 1;
+            cudaGetDevice(&p->device);
+            p->grid = mg.grid;
+            p->threads = mg.threads;
+            p->smem = mg.smem;
+            bq::fill_multi_args(mg, n_ops, reinterpret_cast<const bq::MultiOp *>(ws),
+                                reinterpret_cast<const int *>(ws + off_ct), &p->margs);
+            *plan = p;
+            return BQ_OK;
+        }
+        // a list the multi-op kernel cannot hold falls back to the executor
+    }
     const int64_t off_x = align256((int64_t)n_ops * sizeof(bq::ExecOp));
     const int64_t off_st = off_x + align256((int64_t)n_ops * sizeof(bq::ExecX));
     const int64_t off_cnt = off_st + align256((int64_t)n_stages * sizeof(bq::ExecStage));
@@ -571,9 +722,11 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
         return BQ_ERR_CUDA;
     auto *p = new (std::nothrow) bq_stream_plan;
     if (!p) return BQ_ERR_CUDA;
+    std::memset(p, 0, sizeof *p);
     p->qtype = qtype;
     p->n_ops = n_ops;
     p->n_stages = n_stages;
+    p->multi = 0;
     cudaGetDevice(&p->device);
     p->grid = geo.grid;
     p->threads = geo.threads;
@@ -588,6 +741,14 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
 
 bq_status bq_stream_plan_launch(const bq_stream_plan *plan, void *stream) {
     if (!plan) return BQ_ERR_NULL;
+    if (plan->multi) {
+        const int e = plan->qtype == BQ_Q8_0
+                          ? bq_internal_multi_launch_q8_0(plan->margs, plan->grid, plan->threads,
+                                                          plan->smem, stream)
+                          : bq_internal_multi_launch_q4_0(plan->margs, plan->grid, plan->threads,
+                                                          plan->smem, stream);
+        return from_cuda(e);
+    }
     auto s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(plan->counters, 0, (size_t)plan->n_stages * 4, s) != cudaSuccess)
         return BQ_ERR_CUDA;

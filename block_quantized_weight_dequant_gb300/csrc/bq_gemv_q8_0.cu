@@ -2,6 +2,7 @@
 // translation unit per format so the two compile in parallel) and this
 // unit's device-side error word.
 #include "bq_exec.cuh"
+#include "bq_multi.cuh"
 #include "bq_kernels.cuh"
 
 namespace {
@@ -67,4 +68,20 @@ int bq_internal_status_q8_0(unsigned int *flags, int clear) {
         e = cudaMemcpyToSymbol(g_status_q8_0, &zero, sizeof(unsigned int));
     }
     return (int)e;
+}
+
+int bq_internal_multi_occupancy_q8_0(int threads, size_t smem, int *occ) {
+    auto kern = bq::multi_kernel<bq::QT_Q8_0>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kern, threads, smem);
+}
+
+int bq_internal_multi_launch_q8_0(const bq::MultiArgs &a, int grid, int threads, size_t smem,
+                                void *stream) {
+    unsigned int *status = nullptr;
+    cudaError_t e = status_addr(&status);
+    if (e != cudaSuccess) return (int)e;
+    bq::multi_kernel<bq::QT_Q8_0><<<grid, threads, smem, static_cast<cudaStream_t>(stream)>>>(a, status);
+    return (int)cudaGetLastError();
 }

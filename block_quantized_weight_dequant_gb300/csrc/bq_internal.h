@@ -81,7 +81,32 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
 // kernel arguments for planned tables at the given device addresses
 void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const ExecX *xs,
                     const ExecStage *stages, unsigned int *counters, ExecArgs *a);
+
+struct MultiOp;
+struct MultiArgs;
+constexpr int MULTI_MAX_CTAS = 1024;
+// launch geometry of a multi-op (independent GEMVs) run
+struct MultiGeometry {
+    int grid, threads, NS, stage_bytes, NG, x_off, stage_off;
+    size_t smem;
+};
+// Plan a list of ops none of which depends on another (validated by
+// plan_exec_tables) for the multi-op streaming kernel: per-op tiles and a
+// byte-balanced contiguous tile range per CTA (cta_tiles: room for
+// MULTI_MAX_CTAS + 1 entries).  Touches no device memory.
+bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo, int *cta_tiles,
+                            MultiGeometry *geo);
+void fill_multi_args(const MultiGeometry &geo, int n_ops, const MultiOp *ops,
+                     const int *cta_tiles, MultiArgs *a);
+// whether independent op lists use the multi-op kernel (tuning switch)
+bool tunables_multi();
 }
+int bq_internal_multi_occupancy_q8_0(int threads, size_t smem, int *occ);
+int bq_internal_multi_occupancy_q4_0(int threads, size_t smem, int *occ);
+int bq_internal_multi_launch_q8_0(const bq::MultiArgs &a, int grid, int threads, size_t smem,
+                                  void *stream);
+int bq_internal_multi_launch_q4_0(const bq::MultiArgs &a, int grid, int threads, size_t smem,
+                                  void *stream);
 // persistent per-token stream executor (bq_exec.cuh), one instantiation per format
 int bq_internal_exec_occupancy_q8_0(int threads, size_t smem, int *occ);
 int bq_internal_exec_occupancy_q4_0(int threads, size_t smem, int *occ);

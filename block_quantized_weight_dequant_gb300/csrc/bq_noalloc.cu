@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "bq_exec.cuh"
+#include "bq_multi.cuh"
 #include "bq_internal.h"
 
 namespace {
@@ -31,6 +32,10 @@ constexpr size_t SCRATCH_BYTES = OFF_CNT + al256((size_t)MAX_OPS * sizeof(unsign
 // device address fetched by scratch_address().
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SCRATCH_BYTES];
 static_assert(SCRATCH_BYTES == 66 * 1024, "the documented size of the scratch array");
+// the same array holds the multi-op kernel's tables for independent op lists
+constexpr size_t OFF_CT = al256((size_t)MAX_OPS * sizeof(bq::MultiOp));
+static_assert(OFF_CT + (bq::MULTI_MAX_CTAS + 1) * sizeof(int) <= SCRATCH_BYTES,
+              "multi-op tables fit the scratch array");
 
 std::atomic<unsigned char *> g_scratch_addr[64];
 
@@ -56,6 +61,8 @@ std::mutex g_host_mutex;
 bq::ExecOp g_eo[MAX_OPS];
 bq::ExecX g_ex[MAX_OPS];
 bq::ExecStage g_es[MAX_OPS];
+bq::MultiOp g_mo[MAX_OPS];
+int g_ct[bq::MULTI_MAX_CTAS + 1];
 
 }  // namespace
 
@@ -70,6 +77,24 @@ extern "C" bq_status bq_stream_run_noalloc(int qtype, const bq_op *ops, int n_op
     bq::ExecGeometry geo;
     const bq_status st = bq::plan_exec_tables(qtype, ops, n_ops, g_eo, g_ex, g_es, &geo);
     if (st != BQ_OK) return st;
+    // independent ops run on the multi-op streaming kernel, as in a plan
+    bool independent = bq::tunables_multi();
+    for (int i = 0; i < geo.n_stages; ++i) independent &= !g_es[i].barrier;
+    bq::MultiGeometry mg;
+    if (independent && bq::plan_multi_tables(qtype, ops, n_ops, g_mo, g_ct, &mg) == BQ_OK) {
+        if (cudaMemcpyAsync(scratch, g_mo, (size_t)n_ops * sizeof(bq::MultiOp),
+                            cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(scratch + OFF_CT, g_ct, (size_t)(mg.grid + 1) * sizeof(int),
+                            cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return BQ_ERR_CUDA;
+        bq::MultiArgs ma;
+        bq::fill_multi_args(mg, n_ops, reinterpret_cast<const bq::MultiOp *>(scratch),
+                            reinterpret_cast<const int *>(scratch + OFF_CT), &ma);
+        const int e = qtype == BQ_Q8_0
+                          ? bq_internal_multi_launch_q8_0(ma, mg.grid, mg.threads, mg.smem, stream)
+                          : bq_internal_multi_launch_q4_0(ma, mg.grid, mg.threads, mg.smem, stream);
+        return e == 0 ? BQ_OK : BQ_ERR_CUDA;
+    }
     // the copies read the host tables before returning (pageable source), so
     // the static arrays are free again once the lock is released
     if (cudaMemcpyAsync(scratch, g_eo, (size_t)n_ops * sizeof(bq::ExecOp), cudaMemcpyHostToDevice,

@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab, seed=0):
+def make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab, seed=0, chained=True):
     def packed(M, K, *tag):
         W = wl.normal_torch((M, K), wl.W_STD, seed=seed, stream=wl.stream_id(*tag), device=DEV)
         return bq.quantize_pack(W, qt)
@@ -31,8 +31,8 @@ def make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab, seed=0):
             down=packed(hidden, inter, l, "d"),
             gamma=wl.normal_torch(hidden, 0.1, seed=seed, stream=wl.stream_id(l, "gm"),
                                   device=DEV, mean=1.0)))
-    ds = DecodeStream(qt, layers, packed(vocab, hidden, "lm"))
-    ds.x0.copy_(wl.normal_torch(hidden, 1.0, seed=seed, stream=7, device=DEV))
+    ds = DecodeStream(qt, layers, packed(vocab, hidden, "lm"), chained=chained)
+    ds.inputs.copy_(wl.normal_torch(ds.inputs.numel(), 1.0, seed=seed, stream=7, device=DEV))
     return ds
 
 
@@ -48,9 +48,13 @@ STREAMS = [
 ]
 
 
+@pytest.mark.parametrize("chained", [True, False], ids=["chained", "independent"])
 @pytest.mark.parametrize("qt,n_layers,hidden,q_dim,kv_dim,inter,vocab", STREAMS)
-def test_plan_matches_launch_per_op_bitwise(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab):
-    ds = make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab)
+def test_plan_matches_launch_per_op_bitwise(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab,
+                                            chained):
+    """chained: the stream executor with grid-wide stage barriers; independent:
+    the multi-op streaming kernel (the planner finds no dependence)."""
+    ds = make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab, chained=chained)
     ds.run_per_op()
     want = snapshot(ds)
     for op in ds.ops:
