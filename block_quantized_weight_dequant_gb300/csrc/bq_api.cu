@@ -41,8 +41,8 @@ struct Tunables {
     int exec_rowmode_rows = 0;  // stream executor: row mode up to this many rows per warp (0: off)
     int exec_prefetch = 0;      // stream executor: L2 prefetch distance beyond the ring, in items (measured: no gain)
     int multi = 1;              // independent op lists: multi-op streaming kernel (0: executor)
-    int multi_ng = 2;           // multi-op kernel: consumer groups
-    int multi_stage = 36 * 1024;  // multi-op kernel: bytes per stage
+    int multi_warps = 0;        // multi-op kernel: warps per CTA (0: as many as fit, <= 16)
+    int multi_d = 2;            // multi-op kernel: ring slots per warp
 };
 
 const Tunables &tunables() {
@@ -70,8 +70,8 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "rowmode") && val >= 0 && val <= 32) v.exec_rowmode_rows = val;
             else if (!std::strcmp(tok, "pf") && val >= 0 && val <= 16) v.exec_prefetch = val;
             else if (!std::strcmp(tok, "multi") && val >= 0 && val <= 1) v.multi = val;
-            else if (!std::strcmp(tok, "ng") && val >= 1 && val <= 16) v.multi_ng = val;
-            else if (!std::strcmp(tok, "mstage") && val >= 8192) v.multi_stage = val;
+            else if (!std::strcmp(tok, "mw") && val >= 1 && val <= 16) v.multi_warps = val;
+            else if (!std::strcmp(tok, "md") && val >= 2 && val <= 4) v.multi_d = val;
         }
         return v;
     }();
@@ -408,10 +408,9 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
                             MultiGeometry *geo) {
     const Tunables &t = tunables();
     const int bb = block_bytes(qtype), ub = 8 * bb;
-    const int NG = (MULTI_NWC % t.multi_ng == 0 && t.multi_ng <= 8) ? t.multi_ng : 1,
-              NWG = MULTI_NWC / NG;
-    const int stage_cap = t.multi_stage;
-    int stage_bytes = 0, maxK = 0;
+    const int D = std::min(t.multi_d, MULTI_MAX_D);
+    // pass 1: per-op tiling that does not depend on the slot size
+    int maxK = 0, slot_min = 0;
     long long tiles = 0;
     for (int i = 0; i < n_ops; ++i) {
         const bq_op &o = ops[i];
@@ -430,42 +429,55 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
         m.nsc = m.K / 256;
         m.G = tree_lanes_for_units(m.nsc);
         m.rpw = 32 / m.G;
-        m.TR = NWG * m.rpw;
         m.rb = m.nsc * ub;
-        // whole rows per stage when they fit, else chunks of a multiple of G units
+        m.ntiles = (m.M + m.rpw - 1) / m.rpw;
+        m.tile_base = (int)tiles;
+        tiles += m.ntiles;
+        maxK = std::max(maxK, m.K);
+        // the smallest item: one unit per lane
+        const int k1 = std::min(m.nsc, m.G);
+        slot_min = std::max(slot_min, m.rpw * padded_stride(k1 * ub, m.G));
+    }
+    if (tiles > (1LL << 30)) return BQ_ERR_SHAPE;
+    // shared memory: header | x (one op's) | nwarps rings of D slots
+    const int cap = max_smem_optin();
+    const int x_off = MULTI_X_OFF;
+    const int ring_off = (x_off + maxK * 4 + 127) / 128 * 128;
+    const long long budget = (long long)cap - ring_off;
+    if (budget < (long long)D * slot_min) return BQ_ERR_SHAPE;
+    int nwarps = (int)std::min<long long>(MULTI_MAX_WARPS, budget / ((long long)D * slot_min));
+    if (t.multi_warps) nwarps = std::min(nwarps, t.multi_warps);
+    const int slot_cap = (int)(budget / ((long long)nwarps * D)) / 128 * 128;
+    // pass 2: per op, whole rows in a slot when they fit, else the largest
+    // chunk of a multiple of G units
+    int slot_bytes = 0;
+    for (int i = 0; i < n_ops; ++i) {
+        MultiOp &m = mo[i];
         int KCU = m.nsc, stride = 0, single = 0;
-        if ((long long)m.TR * m.rb <= stage_cap) {
+        if ((long long)m.rpw * m.rb <= slot_cap) {
             single = m.G >= 8 || (m.rb / 16) % 8 == m.G % 8;
             stride = single ? m.rb : padded_stride(m.rb, m.G);
-            if ((long long)m.TR * stride > stage_cap) single = 0, stride = 0;
+            if ((long long)m.rpw * stride > slot_cap) single = 0, stride = 0;
         }
         if (!stride) {
+            single = 0;
             for (int k = (m.nsc + m.G - 1) / m.G; k >= 1; --k) {
                 KCU = std::min(m.nsc, m.G * k);
                 stride = padded_stride(KCU * ub, m.G);
-                if ((long long)m.TR * stride <= stage_cap) break;
+                if ((long long)m.rpw * stride <= slot_cap) break;
             }
+            if ((long long)m.rpw * stride > slot_cap) return BQ_ERR_SHAPE;
         }
         m.KCU = KCU;
         m.row_stride = stride;
         m.single = single;
         m.nchunks = (m.nsc + KCU - 1) / KCU;
-        m.ntiles = (m.M + m.TR - 1) / m.TR;
-        m.tile_base = (int)tiles;
-        tiles += m.ntiles;
-        stage_bytes = std::max(stage_bytes, m.TR * stride);
-        maxK = std::max(maxK, m.K);
+        slot_bytes = std::max(slot_bytes, m.rpw * stride);
     }
-    if (tiles > (1LL << 30)) return BQ_ERR_SHAPE;
-    // shared memory: mbarriers, flags, reduction scratch | x (one op's) | stages
-    const int cap = max_smem_optin();
-    const int x_off = 2048;
-    const int stage_off = (x_off + maxK * 4 + 127) / 128 * 128;
-    // slots: a multiple of NG, at least 2 per group, at most 16
-    const int NS = std::min(16, (cap - stage_off) / std::max(stage_bytes, 1)) / NG * NG;
-    if (NS < 2 * NG) return BQ_ERR_SHAPE;
-    const size_t smem = (size_t)stage_off + (size_t)NS * stage_bytes;
-    const int threads = (MULTI_NWC + 1) * 32;
+    slot_bytes = (slot_bytes + 127) / 128 * 128;
+    const size_t smem = (size_t)ring_off + (size_t)nwarps * D * slot_bytes;
+    if (smem > (size_t)cap) return BQ_ERR_SHAPE;
+    const int threads = nwarps * 32;
     int occ = 0;
     const int err = qtype == BQ_Q8_0 ? bq_internal_multi_occupancy_q8_0(threads, smem, &occ)
                                      : bq_internal_multi_occupancy_q4_0(threads, smem, &occ);
@@ -475,23 +487,23 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
     long long total = 0;
     for (int i = 0; i < n_ops; ++i)
         for (int k = 0; k < mo[i].ntiles; ++k)
-            total += (long long)std::min(mo[i].TR, mo[i].M - k * mo[i].TR) * mo[i].rb * mo[i].nmat;
+            total += (long long)std::min(mo[i].rpw, mo[i].M - k * mo[i].rpw) * mo[i].rb * mo[i].nmat;
     cta_tiles[0] = 0;
     int c = 1;
     long long acc = 0;
     for (int i = 0; i < n_ops && c < grid; ++i)
         for (int k = 0; k < mo[i].ntiles && c < grid; ++k) {
-            acc += (long long)std::min(mo[i].TR, mo[i].M - k * mo[i].TR) * mo[i].rb * mo[i].nmat;
+            acc += (long long)std::min(mo[i].rpw, mo[i].M - k * mo[i].rpw) * mo[i].rb * mo[i].nmat;
             while (c < grid && acc * grid >= total * c) cta_tiles[c++] = mo[i].tile_base + k + 1;
         }
     while (c <= grid) cta_tiles[c++] = (int)tiles;
     geo->grid = grid;
     geo->threads = threads;
-    geo->NS = NS;
-    geo->stage_bytes = stage_bytes;
-    geo->NG = NG;
+    geo->nwarps = nwarps;
+    geo->D = D;
+    geo->slot_bytes = slot_bytes;
     geo->x_off = x_off;
-    geo->stage_off = stage_off;
+    geo->ring_off = ring_off;
     geo->smem = smem;
     return BQ_OK;
 }
@@ -503,11 +515,11 @@ void fill_multi_args(const MultiGeometry &geo, int n_ops, const MultiOp *ops,
     a->ops = ops;
     a->cta_tiles = cta_tiles;
     a->nops = n_ops;
-    a->NS = geo.NS;
-    a->stage_bytes = geo.stage_bytes;
-    a->NG = geo.NG;
+    a->nwarps = geo.nwarps;
+    a->D = geo.D;
+    a->slot_bytes = geo.slot_bytes;
     a->x_off = geo.x_off;
-    a->stage_off = geo.stage_off;
+    a->ring_off = geo.ring_off;
 }
 
 void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const ExecX *xs,

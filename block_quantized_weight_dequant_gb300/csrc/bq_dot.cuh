@@ -53,11 +53,14 @@ __device__ __forceinline__ float q8_raw(uint32_t word, int pos) {
     const uint32_t flipped = word ^ 0x80808080u;
     return __uint_as_float(__byte_perm(flipped, 0x4B000000u, 0x7540u | (uint32_t)pos));
 }
-// Q4_0: the nibble at bit `shift` in the low mantissa of 2^23: the float
-// 2^23 + n, from which subtracting 2^23 + 8 leaves n - 8 exactly.
+// Q4_0: the nibbles of a word are masked into bytes once (low nibbles, or
+// high nibbles shifted down), and the byte at `pos` goes into the low
+// mantissa of 2^23: the float 2^23 + n, from which subtracting 2^23 + 8
+// leaves n - 8 exactly.
 constexpr float Q4_MAGIC = 8388616.0f;  // 2^23 + 8
-__device__ __forceinline__ float q4_raw(uint32_t word, int shift) {
-    return __uint_as_float(((word >> shift) & 0xFu) | 0x4B000000u);
+__device__ __forceinline__ float q4_raw(uint32_t word, bool high, int pos) {
+    const uint32_t nib = (high ? word >> 4 : word) & 0x0F0F0F0Fu;
+    return __uint_as_float(__byte_perm(nib, 0x4B000000u, 0x7540u | (uint32_t)pos));
 }
 
 __device__ __forceinline__ float scale_at(const uint32_t *w, int byte_off) {
@@ -66,7 +69,9 @@ __device__ __forceinline__ float scale_at(const uint32_t *w, int byte_off) {
 }
 
 // ---------------------------------------------------------------------------
-// x sources: element e (a multiple of 4) of input row r, as a float4
+// x sources.  xs.at(e0) returns a view of the x elements from e0 on;
+// view.get(r, B, t) is the float4 of elements e0 + 32B + 4t .. +3 of input
+// row r.  Either e0 is a multiple of 256 (a unit), or only B = 0 is read.
 // ---------------------------------------------------------------------------
 // x staged in shared memory with its 16-byte chunks permuted within each
 // 128-byte line: chunk c (elements 4c..4c+3) sits at chunk position
@@ -80,8 +85,27 @@ __host__ __device__ constexpr int x_pos(int e) { return 4 * x_chunk_pos(e >> 2) 
 struct XSmem {
     const float *base;
     int rstride;  // floats between rows
-    __device__ __forceinline__ float4 get(int r, int e) const {
-        return *reinterpret_cast<const float4 *>(base + r * rstride + 4 * x_chunk_pos(e >> 2));
+    // Step t of block B of the view sits at p[t ^ B] + 32 B floats: with
+    // c0 = e0 / 4 (a multiple of 8) the chunk of (B, t) is at position
+    // c0 + 8B + (t ^ B ^ key), key = (c0 >> 3 ^ c0 >> 6) & 7, when e0 is a
+    // multiple of 256 (then c0 >> 3 has zero low bits) or B = 0.  The eight
+    // pointers are formed once per view, so each load is a register plus an
+    // immediate offset.
+    struct View {
+        const float *p[8];
+        int rstride;
+        __device__ __forceinline__ float4 get(int r, int B, int t) const {
+            return *reinterpret_cast<const float4 *>(p[(t ^ B) & 7] + r * rstride + 32 * B);
+        }
+    };
+    __device__ __forceinline__ View at(int e0) const {
+        const int c0 = e0 >> 2;
+        const int k0 = 4 * (c0 ^ (((c0 >> 3) ^ (c0 >> 6)) & 7));
+        View v;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v.p[j] = base + (k0 ^ (4 * j));
+        v.rstride = rstride;
+        return v;
     }
 };
 // floats of shared memory one staged x of K elements takes (K rounded up to 128 B)
@@ -91,9 +115,14 @@ __host__ __device__ constexpr int x_padded_floats(int K) { return (K + 31) / 32 
 struct XGlobal {
     const float *x;
     int K;
-    __device__ __forceinline__ float4 get(int r, int e) const {
-        return __ldg(reinterpret_cast<const float4 *>(x + (size_t)r * K + e));
-    }
+    struct View {
+        const float *p;
+        int K;
+        __device__ __forceinline__ float4 get(int r, int B, int t) const {
+            return __ldg(reinterpret_cast<const float4 *>(p + (size_t)r * K + 32 * B + 4 * t));
+        }
+    };
+    __device__ __forceinline__ View at(int e0) const { return View{x + e0, K}; }
 };
 
 // RMSNorm applied while reading: xn = (x * rs) * gamma, rs from rms_scale()
@@ -101,12 +130,18 @@ struct XGlobalNorm {
     const float *x;
     const float *gamma;
     float rs;
-    __device__ __forceinline__ float4 get(int, int e) const {
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(x + e));
-        const float4 g = __ldg(reinterpret_cast<const float4 *>(gamma + e));
-        return make_float4(__fmul_rn(__fmul_rn(v.x, rs), g.x), __fmul_rn(__fmul_rn(v.y, rs), g.y),
-                           __fmul_rn(__fmul_rn(v.z, rs), g.z), __fmul_rn(__fmul_rn(v.w, rs), g.w));
-    }
+    struct View {
+        const float *x, *gamma;
+        float rs;
+        __device__ __forceinline__ float4 get(int, int B, int t) const {
+            const int e = 32 * B + 4 * t;
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(x + e));
+            const float4 g = __ldg(reinterpret_cast<const float4 *>(gamma + e));
+            return make_float4(__fmul_rn(__fmul_rn(v.x, rs), g.x), __fmul_rn(__fmul_rn(v.y, rs), g.y),
+                               __fmul_rn(__fmul_rn(v.z, rs), g.z), __fmul_rn(__fmul_rn(v.w, rs), g.w));
+        }
+    };
+    __device__ __forceinline__ View at(int e0) const { return View{x + e0, gamma + e0, rs}; }
 };
 
 __device__ __forceinline__ float f4(const float4 &v, int i) {
@@ -128,18 +163,56 @@ __device__ __forceinline__ float raw_at(const uint32_t *w, int B, int j) {
         return q8_raw(w[byte >> 2], byte & 3);
     } else {
         const int byte = bb * B + 2 + (j & 15);
-        return q4_raw(w[byte >> 2], 8 * (byte & 3) + (j >= 16 ? 4 : 0));
+        return q4_raw(w[byte >> 2], j >= 16, byte & 3);
     }
 }
 
 // The block's scale d and code-x sums s[v][r] = (a_0 + a_1) + (a_2 + a_3),
-// a_i the in-order FMA chain over t of q[4t+i] * x[4t+i].  (Packed fp32x2
-// FMAs give the same bits but measured slower here, so the scalar form stays.)
-template <int QT, int NW, int R, int B, class XS>
-__device__ __forceinline__ void block_sum(const uint32_t *const (&w)[NW], const XS &xs, int e0,
+// a_i the in-order FMA chain over t of q[4t+i] * x[4t+i].  With BQ_F32X2 the
+// chains run in pairs (a_0, a_1) and (a_2, a_3) on packed fp32x2 FMAs: each
+// half is an IEEE fp32 fma with round-to-nearest, so the bits are the same.
+#ifndef BQ_F32X2
+#define BQ_F32X2 1
+#endif
+template <int QT, int NW, int R, int B, class XV>
+__device__ __forceinline__ void block_sum(const uint32_t *const (&w)[NW], const XV &xv_,
                                           float (&s)[NW][R], float (&d)[NW]) {
     constexpr int bb = Fmt<QT>::block_bytes;
     constexpr float M = QT == QT_Q8_0 ? Q8_MAGIC : Q4_MAGIC;
+#if BQ_F32X2
+    const float2 mneg = make_float2(-M, -M);
+    float2 a[NW][R][2];
+#pragma unroll
+    for (int v = 0; v < NW; ++v)
+#pragma unroll
+        for (int r = 0; r < R; ++r) a[v][r][0] = a[v][r][1] = make_float2(-0.0f, -0.0f);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        float4 xv[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) xv[r] = xv_.get(r, B, t);
+#pragma unroll
+        for (int v = 0; v < NW; ++v) {
+            const float2 q01 = __fadd2_rn(
+                make_float2(raw_at<QT>(w[v], B, 4 * t), raw_at<QT>(w[v], B, 4 * t + 1)), mneg);
+            const float2 q23 = __fadd2_rn(
+                make_float2(raw_at<QT>(w[v], B, 4 * t + 2), raw_at<QT>(w[v], B, 4 * t + 3)), mneg);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                a[v][r][0] = __ffma2_rn(q01, make_float2(xv[r].x, xv[r].y), a[v][r][0]);
+                a[v][r][1] = __ffma2_rn(q23, make_float2(xv[r].z, xv[r].w), a[v][r][1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < NW; ++v) {
+        d[v] = scale_at(w[v], bb * B);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            s[v][r] = __fadd_rn(__fadd_rn(a[v][r][0].x, a[v][r][0].y),
+                                __fadd_rn(a[v][r][1].x, a[v][r][1].y));
+    }
+#else
     float a[NW][R][4];
 #pragma unroll
     for (int v = 0; v < NW; ++v)
@@ -151,7 +224,7 @@ __device__ __forceinline__ void block_sum(const uint32_t *const (&w)[NW], const 
     for (int t = 0; t < 8; ++t) {
         float4 xv[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) xv[r] = xs.get(r, e0 + 32 * B + 4 * t);
+        for (int r = 0; r < R; ++r) xv[r] = xv_.get(r, B, t);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
 #pragma unroll
@@ -169,13 +242,14 @@ __device__ __forceinline__ void block_sum(const uint32_t *const (&w)[NW], const 
         for (int r = 0; r < R; ++r)
             s[v][r] = __fadd_rn(__fadd_rn(a[v][r][0], a[v][r][1]), __fadd_rn(a[v][r][2], a[v][r][3]));
     }
+#endif
 }
 
-template <int QT, int NW, int R, int B, class XS>
-__device__ __forceinline__ void block_dot(const uint32_t *const (&w)[NW], const XS &xs, int e0,
+template <int QT, int NW, int R, int B, class XV>
+__device__ __forceinline__ void block_dot(const uint32_t *const (&w)[NW], const XV &xv,
                                           float (&c)[NW][R]) {
     float s[NW][R], d[NW];
-    block_sum<QT, NW, R, B>(w, xs, e0, s, d);
+    block_sum<QT, NW, R, B>(w, xv, s, d);
 #pragma unroll
     for (int v = 0; v < NW; ++v)
 #pragma unroll
@@ -191,14 +265,15 @@ __device__ __forceinline__ void unit_dot(const uint32_t *const (&w)[NW], int nbk
     for (int v = 0; v < NW; ++v)
 #pragma unroll
         for (int r = 0; r < R; ++r) c[v][r] = -0.0f;
-    block_dot<QT, NW, R, 0>(w, xs, e0, c);
-    if (nbk > 1) block_dot<QT, NW, R, 1>(w, xs, e0, c);
-    if (nbk > 2) block_dot<QT, NW, R, 2>(w, xs, e0, c);
-    if (nbk > 3) block_dot<QT, NW, R, 3>(w, xs, e0, c);
-    if (nbk > 4) block_dot<QT, NW, R, 4>(w, xs, e0, c);
-    if (nbk > 5) block_dot<QT, NW, R, 5>(w, xs, e0, c);
-    if (nbk > 6) block_dot<QT, NW, R, 6>(w, xs, e0, c);
-    if (nbk > 7) block_dot<QT, NW, R, 7>(w, xs, e0, c);
+    const auto xv = xs.at(e0);
+    block_dot<QT, NW, R, 0>(w, xv, c);
+    if (nbk > 1) block_dot<QT, NW, R, 1>(w, xv, c);
+    if (nbk > 2) block_dot<QT, NW, R, 2>(w, xv, c);
+    if (nbk > 3) block_dot<QT, NW, R, 3>(w, xv, c);
+    if (nbk > 4) block_dot<QT, NW, R, 4>(w, xv, c);
+    if (nbk > 5) block_dot<QT, NW, R, 5>(w, xv, c);
+    if (nbk > 6) block_dot<QT, NW, R, 6>(w, xv, c);
+    if (nbk > 7) block_dot<QT, NW, R, 7>(w, xv, c);
 }
 
 // load a full unit from shared memory (16-byte aligned)
@@ -275,7 +350,7 @@ __device__ __forceinline__ float row_dot_blockpar(const uint8_t *rowp, int nsc, 
             uint32_t w[(BB + 3) / 4];
             load_block_realigned<QT>(w, rowp + u * UB + b * BB);
             const uint32_t *const ws[1] = {w};
-            block_sum<QT, 1, 1, 0>(ws, xs, 256 * u + 32 * b, s, d);
+            block_sum<QT, 1, 1, 0>(ws, xs.at(256 * u + 32 * b), s, d);
         }
         float c = -0.0f;
 #pragma unroll

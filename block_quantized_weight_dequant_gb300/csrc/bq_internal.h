@@ -87,7 +87,7 @@ struct MultiArgs;
 constexpr int MULTI_MAX_CTAS = 1024;
 // launch geometry of a multi-op (independent GEMVs) run
 struct MultiGeometry {
-    int grid, threads, NS, stage_bytes, NG, x_off, stage_off;
+    int grid, threads, nwarps, D, slot_bytes, x_off, ring_off;
     size_t smem;
 };
 // Plan a list of ops none of which depends on another (validated by

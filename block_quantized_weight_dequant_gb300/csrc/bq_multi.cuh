@@ -1,22 +1,18 @@
 // bq_multi.cuh -- one launch for a list of INDEPENDENT GEMVs (a per-token
 // weight stream whose ops read no output of another op of the list).
 //
-// Without dependences there is no reason to spread every op over every SM:
-// the tiles of all ops are concatenated in list order and each CTA streams a
-// contiguous, byte-balanced range of them, so a CTA meets only the few ops its
-// range crosses.  Inside a CTA this is the pipeline of stream_kernel: one
-// producer warp streams tile chunks from HBM into a ring of shared-memory
-// stages with 1-D bulk copies (TMA), and the consumer warps decode them
-// straight from shared memory.  The consumer warps form NG groups; tile k of
-// the CTA goes to group k mod NG, so a stage only has to hold one group's
-// rows and the ring can be deep (many bytes in flight per SM) while all
-// consumer warps stay busy.  A tile's chunks and matrices (gate, up) go to the
-// same group, so its partial sums stay in registers.  Each group has a ring
-// of its own (NS / NG slots): an mbarrier wait only tells a phase from the one
-// before it, so every waiter must see every phase of the slots it waits on.  The x of an op is staged
-// into shared memory (and RMSNorm-ed) when the CTA's range enters the op.
-// Arithmetic is bq_dot.cuh's fixed tree: every output is bit-identical to the
-// single-op kernels.
+// The tiles of all ops are concatenated in list order; a tile is the rows one
+// warp evaluates at once (32 / G rows, G lanes per row).  Each CTA takes a
+// contiguous, byte-balanced range of tiles and its warps take the range's
+// tiles round-robin.  Every warp feeds itself: it owns a ring of D shared-
+// memory slots, issues the 1-D bulk copies (TMA) of its own next items into
+// them and waits on each slot's mbarrier.  There is no producer warp and no
+// hand-off between warps, so each warp keeps D - 1 items in flight while it
+// decodes one.  An item is one K-chunk (KCU units) of one matrix of a tile.
+// When the range enters a new op, all warps meet at a barrier and stage the
+// op's (RMSNorm-ed) x into shared memory; the copies of the new op's weights
+// are already in flight by then.  Arithmetic is bq_dot.cuh's fixed tree:
+// every output is bit-identical to the single-op kernels.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -34,56 +30,97 @@ struct MultiOp {
     float *y;
     float eps;
     int M, K, rb, nsc;
-    int G, rpw, TR;          // lanes per row, rows per warp, rows per tile
-    int KCU, nchunks, nmat;  // units per stage row, stages per tile and matrix, 1 or 2
+    int G, rpw;              // lanes per row, rows per tile (32 / G)
+    int KCU, nchunks, nmat;  // units per item row, items per tile and matrix, matrices (1 or 2)
     int ntiles, tile_base;   // tiles of this op; its first tile in the whole list
-    int row_stride, single;  // shared-memory bytes per tile row; rows copied as one block
+    int row_stride, single;  // slot bytes per tile row; rows copied as one block
 };
 
 struct MultiArgs {
     const MultiOp *ops;
-    const int *cta_tiles;  // [grid + 1]: CTA c streams tiles [cta_tiles[c], cta_tiles[c+1])
+    const int *cta_tiles;  // [grid + 1]: CTA c takes tiles [cta_tiles[c], cta_tiles[c+1])
     int nops;
-    int NS, stage_bytes, NG;  // NS: slots in all (NS / NG per group)
-    int x_off, stage_off;
+    int nwarps, D, slot_bytes;  // warps per CTA, ring slots per warp, bytes per slot
+    int x_off, ring_off;
 };
 
-#ifndef BQ_MULTI_NWC
-#define BQ_MULTI_NWC 8
-#endif
-constexpr int MULTI_NWC = BQ_MULTI_NWC;  // consumer warps; + 1 producer warp
+constexpr int MULTI_MAX_WARPS = 16;
+constexpr int MULTI_MAX_D = 4;
+// shared memory header: mbarriers [0, 512), reduction scratch [768, 1796),
+// abort flag at 2040, x from MULTI_X_OFF
+constexpr int MULTI_X_OFF = 2048;
+
+// one warp's position in its item sequence: tiles t = first, first + nwarps,
+// ...; per tile its matrices, per matrix its K-chunks
+struct MultiCursor {
+    int t, op, m, c;
+};
+
+// the op holding tile t, walking forward from op index `op`
+__device__ __forceinline__ int multi_op_of(const MultiArgs &a, int t, int op) {
+    while (op + 1 < a.nops && __ldg(&a.ops[op + 1].tile_base) <= t) ++op;
+    return op;
+}
 
 template <int QT>
-__global__ void __launch_bounds__((MULTI_NWC + 1) * 32, 1)
+__device__ __forceinline__ void multi_issue(const MultiArgs &a, const MultiCursor &q,
+                                            uint8_t *st, uint64_t *bar, uint64_t pol, int lane) {
+    constexpr int UB = Fmt<QT>::unit_bytes;
+    const MultiOp &o = a.ops[q.op];
+    const int rpw = __ldg(&o.rpw), tile_base = __ldg(&o.tile_base), M = __ldg(&o.M);
+    const int KCU = __ldg(&o.KCU), nsc = __ldg(&o.nsc), rb = __ldg(&o.rb);
+    const int row0 = (q.t - tile_base) * rpw;
+    const int rows = min(rpw, M - row0);
+    const int u0 = q.c * KCU;
+    const uint32_t rowb = (uint32_t)min(KCU, nsc - u0) * UB;
+    const uint8_t *W = reinterpret_cast<const uint8_t *>(__ldg(reinterpret_cast<const unsigned long long *>(&o.W[q.m])));
+    // the slot's previous contents were read by this warp's generic loads
+    __syncwarp();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (lane == 0) mbar_arrive_expect_tx(bar, rowb * rows);
+    __syncwarp();
+    if (__ldg(&o.single)) {
+        if (lane == 0) bulk_g2s(st, W + (size_t)row0 * rb, rowb * rows, bar, pol);
+    } else if (lane < rows) {
+        bulk_g2s(st + lane * __ldg(&o.row_stride), W + (size_t)(row0 + lane) * rb + (size_t)u0 * UB,
+                 rowb, bar, pol);
+    }
+}
+
+__device__ __forceinline__ void multi_advance(const MultiArgs &a, MultiCursor &q) {
+    const MultiOp &o = a.ops[q.op];
+    if (++q.c < __ldg(&o.nchunks)) return;
+    q.c = 0;
+    if (++q.m < __ldg(&o.nmat)) return;
+    q.m = 0;
+    q.t += a.nwarps;
+    q.op = multi_op_of(a, q.t, q.op);
+}
+
+template <int QT>
+__global__ void __launch_bounds__(MULTI_MAX_WARPS * 32, 1)
     multi_kernel(const MultiArgs a, unsigned int *status) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *empty = full + 16;
-    volatile int *flags = reinterpret_cast<volatile int *>(smem + 256);  // [0] abort [2+g] issued
-    float *red = reinterpret_cast<float *>(smem + 512);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [nwarps][D]
+    float *red = reinterpret_cast<float *>(smem + 768);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 2040);
     float *xsm = reinterpret_cast<float *>(smem + a.x_off);
-    uint8_t *stages = smem + a.stage_off;
     constexpr int UB = Fmt<QT>::unit_bytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NWG = MULTI_NWC / a.NG;  // warps per consumer group
+    const int nthr = blockDim.x;
     const int t_begin = a.cta_tiles[blockIdx.x], t_end = a.cta_tiles[blockIdx.x + 1];
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < a.NS; ++s) {
-            mbar_init(full + s, 1);
-            mbar_init(empty + s, NWG);
-        }
-        for (int i = 0; i < 2 + 8; ++i) flags[i] = 0;
+        for (int i = 0; i < a.nwarps * a.D; ++i) mbar_init(full + i, 1);
+        *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
     if (t_begin >= t_end) return;
 
-    // the op holding tile t, walking forward from op index `op`
-    auto op_of = [&](int t, int op) {
-        while (op + 1 < a.nops && __ldg(&a.ops[op + 1].tile_base) <= t) ++op;
-        return op;
-    };
+    uint64_t *wfull = full + warp * a.D;
+    uint8_t *ring = smem + a.ring_off + (size_t)warp * a.D * a.slot_bytes;
+    const uint64_t pol = l2_policy_evict_first();
     int op0 = 0;
     {
         int lo = 0, hi = a.nops - 1;  // last op with tile_base <= t_begin
@@ -94,147 +131,110 @@ __global__ void __launch_bounds__((MULTI_NWC + 1) * 32, 1)
         }
         op0 = lo;
     }
+    const int op_last = multi_op_of(a, t_end - 1, op0);
 
-    if (warp == MULTI_NWC) {
-        // ------------------------------ producer ------------------------------
-        const uint64_t pol = l2_policy_evict_first();
-        const int NSG = a.NS / a.NG;
-        int cnt_g[8] = {};  // items issued per group (NG <= 8)
-        int op = op0;
-        bool ok = true;
-        for (int t = t_begin; ok && t < t_end; ++t) {
-            op = op_of(t, op);
-            const MultiOp &o = a.ops[op];
-            const int row0 = (t - o.tile_base) * o.TR;
-            const int rows = min(o.TR, o.M - row0);
-            const int g = (t - t_begin) % a.NG;
-            for (int m = 0; ok && m < o.nmat; ++m)
-                for (int c = 0; c < o.nchunks; ++c) {
-                    const int it = cnt_g[g];
-                    const int slot = g * NSG + it % NSG;
-                    if (it >= NSG) {
-                        if (lane == 0 && !mbar_wait_bounded(empty + slot, ((it / NSG) - 1) & 1)) {
-                            flags[0] = 1;
-                            atomicOr(status, BQ_DEVERR_EMPTY_WAIT);
-                        }
-                        __syncwarp();
-                    }
-                    if (flags[0]) {
-                        ok = false;
-                        break;
-                    }
-                    const int u0 = c * o.KCU;
-                    const int cnt = min(o.KCU, o.nsc - u0);
-                    const uint32_t rowb = (uint32_t)cnt * UB;
-                    uint8_t *st = stages + (size_t)slot * a.stage_bytes;
-                    if (lane == 0) mbar_arrive_expect_tx(full + slot, rowb * rows);
-                    __syncwarp();
-                    if (o.single) {
-                        if (lane == 0)
-                            bulk_g2s(st, o.W[m] + (size_t)row0 * o.rb, rowb * rows, full + slot, pol);
-                    } else {
-                        for (int r = lane; r < rows; r += 32)
-                            bulk_g2s(st + r * o.row_stride,
-                                     o.W[m] + (size_t)(row0 + r) * o.rb + (size_t)u0 * UB, rowb,
-                                     full + slot, pol);
-                    }
-                    ++cnt_g[g];
-                }
-        }
-        if (lane == 0)
-            for (int g = 0; g < a.NG; ++g) flags[2 + g] = cnt_g[g];
-    } else {
-        // ------------------------------ consumers -----------------------------
-        // After an error a consumer keeps walking its tiles without waiting or
-        // computing, so that every consumer still reaches every op-boundary
-        // barrier (those have no timeout of their own).
-        const int group = warp / NWG, wg = warp % NWG;
-        const int nthr = MULTI_NWC * 32;
-        auto csync = [nthr]() { named_bar_sync(1, nthr); };
-        const int NSG = a.NS / a.NG;
-        int it = 0, op = -1;  // it: this group's items so far
-        bool ok = true;
-        for (int t = t_begin; t < t_end; ++t) {
-            const int nop = op_of(t, op < 0 ? op0 : op);
-            const MultiOp &o = a.ops[nop];
-            if (nop != op) {
-                // entering a new op: every consumer is done with the previous
-                // op's x; stage this op's (RMSNorm-ed) x
-                op = nop;
-                csync();
-                float rs = 1.0f;
-                if (o.gamma) rs = rms_scale(o.x, o.K, o.eps, red, threadIdx.x, nthr, csync);
-                for (int e = 4 * threadIdx.x; e < o.K; e += 4 * nthr) {
-                    float4 v = __ldg(reinterpret_cast<const float4 *>(o.x + e));
-                    if (o.gamma) {
-                        const float4 g = __ldg(reinterpret_cast<const float4 *>(o.gamma + e));
-                        v = make_float4(__fmul_rn(__fmul_rn(v.x, rs), g.x),
-                                        __fmul_rn(__fmul_rn(v.y, rs), g.y),
-                                        __fmul_rn(__fmul_rn(v.z, rs), g.z),
-                                        __fmul_rn(__fmul_rn(v.w, rs), g.w));
-                    }
-                    *reinterpret_cast<float4 *>(xsm + 4 * x_chunk_pos(e >> 2)) = v;
-                }
-                csync();
+    // fill the ring with this warp's first D items
+    MultiCursor q{t_begin + warp, 0, 0, 0};
+    q.op = multi_op_of(a, q.t, op0);
+    int issued = 0;
+    for (; issued < a.D && q.t < t_end; ++issued) {
+        multi_issue<QT>(a, q, ring + (size_t)issued * a.slot_bytes, wfull + issued, pol, lane);
+        multi_advance(a, q);
+    }
+
+    int e = 0, landed = 0;  // items consumed (or skipped after an error); items seen landed
+    bool ok = true;
+    auto sync = []() { __syncthreads(); };
+    for (int op = op0; op <= op_last; ++op) {
+        const MultiOp &o = a.ops[op];
+        const float *x = o.x, *gamma = o.gamma;
+        float *y = o.y;
+        const int M = o.M, K = o.K, nsc = o.nsc, G = o.G, rpw = o.rpw, KCU = o.KCU;
+        const int nchunks = o.nchunks, nmat = o.nmat, tile_base = o.tile_base, ntiles = o.ntiles;
+        const int row_stride = o.row_stride;
+        // every warp is done with the previous op's x: stage this op's
+        sync();
+        float rs = 1.0f;
+        if (gamma) rs = rms_scale(x, K, o.eps, red, threadIdx.x, nthr, sync);
+        for (int k = 4 * threadIdx.x; k < K; k += 4 * nthr) {
+            float4 v = __ldg(reinterpret_cast<const float4 *>(x + k));
+            if (gamma) {
+                const float4 g = __ldg(reinterpret_cast<const float4 *>(gamma + k));
+                v = make_float4(__fmul_rn(__fmul_rn(v.x, rs), g.x), __fmul_rn(__fmul_rn(v.y, rs), g.y),
+                                __fmul_rn(__fmul_rn(v.z, rs), g.z), __fmul_rn(__fmul_rn(v.w, rs), g.w));
             }
-            if (((t - t_begin) % a.NG) != group) continue;
-            const int G = o.G;
-            const int rho = wg * o.rpw + lane / G;  // row within the tile
-            const int l = lane & (G - 1);
-            const int row0 = (t - o.tile_base) * o.TR;
-            const int rows = min(o.TR, o.M - row0);
-            const XSmem xs{xsm, 0};
-            float p[2] = {-0.0f, -0.0f};
-            for (int m = 0; m < o.nmat; ++m)
-                for (int c = 0; c < o.nchunks; ++c, ++it) {
-                    const int slot = group * NSG + it % NSG;
-                    if (ok && !__all_sync(0xffffffffu, mbar_wait_bounded(full + slot, (it / NSG) & 1))) {
-                        if (lane == 0) {
-                            flags[0] = 1;
-                            atomicOr(status, BQ_DEVERR_FULL_WAIT);
-                        }
-                        ok = false;
-                    }
+            *reinterpret_cast<float4 *>(xsm + 4 * x_chunk_pos(k >> 2)) = v;
+        }
+        sync();
+
+        const int lo = max(t_begin, tile_base), hi = min(t_end, tile_base + ntiles);
+        // this warp's first tile in [lo, hi): (t - t_begin) mod nwarps == warp
+        int t = lo + ((warp - (lo - t_begin) % a.nwarps) + a.nwarps) % a.nwarps;
+        const int rho = lane / G, l = lane & (G - 1);
+        const XSmem xs{xsm, 0};
+        for (; t < hi; t += a.nwarps) {
+            const int row0 = (t - tile_base) * rpw;
+            const int rows = min(rpw, M - row0);
+            float p0 = -0.0f, p1 = -0.0f;
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                if (m >= nmat) break;
+                for (int c = 0; c < nchunks; ++c, ++e) {
+                    const int slot = e % a.D;
                     if (ok) {
-                        const int u0 = c * o.KCU;
-                        const int cnt = min(o.KCU, o.nsc - u0);
-                        const uint8_t *stp = stages + (size_t)slot * a.stage_bytes + rho * o.row_stride;
-                        if (rho < rows) {
-                            for (int ul = l; ul < cnt; ul += G) {
-                                uint32_t w[Fmt<QT>::unit_words];
-                                load_unit_smem<QT>(w, stp + ul * UB);
-                                const uint32_t *const ws[1] = {w};
-                                float cc[1][1];
-                                unit_dot<QT, 1, 1>(ws, 8, xs, (u0 + ul) * 256, cc);
-                                p[m] = __fadd_rn(p[m], cc[0][0]);
+                        if (*abort_flag) {
+                            ok = false;
+                        } else if (!__all_sync(0xffffffffu,
+                                               mbar_wait_bounded(wfull + slot, (e / a.D) & 1))) {
+                            if (lane == 0) {
+                                *abort_flag = 1;
+                                atomicOr(status, BQ_DEVERR_FULL_WAIT);
                             }
+                            ok = false;
+                        } else {
+                            ++landed;
                         }
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty + slot);
+                    if (!ok) continue;
+                    const int u0 = c * KCU;
+                    const int cnt = min(KCU, nsc - u0);
+                    const uint8_t *stp = ring + (size_t)slot * a.slot_bytes + rho * row_stride;
+                    if (rho < rows) {
+                        for (int ul = l; ul < cnt; ul += G) {
+                            uint32_t w[Fmt<QT>::unit_words];
+                            load_unit_smem<QT>(w, stp + ul * UB);
+                            const uint32_t *const ws[1] = {w};
+                            float cc[1][1];
+                            unit_dot<QT, 1, 1>(ws, 8, xs, (u0 + ul) * 256, cc);
+                            if (m == 0) p0 = __fadd_rn(p0, cc[0][0]);
+                            else p1 = __fadd_rn(p1, cc[0][0]);
+                        }
+                    }
+                    // refill the slot just read with the item D places ahead
+                    if (q.t < t_end) {
+                        multi_issue<QT>(a, q, ring + (size_t)slot * a.slot_bytes, wfull + slot, pol,
+                                        lane);
+                        multi_advance(a, q);
+                        ++issued;
+                    }
                 }
+            }
             if (!ok) continue;
-            const float g = fold_lanes(p[0], G);
-            if (o.nmat == 2) {
-                const float u = fold_lanes(p[1], G);
-                if (rho < rows && l == 0) o.y[row0 + rho] = silu_mul(g, u);
+            const float g = fold_lanes(p0, G);
+            if (nmat == 2) {
+                const float u = fold_lanes(p1, G);
+                if (rho < rows && l == 0) y[row0 + rho] = silu_mul(g, u);
             } else if (rho < rows && l == 0) {
-                o.y[row0 + rho] = g;
+                y[row0 + rho] = g;
             }
         }
     }
 
-    __syncthreads();
-    if (flags[0] && threadIdx.x == 0) {
-        // an error unwound the pipeline: let every copy still in flight land
-        const int NSG = a.NS / a.NG;
-        for (int g = 0; g < a.NG; ++g) {
-            const int issued = flags[2 + g];
-            for (int i = issued > NSG ? issued - NSG : 0; i < issued; ++i)
-                if (!mbar_wait_bounded(full + g * NSG + i % NSG, (i / NSG) & 1))
-                    atomicOr(status, BQ_DEVERR_DRAIN_WAIT);
-        }
-    }
+    // after an error: let this warp's copies still in flight land before exit
+    if (!ok && lane == 0)
+        for (int i = landed; i < issued; ++i)
+            if (!mbar_wait_bounded(wfull + i % a.D, (i / a.D) & 1))
+                atomicOr(status, BQ_DEVERR_DRAIN_WAIT);
 }
 
 }  // namespace bq
