@@ -4,14 +4,18 @@
 Default workload (a "step" = one token of the Qwen3-0.6B-shaped Q8_0 weight
 stream): 28 layers of q 2048x1024, k 512x1024, v 512x1024, o 1024x2048,
 gate+up 3072x1024 (fused RMSNorm+gate+up+SiLU), down 1024x3072, then the LM
-head 151936x1024 -- 113 dependent stages, each reading the previous stage's
-output (block_quantized_weight_dequant_gb300.decode).  By default the whole
-step is one cooperative launch of the stream executor (--launch per_op: one
-launch per op instead), captured once in a CUDA graph and replayed.  Weights
-N(0, 0.02) packed to Q8_0 on the GPU, first input N(0, 1), RMSNorm gains
-N(1, 0.1), all seeded and synthetic (the pages' real checkpoints are not
-available).  The packed weights (602 MB) are larger than the 129 MB L2, so
-every step reads them from HBM; no flush is needed.
+head 151936x1024: 169 ops, 197 GEMVs, 602 MB of packed weights.  Every op
+reads an N(0, 1) input of its own (--inputs independent), so the step is the
+pure per-token weight stream; the whole step is one launch of the multi-op
+streaming kernel, captured once in a CUDA graph and replayed.  The same
+weights are also timed with each stage reading the previous stage's output
+(113 dependent stages, one cooperative launch of the stream executor with
+grid-wide barriers) and reported under "other_inputs"; --inputs chained swaps
+the two.  --launch per_op: one launch per op instead.  Weights N(0, 0.02)
+packed to Q8_0 on the GPU, inputs N(0, 1), RMSNorm gains N(1, 0.1), all
+seeded and synthetic (the pages' real checkpoints are not available).  The
+packed weights (602 MB) are larger than the 129 MB L2, so every step reads
+them from HBM; no flush is needed.
 
 Other workloads (--config): cfg1 (one Q8_0 GEMV 3072x1024, 96 rotated
 copies), cfg3 (7B-shaped Q4_0 token stream), cfg4 (RMSNorm+gate+up+SiLU Q8_0
@@ -42,6 +46,37 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ---------------------------------------------------------------------------
 # helpers
+# DRAM traffic per launch of the dominant kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum) from one ncu capture of the same workload; the
+# summaries under profiles/ give the commands.  An entry is reported only while
+# the CUDA sources hash to the state that was captured; after any kernel change
+# the traffic is null until it is captured again.
+NCU_TRAFFIC = {
+    # (config, inputs): (bytes per launch, sha256 of csrc/ at capture, summary)
+    ("cfg2", "independent"): (606694656, "4b2fc51e57db864a47b43648db2154cbcc8d63cf6c9fd8fae207cd34bd5ab6b9",
+                              "profiles/multi_kernel_q8_0_qwen3_0.6b_stream.md"),
+}
+
+
+def csrc_digest():
+    import hashlib
+    d = os.path.join(ROOT, "block_quantized_weight_dequant_gb300", "csrc")
+    h = hashlib.sha256()
+    for n in sorted(os.listdir(d)):
+        if n.endswith((".cu", ".cuh", ".h")):
+            h.update(n.encode())
+            with open(os.path.join(d, n), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(config, inputs):
+    e = NCU_TRAFFIC.get((config, inputs if config in ("cfg2", "cfg3") else None))
+    if e is None or e[1] != csrc_digest():
+        return None, None
+    return e[0], e[2]
+
+
 # ---------------------------------------------------------------------------
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -143,16 +178,11 @@ def _packed(bq, wl, qt, M, K, seed, tag, dev):
     return P
 
 
-def build_token_stream(cfg, dev, seed=0, mode="plan", chained=True):
-    """One decode step's GEMV stream (block_quantized_weight_dequant_gb300.decode).
-    chained: every stage reads the previous stage's output (113 dependent
-    stages, grid-wide barriers); unchained: every op reads its own input (the
-    pure weight stream).  mode "plan": one cooperative launch per step; mode
-    "per_op": one launch per op."""
-    import torch
+def build_token_layers(cfg, dev, seed=0):
+    """Packed weights of one token's stream (every layer's matrices, RMSNorm
+    gains and the LM head), drawn and packed on the GPU."""
     import block_quantized_weight_dequant_gb300 as bq
     from block_quantized_weight_dequant_gb300 import workloads as wl
-    from block_quantized_weight_dequant_gb300.decode import DecodeStream
 
     qt = cfg["qtype"]
     shapes = {n: (M, K) for n, M, K in cfg["mats"]}
@@ -166,6 +196,23 @@ def build_token_stream(cfg, dev, seed=0, mode="plan", chained=True):
         layers.append(L)
     M, K = cfg["lm_head"]
     lm = _packed(bq, wl, qt, M, K, seed, (cfg["name"], "lm_head"), dev)
+    return layers, lm
+
+
+def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None):
+    """One decode step's GEMV stream (block_quantized_weight_dequant_gb300.decode).
+    chained=False (default): every op reads an N(0, 1) input of its own, the
+    pure per-token weight stream; chained: every stage reads the previous
+    stage's output (113 dependent stages, grid-wide barriers).  mode "plan":
+    one launch per step; mode "per_op": one launch per op.  `packed`: layers
+    from build_token_layers, shared between the two input modes."""
+    import torch
+    import block_quantized_weight_dequant_gb300 as bq
+    from block_quantized_weight_dequant_gb300 import workloads as wl
+    from block_quantized_weight_dequant_gb300.decode import DecodeStream
+
+    qt = cfg["qtype"]
+    layers, lm = packed if packed is not None else build_token_layers(cfg, dev, seed)
     ds = DecodeStream(qt, layers, lm, chained=chained)
     ds.inputs.copy_(wl.normal_torch(ds.inputs.numel(), 1.0, seed=seed, stream=wl.stream_id("x0"),
                                     device=dev))
@@ -190,7 +237,7 @@ def build_token_stream(cfg, dev, seed=0, mode="plan", chained=True):
               "stages_per_step": ds.n_stages, "weight_bytes_per_step": ds.weight_bytes(),
               "weight_format": qt, "launch": mode,
               "inputs": "chained (each stage reads the previous stage's output)" if chained
-              else "independent (each op reads its own input)"}
+              else "independent (each op reads an N(0,1) input of its own)"}
     return w
 
 
@@ -258,10 +305,14 @@ def build_verify(dev, cfg, R, copies=7, seed=0):
 def build_workload(args, dev):
     from block_quantized_weight_dequant_gb300 import workloads as wl
     chained = args.inputs == "chained"
-    if args.config == "cfg2":
-        return build_token_stream(wl.QWEN3_0_6B, dev, mode=args.launch, chained=chained)
-    if args.config == "cfg3":
-        return build_token_stream(wl.Q7B, dev, mode=args.launch, chained=chained)
+    if args.config in ("cfg2", "cfg3"):
+        cfg = wl.QWEN3_0_6B if args.config == "cfg2" else wl.Q7B
+        packed = build_token_layers(cfg, dev)
+        w = build_token_stream(cfg, dev, mode=args.launch, chained=chained, packed=packed)
+        if args.other_inputs:
+            w.other = build_token_stream(cfg, dev, mode=args.launch, chained=not chained,
+                                         packed=packed)
+        return w
     if args.config == "cfg1":
         c = wl.CFG1
         return build_rotated_gemv(dev, c["qtype"], c["M"], c["K"], copies=96)
@@ -298,6 +349,25 @@ def time_graph(graph, stream, steps, dist_barrier):
     dist_barrier()
     per = [s.elapsed_time(e) for s, e in ev]
     return start_all.elapsed_time(end_all), per
+
+
+def capture(w, stream, warmup):
+    """Run the step once eagerly (module load, kernel attributes), capture it
+    in a CUDA graph and replay it `warmup` times."""
+    import torch
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        w.run()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        w.run()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    return graph
 
 
 # ---------------------------------------------------------------------------
@@ -400,8 +470,11 @@ def main():
                     help="seconds of oracle work for cpu_baseline (0 disables)")
     ap.add_argument("--launch", choices=["plan", "per_op"], default="plan",
                     help="cfg2/cfg3: one cooperative launch per token, or one launch per op")
-    ap.add_argument("--inputs", choices=["chained", "independent"], default="chained",
-                    help="cfg2/cfg3: stages read the previous stage's output, or own inputs")
+    ap.add_argument("--inputs", choices=["chained", "independent"], default="independent",
+                    help="cfg2/cfg3: each op reads an input of its own (the per-token weight "
+                         "stream), or each stage reads the previous stage's output")
+    ap.add_argument("--no-other-inputs", dest="other_inputs", action="store_false",
+                    help="cfg2/cfg3: skip timing the other input mode as a secondary figure")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -428,23 +501,24 @@ def main():
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=dev)
-    with torch.cuda.stream(stream):
-        w.run()  # eager warm-up: module load, kernel attributes
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        w.run()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            graph.replay()
-    torch.cuda.synchronize()
+    graph = capture(w, stream, args.warmup)
 
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     total_ms, per = time_graph(graph, stream, args.steps, barrier)
     clk = clocks.stop()
+    other = None
+    if getattr(w, "other", None) is not None:
+        og = capture(w.other, stream, args.warmup)
+        o_ms, o_per = time_graph(og, stream, args.steps, barrier)
+        other = {"inputs": w.other.desc["inputs"], "stages_per_step": w.other.desc["stages_per_step"],
+                 "ms_per_step": round(o_ms / args.steps, 5),
+                 "step_ms_median": round(statistics.median(o_per), 5),
+                 "value": round(w.other.step_bytes * args.steps / (o_ms * 1e-3) / 1e9, 2),
+                 "unit": "GB/s",
+                 "tok_per_s": round(args.steps / (o_ms * 1e-3), 2)}
+        del og
 
     t = torch.tensor([total_ms], device=dev)
     if world > 1:
@@ -489,6 +563,7 @@ def main():
     if rank != 0:
         return 0
     ms_step = total_ms / args.steps
+    traffic, traffic_src = ncu_traffic(args.config, args.inputs)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -505,13 +580,15 @@ def main():
                             round(sorted(per)[(9 * len(per)) // 10], 5)],
         "roofline": {"bound": "hbm", "kernel": dom, "launches_per_step": n_launch,
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
-                     "peak_kind": peak_kind},
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "traffic_source": traffic_src, "peak_kind": peak_kind},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": y_host.numel() * 4},
         "clocks": clk,
         "gpu_launches": len(w.launches) * args.steps,
     }
+    if other is not None:
+        line["other_inputs"] = other
     if tokens_per_step(args):
         line["tok_per_s"] = round(value * 1e9 / step_bytes / world, 2)
         ds = w.stream_obj
