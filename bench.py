@@ -306,7 +306,9 @@ def build_workload(args, dev):
     from block_quantized_weight_dequant_gb300 import workloads as wl
     chained = args.inputs == "chained"
     if args.config in ("cfg2", "cfg3"):
-        cfg = wl.QWEN3_0_6B if args.config == "cfg2" else wl.Q7B
+        cfg = dict(wl.QWEN3_0_6B if args.config == "cfg2" else wl.Q7B)
+        if args.layers:
+            cfg["layers"] = args.layers
         packed = build_token_layers(cfg, dev)
         w = build_token_stream(cfg, dev, mode=args.launch, chained=chained, packed=packed)
         if args.other_inputs:
@@ -473,6 +475,8 @@ def main():
     ap.add_argument("--inputs", choices=["chained", "independent"], default="independent",
                     help="cfg2/cfg3: each op reads an input of its own (the per-token weight "
                          "stream), or each stage reads the previous stage's output")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="cfg2/cfg3: fewer layers than the model's (smaller cases for profiling)")
     ap.add_argument("--no-other-inputs", dest="other_inputs", action="store_false",
                     help="cfg2/cfg3: skip timing the other input mode as a secondary figure")
     args = ap.parse_args()
@@ -563,7 +567,7 @@ def main():
     if rank != 0:
         return 0
     ms_step = total_ms / args.steps
-    traffic, traffic_src = ncu_traffic(args.config, args.inputs)
+    traffic, traffic_src = ncu_traffic(args.config, args.inputs) if not args.layers else (None, None)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),

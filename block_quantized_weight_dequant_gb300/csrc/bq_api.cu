@@ -43,6 +43,7 @@ struct Tunables {
     int multi = 1;              // independent op lists: multi-op streaming kernel (0: executor)
     int multi_warps = 0;        // multi-op kernel: warps per CTA (0: as many as fit, <= 16)
     int multi_d = 2;            // multi-op kernel: ring slots per warp
+    int multi_nr = 1;           // multi-op kernel: weight rows per lane (1, 2 or 4)
 };
 
 const Tunables &tunables() {
@@ -72,6 +73,7 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "multi") && val >= 0 && val <= 1) v.multi = val;
             else if (!std::strcmp(tok, "mw") && val >= 1 && val <= 16) v.multi_warps = val;
             else if (!std::strcmp(tok, "md") && val >= 2 && val <= 4) v.multi_d = val;
+            else if (!std::strcmp(tok, "mnr") && (val == 1 || val == 2 || val == 4)) v.multi_nr = val;
         }
         return v;
     }();
@@ -409,6 +411,7 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
     const Tunables &t = tunables();
     const int bb = block_bytes(qtype), ub = 8 * bb;
     const int D = std::min(t.multi_d, MULTI_MAX_D);
+    const int NR = t.multi_nr;
     // pass 1: per-op tiling that does not depend on the slot size
     int maxK = 0, slot_min = 0;
     long long tiles = 0;
@@ -428,7 +431,7 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
         m.K = (int)o.K;
         m.nsc = m.K / 256;
         m.G = tree_lanes_for_units(m.nsc);
-        m.rpw = 32 / m.G;
+        m.rpw = NR * (32 / m.G);
         m.rb = m.nsc * ub;
         m.ntiles = (m.M + m.rpw - 1) / m.rpw;
         m.tile_base = (int)tiles;
@@ -479,8 +482,8 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
     if (smem > (size_t)cap) return BQ_ERR_SHAPE;
     const int threads = nwarps * 32;
     int occ = 0;
-    const int err = qtype == BQ_Q8_0 ? bq_internal_multi_occupancy_q8_0(threads, smem, &occ)
-                                     : bq_internal_multi_occupancy_q4_0(threads, smem, &occ);
+    const int err = qtype == BQ_Q8_0 ? bq_internal_multi_occupancy_q8_0(NR, threads, smem, &occ)
+                                     : bq_internal_multi_occupancy_q4_0(NR, threads, smem, &occ);
     if (err != 0 || occ < 1) return BQ_ERR_CUDA;
     const int grid = std::min(MULTI_MAX_CTAS, num_sms_current() * occ);
     // byte-balanced contiguous tile ranges
@@ -505,6 +508,7 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
     geo->x_off = x_off;
     geo->ring_off = ring_off;
     geo->smem = smem;
+    geo->nr = NR;
     return BQ_OK;
 }
 
@@ -520,6 +524,7 @@ void fill_multi_args(const MultiGeometry &geo, int n_ops, const MultiOp *ops,
     a->slot_bytes = geo.slot_bytes;
     a->x_off = geo.x_off;
     a->ring_off = geo.ring_off;
+    a->nr = geo.nr;
 }
 
 void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const ExecX *xs,

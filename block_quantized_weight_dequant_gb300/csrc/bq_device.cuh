@@ -63,13 +63,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same with a suspend-time hint: a thread whose phase has not completed
+// sleeps until it completes or about `hint_ns` pass, instead of returning at
+// once, so waiting warps take no issue slots from the warps that compute.
+constexpr uint32_t BQ_SUSPEND_HINT_NS = 1000000u;  // 1 ms; a completed phase wakes it earlier
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(BQ_SUSPEND_HINT_NS)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete; false after the limit.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && globaltimer() - t0 > BQ_WAIT_LIMIT_NS) return false;
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (globaltimer() - t0 > BQ_WAIT_LIMIT_NS) return false;
     }
 }
 

@@ -155,14 +155,14 @@ __device__ __forceinline__ float f4(const float4 &v, int i) {
 // gate+up (two matrices, one x).  Each (v, r) pair sees exactly the operation
 // sequence of the NW = 1, R = 1 case, so results do not depend on NW or R.
 // ---------------------------------------------------------------------------
+// code j of the block whose first byte (its scale) is byte `base` of w
 template <int QT>
-__device__ __forceinline__ float raw_at(const uint32_t *w, int B, int j) {
-    constexpr int bb = Fmt<QT>::block_bytes;
+__device__ __forceinline__ float raw_at_byte(const uint32_t *w, int base, int j) {
     if constexpr (QT == QT_Q8_0) {
-        const int byte = bb * B + 2 + j;
+        const int byte = base + 2 + j;
         return q8_raw(w[byte >> 2], byte & 3);
     } else {
-        const int byte = bb * B + 2 + (j & 15);
+        const int byte = base + 2 + (j & 15);
         return q4_raw(w[byte >> 2], j >= 16, byte & 3);
     }
 }
@@ -174,10 +174,9 @@ __device__ __forceinline__ float raw_at(const uint32_t *w, int B, int j) {
 #ifndef BQ_F32X2
 #define BQ_F32X2 1
 #endif
-template <int QT, int NW, int R, int B, class XV>
-__device__ __forceinline__ void block_sum(const uint32_t *const (&w)[NW], const XV &xv_,
-                                          float (&s)[NW][R], float (&d)[NW]) {
-    constexpr int bb = Fmt<QT>::block_bytes;
+template <int QT, int NW, int R, int B, int WB, class XV>
+__device__ __forceinline__ void block_sum_at(const uint32_t *const (&w)[NW], const XV &xv_,
+                                             float (&s)[NW][R], float (&d)[NW]) {
     constexpr float M = QT == QT_Q8_0 ? Q8_MAGIC : Q4_MAGIC;
 #if BQ_F32X2
     const float2 mneg = make_float2(-M, -M);
@@ -194,9 +193,11 @@ __device__ __forceinline__ void block_sum(const uint32_t *const (&w)[NW], const 
 #pragma unroll
         for (int v = 0; v < NW; ++v) {
             const float2 q01 = __fadd2_rn(
-                make_float2(raw_at<QT>(w[v], B, 4 * t), raw_at<QT>(w[v], B, 4 * t + 1)), mneg);
+                make_float2(raw_at_byte<QT>(w[v], WB, 4 * t), raw_at_byte<QT>(w[v], WB, 4 * t + 1)),
+                mneg);
             const float2 q23 = __fadd2_rn(
-                make_float2(raw_at<QT>(w[v], B, 4 * t + 2), raw_at<QT>(w[v], B, 4 * t + 3)), mneg);
+                make_float2(raw_at_byte<QT>(w[v], WB, 4 * t + 2), raw_at_byte<QT>(w[v], WB, 4 * t + 3)),
+                mneg);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 a[v][r][0] = __ffma2_rn(q01, make_float2(xv[r].x, xv[r].y), a[v][r][0]);
@@ -206,7 +207,7 @@ __device__ __forceinline__ void block_sum(const uint32_t *const (&w)[NW], const 
     }
 #pragma unroll
     for (int v = 0; v < NW; ++v) {
-        d[v] = scale_at(w[v], bb * B);
+        d[v] = scale_at(w[v], WB);
 #pragma unroll
         for (int r = 0; r < R; ++r)
             s[v][r] = __fadd_rn(__fadd_rn(a[v][r][0].x, a[v][r][0].y),
@@ -229,7 +230,7 @@ __device__ __forceinline__ void block_sum(const uint32_t *const (&w)[NW], const 
         for (int i = 0; i < 4; ++i) {
 #pragma unroll
             for (int v = 0; v < NW; ++v) {
-                const float q = __fsub_rn(raw_at<QT>(w[v], B, 4 * t + i), M);
+                const float q = __fsub_rn(raw_at_byte<QT>(w[v], WB, 4 * t + i), M);
 #pragma unroll
                 for (int r = 0; r < R; ++r) a[v][r][i] = __fmaf_rn(q, f4(xv[r], i), a[v][r][i]);
             }
@@ -237,12 +238,19 @@ __device__ __forceinline__ void block_sum(const uint32_t *const (&w)[NW], const 
     }
 #pragma unroll
     for (int v = 0; v < NW; ++v) {
-        d[v] = scale_at(w[v], bb * B);
+        d[v] = scale_at(w[v], WB);
 #pragma unroll
         for (int r = 0; r < R; ++r)
             s[v][r] = __fadd_rn(__fadd_rn(a[v][r][0], a[v][r][1]), __fadd_rn(a[v][r][2], a[v][r][3]));
     }
 #endif
+}
+
+// block B of a unit whose bytes w holds from the unit's start
+template <int QT, int NW, int R, int B, class XV>
+__device__ __forceinline__ void block_sum(const uint32_t *const (&w)[NW], const XV &xv,
+                                          float (&s)[NW][R], float (&d)[NW]) {
+    block_sum_at<QT, NW, R, B, Fmt<QT>::block_bytes * B>(w, xv, s, d);
 }
 
 template <int QT, int NW, int R, int B, class XV>
@@ -274,6 +282,56 @@ __device__ __forceinline__ void unit_dot(const uint32_t *const (&w)[NW], int nbk
     if (nbk > 5) block_dot<QT, NW, R, 5>(w, xv, c);
     if (nbk > 6) block_dot<QT, NW, R, 6>(w, xv, c);
     if (nbk > 7) block_dot<QT, NW, R, 7>(w, xv, c);
+}
+
+// NR weight rows against one x view, one full unit each: c[r] receives row
+// r's unit partial with exactly unit_dot's operation sequence, so the bits do
+// not depend on NR.  up[r] is the unit's first byte in shared memory (16-byte
+// aligned).  Weights are read block by block: the bytes of block b lie in the
+// 16-byte chunks floor(34b/16) .. +2 for Q8_0 (always three chunks) and
+// floor(18b/16) .. +1 for Q4_0 (always two), so a row holds one block's words
+// in registers while every x value read from shared memory serves NR rows.
+template <int QT, int NR, int B, class XV>
+__device__ __forceinline__ void rows_block(const uint8_t *const (&up)[NR], const XV &xv,
+                                           float (&c)[NR]) {
+    constexpr int bb = Fmt<QT>::block_bytes;
+    constexpr int off = bb * B;
+    constexpr int c0 = off / 16;
+    constexpr int nch = (off + bb - 1) / 16 - c0 + 1;
+    uint32_t w[NR][4 * nch];
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int k = 0; k < nch; ++k) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(up[r] + 16 * (c0 + k));
+            w[r][4 * k + 0] = v.x;
+            w[r][4 * k + 1] = v.y;
+            w[r][4 * k + 2] = v.z;
+            w[r][4 * k + 3] = v.w;
+        }
+    const uint32_t *ws[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) ws[r] = w[r];
+    float s[NR][1], d[NR];
+    block_sum_at<QT, NR, 1, B, off - 16 * c0>(ws, xv, s, d);
+#pragma unroll
+    for (int r = 0; r < NR; ++r) c[r] = __fmaf_rn(d[r], s[r][0], c[r]);
+}
+
+template <int QT, int NR, class XS>
+__device__ __forceinline__ void unit_dot_rows(const uint8_t *const (&up)[NR], const XS &xs, int e0,
+                                              float (&c)[NR]) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) c[r] = -0.0f;
+    const auto xv = xs.at(e0);
+    rows_block<QT, NR, 0>(up, xv, c);
+    rows_block<QT, NR, 1>(up, xv, c);
+    rows_block<QT, NR, 2>(up, xv, c);
+    rows_block<QT, NR, 3>(up, xv, c);
+    rows_block<QT, NR, 4>(up, xv, c);
+    rows_block<QT, NR, 5>(up, xv, c);
+    rows_block<QT, NR, 6>(up, xv, c);
+    rows_block<QT, NR, 7>(up, xv, c);
 }
 
 // load a full unit from shared memory (16-byte aligned)

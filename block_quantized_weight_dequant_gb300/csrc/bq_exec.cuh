@@ -234,9 +234,9 @@ __device__ __forceinline__ bool exec_next_any(const ExecTables &T, ExecItem &it,
 __device__ __forceinline__ bool exec_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && (*abort_flag || globaltimer() - t0 > BQ_WAIT_LIMIT_NS)) return false;
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (*abort_flag || globaltimer() - t0 > BQ_WAIT_LIMIT_NS) return false;
     }
 }
 

@@ -70,11 +70,23 @@ int bq_internal_status_q8_0(unsigned int *flags, int clear) {
     return (int)e;
 }
 
-int bq_internal_multi_occupancy_q8_0(int threads, size_t smem, int *occ) {
-    auto kern = bq::multi_kernel<bq::QT_Q8_0>;
+namespace {
+template <int NR>
+int multi_occupancy(int threads, size_t smem, int *occ) {
+    auto kern = bq::multi_kernel<bq::QT_Q8_0, NR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kern, threads, smem);
+}
+}  // namespace
+
+int bq_internal_multi_occupancy_q8_0(int nr, int threads, size_t smem, int *occ) {
+    switch (nr) {
+        case 1: return multi_occupancy<1>(threads, smem, occ);
+        case 2: return multi_occupancy<2>(threads, smem, occ);
+        case 4: return multi_occupancy<4>(threads, smem, occ);
+        default: return (int)cudaErrorInvalidValue;
+    }
 }
 
 int bq_internal_multi_launch_q8_0(const bq::MultiArgs &a, int grid, int threads, size_t smem,
@@ -82,6 +94,12 @@ int bq_internal_multi_launch_q8_0(const bq::MultiArgs &a, int grid, int threads,
     unsigned int *status = nullptr;
     cudaError_t e = status_addr(&status);
     if (e != cudaSuccess) return (int)e;
-    bq::multi_kernel<bq::QT_Q8_0><<<grid, threads, smem, static_cast<cudaStream_t>(stream)>>>(a, status);
+    auto s = static_cast<cudaStream_t>(stream);
+    switch (a.nr) {
+        case 1: bq::multi_kernel<bq::QT_Q8_0, 1><<<grid, threads, smem, s>>>(a, status); break;
+        case 2: bq::multi_kernel<bq::QT_Q8_0, 2><<<grid, threads, smem, s>>>(a, status); break;
+        case 4: bq::multi_kernel<bq::QT_Q8_0, 4><<<grid, threads, smem, s>>>(a, status); break;
+        default: return (int)cudaErrorInvalidValue;
+    }
     return (int)cudaGetLastError();
 }

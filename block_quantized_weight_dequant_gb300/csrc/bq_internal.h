@@ -87,7 +87,7 @@ struct MultiArgs;
 constexpr int MULTI_MAX_CTAS = 1024;
 // launch geometry of a multi-op (independent GEMVs) run
 struct MultiGeometry {
-    int grid, threads, nwarps, D, slot_bytes, x_off, ring_off;
+    int grid, threads, nwarps, D, slot_bytes, x_off, ring_off, nr;
     size_t smem;
 };
 // Plan a list of ops none of which depends on another (validated by
@@ -101,8 +101,8 @@ void fill_multi_args(const MultiGeometry &geo, int n_ops, const MultiOp *ops,
 // whether independent op lists use the multi-op kernel (tuning switch)
 bool tunables_multi();
 }
-int bq_internal_multi_occupancy_q8_0(int threads, size_t smem, int *occ);
-int bq_internal_multi_occupancy_q4_0(int threads, size_t smem, int *occ);
+int bq_internal_multi_occupancy_q8_0(int nr, int threads, size_t smem, int *occ);
+int bq_internal_multi_occupancy_q4_0(int nr, int threads, size_t smem, int *occ);
 int bq_internal_multi_launch_q8_0(const bq::MultiArgs &a, int grid, int threads, size_t smem,
                                   void *stream);
 int bq_internal_multi_launch_q4_0(const bq::MultiArgs &a, int grid, int threads, size_t smem,

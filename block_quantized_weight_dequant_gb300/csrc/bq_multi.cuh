@@ -30,7 +30,7 @@ struct MultiOp {
     float *y;
     float eps;
     int M, K, rb, nsc;
-    int G, rpw;              // lanes per row, rows per tile (32 / G)
+    int G, rpw;              // lanes per row, rows per tile (NR * 32 / G)
     int KCU, nchunks, nmat;  // units per item row, items per tile and matrix, matrices (1 or 2)
     int ntiles, tile_base;   // tiles of this op; its first tile in the whole list
     int row_stride, single;  // slot bytes per tile row; rows copied as one block
@@ -42,6 +42,7 @@ struct MultiArgs {
     int nops;
     int nwarps, D, slot_bytes;  // warps per CTA, ring slots per warp, bytes per slot
     int x_off, ring_off;
+    int nr;                     // weight rows per lane (the kernel's NR)
 };
 
 constexpr int MULTI_MAX_WARPS = 16;
@@ -50,10 +51,14 @@ constexpr int MULTI_MAX_D = 4;
 // abort flag at 2040, x from MULTI_X_OFF
 constexpr int MULTI_X_OFF = 2048;
 
-// one warp's position in its item sequence: tiles t = first, first + nwarps,
-// ...; per tile its matrices, per matrix its K-chunks
+// One warp's position in its item sequence (tiles t = first, first + nwarps,
+// ...; per tile its matrices, per matrix its K-chunks) together with the
+// fields of its op that issuing needs, read from the table only when the
+// cursor enters a new op.
 struct MultiCursor {
     int t, op, m, c;
+    const uint8_t *W0, *W1;
+    int rpw, tile_base, tile_end, M, KCU, nsc, rb, nchunks, nmat, single, row_stride;
 };
 
 // the op holding tile t, walking forward from op index `op`
@@ -62,42 +67,62 @@ __device__ __forceinline__ int multi_op_of(const MultiArgs &a, int t, int op) {
     return op;
 }
 
-template <int QT>
-__device__ __forceinline__ void multi_issue(const MultiArgs &a, const MultiCursor &q,
-                                            uint8_t *st, uint64_t *bar, uint64_t pol, int lane) {
-    constexpr int UB = Fmt<QT>::unit_bytes;
+__device__ __forceinline__ void multi_load_op(const MultiArgs &a, MultiCursor &q) {
     const MultiOp &o = a.ops[q.op];
-    const int rpw = __ldg(&o.rpw), tile_base = __ldg(&o.tile_base), M = __ldg(&o.M);
-    const int KCU = __ldg(&o.KCU), nsc = __ldg(&o.nsc), rb = __ldg(&o.rb);
-    const int row0 = (q.t - tile_base) * rpw;
-    const int rows = min(rpw, M - row0);
-    const int u0 = q.c * KCU;
-    const uint32_t rowb = (uint32_t)min(KCU, nsc - u0) * UB;
-    const uint8_t *W = reinterpret_cast<const uint8_t *>(__ldg(reinterpret_cast<const unsigned long long *>(&o.W[q.m])));
+    q.W0 = reinterpret_cast<const uint8_t *>(__ldg(reinterpret_cast<const unsigned long long *>(&o.W[0])));
+    q.W1 = reinterpret_cast<const uint8_t *>(__ldg(reinterpret_cast<const unsigned long long *>(&o.W[1])));
+    q.rpw = __ldg(&o.rpw);
+    q.tile_base = __ldg(&o.tile_base);
+    q.tile_end = q.tile_base + __ldg(&o.ntiles);
+    q.M = __ldg(&o.M);
+    q.KCU = __ldg(&o.KCU);
+    q.nsc = __ldg(&o.nsc);
+    q.rb = __ldg(&o.rb);
+    q.nchunks = __ldg(&o.nchunks);
+    q.nmat = __ldg(&o.nmat);
+    q.single = __ldg(&o.single);
+    q.row_stride = __ldg(&o.row_stride);
+}
+
+template <int QT>
+__device__ __forceinline__ void multi_issue(const MultiCursor &q, uint8_t *st, uint64_t *bar,
+                                            uint64_t pol, int lane) {
+    constexpr int UB = Fmt<QT>::unit_bytes;
+    const int row0 = (q.t - q.tile_base) * q.rpw;
+    const int rows = min(q.rpw, q.M - row0);
+    const int u0 = q.c * q.KCU;
+    const uint32_t rowb = (uint32_t)min(q.KCU, q.nsc - u0) * UB;
+    const uint8_t *W = q.m ? q.W1 : q.W0;
     // the slot's previous contents were read by this warp's generic loads
     __syncwarp();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (lane == 0) mbar_arrive_expect_tx(bar, rowb * rows);
     __syncwarp();
-    if (__ldg(&o.single)) {
-        if (lane == 0) bulk_g2s(st, W + (size_t)row0 * rb, rowb * rows, bar, pol);
-    } else if (lane < rows) {
-        bulk_g2s(st + lane * __ldg(&o.row_stride), W + (size_t)(row0 + lane) * rb + (size_t)u0 * UB,
-                 rowb, bar, pol);
+    if (q.single) {
+        if (lane == 0) bulk_g2s(st, W + (size_t)row0 * q.rb, rowb * rows, bar, pol);
+    } else {
+        for (int r = lane; r < rows; r += 32)
+            bulk_g2s(st + r * q.row_stride, W + (size_t)(row0 + r) * q.rb + (size_t)u0 * UB, rowb,
+                     bar, pol);
     }
 }
 
 __device__ __forceinline__ void multi_advance(const MultiArgs &a, MultiCursor &q) {
-    const MultiOp &o = a.ops[q.op];
-    if (++q.c < __ldg(&o.nchunks)) return;
+    if (++q.c < q.nchunks) return;
     q.c = 0;
-    if (++q.m < __ldg(&o.nmat)) return;
+    if (++q.m < q.nmat) return;
     q.m = 0;
     q.t += a.nwarps;
-    q.op = multi_op_of(a, q.t, q.op);
+    if (q.t >= q.tile_end && q.op + 1 < a.nops) {
+        q.op = multi_op_of(a, q.t, q.op);
+        multi_load_op(a, q);
+    }
 }
 
-template <int QT>
+// NR: weight rows per lane.  A tile is NR * 32/G rows; lane (rho, l) of a
+// warp takes rows rho, rho + 32/G, ... of the tile and units l, l + G, ... of
+// each, so every x value it reads from shared memory serves NR rows.
+template <int QT, int NR>
 __global__ void __launch_bounds__(MULTI_MAX_WARPS * 32, 1)
     multi_kernel(const MultiArgs a, unsigned int *status) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -134,11 +159,14 @@ __global__ void __launch_bounds__(MULTI_MAX_WARPS * 32, 1)
     const int op_last = multi_op_of(a, t_end - 1, op0);
 
     // fill the ring with this warp's first D items
-    MultiCursor q{t_begin + warp, 0, 0, 0};
+    MultiCursor q;
+    q.t = t_begin + warp;
+    q.m = q.c = 0;
     q.op = multi_op_of(a, q.t, op0);
+    multi_load_op(a, q);
     int issued = 0;
     for (; issued < a.D && q.t < t_end; ++issued) {
-        multi_issue<QT>(a, q, ring + (size_t)issued * a.slot_bytes, wfull + issued, pol, lane);
+        multi_issue<QT>(q, ring + (size_t)issued * a.slot_bytes, wfull + issued, pol, lane);
         multi_advance(a, q);
     }
 
@@ -170,12 +198,14 @@ __global__ void __launch_bounds__(MULTI_MAX_WARPS * 32, 1)
         const int lo = max(t_begin, tile_base), hi = min(t_end, tile_base + ntiles);
         // this warp's first tile in [lo, hi): (t - t_begin) mod nwarps == warp
         int t = lo + ((warp - (lo - t_begin) % a.nwarps) + a.nwarps) % a.nwarps;
-        const int rho = lane / G, l = lane & (G - 1);
+        const int rho = lane / G, l = lane & (G - 1), rg = 32 / G;
         const XSmem xs{xsm, 0};
         for (; t < hi; t += a.nwarps) {
             const int row0 = (t - tile_base) * rpw;
             const int rows = min(rpw, M - row0);
-            float p0 = -0.0f, p1 = -0.0f;
+            float p0[NR], p1[NR];
+#pragma unroll
+            for (int r = 0; r < NR; ++r) p0[r] = p1[r] = -0.0f;
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 if (m >= nmat) break;
@@ -199,20 +229,25 @@ __global__ void __launch_bounds__(MULTI_MAX_WARPS * 32, 1)
                     const int u0 = c * KCU;
                     const int cnt = min(KCU, nsc - u0);
                     const uint8_t *stp = ring + (size_t)slot * a.slot_bytes + rho * row_stride;
+                    // rows past the tile's end read stale slot bytes; their
+                    // results are dropped below
                     if (rho < rows) {
                         for (int ul = l; ul < cnt; ul += G) {
-                            uint32_t w[Fmt<QT>::unit_words];
-                            load_unit_smem<QT>(w, stp + ul * UB);
-                            const uint32_t *const ws[1] = {w};
-                            float cc[1][1];
-                            unit_dot<QT, 1, 1>(ws, 8, xs, (u0 + ul) * 256, cc);
-                            if (m == 0) p0 = __fadd_rn(p0, cc[0][0]);
-                            else p1 = __fadd_rn(p1, cc[0][0]);
+                            const uint8_t *up[NR];
+#pragma unroll
+                            for (int r = 0; r < NR; ++r) up[r] = stp + r * rg * row_stride + ul * UB;
+                            float cc[NR];
+                            unit_dot_rows<QT, NR>(up, xs, (u0 + ul) * 256, cc);
+#pragma unroll
+                            for (int r = 0; r < NR; ++r) {
+                                if (m == 0) p0[r] = __fadd_rn(p0[r], cc[r]);
+                                else p1[r] = __fadd_rn(p1[r], cc[r]);
+                            }
                         }
                     }
                     // refill the slot just read with the item D places ahead
                     if (q.t < t_end) {
-                        multi_issue<QT>(a, q, ring + (size_t)slot * a.slot_bytes, wfull + slot, pol,
+                        multi_issue<QT>(q, ring + (size_t)slot * a.slot_bytes, wfull + slot, pol,
                                         lane);
                         multi_advance(a, q);
                         ++issued;
@@ -220,12 +255,16 @@ __global__ void __launch_bounds__(MULTI_MAX_WARPS * 32, 1)
                 }
             }
             if (!ok) continue;
-            const float g = fold_lanes(p0, G);
-            if (nmat == 2) {
-                const float u = fold_lanes(p1, G);
-                if (rho < rows && l == 0) y[row0 + rho] = silu_mul(g, u);
-            } else if (rho < rows && l == 0) {
-                y[row0 + rho] = g;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const float g = fold_lanes(p0[r], G);
+                const int row = rho + r * rg;
+                if (nmat == 2) {
+                    const float u = fold_lanes(p1[r], G);
+                    if (row < rows && l == 0) y[row0 + row] = silu_mul(g, u);
+                } else if (row < rows && l == 0) {
+                    y[row0 + row] = g;
+                }
             }
         }
     }
