@@ -26,15 +26,9 @@ namespace {
 constexpr long long K_MAX = 1LL << 18;
 constexpr long long M_MAX = (1LL << 31) - 1;
 
-// launch-geometry defaults; BQ_PLAN="nwc=4,stage=32768,inflight=98304,ns=4"
+// launch-geometry defaults; BQ_PLAN="md=3,mw=8,pdl=0"
 // overrides them for tuning sweeps (read once)
 struct Tunables {
-    int max_nwc = 8;
-    int stage_target = 32 * 1024;
-    int stage_max = 64 * 1024;
-    int inflight = 96 * 1024;
-    int ns_force = 0;
-    int xres_max = 100 * 1024;
     int exec_slot = 0;     // stream executor: bytes per ring slot (0 = one warp tile of 32 units)
     int exec_nsw = 0;      // stream executor: slots per warp (0 = as many as fit, <= 4)
     int exec_warps = 8;    // stream executor: warps per CTA
@@ -43,7 +37,10 @@ struct Tunables {
     int multi = 1;              // independent op lists: multi-op streaming kernel (0: executor)
     int multi_warps = 0;        // multi-op kernel: warps per CTA (0: as many as fit, <= 16)
     int multi_d = 2;            // multi-op kernel: ring slots per warp
-    int multi_nr = 1;           // multi-op kernel: weight rows per lane (1, 2 or 4)
+    int multi_nr = 1;           // multi-op kernel: weight rows per lane (1 or 2)
+    int multi_x2_max = 32 * 1024;    // op lists: two x buffers when together at most this
+    int single_x_max = 128 * 1024;   // single calls: largest staged R x K input (else panels)
+    int single_pdl = 1;              // single calls: allow programmatic dependent launch
 };
 
 const Tunables &tunables() {
@@ -59,13 +56,7 @@ const Tunables &tunables() {
             if (!eq) continue;
             *eq = 0;
             const int val = std::atoi(eq + 1);
-            if (!std::strcmp(tok, "nwc") && val >= 1 && val <= 8) v.max_nwc = val;
-            else if (!std::strcmp(tok, "stage") && val >= 4096) v.stage_target = val;
-            else if (!std::strcmp(tok, "stagemax") && val >= 4096) v.stage_max = val;
-            else if (!std::strcmp(tok, "inflight") && val >= 8192) v.inflight = val;
-            else if (!std::strcmp(tok, "ns") && val >= 2 && val <= 8) v.ns_force = val;
-            else if (!std::strcmp(tok, "xres") && val >= 0) v.xres_max = val;
-            else if (!std::strcmp(tok, "slot") && val >= 4096) v.exec_slot = val;
+            if (!std::strcmp(tok, "slot") && val >= 4096) v.exec_slot = val;
             else if (!std::strcmp(tok, "nsw") && val >= 2 && val <= 8) v.exec_nsw = val;
             else if (!std::strcmp(tok, "ewarps") && val >= 1 && val <= 8) v.exec_warps = val;
             else if (!std::strcmp(tok, "rowmode") && val >= 0 && val <= 32) v.exec_rowmode_rows = val;
@@ -73,7 +64,10 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "multi") && val >= 0 && val <= 1) v.multi = val;
             else if (!std::strcmp(tok, "mw") && val >= 1 && val <= 16) v.multi_warps = val;
             else if (!std::strcmp(tok, "md") && val >= 2 && val <= 4) v.multi_d = val;
-            else if (!std::strcmp(tok, "mnr") && (val == 1 || val == 2 || val == 4)) v.multi_nr = val;
+            else if (!std::strcmp(tok, "mnr") && (val == 1 || val == 2)) v.multi_nr = val;
+            else if (!std::strcmp(tok, "x2") && val >= 0) v.multi_x2_max = val;
+            else if (!std::strcmp(tok, "sx") && val >= 16384) v.single_x_max = val;
+            else if (!std::strcmp(tok, "pdl") && val >= 0 && val <= 1) v.single_pdl = val;
         }
         return v;
     }();
@@ -117,76 +111,10 @@ int tree_lanes_for_units(long long nsc) {
     return 1;
 }
 
-bool plan_gemv(const GemvCall &c, LaunchPlan *p) {
-    const Tunables &t = tunables();
-    std::memset(p, 0, sizeof *p);
-    const int bb = block_bytes(c.qtype);
-    const int ub = 8 * bb;
+void plan_gemv(const GemvCall &c, LaunchPlan *p) {
     const long long nb = c.K / 32;
-    p->nsc = (int)((nb + 7) / 8);
-    p->G = tree_lanes_for_units(p->nsc);
-    p->rb = nb * bb;
-    p->num_sms = num_sms_current();
-    if (p->num_sms <= 0) return false;
-    const int rpw = 32 / p->G;
-    if (c.K % 256 != 0) {
-        p->kind = PLAN_GENERIC;
-        return true;
-    }
-    p->kind = PLAN_STREAM;
-    const int nmat = c.mode == MODE_GATE_UP ? 2 : 1;
-    const int smem_cap = max_smem_optin();
-    const int xpad = x_padded_floats((int)c.K);
-    p->xres = (long long)c.R * xpad * 4 <= t.xres_max;
-    const int x_bytes = p->xres ? c.R * xpad * 4 : 0;
-    int nwc = t.max_nwc;
-    while (nwc > 1 && (c.M + (long long)nwc * rpw - 1) / ((long long)nwc * rpw) < p->num_sms)
-        nwc >>= 1;
-    for (;; nwc >>= 1) {
-        const int TR = nwc * rpw;
-        int KCU;
-        if ((long long)TR * p->rb * nmat <= t.stage_target) {
-            KCU = p->nsc;
-        } else {
-            const long long per = (long long)TR * p->G * ub * nmat;
-            const long long k = t.stage_target / per;
-            KCU = p->G * (int)(k > 1 ? k : 1);
-            if (KCU > p->nsc) KCU = p->nsc;
-        }
-        const bool single = KCU == p->nsc && (p->G >= 8 || (p->rb / 16) % 8 == p->G % 8);
-        int stride;
-        if (single) {
-            stride = (int)p->rb;
-        } else {
-            int s16 = KCU * ub / 16;
-            if (p->G < 8)
-                while (s16 % 8 != p->G % 8) ++s16;
-            stride = s16 * 16;
-        }
-        const long long stage = (long long)TR * stride * nmat;
-        const long long room = (long long)smem_cap - HDR_BYTES - x_bytes;
-        if ((stage > t.stage_max || 2 * stage > room) && nwc > 1) continue;
-        if (2 * stage > room) return false;
-        int NS = t.ns_force ? t.ns_force : (int)(t.inflight / stage);
-        if (NS < 2) NS = 2;
-        if (NS > 8) NS = 8;
-        while (NS > 2 && NS * stage > room) --NS;
-        p->NWC = nwc;
-        p->TR = TR;
-        p->KCU = KCU;
-        p->NS = NS;
-        p->nchunks = (p->nsc + KCU - 1) / KCU;
-        p->ntiles = (int)((c.M + TR - 1) / TR);
-        p->single_copy = single;
-        p->row_stride = stride;
-        p->mat_stride = TR * stride;
-        p->stage_bytes = (int)stage;
-        p->x_off = HDR_BYTES;
-        p->x_rstride = xpad;
-        p->stage_off = (HDR_BYTES + x_bytes + 127) / 128 * 128;
-        p->smem = (size_t)p->stage_off + (size_t)NS * stage;
-        return true;
-    }
+    p->G = tree_lanes_for_units((nb + 7) / 8);
+    p->rb = nb * block_bytes(c.qtype);
 }
 
 // padded shared-memory row stride for `bytes` of units: conflict-free LDS.128
@@ -406,6 +334,8 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
     return BQ_OK;
 }
 
+bool multi_chunking(MultiOp &m, int ub, int slot_cap);
+
 bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo, int *cta_tiles,
                             MultiGeometry *geo) {
     const Tunables &t = tunables();
@@ -442,13 +372,17 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
         slot_min = std::max(slot_min, m.rpw * padded_stride(k1 * ub, m.G));
     }
     if (tiles > (1LL << 30)) return BQ_ERR_SHAPE;
-    // shared memory: header | x (one op's) | nwarps rings of D slots
+    // shared memory: header | x buffers | nwarps rings of D slots.  Two x
+    // buffers (the next op's x copied while this op computes) when they are
+    // small beside the rings.
     const int cap = max_smem_optin();
     const int x_off = MULTI_X_OFF;
-    const int ring_off = (x_off + maxK * 4 + 127) / 128 * 128;
+    const int x_floats = x_padded_floats(maxK);
+    const int x_buffers = 2 * x_floats * 4 <= t.multi_x2_max ? 2 : 1;
+    const int ring_off = (x_off + x_buffers * x_floats * 4 + 127) / 128 * 128;
     const long long budget = (long long)cap - ring_off;
     if (budget < (long long)D * slot_min) return BQ_ERR_SHAPE;
-    int nwarps = (int)std::min<long long>(MULTI_MAX_WARPS, budget / ((long long)D * slot_min));
+    int nwarps = (int)std::min<long long>(multi_max_warps(qtype, 1), budget / ((long long)D * slot_min));
     if (t.multi_warps) nwarps = std::min(nwarps, t.multi_warps);
     const int slot_cap = (int)(budget / ((long long)nwarps * D)) / 128 * 128;
     // pass 2: per op, whole rows in a slot when they fit, else the largest
@@ -456,34 +390,16 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
     int slot_bytes = 0;
     for (int i = 0; i < n_ops; ++i) {
         MultiOp &m = mo[i];
-        int KCU = m.nsc, stride = 0, single = 0;
-        if ((long long)m.rpw * m.rb <= slot_cap) {
-            single = m.G >= 8 || (m.rb / 16) % 8 == m.G % 8;
-            stride = single ? m.rb : padded_stride(m.rb, m.G);
-            if ((long long)m.rpw * stride > slot_cap) single = 0, stride = 0;
-        }
-        if (!stride) {
-            single = 0;
-            for (int k = (m.nsc + m.G - 1) / m.G; k >= 1; --k) {
-                KCU = std::min(m.nsc, m.G * k);
-                stride = padded_stride(KCU * ub, m.G);
-                if ((long long)m.rpw * stride <= slot_cap) break;
-            }
-            if ((long long)m.rpw * stride > slot_cap) return BQ_ERR_SHAPE;
-        }
-        m.KCU = KCU;
-        m.row_stride = stride;
-        m.single = single;
-        m.nchunks = (m.nsc + KCU - 1) / KCU;
-        slot_bytes = std::max(slot_bytes, m.rpw * stride);
+        if (!multi_chunking(m, ub, slot_cap)) return BQ_ERR_SHAPE;
+        slot_bytes = std::max(slot_bytes, m.rpw * m.row_stride);
     }
     slot_bytes = (slot_bytes + 127) / 128 * 128;
     const size_t smem = (size_t)ring_off + (size_t)nwarps * D * slot_bytes;
     if (smem > (size_t)cap) return BQ_ERR_SHAPE;
     const int threads = nwarps * 32;
     int occ = 0;
-    const int err = qtype == BQ_Q8_0 ? bq_internal_multi_occupancy_q8_0(NR, threads, smem, &occ)
-                                     : bq_internal_multi_occupancy_q4_0(NR, threads, smem, &occ);
+    const int err = qtype == BQ_Q8_0 ? bq_internal_multi_occupancy_q8_0(NR, 1, threads, smem, &occ)
+                                     : bq_internal_multi_occupancy_q4_0(NR, 1, threads, smem, &occ);
     if (err != 0 || occ < 1) return BQ_ERR_CUDA;
     const int grid = std::min(MULTI_MAX_CTAS, num_sms_current() * occ);
     // byte-balanced contiguous tile ranges
@@ -509,7 +425,140 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
     geo->ring_off = ring_off;
     geo->smem = smem;
     geo->nr = NR;
+    geo->R = 1;
+    geo->x_rstride = x_floats;
+    geo->x_floats = x_floats;
+    geo->x_buffers = x_buffers;
+    geo->panel_units = 0;
     return BQ_OK;
+}
+
+// One warp-tile item layout for op m: whole rows in a slot of slot_cap bytes
+// when they fit, else chunks of a multiple of G units (bank-padded rows).
+bool multi_chunking(MultiOp &m, int ub, int slot_cap) {
+    int KCU = m.nsc, stride = 0, single = 0;
+    if ((long long)m.rpw * m.rb <= slot_cap) {
+        single = m.G >= 8 || (m.rb / 16) % 8 == m.G % 8;
+        stride = single ? m.rb : padded_stride(m.rb, m.G);
+        if ((long long)m.rpw * stride > slot_cap) single = 0, stride = 0;
+    }
+    if (!stride) {
+        single = 0;
+        for (int k = (m.nsc + m.G - 1) / m.G; k >= 1; --k) {
+            KCU = std::min(m.nsc, m.G * k);
+            stride = padded_stride(KCU * ub, m.G);
+            if ((long long)m.rpw * stride <= slot_cap) break;
+        }
+        if ((long long)m.rpw * stride > slot_cap) return false;
+    }
+    m.KCU = KCU;
+    m.row_stride = stride;
+    m.single = single;
+    m.nchunks = (m.nsc + KCU - 1) / KCU;
+    return true;
+}
+
+bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
+    const Tunables &t = tunables();
+    const int bb = block_bytes(c.qtype), ub = 8 * bb;
+    const int D = std::min(t.multi_d, MULTI_MAX_D);
+    const int R = c.R;
+    const int NR = 1;
+    const int nsms = num_sms_current();
+    const int cap = max_smem_optin();
+    if (nsms <= 0 || cap <= 0) return false;
+    std::memset(a, 0, sizeof *a);
+    MultiOp &m = a->op;
+    const bool gu = c.mode == MODE_GATE_UP;
+    m.W[0] = static_cast<const uint8_t *>(c.W0);
+    m.W[1] = gu ? static_cast<const uint8_t *>(c.W1) : nullptr;
+    m.x = c.x;
+    m.gamma = gu ? c.gamma : nullptr;
+    m.y = c.y;
+    m.eps = c.eps;
+    m.M = (int)c.M;
+    m.K = (int)c.K;
+    m.nsc = m.K / 256;
+    m.G = tree_lanes_for_units(m.nsc);
+    m.rpw = NR * (32 / m.G);
+    m.rb = m.nsc * ub;
+    m.nmat = gu ? 2 : 1;
+    m.ntiles = (int)((c.M + m.rpw - 1) / m.rpw);
+    m.tile_base = 0;
+    // x: the whole R x K input, or (verify with a large input) double-buffered
+    // panels of a multiple of G units
+    const int xpad = x_padded_floats(m.K);
+    int PU = 0, x_floats = R * xpad, x_rstride = xpad, x_buffers = 1;
+    if ((long long)R * xpad * 4 > t.single_x_max) {
+        if (gu || R == 1) return false;
+        PU = (int)(t.single_x_max / 2 / ((long long)R * 256 * 4)) / m.G * m.G;
+        if (PU < m.G) return false;
+        x_rstride = PU * 256;
+        x_floats = R * x_rstride;
+        x_buffers = 2;
+    }
+    const int ring_off = (MULTI_X_OFF + x_buffers * x_floats * 4 + 127) / 128 * 128;
+    const long long budget = (long long)cap - ring_off;
+    // warps: enough for the tiles of one CTA per SM, at most what fits
+    const int k1 = std::min(m.nsc, m.G);
+    const int slot_min = m.rpw * padded_stride(k1 * ub, m.G);
+    if (budget < (long long)D * slot_min) return false;
+    const int fit = (int)std::min<long long>(multi_max_warps(c.qtype, R), budget / ((long long)D * slot_min));
+    const int want = (int)std::min<long long>(fit, (m.ntiles + nsms - 1) / nsms);
+    int nwarps = std::max(1, want);
+    int slot_cap = (int)(budget / ((long long)nwarps * D)) / 128 * 128;
+    if (PU) {
+        // one unit per lane per item, so chunks never straddle a panel
+        m.KCU = m.G;
+        m.row_stride = padded_stride(m.G * ub, m.G);
+        m.single = 0;
+        m.nchunks = (m.nsc + m.G - 1) / m.G;
+        if ((long long)m.rpw * m.row_stride > slot_cap) return false;
+    } else if (!multi_chunking(m, ub, slot_cap)) {
+        return false;
+    }
+    const int slot_bytes = (m.rpw * m.row_stride + 127) / 128 * 128;
+    const size_t smem = (size_t)ring_off + (size_t)nwarps * D * slot_bytes;
+    if (smem > (size_t)cap) return false;
+    const int threads = nwarps * 32;
+    int occ = 0;
+    const int err = c.qtype == BQ_Q8_0 ? bq_internal_multi_occupancy_q8_0(NR, R, threads, smem, &occ)
+                                       : bq_internal_multi_occupancy_q4_0(NR, R, threads, smem, &occ);
+    if (err != 0 || occ < 1) return false;
+    // panel mode: every CTA holds at most nwarps tiles (one per warp); else a
+    // CTA's warps take its tiles round-robin, at most one CTA wave
+    long long grid = (m.ntiles + nwarps - 1) / nwarps;
+    if (!PU) grid = std::min<long long>(grid, (long long)nsms * occ);
+    a->ops = nullptr;
+    a->cta_tiles = nullptr;
+    a->nops = 1;
+    a->nwarps = nwarps;
+    a->D = D;
+    a->slot_bytes = slot_bytes;
+    a->x_off = MULTI_X_OFF;
+    a->ring_off = ring_off;
+    a->nr = NR;
+    a->R = R;
+    a->x_rstride = x_rstride;
+    a->x_floats = x_floats;
+    a->x_buffers = x_buffers;
+    a->panel_units = PU;
+    a->inline_op = 1;
+    geo->grid = (int)grid;
+    geo->threads = threads;
+    geo->nwarps = nwarps;
+    geo->D = D;
+    geo->slot_bytes = slot_bytes;
+    geo->x_off = MULTI_X_OFF;
+    geo->ring_off = ring_off;
+    geo->smem = smem;
+    geo->nr = NR;
+    geo->R = R;
+    geo->x_rstride = x_rstride;
+    geo->x_floats = x_floats;
+    geo->x_buffers = x_buffers;
+    geo->panel_units = PU;
+    return true;
 }
 
 bool tunables_multi() { return tunables().multi != 0; }
@@ -525,6 +574,12 @@ void fill_multi_args(const MultiGeometry &geo, int n_ops, const MultiOp *ops,
     a->x_off = geo.x_off;
     a->ring_off = geo.ring_off;
     a->nr = geo.nr;
+    a->R = geo.R;
+    a->x_rstride = geo.x_rstride;
+    a->x_floats = geo.x_floats;
+    a->x_buffers = geo.x_buffers;
+    a->panel_units = geo.panel_units;
+    a->inline_op = 0;
 }
 
 void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const ExecX *xs,
@@ -576,8 +631,18 @@ bq_status check_shape(long long M, long long K) {
 }
 
 bq_status run_gemv(const GemvCall &c) {
+    if (c.K % 256 == 0) {
+        bq::MultiArgs a;
+        bq::MultiGeometry g;
+        if (!bq::plan_multi_single(c, &a, &g)) return BQ_ERR_CUDA;
+        const int pdl = bq::tunables().single_pdl;
+        const int e = c.qtype == BQ_Q8_0
+                          ? bq_internal_multi_launch_q8_0(a, g.grid, g.threads, g.smem, c.stream, pdl)
+                          : bq_internal_multi_launch_q4_0(a, g.grid, g.threads, g.smem, c.stream, pdl);
+        return from_cuda(e);
+    }
     LaunchPlan p;
-    if (!bq::plan_gemv(c, &p)) return BQ_ERR_CUDA;
+    bq::plan_gemv(c, &p);
     const int e = c.qtype == BQ_Q8_0 ? bq_internal_launch_q8_0(c, p) : bq_internal_launch_q4_0(c, p);
     return from_cuda(e);
 }
@@ -761,9 +826,9 @@ bq_status bq_stream_plan_launch(const bq_stream_plan *plan, void *stream) {
     if (plan->multi) {
         const int e = plan->qtype == BQ_Q8_0
                           ? bq_internal_multi_launch_q8_0(plan->margs, plan->grid, plan->threads,
-                                                          plan->smem, stream)
+                                                          plan->smem, stream, 0)
                           : bq_internal_multi_launch_q4_0(plan->margs, plan->grid, plan->threads,
-                                                          plan->smem, stream);
+                                                          plan->smem, stream, 0);
         return from_cuda(e);
     }
     auto s = static_cast<cudaStream_t>(stream);

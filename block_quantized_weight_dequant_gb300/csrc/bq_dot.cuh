@@ -284,54 +284,59 @@ __device__ __forceinline__ void unit_dot(const uint32_t *const (&w)[NW], int nbk
     if (nbk > 7) block_dot<QT, NW, R, 7>(w, xv, c);
 }
 
-// NR weight rows against one x view, one full unit each: c[r] receives row
-// r's unit partial with exactly unit_dot's operation sequence, so the bits do
-// not depend on NR.  up[r] is the unit's first byte in shared memory (16-byte
-// aligned).  Weights are read block by block: the bytes of block b lie in the
-// 16-byte chunks floor(34b/16) .. +2 for Q8_0 (always three chunks) and
+// NR weight rows against R input rows of one x view, one full unit each:
+// c[v][r] receives the unit partial of weight row v against input row r with
+// exactly unit_dot's operation sequence, so the bits depend on neither NR nor
+// R.  up[v] is the unit's first byte in shared memory (16-byte aligned).
+// Weights are read block by block: the bytes of block b lie in the 16-byte
+// chunks floor(34b/16) .. +2 for Q8_0 (always three chunks) and
 // floor(18b/16) .. +1 for Q4_0 (always two), so a row holds one block's words
 // in registers while every x value read from shared memory serves NR rows.
-template <int QT, int NR, int B, class XV>
+template <int QT, int NR, int R, int B, class XV>
 __device__ __forceinline__ void rows_block(const uint8_t *const (&up)[NR], const XV &xv,
-                                           float (&c)[NR]) {
+                                           float (&c)[NR][R]) {
     constexpr int bb = Fmt<QT>::block_bytes;
     constexpr int off = bb * B;
     constexpr int c0 = off / 16;
     constexpr int nch = (off + bb - 1) / 16 - c0 + 1;
     uint32_t w[NR][4 * nch];
 #pragma unroll
-    for (int r = 0; r < NR; ++r)
+    for (int v = 0; v < NR; ++v)
 #pragma unroll
         for (int k = 0; k < nch; ++k) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(up[r] + 16 * (c0 + k));
-            w[r][4 * k + 0] = v.x;
-            w[r][4 * k + 1] = v.y;
-            w[r][4 * k + 2] = v.z;
-            w[r][4 * k + 3] = v.w;
+            const uint4 q = *reinterpret_cast<const uint4 *>(up[v] + 16 * (c0 + k));
+            w[v][4 * k + 0] = q.x;
+            w[v][4 * k + 1] = q.y;
+            w[v][4 * k + 2] = q.z;
+            w[v][4 * k + 3] = q.w;
         }
     const uint32_t *ws[NR];
 #pragma unroll
-    for (int r = 0; r < NR; ++r) ws[r] = w[r];
-    float s[NR][1], d[NR];
-    block_sum_at<QT, NR, 1, B, off - 16 * c0>(ws, xv, s, d);
+    for (int v = 0; v < NR; ++v) ws[v] = w[v];
+    float s[NR][R], d[NR];
+    block_sum_at<QT, NR, R, B, off - 16 * c0>(ws, xv, s, d);
 #pragma unroll
-    for (int r = 0; r < NR; ++r) c[r] = __fmaf_rn(d[r], s[r][0], c[r]);
+    for (int v = 0; v < NR; ++v)
+#pragma unroll
+        for (int r = 0; r < R; ++r) c[v][r] = __fmaf_rn(d[v], s[v][r], c[v][r]);
 }
 
-template <int QT, int NR, class XS>
+template <int QT, int NR, int R, class XS>
 __device__ __forceinline__ void unit_dot_rows(const uint8_t *const (&up)[NR], const XS &xs, int e0,
-                                              float (&c)[NR]) {
+                                              float (&c)[NR][R]) {
 #pragma unroll
-    for (int r = 0; r < NR; ++r) c[r] = -0.0f;
+    for (int v = 0; v < NR; ++v)
+#pragma unroll
+        for (int r = 0; r < R; ++r) c[v][r] = -0.0f;
     const auto xv = xs.at(e0);
-    rows_block<QT, NR, 0>(up, xv, c);
-    rows_block<QT, NR, 1>(up, xv, c);
-    rows_block<QT, NR, 2>(up, xv, c);
-    rows_block<QT, NR, 3>(up, xv, c);
-    rows_block<QT, NR, 4>(up, xv, c);
-    rows_block<QT, NR, 5>(up, xv, c);
-    rows_block<QT, NR, 6>(up, xv, c);
-    rows_block<QT, NR, 7>(up, xv, c);
+    rows_block<QT, NR, R, 0>(up, xv, c);
+    rows_block<QT, NR, R, 1>(up, xv, c);
+    rows_block<QT, NR, R, 2>(up, xv, c);
+    rows_block<QT, NR, R, 3>(up, xv, c);
+    rows_block<QT, NR, R, 4>(up, xv, c);
+    rows_block<QT, NR, R, 5>(up, xv, c);
+    rows_block<QT, NR, R, 6>(up, xv, c);
+    rows_block<QT, NR, R, 7>(up, xv, c);
 }
 
 // load a full unit from shared memory (16-byte aligned)
@@ -438,13 +443,15 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 // depend on the number of threads: 256 virtual lanes v each sum x[v],
 // x[v+256], ... in order; the 256 lane sums are folded by a fixed tree.
 // Called by `nthr` threads (thread index tid) sharing `red` (>= 257 floats);
-// `sync` is a barrier over exactly those threads.
-template <class Sync>
-__device__ float rms_scale(const float *x, int K, float eps, float *red, int tid, int nthr,
-                           Sync sync) {
+// `sync` is a barrier over exactly those threads; `xat(k)` returns x[k].
+template <class XAt, class Sync>
+__device__ float rms_scale_at(XAt xat, int K, float eps, float *red, int tid, int nthr, Sync sync) {
     for (int v = tid; v < 256; v += nthr) {
         float s = 0.0f;
-        for (int k = v; k < K; k += 256) s = __fmaf_rn(x[k], x[k], s);
+        for (int k = v; k < K; k += 256) {
+            const float t = xat(k);
+            s = __fmaf_rn(t, t, s);
+        }
         red[v] = s;
     }
     sync();
@@ -458,6 +465,12 @@ __device__ float rms_scale(const float *x, int K, float eps, float *red, int tid
     sync();
     const float ms = __fdiv_rn(red[256], (float)K);
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+template <class Sync>
+__device__ float rms_scale(const float *x, int K, float eps, float *red, int tid, int nthr,
+                           Sync sync) {
+    return rms_scale_at([x](int k) { return x[k]; }, K, eps, red, tid, nthr, sync);
 }
 
 }  // namespace bq

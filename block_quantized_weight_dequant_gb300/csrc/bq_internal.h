@@ -10,12 +10,6 @@ namespace bq {
 constexpr int MODE_PLAIN = 0;    // y = W x  (R input rows: R = 1 decode, R > 1 verify)
 constexpr int MODE_GATE_UP = 1;  // y = silu(Wg xn) * (Wu xn)
 
-constexpr int PLAN_STREAM = 0;   // TMA-staged streaming kernel (K % 256 == 0)
-constexpr int PLAN_GENERIC = 1;  // direct global loads (any K % 32 == 0)
-
-// shared-memory header of the streaming kernel: mbarriers, flags, reduction scratch
-constexpr int HDR_BYTES = 2048;
-
 struct GemvCall {
     int qtype, mode, R;
     const void *W0, *W1;
@@ -26,39 +20,22 @@ struct GemvCall {
     void *stream;
 };
 
-// Launch geometry.  Only G affects results (it fixes the row's summation
-// tree); everything else is free to tune.
+// generic-kernel geometry (K % 256 != 0).  G fixes the row's summation tree.
 struct LaunchPlan {
-    int kind;
     int G;           // lanes per row
-    int nsc;         // 8-block units per row
     long long rb;    // packed bytes per row
-    int NWC;         // consumer warps per CTA
-    int TR;          // rows per tile
-    int KCU;         // units per row per stage
-    int NS;          // stages in the ring
-    int nchunks;     // stages per tile
-    int ntiles;
-    int row_stride;  // shared-memory bytes per row in a stage
-    int mat_stride;  // shared-memory bytes per matrix in a stage
-    int stage_bytes;
-    int single_copy; // one bulk copy per stage (rows contiguous, no padding)
-    int xres;        // x resident in shared memory
-    int x_off, x_rstride, stage_off;
-    size_t smem;
-    int num_sms;
 };
 
 // lanes per row for a row of nsc units: the largest power of two G <= 32 whose
 // padding to a multiple of G wastes at most 1/8 of the lane slots
 int tree_lanes_for_units(long long nsc);
 
-// plan a GEMV call on the current device; returns false if it cannot be planned
-bool plan_gemv(const GemvCall &c, LaunchPlan *p);
+// plan a generic-kernel GEMV call
+void plan_gemv(const GemvCall &c, LaunchPlan *p);
 
 }  // namespace bq
 
-// per-format launchers (one translation unit each) and their device status words
+// per-format generic launchers (one translation unit each) and their device status words
 int bq_internal_launch_q8_0(const bq::GemvCall &c, const bq::LaunchPlan &p);
 int bq_internal_launch_q4_0(const bq::GemvCall &c, const bq::LaunchPlan &p);
 int bq_internal_status_q8_0(unsigned int *flags, int clear);
@@ -85,9 +62,10 @@ void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const
 struct MultiOp;
 struct MultiArgs;
 constexpr int MULTI_MAX_CTAS = 1024;
-// launch geometry of a multi-op (independent GEMVs) run
+// launch geometry of a multi-op kernel run
 struct MultiGeometry {
-    int grid, threads, nwarps, D, slot_bytes, x_off, ring_off, nr;
+    int grid, threads, nwarps, D, slot_bytes, x_off, ring_off, nr, R;
+    int x_rstride, x_floats, x_buffers, panel_units;
     size_t smem;
 };
 // Plan a list of ops none of which depends on another (validated by
@@ -98,15 +76,20 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
                             MultiGeometry *geo);
 void fill_multi_args(const MultiGeometry &geo, int n_ops, const MultiOp *ops,
                      const int *cta_tiles, MultiArgs *a);
+// Plan one GEMV, gate+up or verify call (K % 256 == 0) as an inline op of the
+// multi-op kernel; false if it cannot be planned.
+bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo);
 // whether independent op lists use the multi-op kernel (tuning switch)
 bool tunables_multi();
 }
-int bq_internal_multi_occupancy_q8_0(int nr, int threads, size_t smem, int *occ);
-int bq_internal_multi_occupancy_q4_0(int nr, int threads, size_t smem, int *occ);
+// per-format occupancy and launch of the multi-op kernel instance (nr, R);
+// `pdl` allows programmatic dependent launch (single calls)
+int bq_internal_multi_occupancy_q8_0(int nr, int R, int threads, size_t smem, int *occ);
+int bq_internal_multi_occupancy_q4_0(int nr, int R, int threads, size_t smem, int *occ);
 int bq_internal_multi_launch_q8_0(const bq::MultiArgs &a, int grid, int threads, size_t smem,
-                                  void *stream);
+                                  void *stream, int pdl);
 int bq_internal_multi_launch_q4_0(const bq::MultiArgs &a, int grid, int threads, size_t smem,
-                                  void *stream);
+                                  void *stream, int pdl);
 // persistent per-token stream executor (bq_exec.cuh), one instantiation per format
 int bq_internal_exec_occupancy_q8_0(int threads, size_t smem, int *occ);
 int bq_internal_exec_occupancy_q4_0(int threads, size_t smem, int *occ);

@@ -1,18 +1,38 @@
-// bq_multi.cuh -- one launch for a list of INDEPENDENT GEMVs (a per-token
-// weight stream whose ops read no output of another op of the list).
+// bq_multi.cuh -- the streaming GEMV kernel: one launch for a list of
+// INDEPENDENT GEMVs (a per-token weight stream whose ops read no output of
+// another op of the list), or for one single call (decode GEMV, gate+up+SiLU,
+// or the R-row verify GEMV).
 //
 // The tiles of all ops are concatenated in list order; a tile is the rows one
-// warp evaluates at once (32 / G rows, G lanes per row).  Each CTA takes a
+// warp evaluates at once (NR * 32/G rows, G lanes per row).  Each CTA takes a
 // contiguous, byte-balanced range of tiles and its warps take the range's
 // tiles round-robin.  Every warp feeds itself: it owns a ring of D shared-
 // memory slots, issues the 1-D bulk copies (TMA) of its own next items into
-// them and waits on each slot's mbarrier.  There is no producer warp and no
-// hand-off between warps, so each warp keeps D - 1 items in flight while it
-// decodes one.  An item is one K-chunk (KCU units) of one matrix of a tile.
-// When the range enters a new op, all warps meet at a barrier and stage the
-// op's (RMSNorm-ed) x into shared memory; the copies of the new op's weights
-// are already in flight by then.  Arithmetic is bq_dot.cuh's fixed tree:
-// every output is bit-identical to the single-op kernels.
+// them and waits on each slot's mbarrier, sleeping in the wait (suspend-time
+// hint) rather than spinning.  There is no producer warp and no hand-off
+// between warps, so each warp keeps D - 1 items in flight while it decodes
+// one.  An item is one K-chunk (KCU units) of one matrix of a tile.
+//
+// x phases.  All warps meet at the start of each op (or, in panel mode, each
+// K-panel of the single op) to stage its x -- R input rows, RMSNorm-ed for
+// gate+up -- into shared memory with 16-byte cp.async copies; the weight
+// copies of the new op are already in flight by then.  With two x buffers the
+// next phase's x is copied while the current phase computes.  Panel mode
+// serves a verify call whose R x K input does not fit in shared memory: the
+// op's K range is cut into panels of whole chunks, each warp holds at most one
+// tile (its partial sums persist across panels), and the panels are staged in
+// order.
+//
+// Single calls carry their one op in the kernel parameters ("inline"), so no
+// descriptor table is needed; they are launched with programmatic dependent
+// launch allowed: the kernel lets its dependents start at once, prefetches
+// its first weight items into L2, and only then waits for the kernel before it
+// in the stream (griddepcontrol.wait) before reading any input.  A prefetch is
+// a hint that binds no value, so this is safe even if the kernel before wrote
+// the weights.
+//
+// Arithmetic is bq_dot.cuh's fixed tree: every output is bit-identical to the
+// single-op kernels and across R.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -25,9 +45,9 @@ namespace bq {
 
 struct MultiOp {
     const uint8_t *W[2];
-    const float *x;
-    const float *gamma;
-    float *y;
+    const float *x;          // [R][K]
+    const float *gamma;      // gate+up RMSNorm gain, or null
+    float *y;                // [R][M]
     float eps;
     int M, K, rb, nsc;
     int G, rpw;              // lanes per row, rows per tile (NR * 32 / G)
@@ -37,19 +57,33 @@ struct MultiOp {
 };
 
 struct MultiArgs {
-    const MultiOp *ops;
+    const MultiOp *ops;    // op table in global memory (not used with an inline op)
     const int *cta_tiles;  // [grid + 1]: CTA c takes tiles [cta_tiles[c], cta_tiles[c+1])
     int nops;
     int nwarps, D, slot_bytes;  // warps per CTA, ring slots per warp, bytes per slot
-    int x_off, ring_off;
-    int nr;                     // weight rows per lane (the kernel's NR)
+    int x_off, ring_off;        // shared-memory offsets of the x buffers and the rings
+    int nr, R;                  // weight rows per lane; input rows (1, or 2..6 for verify)
+    int x_rstride;              // floats between staged input rows
+    int x_floats;               // floats per x buffer
+    int x_buffers;              // 1 or 2
+    int panel_units;            // 0: an op's whole x is staged; else units of K per panel
+    int inline_op;              // 1: `op` is the only op; CTA c takes tiles [cT/grid, (c+1)T/grid)
+    MultiOp op;
 };
 
 constexpr int MULTI_MAX_WARPS = 16;
+// Warps per CTA at most, per instance: verify instances (R > 1) hold R partial
+// sums per row and run at most 8 warps; Q8_0 decode runs at most 12 (its
+// items are large, so shared memory allows about 12 anyway, and the bound
+// leaves registers for the unrolled dot product); Q4_0 decode up to 16.
+__host__ __device__ constexpr int multi_max_warps(int QT, int R) {
+    return R > 1 ? 8 : QT == 8 ? 12 : MULTI_MAX_WARPS;
+}
 constexpr int MULTI_MAX_D = 4;
-// shared memory header: mbarriers [0, 512), reduction scratch [768, 1796),
-// abort flag at 2040, x from MULTI_X_OFF
+// shared memory header: mbarriers [0, 512), inline op [512, 768), reduction
+// scratch [768, 1796), abort flag at 2040, x buffers from MULTI_X_OFF
 constexpr int MULTI_X_OFF = 2048;
+static_assert(sizeof(MultiOp) <= 256, "the inline op fits its header slot");
 
 // One warp's position in its item sequence (tiles t = first, first + nwarps,
 // ...; per tile its matrices, per matrix its K-chunks) together with the
@@ -57,90 +91,148 @@ constexpr int MULTI_X_OFF = 2048;
 // cursor enters a new op.
 struct MultiCursor {
     int t, op, m, c;
-    const uint8_t *W0, *W1;
-    int rpw, tile_base, tile_end, M, KCU, nsc, rb, nchunks, nmat, single, row_stride;
+    const uint8_t *W;  // the current matrix (W[m] of the op)
+    int rpw, tile_base, tile_end, M, KCU, rb, nchunks, nmat;
+    int row_stride;    // slot bytes per tile row; negative: rows copied as one block
 };
 
 // the op holding tile t, walking forward from op index `op`
-__device__ __forceinline__ int multi_op_of(const MultiArgs &a, int t, int op) {
-    while (op + 1 < a.nops && __ldg(&a.ops[op + 1].tile_base) <= t) ++op;
+__device__ __forceinline__ int multi_op_of(const MultiOp *ops, int nops, int t, int op) {
+    while (op + 1 < nops && ops[op + 1].tile_base <= t) ++op;
     return op;
 }
 
-__device__ __forceinline__ void multi_load_op(const MultiArgs &a, MultiCursor &q) {
-    const MultiOp &o = a.ops[q.op];
-    q.W0 = reinterpret_cast<const uint8_t *>(__ldg(reinterpret_cast<const unsigned long long *>(&o.W[0])));
-    q.W1 = reinterpret_cast<const uint8_t *>(__ldg(reinterpret_cast<const unsigned long long *>(&o.W[1])));
-    q.rpw = __ldg(&o.rpw);
-    q.tile_base = __ldg(&o.tile_base);
-    q.tile_end = q.tile_base + __ldg(&o.ntiles);
-    q.M = __ldg(&o.M);
-    q.KCU = __ldg(&o.KCU);
-    q.nsc = __ldg(&o.nsc);
-    q.rb = __ldg(&o.rb);
-    q.nchunks = __ldg(&o.nchunks);
-    q.nmat = __ldg(&o.nmat);
-    q.single = __ldg(&o.single);
-    q.row_stride = __ldg(&o.row_stride);
+__device__ __forceinline__ void multi_load_op(const MultiOp *ops, MultiCursor &q) {
+    const MultiOp &o = ops[q.op];
+    q.W = o.W[0];
+    q.rpw = o.rpw;
+    q.tile_base = o.tile_base;
+    q.tile_end = o.tile_base + o.ntiles;
+    q.M = o.M;
+    q.KCU = o.KCU;
+    q.rb = o.rb;
+    q.nchunks = o.nchunks;
+    q.nmat = o.nmat;
+    q.row_stride = o.single ? -1 : o.row_stride;
+}
+
+// the rows and byte range of the item under the cursor
+struct MultiItem {
+    const uint8_t *src;
+    int rows;
+    uint32_t rowb;
+};
+template <int QT>
+__device__ __forceinline__ MultiItem multi_item(const MultiCursor &q) {
+    constexpr int UB = Fmt<QT>::unit_bytes;
+    const int row0 = (q.t - q.tile_base) * q.rpw;
+    const int b0 = q.c * q.KCU * UB;
+    MultiItem it;
+    it.rows = min(q.rpw, q.M - row0);
+    it.rowb = (uint32_t)min(q.KCU * UB, q.rb - b0);
+    it.src = q.W + (size_t)row0 * q.rb + b0;
+    return it;
 }
 
 template <int QT>
 __device__ __forceinline__ void multi_issue(const MultiCursor &q, uint8_t *st, uint64_t *bar,
                                             uint64_t pol, int lane) {
-    constexpr int UB = Fmt<QT>::unit_bytes;
-    const int row0 = (q.t - q.tile_base) * q.rpw;
-    const int rows = min(q.rpw, q.M - row0);
-    const int u0 = q.c * q.KCU;
-    const uint32_t rowb = (uint32_t)min(q.KCU, q.nsc - u0) * UB;
-    const uint8_t *W = q.m ? q.W1 : q.W0;
+    const MultiItem it = multi_item<QT>(q);
     // the slot's previous contents were read by this warp's generic loads
     __syncwarp();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    if (lane == 0) mbar_arrive_expect_tx(bar, rowb * rows);
+    if (lane == 0) mbar_arrive_expect_tx(bar, it.rowb * it.rows);
     __syncwarp();
-    if (q.single) {
-        if (lane == 0) bulk_g2s(st, W + (size_t)row0 * q.rb, rowb * rows, bar, pol);
+    if (q.row_stride < 0) {
+        if (lane == 0) bulk_g2s(st, it.src, it.rowb * it.rows, bar, pol);
     } else {
-        for (int r = lane; r < rows; r += 32)
-            bulk_g2s(st + r * q.row_stride, W + (size_t)(row0 + r) * q.rb + (size_t)u0 * UB, rowb,
-                     bar, pol);
+        for (int r = lane; r < it.rows; r += 32)
+            bulk_g2s(st + r * q.row_stride, it.src + (size_t)r * q.rb, it.rowb, bar, pol);
     }
 }
 
-__device__ __forceinline__ void multi_advance(const MultiArgs &a, MultiCursor &q) {
+// the same bytes into L2 only (a hint: no completion, no value bound)
+template <int QT>
+__device__ __forceinline__ void multi_prefetch(const MultiCursor &q, int lane) {
+    const MultiItem it = multi_item<QT>(q);
+    if (q.row_stride < 0) {
+        if (lane == 0) bulk_prefetch_l2(it.src, it.rowb * it.rows);
+    } else {
+        for (int r = lane; r < it.rows; r += 32) bulk_prefetch_l2(it.src + (size_t)r * q.rb, it.rowb);
+    }
+}
+
+__device__ __forceinline__ void multi_advance(const MultiOp *ops, int nops, int nwarps,
+                                              MultiCursor &q) {
     if (++q.c < q.nchunks) return;
     q.c = 0;
-    if (++q.m < q.nmat) return;
+    if (++q.m < q.nmat) {
+        q.W = ops[q.op].W[q.m];
+        return;
+    }
     q.m = 0;
-    q.t += a.nwarps;
-    if (q.t >= q.tile_end && q.op + 1 < a.nops) {
-        q.op = multi_op_of(a, q.t, q.op);
-        multi_load_op(a, q);
+    q.t += nwarps;
+    if (q.t >= q.tile_end && q.op + 1 < nops) {
+        q.op = multi_op_of(ops, nops, q.t, q.op);
+        multi_load_op(ops, q);
+    } else if (q.nmat > 1) {
+        q.W = ops[q.op].W[0];
     }
 }
 
-// NR: weight rows per lane.  A tile is NR * 32/G rows; lane (rho, l) of a
-// warp takes rows rho, rho + 32/G, ... of the tile and units l, l + G, ... of
-// each, so every x value it reads from shared memory serves NR rows.
-template <int QT, int NR>
-__global__ void __launch_bounds__(MULTI_MAX_WARPS * 32, 1)
-    multi_kernel(const MultiArgs a, unsigned int *status) {
+__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
+                 : "memory");
+}
+
+// All threads: start the copies of elements [k0, k1) of every input row into
+// an x buffer (permuted chunk layout of XSmem, relative to k0), one group.
+__device__ __forceinline__ void multi_stage_x(const MultiOp &o, int R, int k0, int k1, float *dst,
+                                              int rstride, int tid, int nthr) {
+    const int n4 = (k1 - k0) >> 2;
+    for (int i = tid; i < R * n4; i += nthr) {
+        const int r = i / n4, c = i - r * n4;
+        cp_async_16(dst + r * rstride + 4 * x_chunk_pos(c), o.x + (size_t)r * o.K + k0 + 4 * c);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// NR: weight rows per lane; R: input rows.  A tile is NR * 32/G rows; lane
+// (rho, l) of a warp takes rows rho, rho + 32/G, ... of the tile and units
+// l, l + G, ... of each, so every x value it reads from shared memory serves
+// NR weight rows.
+template <int QT, int NR, int R>
+__global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
+    multi_kernel(const __grid_constant__ MultiArgs a, unsigned int *status) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [nwarps][D]
+    MultiOp *op_inline = reinterpret_cast<MultiOp *>(smem + 512);
     float *red = reinterpret_cast<float *>(smem + 768);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 2040);
-    float *xsm = reinterpret_cast<float *>(smem + a.x_off);
     constexpr int UB = Fmt<QT>::unit_bytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nthr = blockDim.x;
-    const int t_begin = a.cta_tiles[blockIdx.x], t_end = a.cta_tiles[blockIdx.x + 1];
 
+    // dependents may start now; they wait for this grid before reading
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.nwarps * a.D; ++i) mbar_init(full + i, 1);
         *abort_flag = 0;
+        if (a.inline_op) *op_inline = a.op;
         fence_mbar_init();
     }
     __syncthreads();
+    const MultiOp *ops = a.inline_op ? op_inline : a.ops;
+    const int nops = a.inline_op ? 1 : a.nops;
+    int t_begin, t_end;
+    if (a.inline_op) {
+        const long long T = op_inline->ntiles;
+        t_begin = (int)(T * blockIdx.x / gridDim.x);
+        t_end = (int)(T * (blockIdx.x + 1) / gridDim.x);
+    } else {
+        t_begin = a.cta_tiles[blockIdx.x];
+        t_end = a.cta_tiles[blockIdx.x + 1];
+    }
     if (t_begin >= t_end) return;
 
     uint64_t *wfull = full + warp * a.D;
@@ -148,123 +240,187 @@ __global__ void __launch_bounds__(MULTI_MAX_WARPS * 32, 1)
     const uint64_t pol = l2_policy_evict_first();
     int op0 = 0;
     {
-        int lo = 0, hi = a.nops - 1;  // last op with tile_base <= t_begin
+        int lo = 0, hi = nops - 1;  // last op with tile_base <= t_begin
         while (lo < hi) {
             const int mid = (lo + hi + 1) / 2;
-            if (__ldg(&a.ops[mid].tile_base) <= t_begin) lo = mid;
+            if (ops[mid].tile_base <= t_begin) lo = mid;
             else hi = mid - 1;
         }
         op0 = lo;
     }
-    const int op_last = multi_op_of(a, t_end - 1, op0);
+    const int op_last = multi_op_of(ops, nops, t_end - 1, op0);
 
-    // fill the ring with this warp's first D items
     MultiCursor q;
     q.t = t_begin + warp;
     q.m = q.c = 0;
-    q.op = multi_op_of(a, q.t, op0);
-    multi_load_op(a, q);
+    q.op = multi_op_of(ops, nops, q.t, op0);
+    multi_load_op(ops, q);
+    // this warp's first items into L2 while the kernel before may still run
+    {
+        MultiCursor f = q;
+        for (int i = 0; i < a.D && f.t < t_end; ++i) {
+            multi_prefetch<QT>(f, lane);
+            multi_advance(ops, nops, a.nwarps, f);
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // fill the ring with this warp's first D items
     int issued = 0;
     for (; issued < a.D && q.t < t_end; ++issued) {
         multi_issue<QT>(q, ring + (size_t)issued * a.slot_bytes, wfull + issued, pol, lane);
-        multi_advance(a, q);
+        multi_advance(ops, nops, a.nwarps, q);
+    }
+
+    auto sync = []() { __syncthreads(); };
+    auto xbuf = [&](int i) {
+        return reinterpret_cast<float *>(smem + a.x_off) + (size_t)(i % a.x_buffers) * a.x_floats;
+    };
+    // panel mode exists only in the verify instances (R > 1)
+    const int PU = R > 1 ? a.panel_units : 0;
+    auto n_panels = [&](const MultiOp &o) { return PU ? (o.nsc + PU - 1) / PU : 1; };
+    // x phase i = (op, panel); the first phase's copies start now
+    {
+        const MultiOp &o = ops[op0];
+        multi_stage_x(o, R, 0, PU ? min(o.K, PU * 256) : o.K, xbuf(0), a.x_rstride, threadIdx.x, nthr);
     }
 
     int e = 0, landed = 0;  // items consumed (or skipped after an error); items seen landed
     bool ok = true;
-    auto sync = []() { __syncthreads(); };
+    int phase = 0;
     for (int op = op0; op <= op_last; ++op) {
-        const MultiOp &o = a.ops[op];
-        const float *x = o.x, *gamma = o.gamma;
+        const MultiOp &o = ops[op];
+        const float *gamma = o.gamma;
         float *y = o.y;
         const int M = o.M, K = o.K, nsc = o.nsc, G = o.G, rpw = o.rpw, KCU = o.KCU;
         const int nchunks = o.nchunks, nmat = o.nmat, tile_base = o.tile_base, ntiles = o.ntiles;
         const int row_stride = o.row_stride;
-        // every warp is done with the previous op's x: stage this op's
-        sync();
-        float rs = 1.0f;
-        if (gamma) rs = rms_scale(x, K, o.eps, red, threadIdx.x, nthr, sync);
-        for (int k = 4 * threadIdx.x; k < K; k += 4 * nthr) {
-            float4 v = __ldg(reinterpret_cast<const float4 *>(x + k));
-            if (gamma) {
-                const float4 g = __ldg(reinterpret_cast<const float4 *>(gamma + k));
-                v = make_float4(__fmul_rn(__fmul_rn(v.x, rs), g.x), __fmul_rn(__fmul_rn(v.y, rs), g.y),
-                                __fmul_rn(__fmul_rn(v.z, rs), g.z), __fmul_rn(__fmul_rn(v.w, rs), g.w));
-            }
-            *reinterpret_cast<float4 *>(xsm + 4 * x_chunk_pos(k >> 2)) = v;
-        }
-        sync();
-
+        const int np = n_panels(o);
         const int lo = max(t_begin, tile_base), hi = min(t_end, tile_base + ntiles);
         // this warp's first tile in [lo, hi): (t - t_begin) mod nwarps == warp
-        int t = lo + ((warp - (lo - t_begin) % a.nwarps) + a.nwarps) % a.nwarps;
+        const int t_first = lo + ((warp - (lo - t_begin) % a.nwarps) + a.nwarps) % a.nwarps;
         const int rho = lane / G, l = lane & (G - 1), rg = 32 / G;
-        const XSmem xs{xsm, 0};
-        for (; t < hi; t += a.nwarps) {
-            const int row0 = (t - tile_base) * rpw;
-            const int rows = min(rpw, M - row0);
-            float p0[NR], p1[NR];
+        float p0[NR][R], p1[NR];
+        for (int pn = 0; pn < np; ++pn, ++phase) {
+            // ---- x of this phase: landed, visible to all, and the other buffer free ----
+            float *xa = xbuf(phase);
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            sync();
+            // the next phase's copies: at once into the other buffer, or, with
+            // one buffer, after every warp is done with this phase (below)
+            int nop = op, npn = pn + 1;
+            if (npn == np) {
+                nop = op + 1;
+                npn = 0;
+            }
+            const bool has_next = nop <= op_last;
+            auto stage_next = [&](float *dst) {
+                const MultiOp &n = ops[nop];
+                const int k0 = npn * PU * 256;
+                const int k1 = PU ? min(n.K, k0 + PU * 256) : n.K;
+                multi_stage_x(n, R, k0, k1, dst, a.x_rstride, threadIdx.x, nthr);
+            };
+            if (has_next && a.x_buffers == 2) stage_next(xbuf(phase + 1));
+            if (gamma) {
+                // RMSNorm in place (R == 1, whole K): the fixed tree of rms_scale
+                const float rs = rms_scale_at([xa](int k) { return xa[x_pos(k)]; }, K, o.eps, red,
+                                              threadIdx.x, nthr, sync);
+                for (int c = threadIdx.x; c < K / 4; c += nthr) {
+                    float4 *p = reinterpret_cast<float4 *>(xa + 4 * x_chunk_pos(c));
+                    const float4 v = *p;
+                    const float4 g = __ldg(reinterpret_cast<const float4 *>(gamma) + c);
+                    *p = make_float4(__fmul_rn(__fmul_rn(v.x, rs), g.x), __fmul_rn(__fmul_rn(v.y, rs), g.y),
+                                     __fmul_rn(__fmul_rn(v.z, rs), g.z), __fmul_rn(__fmul_rn(v.w, rs), g.w));
+                }
+                sync();
+            }
+            const XSmem xs{xa, a.x_rstride};
+            const int k0u = pn * PU;  // first unit of the panel
+            const int c_lo = PU ? k0u / KCU : 0;
+            const int c_hi = PU ? min(nchunks, (k0u + PU) / KCU) : nchunks;
+
+            for (int t = t_first; t < hi; t += a.nwarps) {
+                const int row0 = (t - tile_base) * rpw;
+                const int rows = min(rpw, M - row0);
+                if (pn == 0) {
 #pragma unroll
-            for (int r = 0; r < NR; ++r) p0[r] = p1[r] = -0.0f;
+                    for (int v = 0; v < NR; ++v) {
+                        p1[v] = -0.0f;
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                if (m >= nmat) break;
-                for (int c = 0; c < nchunks; ++c, ++e) {
-                    const int slot = e % a.D;
-                    if (ok) {
-                        if (*abort_flag) {
-                            ok = false;
-                        } else if (!__all_sync(0xffffffffu,
-                                               mbar_wait_bounded(wfull + slot, (e / a.D) & 1))) {
-                            if (lane == 0) {
-                                *abort_flag = 1;
-                                atomicOr(status, BQ_DEVERR_FULL_WAIT);
+                        for (int r = 0; r < R; ++r) p0[v][r] = -0.0f;
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    if (m >= nmat) break;
+                    for (int c = c_lo; c < c_hi; ++c, ++e) {
+                        const int slot = e % a.D;
+                        if (ok) {
+                            if (*abort_flag) {
+                                ok = false;
+                            } else if (!__all_sync(0xffffffffu,
+                                                   mbar_wait_bounded(wfull + slot, (e / a.D) & 1))) {
+                                if (lane == 0) {
+                                    *abort_flag = 1;
+                                    atomicOr(status, BQ_DEVERR_FULL_WAIT);
+                                }
+                                ok = false;
+                            } else {
+                                ++landed;
                             }
-                            ok = false;
-                        } else {
-                            ++landed;
+                        }
+                        if (!ok) continue;
+                        const int u0 = c * KCU;
+                        const int cnt = min(KCU, nsc - u0);
+                        const uint8_t *stp = ring + (size_t)slot * a.slot_bytes + rho * row_stride;
+                        // rows past the tile's end read stale slot bytes; their
+                        // results are dropped below
+                        if (rho < rows) {
+                            for (int ul = l; ul < cnt; ul += G) {
+                                const uint8_t *up[NR];
+#pragma unroll
+                                for (int v = 0; v < NR; ++v) up[v] = stp + v * rg * row_stride + ul * UB;
+                                float cc[NR][R];
+                                unit_dot_rows<QT, NR, R>(up, xs, (u0 + ul - k0u) * 256, cc);
+#pragma unroll
+                                for (int v = 0; v < NR; ++v) {
+                                    if (m == 0) {
+#pragma unroll
+                                        for (int r = 0; r < R; ++r) p0[v][r] = __fadd_rn(p0[v][r], cc[v][r]);
+                                    } else {
+                                        p1[v] = __fadd_rn(p1[v], cc[v][0]);
+                                    }
+                                }
+                            }
+                        }
+                        // refill the slot just read with the item D places ahead
+                        if (q.t < t_end) {
+                            multi_issue<QT>(q, ring + (size_t)slot * a.slot_bytes, wfull + slot, pol,
+                                            lane);
+                            multi_advance(ops, nops, a.nwarps, q);
+                            ++issued;
                         }
                     }
-                    if (!ok) continue;
-                    const int u0 = c * KCU;
-                    const int cnt = min(KCU, nsc - u0);
-                    const uint8_t *stp = ring + (size_t)slot * a.slot_bytes + rho * row_stride;
-                    // rows past the tile's end read stale slot bytes; their
-                    // results are dropped below
-                    if (rho < rows) {
-                        for (int ul = l; ul < cnt; ul += G) {
-                            const uint8_t *up[NR];
+                }
+                if (!ok || pn + 1 < np) continue;
 #pragma unroll
-                            for (int r = 0; r < NR; ++r) up[r] = stp + r * rg * row_stride + ul * UB;
-                            float cc[NR];
-                            unit_dot_rows<QT, NR>(up, xs, (u0 + ul) * 256, cc);
+                for (int v = 0; v < NR; ++v) {
+                    const int row = rho + v * rg;
 #pragma unroll
-                            for (int r = 0; r < NR; ++r) {
-                                if (m == 0) p0[r] = __fadd_rn(p0[r], cc[r]);
-                                else p1[r] = __fadd_rn(p1[r], cc[r]);
-                            }
+                    for (int r = 0; r < R; ++r) {
+                        const float g = fold_lanes(p0[v][r], G);
+                        if (nmat == 2) {
+                            const float u = fold_lanes(p1[v], G);
+                            if (row < rows && l == 0) y[row0 + row] = silu_mul(g, u);
+                        } else if (row < rows && l == 0) {
+                            y[(size_t)r * M + row0 + row] = g;
                         }
-                    }
-                    // refill the slot just read with the item D places ahead
-                    if (q.t < t_end) {
-                        multi_issue<QT>(q, ring + (size_t)slot * a.slot_bytes, wfull + slot, pol,
-                                        lane);
-                        multi_advance(a, q);
-                        ++issued;
                     }
                 }
             }
-            if (!ok) continue;
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                const float g = fold_lanes(p0[r], G);
-                const int row = rho + r * rg;
-                if (nmat == 2) {
-                    const float u = fold_lanes(p1[r], G);
-                    if (row < rows && l == 0) y[row0 + row] = silu_mul(g, u);
-                } else if (row < rows && l == 0) {
-                    y[row0 + row] = g;
-                }
+            if (has_next && a.x_buffers == 1) {
+                sync();  // every warp is done reading this phase's x
+                stage_next(xa);
             }
         }
     }
@@ -274,6 +430,7 @@ __global__ void __launch_bounds__(MULTI_MAX_WARPS * 32, 1)
         for (int i = landed; i < issued; ++i)
             if (!mbar_wait_bounded(wfull + i % a.D, (i / a.D) & 1))
                 atomicOr(status, BQ_DEVERR_DRAIN_WAIT);
+    asm volatile("cp.async.wait_all;" ::: "memory");  // nor any x copy
 }
 
 }  // namespace bq

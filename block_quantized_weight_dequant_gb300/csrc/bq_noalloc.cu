@@ -91,8 +91,8 @@ extern "C" bq_status bq_stream_run_noalloc(int qtype, const bq_op *ops, int n_op
         bq::fill_multi_args(mg, n_ops, reinterpret_cast<const bq::MultiOp *>(scratch),
                             reinterpret_cast<const int *>(scratch + OFF_CT), &ma);
         const int e = qtype == BQ_Q8_0
-                          ? bq_internal_multi_launch_q8_0(ma, mg.grid, mg.threads, mg.smem, stream)
-                          : bq_internal_multi_launch_q4_0(ma, mg.grid, mg.threads, mg.smem, stream);
+                          ? bq_internal_multi_launch_q8_0(ma, mg.grid, mg.threads, mg.smem, stream, 0)
+                          : bq_internal_multi_launch_q4_0(ma, mg.grid, mg.threads, mg.smem, stream, 0);
         return e == 0 ? BQ_OK : BQ_ERR_CUDA;
     }
     // the copies read the host tables before returning (pageable source), so
