@@ -32,7 +32,7 @@ struct Tunables {
     int exec_slot = 0;     // stream executor: bytes per ring slot (0 = one warp tile of 32 units)
     int exec_nsw = 0;      // stream executor: slots per warp (0 = as many as fit, <= 4)
     int exec_warps = 8;    // stream executor: warps per CTA
-    int exec_rowmode_rows = 0;  // stream executor: row mode up to this many rows per warp (0: off)
+    int exec_rowmode_rows = 4;  // stream executor: row mode up to this many rows per warp (0: off)
     int exec_prefetch = 0;      // stream executor: L2 prefetch distance beyond the ring, in items (measured: no gain)
     int multi = 1;              // independent op lists: multi-op streaming kernel (0: executor)
     int multi_warps = 0;        // multi-op kernel: warps per CTA (0: as many as fit, <= 16)
@@ -41,6 +41,7 @@ struct Tunables {
     int multi_x2_max = 32 * 1024;    // op lists: two x buffers when together at most this
     int single_x_max = 128 * 1024;   // single calls: largest staged R x K input (else panels)
     int single_pdl = 1;              // single calls: allow programmatic dependent launch
+    int single_rowmode = 4;          // single calls: row mode up to this many unit tiles per SM (0: off)
 };
 
 const Tunables &tunables() {
@@ -68,6 +69,7 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "x2") && val >= 0) v.multi_x2_max = val;
             else if (!std::strcmp(tok, "sx") && val >= 16384) v.single_x_max = val;
             else if (!std::strcmp(tok, "pdl") && val >= 0 && val <= 1) v.single_pdl = val;
+            else if (!std::strcmp(tok, "srow") && val >= 0 && val <= 64) v.single_rowmode = val;
         }
         return v;
     }();
@@ -185,8 +187,8 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
         for (int j = st.x_begin; j < st.x_end; ++j)
             if (ex[j].x == o.x && ex[j].gamma == g && ex[j].eps == eps && ex[j].K == K) found = j;
         if (found < 0) {
-            ex[n_x] = ExecX{o.x, g, eps, K, stage_x, 0};
-            stage_x += x_padded_floats(K);
+            ex[n_x] = ExecX{o.x, g, eps, K, stage_x, g ? stage_x + x_padded_floats(K) : -1};
+            stage_x += (g ? 2 : 1) * x_padded_floats(K);
             found = n_x++;
             st.x_end = n_x;
         }
@@ -463,7 +465,7 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     const int bb = block_bytes(c.qtype), ub = 8 * bb;
     const int D = std::min(t.multi_d, MULTI_MAX_D);
     const int R = c.R;
-    const int NR = 1;
+    int NR = 1;
     const int nsms = num_sms_current();
     const int cap = max_smem_optin();
     if (nsms <= 0 || cap <= 0) return false;
@@ -499,15 +501,37 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     }
     const int ring_off = (MULTI_X_OFF + x_buffers * x_floats * 4 + 127) / 128 * 128;
     const long long budget = (long long)cap - ring_off;
+    const int maxw = multi_max_warps(c.qtype, R);
+    // Row mode for ops too small to give every warp a few tiles: a tile is a
+    // few whole rows and each row is evaluated block-parallel by the whole
+    // warp (same tree, about 8x shorter per-lane chains).  Latency-bound
+    // calls gain; large calls keep one unit per lane.
+    const bool rowmode = R == 1 && !PU && t.single_rowmode && m.nsc <= 16 &&
+                         m.ntiles <= (long long)t.single_rowmode * nsms &&
+                         D * (long long)m.rb <= budget;
+    if (rowmode) {
+        const long long per = (long long)nsms * maxw;
+        int rows = (int)std::min<long long>(32, std::max<long long>(1, (c.M + per - 1) / per));
+        while (rows > 1 && (long long)D * rows * m.rb > budget) --rows;
+        m.rowmode = 1;
+        m.rpw = rows;
+        m.ntiles = (int)((c.M + rows - 1) / rows);
+        NR = 0;
+    }
     // warps: enough for the tiles of one CTA per SM, at most what fits
     const int k1 = std::min(m.nsc, m.G);
-    const int slot_min = m.rpw * padded_stride(k1 * ub, m.G);
+    const int slot_min = rowmode ? m.rpw * m.rb : m.rpw * padded_stride(k1 * ub, m.G);
     if (budget < (long long)D * slot_min) return false;
-    const int fit = (int)std::min<long long>(multi_max_warps(c.qtype, R), budget / ((long long)D * slot_min));
+    const int fit = (int)std::min<long long>(maxw, budget / ((long long)D * slot_min));
     const int want = (int)std::min<long long>(fit, (m.ntiles + nsms - 1) / nsms);
     int nwarps = std::max(1, want);
     int slot_cap = (int)(budget / ((long long)nwarps * D)) / 128 * 128;
-    if (PU) {
+    if (rowmode) {
+        m.KCU = m.nsc;
+        m.row_stride = m.rb;
+        m.single = 1;
+        m.nchunks = 1;
+    } else if (PU) {
         // one unit per lane per item, so chunks never straddle a panel
         m.KCU = m.G;
         m.row_stride = padded_stride(m.G * ub, m.G);
@@ -518,7 +542,8 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
         return false;
     }
     const int slot_bytes = (m.rpw * m.row_stride + 127) / 128 * 128;
-    const size_t smem = (size_t)ring_off + (size_t)nwarps * D * slot_bytes;
+    // + slack: block-parallel rows read up to 4 bytes past a slot's last block
+    const size_t smem = (size_t)ring_off + (size_t)nwarps * D * slot_bytes + 128;
     if (smem > (size_t)cap) return false;
     const int threads = nwarps * 32;
     int occ = 0;

@@ -68,7 +68,7 @@ struct ExecX {
     const float *gamma;
     float eps;
     int K, off;  // off: float offset in the x area
-    int pad;
+    int goff;    // float offset of the gain's staged copy (gamma set), else -1
 };
 
 // 32 bytes
@@ -120,8 +120,8 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// One warp starts the copies of stage st's inputs into x buffer `xa`
-// (permuted layout of XSmem) with cp.async (16 bytes per lane and copy,
+// One warp starts the copies of stage st's inputs (and the RMSNorm gains)
+// into x buffer `xa` (x in the permuted layout of XSmem) with cp.async (16 bytes per lane and copy,
 // through L2, so data written by other CTAs before a stage barrier is seen),
 // then every lane arrives on `xfull` once its copies have landed (the
 // barrier expects 32 arrivals).
@@ -131,6 +131,10 @@ __device__ __forceinline__ void exec_load_x(const ExecStage &st, const ExecX *xs
         const ExecX &xd = xs[j];
         for (int c = lane; c < xd.K / 4; c += 32)
             cp_async16(xa + xd.off + 4 * x_chunk_pos(c), xd.x + 4 * c);
+        // the gain rides along (linear layout), so the RMSNorm reads it from
+        // shared memory instead of waiting on global loads one by one
+        if (xd.goff >= 0)
+            for (int c = lane; c < xd.K / 4; c += 32) cp_async16(xa + xd.goff + 4 * c, xd.gamma + 4 * c);
     }
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(xfull))
                  : "memory");
@@ -164,7 +168,7 @@ __device__ __forceinline__ void exec_norm_x_warp(const ExecStage &st, const Exec
         for (int c = lane; c < xd.K / 4; c += 32) {
             float4 *p = reinterpret_cast<float4 *>(xv + 4 * x_chunk_pos(c));
             const float4 x4 = *p;
-            const float4 g = __ldg(reinterpret_cast<const float4 *>(xd.gamma) + c);
+            const float4 g = *reinterpret_cast<const float4 *>(xa + xd.goff + 4 * c);
             *p = make_float4(__fmul_rn(__fmul_rn(x4.x, rs), g.x), __fmul_rn(__fmul_rn(x4.y, rs), g.y),
                              __fmul_rn(__fmul_rn(x4.z, rs), g.z), __fmul_rn(__fmul_rn(x4.w, rs), g.w));
         }

@@ -99,9 +99,11 @@ int multi_launch(const bq::MultiArgs &a, int grid, int threads, size_t smem, voi
 }
 }  // namespace
 
-// instances: NR = 1 for R = 1..6 (decode, gate+up, verify); NR = 2 for R = 1
+// instances: NR = 1 for R = 1..6 (decode, gate+up, verify); NR = 2 and row mode
+// (NR = 0) for R = 1
 int bq_internal_multi_occupancy_q4_0(int nr, int R, int threads, size_t smem, int *occ) {
     if (nr == 2 && R == 1) return multi_occupancy<2, 1>(threads, smem, occ);
+    if (nr == 0 && R == 1) return multi_occupancy<0, 1>(threads, smem, occ);
     if (nr != 1) return (int)cudaErrorInvalidValue;
     switch (R) {
         case 1: return multi_occupancy<1, 1>(threads, smem, occ);
@@ -120,6 +122,7 @@ int bq_internal_multi_launch_q4_0(const bq::MultiArgs &a, int grid, int threads,
     cudaError_t e = status_addr(&status);
     if (e != cudaSuccess) return (int)e;
     if (a.nr == 2 && a.R == 1) return multi_launch<2, 1>(a, grid, threads, smem, stream, pdl, status);
+    if (a.nr == 0 && a.R == 1) return multi_launch<0, 1>(a, grid, threads, smem, stream, pdl, status);
     if (a.nr != 1) return (int)cudaErrorInvalidValue;
     switch (a.R) {
         case 1: return multi_launch<1, 1>(a, grid, threads, smem, stream, pdl, status);

@@ -54,6 +54,7 @@ struct MultiOp {
     int KCU, nchunks, nmat;  // units per item row, items per tile and matrix, matrices (1 or 2)
     int ntiles, tile_base;   // tiles of this op; its first tile in the whole list
     int row_stride, single;  // slot bytes per tile row; rows copied as one block
+    int rowmode;             // 1: a tile is rpw whole rows, each evaluated by the whole warp
 };
 
 struct MultiArgs {
@@ -79,6 +80,7 @@ constexpr int MULTI_MAX_WARPS = 16;
 __host__ __device__ constexpr int multi_max_warps(int QT, int R) {
     return R > 1 ? 8 : QT == 8 ? 12 : MULTI_MAX_WARPS;
 }
+static_assert(MULTI_MAX_WARPS * 32 <= 1024, "one CTA");
 constexpr int MULTI_MAX_D = 4;
 // shared memory header: mbarriers [0, 512), inline op [512, 768), reduction
 // scratch [768, 1796), abort flag at 2040, x buffers from MULTI_X_OFF
@@ -200,7 +202,9 @@ __device__ __forceinline__ void multi_stage_x(const MultiOp &o, int R, int k0, i
 // NR: weight rows per lane; R: input rows.  A tile is NR * 32/G rows; lane
 // (rho, l) of a warp takes rows rho, rho + 32/G, ... of the tile and units
 // l, l + G, ... of each, so every x value it reads from shared memory serves
-// NR weight rows.
+// NR weight rows.  NR = 0 is row mode (R = 1): a tile is rpw whole rows, each
+// evaluated block-parallel by the whole warp (row_dot_blockpar: the same tree
+// with one block per lane), for calls too small to keep every lane busy.
 template <int QT, int NR, int R>
 __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
     multi_kernel(const __grid_constant__ MultiArgs a, unsigned int *status) {
@@ -300,7 +304,8 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
         // this warp's first tile in [lo, hi): (t - t_begin) mod nwarps == warp
         const int t_first = lo + ((warp - (lo - t_begin) % a.nwarps) + a.nwarps) % a.nwarps;
         const int rho = lane / G, l = lane & (G - 1), rg = 32 / G;
-        float p0[NR][R], p1[NR];
+        constexpr int NRA = NR ? NR : 1;
+        float p0[NRA][R], p1[NRA];
         for (int pn = 0; pn < np; ++pn, ++phase) {
             // ---- x of this phase: landed, visible to all, and the other buffer free ----
             float *xa = xbuf(phase);
@@ -344,7 +349,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                 const int rows = min(rpw, M - row0);
                 if (pn == 0) {
 #pragma unroll
-                    for (int v = 0; v < NR; ++v) {
+                    for (int v = 0; v < NRA; ++v) {
                         p1[v] = -0.0f;
 #pragma unroll
                         for (int r = 0; r < R; ++r) p0[v][r] = -0.0f;
@@ -370,20 +375,50 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                             }
                         }
                         if (!ok) continue;
+                        if constexpr (NR == 0) {
+                            {
+                                // whole rows, one by one, each block-parallel over the
+                                // warp (same tree); lane r keeps row r's gate value
+                                // between the two matrices of gate+up
+                                const uint8_t *base = ring + (size_t)slot * a.slot_bytes;
+                                for (int r = 0; r < rows; ++r) {
+                                    const float v = __shfl_sync(
+                                        0xffffffffu,
+                                        row_dot_blockpar<QT>(base + (size_t)r * row_stride, nsc, G, xs,
+                                                             lane),
+                                        0);
+                                    if (nmat == 1) {
+                                        if (lane == 0) y[row0 + r] = v;
+                                    } else if (m == 0) {
+                                        if (lane == r) p1[0] = v;
+                                    } else {
+                                        const float gr = __shfl_sync(0xffffffffu, p1[0], r);
+                                        if (lane == 0) y[row0 + r] = silu_mul(gr, v);
+                                    }
+                                }
+                                if (q.t < t_end) {
+                                    multi_issue<QT>(q, ring + (size_t)slot * a.slot_bytes,
+                                                    wfull + slot, pol, lane);
+                                    multi_advance(ops, nops, a.nwarps, q);
+                                    ++issued;
+                                }
+                                continue;
+                            }
+                        }
                         const int u0 = c * KCU;
                         const int cnt = min(KCU, nsc - u0);
                         const uint8_t *stp = ring + (size_t)slot * a.slot_bytes + rho * row_stride;
                         // rows past the tile's end read stale slot bytes; their
                         // results are dropped below
-                        if (rho < rows) {
+                        if (NR > 0 && rho < rows) {
                             for (int ul = l; ul < cnt; ul += G) {
-                                const uint8_t *up[NR];
+                                const uint8_t *up[NRA];
 #pragma unroll
-                                for (int v = 0; v < NR; ++v) up[v] = stp + v * rg * row_stride + ul * UB;
-                                float cc[NR][R];
-                                unit_dot_rows<QT, NR, R>(up, xs, (u0 + ul - k0u) * 256, cc);
+                                for (int v = 0; v < NRA; ++v) up[v] = stp + v * rg * row_stride + ul * UB;
+                                float cc[NRA][R];
+                                unit_dot_rows<QT, NRA, R>(up, xs, (u0 + ul - k0u) * 256, cc);
 #pragma unroll
-                                for (int v = 0; v < NR; ++v) {
+                                for (int v = 0; v < NRA; ++v) {
                                     if (m == 0) {
 #pragma unroll
                                         for (int r = 0; r < R; ++r) p0[v][r] = __fadd_rn(p0[v][r], cc[v][r]);
@@ -402,9 +437,9 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                         }
                     }
                 }
-                if (!ok || pn + 1 < np) continue;
+                if (!ok || pn + 1 < np || NR == 0) continue;
 #pragma unroll
-                for (int v = 0; v < NR; ++v) {
+                for (int v = 0; v < NRA; ++v) {
                     const int row = rho + v * rg;
 #pragma unroll
                     for (int r = 0; r < R; ++r) {

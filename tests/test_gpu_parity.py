@@ -100,6 +100,49 @@ def test_gemv_within_bound(qt, M, K):
     assert_gemv_close(y.cpu().numpy(), y_ref, S, f"{qt} {M}x{K}")
 
 
+# Large M: enough warp tiles per SM that single calls take the unit-per-lane
+# path of the streaming kernel (the small shapes above take row mode).
+LARGE = [(40000, 1024), (24000, 2048), (6000, 5120)]
+
+
+@pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("M,K", LARGE)
+def test_gemv_large_m_within_bound(qt, M, K):
+    W = weights(M, K, seed=12)
+    x = xvec(K, seed=12)
+    P = gpu_pack(qt, W)
+    y = torch.full((M,), float("nan"), device=DEV)
+    bq.gemv(qt, P, cuda(x), y)
+    y_ref, S = ora().gemv(QT[qt], P.cpu().numpy(), M, K, x.astype(np.float64))
+    assert_gemv_close(y.cpu().numpy(), y_ref, S, f"{qt} {M}x{K}")
+
+
+@pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
+def test_large_and_small_calls_agree_bitwise(qt):
+    """Rows evaluated by the unit-per-lane path (a large call) and by row
+    mode (a call over a few of the same rows) give the same bits."""
+    M, K = 40000, 1024
+    P = gpu_pack(qt, weights(M, K, seed=13))
+    x = cuda(xvec(K, seed=13))
+    y = bq.gemv(qt, P, x)
+    for r0 in (0, 777, M - 5):
+        ys = bq.gemv(qt, P[r0:r0 + 5].contiguous(), x)
+        assert torch.equal(ys.view(torch.int32), y[r0:r0 + 5].view(torch.int32)), f"rows {r0}.."
+
+
+@pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
+def test_gate_up_large_m_within_bound(qt):
+    M, K = 40000, 1024
+    Wg, Wu = weights(M, K, seed=14, spread=False), weights(M, K, seed=15, spread=False)
+    x = xvec(K, seed=14)
+    gamma = wl.normal_np(K, 0.1, seed=14, stream=wl.stream_id("gamma", K), mean=1.0)
+    Pg, Pu = gpu_pack(qt, Wg), gpu_pack(qt, Wu)
+    y = bq.gemv_gate_up_silu(qt, Pg, Pu, cuda(x), cuda(gamma), 1e-6).cpu().numpy()
+    o = ora()
+    r = o.gate_up_silu(QT[qt], Pg.cpu().numpy(), Pu.cpu().numpy(), M, K, o.rmsnorm(x, gamma, 1e-6))
+    assert_gate_up_close(y, r, f"{qt} {M}x{K} large")
+
+
 @pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
 @pytest.mark.parametrize("M,K", [(33, 256), (9, 288), (70, 1024), (5, 1056), (11, 2048)])
 def test_gemv_exact_on_dyadic_inputs(qt, M, K):
