@@ -42,6 +42,7 @@ struct Tunables {
     int single_x_max = 128 * 1024;   // single calls: largest staged R x K input (else panels)
     int single_pdl = 1;              // single calls: allow programmatic dependent launch
     int single_rowmode = 4;          // single calls: row mode up to this many unit tiles per SM (0: off)
+    int verify_nr = 2;               // verify calls (R > 1): weight rows per lane (1 or 2)
 };
 
 const Tunables &tunables() {
@@ -70,6 +71,7 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "sx") && val >= 16384) v.single_x_max = val;
             else if (!std::strcmp(tok, "pdl") && val >= 0 && val <= 1) v.single_pdl = val;
             else if (!std::strcmp(tok, "srow") && val >= 0 && val <= 64) v.single_rowmode = val;
+            else if (!std::strcmp(tok, "vnr") && (val == 1 || val == 2)) v.verify_nr = val;
         }
         return v;
     }();
@@ -465,7 +467,7 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     const int bb = block_bytes(c.qtype), ub = 8 * bb;
     const int D = std::min(t.multi_d, MULTI_MAX_D);
     const int R = c.R;
-    int NR = 1;
+    int NR = R > 1 ? t.verify_nr : 1;
     const int nsms = num_sms_current();
     const int cap = max_smem_optin();
     if (nsms <= 0 || cap <= 0) return false;
