@@ -41,6 +41,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "achieved HBM GB/s (% of GB300 peak) and per-token weight-stream tok/s, batch 1"
 NOMINAL_HBM_GBS = 8000.0
+CFG1_COPIES = 96   # rotated weight copies: 321 MB per sweep, 2.5x the 129 MB L2
+CFG5_COPIES = 7    # of each verify matrix: 702 MB per sweep
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -233,11 +235,9 @@ def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None
     w.x_dev = ds.inputs
     w.y_dev = ds.logits if chained else torch.cat([op.y for op in ds.ops])
     w.stream_obj = ds
-    w.desc = {"workload": cfg["name"], "layers": cfg["layers"], "ops_per_step": len(ds.ops),
-              "stages_per_step": ds.n_stages, "weight_bytes_per_step": ds.weight_bytes(),
-              "weight_format": qt, "launch": mode,
-              "inputs": "chained (each stage reads the previous stage's output)" if chained
-              else "independent (each op reads an N(0,1) input of its own)"}
+    w.desc = token_desc(cfg, mode, chained)
+    assert (w.desc["ops_per_step"], w.desc["stages_per_step"], w.desc["weight_bytes_per_step"]) == \
+        (len(ds.ops), ds.n_stages, ds.weight_bytes())
     return w
 
 
@@ -302,6 +302,55 @@ def build_verify(dev, cfg, R, copies=7, seed=0):
     return w
 
 
+def token_desc(cfg, mode, chained):
+    """Config entries of a token-stream step (no GPU needed)."""
+    from block_quantized_weight_dequant_gb300 import workloads as wl
+    bb = 34 if cfg["qtype"] == "q8_0" else 18
+    wbytes = sum(M * K // 32 * bb for _, M, K in wl.token_weight_shapes(cfg))
+    return {"workload": cfg["name"], "layers": cfg["layers"],
+            "ops_per_step": len(wl.token_stream_ops(cfg)), "stages_per_step": 4 * cfg["layers"] + 1,
+            "weight_bytes_per_step": wbytes, "weight_format": cfg["qtype"], "launch": mode,
+            "inputs": "chained (each stage reads the previous stage's output)" if chained
+            else "independent (each op reads an N(0,1) input of its own)"}
+
+
+def workload_desc(args):
+    """The step's config entries, identical in both arms (no GPU needed)."""
+    from block_quantized_weight_dequant_gb300 import workloads as wl
+    if args.config in ("cfg2", "cfg3"):
+        cfg = dict(wl.QWEN3_0_6B if args.config == "cfg2" else wl.Q7B)
+        if args.layers:
+            cfg["layers"] = args.layers
+        return token_desc(cfg, args.launch, args.inputs == "chained")
+    if args.config == "cfg1":
+        c = wl.CFG1
+        return {"workload": f"{c['qtype']} gemv {c['M']}x{c['K']}, {CFG1_COPIES} rotated copies",
+                "M": c["M"], "K": c["K"]}
+    if args.config == "cfg4":
+        c = wl.CFG4
+        return {"workload": c["name"], "M": c["M"], "K": c["K"], "pairs": c["pairs"]}
+    return {"workload": wl.CFG5["name"], "R": args.rows, "copies": CFG5_COPIES}
+
+
+def step_bytes_static(args):
+    """Algorithmic bytes of one step (packed weights + x read + y written
+    (+ gamma)), computed from the shapes alone."""
+    from block_quantized_weight_dequant_gb300 import workloads as wl
+    if args.config in ("cfg2", "cfg3"):
+        cfg = dict(wl.QWEN3_0_6B if args.config == "cfg2" else wl.Q7B)
+        if args.layers:
+            cfg["layers"] = args.layers
+        return token_bytes_cfg(cfg)
+    if args.config == "cfg1":
+        c = wl.CFG1
+        return CFG1_COPIES * (c["M"] * c["K"] // 32 * 34 + 4 * (c["M"] + c["K"]))
+    if args.config == "cfg4":
+        c = wl.CFG4
+        return c["pairs"] * (2 * c["M"] * c["K"] // 32 * 34 + 8 * c["K"] + 4 * c["M"])
+    R = args.rows
+    return CFG5_COPIES * sum(M * K // 32 * 18 + 4 * R * (M + K) for _, M, K in wl.CFG5["mats"])
+
+
 def build_workload(args, dev):
     from block_quantized_weight_dequant_gb300 import workloads as wl
     chained = args.inputs == "chained"
@@ -317,11 +366,11 @@ def build_workload(args, dev):
         return w
     if args.config == "cfg1":
         c = wl.CFG1
-        return build_rotated_gemv(dev, c["qtype"], c["M"], c["K"], copies=96)
+        return build_rotated_gemv(dev, c["qtype"], c["M"], c["K"], copies=CFG1_COPIES)
     if args.config == "cfg4":
         return build_rotated_gate_up(dev, wl.CFG4)
     if args.config == "cfg5":
-        return build_verify(dev, wl.CFG5, args.rows)
+        return build_verify(dev, wl.CFG5, args.rows, copies=CFG5_COPIES)
     raise SystemExit(f"unknown config {args.config}")
 
 
@@ -418,10 +467,9 @@ def oracle_sample(config, budget_s):
     return done / dt / 1e9, dt, done, desc
 
 
-def token_bytes(config):
-    from block_quantized_weight_dequant_gb300 import workloads as wl
-    cfg = wl.QWEN3_0_6B if config == "cfg2" else wl.Q7B
+def token_bytes_cfg(cfg):
     bb = 34 if cfg["qtype"] == "q8_0" else 18
+    from block_quantized_weight_dequant_gb300 import workloads as wl
     total = 0
     for kind, name, M, K in wl.token_stream_ops(cfg):
         if kind == "gemv":
@@ -429,6 +477,25 @@ def token_bytes(config):
         else:
             total += 2 * M * K // 32 * bb + 8 * K + 4 * M
     return total
+
+
+# ---------------------------------------------------------------------------
+# ranks: independent replicas; the job's time is the slowest rank's
+# ---------------------------------------------------------------------------
+def max_over_ranks(v, device, world):
+    """The largest of every rank's v (all ranks get it)."""
+    if world <= 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(step_bytes, steps, ms, world):
+    """Bytes that all `world` replicas processed over the slowest rank's time."""
+    return world * step_bytes * steps / (ms * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -449,13 +516,15 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * t_total / max(1, args.steps), 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.config},
+            "data": "synthetic: seeded N(0,0.02) weights packed by the oracle, N(0,1) inputs",
+            "config": dict(workload_desc(args), config=args.config, bytes_per_step=step_bytes_static(args),
+                           parallelism="replicas1"),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
                              "kind": "oracle", "sample": desc + ", one pass per step"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     if args.config in ("cfg2", "cfg3"):
-        line["tok_per_s"] = round(value * 1e9 / token_bytes(args.config), 4)
+        line["tok_per_s"] = round(value * 1e9 / step_bytes_static(args), 4)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -524,12 +593,10 @@ def main():
                  "tok_per_s": round(args.steps / (o_ms * 1e-3), 2)}
         del og
 
-    t = torch.tensor([total_ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev, world)
     step_bytes = w.step_bytes
-    value = world * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    assert step_bytes == step_bytes_static(args)
+    value = whole_job_gbs(step_bytes, args.steps, total_ms, world)
 
     # e2e: the same step through the public API with host buffers: H2D of the
     # step's inputs from pinned memory, the graph, D2H of the step's outputs
@@ -549,10 +616,8 @@ def main():
     torch.cuda.synchronize()
     barrier()
     e2e_ms = e_s.elapsed_time(e_e)
-    te = torch.tensor([e2e_ms], device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = world * step_bytes * args.steps / (float(te.item()) * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e2e_ms, dev, world)
+    e2e_value = whole_job_gbs(step_bytes, args.steps, e2e_ms, world)
 
     # every step is one kernel family (the stream executor for cfg2/cfg3, one
     # GEMV family for the rotated configs), so the dominant kernel's launch
