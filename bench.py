@@ -55,8 +55,12 @@ FALLBACK_HBM_GBS = 6800.0
 # the traffic is null until it is captured again.
 NCU_TRAFFIC = {
     # (config, inputs): (bytes per launch, sha256 of csrc/ at capture, summary)
-    ("cfg2", "independent"): (606694656, "4b2fc51e57db864a47b43648db2154cbcc8d63cf6c9fd8fae207cd34bd5ab6b9",
+    ("cfg2", "independent"): (607008768, "bc85a9b9b3f546b6b335ccf8cef4145b8c1034a533dbff27faeac6a1b844f2e4",
                               "profiles/multi_kernel_q8_0_qwen3_0.6b_stream.md"),
+    # captured on 2 of the 28 layers (+ LM head) and scaled by algorithmic bytes
+    ("cfg3", "independent"): (4006005897, "bc85a9b9b3f546b6b335ccf8cef4145b8c1034a533dbff27faeac6a1b844f2e4",
+                              "profiles/multi_kernel_q4_0_7b_stream.md"),
+    ("cfg1", None): (3400192, "bc85a9b9b3f546b6b335ccf8cef4145b8c1034a533dbff27faeac6a1b844f2e4", "profiles/multi_kernel_q8_0_gemv_3072x1024.md"),
 }
 
 
@@ -479,6 +483,32 @@ def token_bytes_cfg(cfg):
     return total
 
 
+# FMA pipe of GB300: 152 SMs x 128 fp32 lane-ops per clock x 2.07 GHz (max SM
+# clock).  The packed FFMA2/FADD2 issue in two cycles, so they do not raise it.
+FMA_LANE_OPS_PER_S = 152 * 128 * 2.07e9
+
+
+def roofline(args, dom, n_launch, achieved, peak, peak_kind, traffic, traffic_src, total_ms):
+    """The dominant kernel against its bound.  HBM for the streams and the
+    decode GEMVs; for verify with R >= 2 the FMA pipe, since every weight then
+    costs R fp32 FMAs plus one fp32 add of its exact code conversion."""
+    hbm = {"bound": "hbm", "kernel": dom, "launches_per_step": n_launch,
+           "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+           "frac": round(achieved / peak, 4), "traffic": traffic,
+           "traffic_source": traffic_src, "peak_kind": peak_kind}
+    if args.config != "cfg5" or args.rows < 2:
+        return hbm
+    from block_quantized_weight_dequant_gb300 import workloads as wl
+    R = args.rows
+    weights = CFG5_COPIES * sum(M * K for _, M, K in wl.CFG5["mats"])
+    ops_per_s = weights * (R + 1) * args.steps / (total_ms * 1e-3)
+    return {"bound": "alu", "kernel": dom, "launches_per_step": n_launch,
+            "achieved": round(ops_per_s / 1e9, 1), "peak": round(FMA_LANE_OPS_PER_S / 1e9, 1),
+            "unit": "G FMA-pipe lane-ops/s", "frac": round(ops_per_s / FMA_LANE_OPS_PER_S, 4),
+            "ops_per_weight": R + 1, "traffic": traffic, "traffic_source": traffic_src,
+            "peak_kind": "derived: 152 SMs x 128 lanes x 2.07 GHz", "hbm": hbm}
+
+
 # ---------------------------------------------------------------------------
 # ranks: independent replicas; the job's time is the slowest rank's
 # ---------------------------------------------------------------------------
@@ -632,7 +662,8 @@ def main():
     if rank != 0:
         return 0
     ms_step = total_ms / args.steps
-    traffic, traffic_src = ncu_traffic(args.config, args.inputs) if not args.layers else (None, None)
+    traffic, traffic_src = ncu_traffic(args.config, args.inputs) \
+        if not args.layers and args.launch == "plan" else (None, None)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -647,10 +678,8 @@ def main():
         "step_ms_median": round(statistics.median(per), 5),
         "step_ms_p10_p90": [round(sorted(per)[len(per) // 10], 5),
                             round(sorted(per)[(9 * len(per)) // 10], 5)],
-        "roofline": {"bound": "hbm", "kernel": dom, "launches_per_step": n_launch,
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "traffic_source": traffic_src, "peak_kind": peak_kind},
+        "roofline": roofline(args, dom, n_launch, achieved, peak, peak_kind, traffic, traffic_src,
+                             total_ms),
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": y_host.numel() * 4},
         "clocks": clk,
