@@ -5,9 +5,10 @@ parcelled out to weight and KV-cache pools, a framework that forbids raw
 cudaMalloc beside its own caching allocator, a latency-critical path that
 cannot afford an allocation's device synchronisation -- use this entry point
 instead of a plan with a caller-allocated workspace.  This test calls it
-through the C ABI on a chained decode stream, twice in a row (the second call
-must clear the barrier counters the first left behind), and checks every
-output against the workspace-based plan, which is the existing entry point:
+through the C ABI on a decode stream, chained (the stream executor) and with
+independent inputs (the multi-op kernel), twice in a row (the second call must
+clear the barrier counters the first left behind), and checks every output
+against the workspace-based plan, which is the existing entry point:
 bit for bit, and the final logits within the library's GEMV bound against the
 oracle.  It lives in a file of its own that pytest collects last, and it
 passes alone in a fresh process (its first call does the per-device set-up)
@@ -31,7 +32,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def chained_stream(qt, seed=11):
+def chained_stream(qt, seed=11, chained=True):
     def packed(M, K, *tag):
         W = wl.normal_torch((M, K), wl.W_STD, seed=seed, stream=wl.stream_id(*tag), device=DEV)
         return bq.quantize_pack(W, qt)
@@ -44,8 +45,8 @@ def chained_stream(qt, seed=11):
                    gamma=wl.normal_torch(hidden, 0.1, seed=seed, stream=wl.stream_id(l, "gm"),
                                          device=DEV, mean=1.0))
               for l in range(2)]
-    ds = DecodeStream(qt, layers, packed(5000, hidden, "lm"))
-    ds.x0.copy_(wl.normal_torch(hidden, 1.0, seed=seed, stream=3, device=DEV))
+    ds = DecodeStream(qt, layers, packed(5000, hidden, "lm"), chained=chained)
+    ds.inputs.copy_(wl.normal_torch(ds.inputs.numel(), 1.0, seed=seed, stream=3, device=DEV))
     return ds
 
 
@@ -63,9 +64,11 @@ def op_array(ds):
     return arr
 
 
+@pytest.mark.parametrize("chained", [True, False], ids=["chained", "independent"])
 @pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
-def test_noalloc_matches_workspace_plan_on_two_calls(qt):
-    ds = chained_stream(qt)
+def test_noalloc_matches_workspace_plan_on_two_calls(qt, chained):
+    """chained: the stream executor; independent: the multi-op kernel."""
+    ds = chained_stream(qt, chained=chained)
     ds.run_plan()  # the existing entry point: caller-allocated workspace
     torch.cuda.synchronize()
     want = [op.y.clone() for op in ds.ops]
