@@ -184,7 +184,7 @@ def _packed(bq, wl, qt, M, K, seed, tag, dev):
     return P
 
 
-def build_token_layers(cfg, dev, seed=0):
+def build_token_layers(cfg, dev, seed=0, fused_qkv=False):
     """Packed weights of one token's stream (every layer's matrices, RMSNorm
     gains and the LM head), drawn and packed on the GPU."""
     import block_quantized_weight_dequant_gb300 as bq
@@ -200,12 +200,19 @@ def build_token_layers(cfg, dev, seed=0):
                                      stream=wl.stream_id(cfg["name"], l, "gamma"), device=dev,
                                      mean=1.0)
         layers.append(L)
+    if fused_qkv:
+        for l, L in enumerate(layers):
+            L["qkv"] = bq.concat_packed([L.pop("q"), L.pop("k"), L.pop("v")])
+            L["qkv_bias"] = wl.normal_torch(L["qkv"].shape[0], 0.1, seed=seed,
+                                            stream=wl.stream_id(cfg["name"], l, "qkv_bias"),
+                                            device=dev)
     M, K = cfg["lm_head"]
     lm = _packed(bq, wl, qt, M, K, seed, (cfg["name"], "lm_head"), dev)
     return layers, lm
 
 
-def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None):
+def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None,
+                       fused_qkv=False):
     """One decode step's GEMV stream (block_quantized_weight_dequant_gb300.decode).
     chained=False (default): every op reads an N(0, 1) input of its own, the
     pure per-token weight stream; chained: every stage reads the previous
@@ -218,8 +225,8 @@ def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None
     from block_quantized_weight_dequant_gb300.decode import DecodeStream
 
     qt = cfg["qtype"]
-    layers, lm = packed if packed is not None else build_token_layers(cfg, dev, seed)
-    ds = DecodeStream(qt, layers, lm, chained=chained)
+    layers, lm = packed if packed is not None else build_token_layers(cfg, dev, seed, fused_qkv)
+    ds = DecodeStream(qt, layers, lm, chained=chained, fused_qkv=fused_qkv)
     ds.inputs.copy_(wl.normal_torch(ds.inputs.numel(), 1.0, seed=seed, stream=wl.stream_id("x0"),
                                     device=dev))
     w = Workload()
@@ -231,7 +238,11 @@ def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None
         for op in ds.ops:
             nb = op.W.numel() + (op.W_up.numel() if op.W_up is not None else 0) + \
                 4 * (op.x.numel() + op.y.numel() + (op.gamma.numel() if op.gamma is not None else 0))
-            if op.W_up is None:
+            nb += 4 * (op.bias.numel() if op.bias is not None else 0)
+            if op.W_up is None and op.bias is not None:
+                w.add(lambda op=op: bq.gemv_qkv_bias(qt, op.W, op.x, op.bias, op.y),
+                      f"gemv_qkv_bias_{qt}", nb)
+            elif op.W_up is None:
                 w.add(lambda op=op: bq.gemv(qt, op.W, op.x, op.y), f"gemv_{qt}", nb)
             else:
                 w.add(lambda op=op: bq.gemv_gate_up_silu(qt, op.W, op.W_up, op.x, op.gamma,
@@ -239,7 +250,7 @@ def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None
     w.x_dev = ds.inputs
     w.y_dev = ds.logits if chained else torch.cat([op.y for op in ds.ops])
     w.stream_obj = ds
-    w.desc = token_desc(cfg, mode, chained)
+    w.desc = token_desc(cfg, mode, chained, fused_qkv)
     assert (w.desc["ops_per_step"], w.desc["stages_per_step"], w.desc["weight_bytes_per_step"]) == \
         (len(ds.ops), ds.n_stages, ds.weight_bytes())
     return w
@@ -306,16 +317,20 @@ def build_verify(dev, cfg, R, copies=7, seed=0):
     return w
 
 
-def token_desc(cfg, mode, chained):
+def token_desc(cfg, mode, chained, fused_qkv=False):
     """Config entries of a token-stream step (no GPU needed)."""
     from block_quantized_weight_dequant_gb300 import workloads as wl
     bb = 34 if cfg["qtype"] == "q8_0" else 18
     wbytes = sum(M * K // 32 * bb for _, M, K in wl.token_weight_shapes(cfg))
-    return {"workload": cfg["name"], "layers": cfg["layers"],
-            "ops_per_step": len(wl.token_stream_ops(cfg)), "stages_per_step": 4 * cfg["layers"] + 1,
-            "weight_bytes_per_step": wbytes, "weight_format": cfg["qtype"], "launch": mode,
-            "inputs": "chained (each stage reads the previous stage's output)" if chained
-            else "independent (each op reads an N(0,1) input of its own)"}
+    d = {"workload": cfg["name"], "layers": cfg["layers"],
+         "ops_per_step": len(wl.token_stream_ops(cfg, fused_qkv)),
+         "stages_per_step": 4 * cfg["layers"] + 1,
+         "weight_bytes_per_step": wbytes, "weight_format": cfg["qtype"], "launch": mode,
+         "inputs": "chained (each stage reads the previous stage's output)" if chained
+         else "independent (each op reads an N(0,1) input of its own)"}
+    if fused_qkv:
+        d["qkv"] = "fused: q|k|v rows concatenated at load time, one op with an N(0,0.1) bias"
+    return d
 
 
 def workload_desc(args):
@@ -325,7 +340,7 @@ def workload_desc(args):
         cfg = dict(wl.QWEN3_0_6B if args.config == "cfg2" else wl.Q7B)
         if args.layers:
             cfg["layers"] = args.layers
-        return token_desc(cfg, args.launch, args.inputs == "chained")
+        return token_desc(cfg, args.launch, args.inputs == "chained", args.qkv == "fused")
     if args.config == "cfg1":
         c = wl.CFG1
         return {"workload": f"{c['qtype']} gemv {c['M']}x{c['K']}, {CFG1_COPIES} rotated copies",
@@ -344,7 +359,7 @@ def step_bytes_static(args):
         cfg = dict(wl.QWEN3_0_6B if args.config == "cfg2" else wl.Q7B)
         if args.layers:
             cfg["layers"] = args.layers
-        return token_bytes_cfg(cfg)
+        return token_bytes_cfg(cfg, args.qkv == "fused")
     if args.config == "cfg1":
         c = wl.CFG1
         return CFG1_COPIES * (c["M"] * c["K"] // 32 * 34 + 4 * (c["M"] + c["K"]))
@@ -362,11 +377,13 @@ def build_workload(args, dev):
         cfg = dict(wl.QWEN3_0_6B if args.config == "cfg2" else wl.Q7B)
         if args.layers:
             cfg["layers"] = args.layers
-        packed = build_token_layers(cfg, dev)
-        w = build_token_stream(cfg, dev, mode=args.launch, chained=chained, packed=packed)
+        fq = args.qkv == "fused"
+        packed = build_token_layers(cfg, dev, fused_qkv=fq)
+        w = build_token_stream(cfg, dev, mode=args.launch, chained=chained, packed=packed,
+                               fused_qkv=fq)
         if args.other_inputs:
             w.other = build_token_stream(cfg, dev, mode=args.launch, chained=not chained,
-                                         packed=packed)
+                                         packed=packed, fused_qkv=fq)
         return w
     if args.config == "cfg1":
         c = wl.CFG1
@@ -471,13 +488,15 @@ def oracle_sample(config, budget_s):
     return done / dt / 1e9, dt, done, desc
 
 
-def token_bytes_cfg(cfg):
+def token_bytes_cfg(cfg, fused_qkv=False):
     bb = 34 if cfg["qtype"] == "q8_0" else 18
     from block_quantized_weight_dequant_gb300 import workloads as wl
     total = 0
-    for kind, name, M, K in wl.token_stream_ops(cfg):
+    for kind, name, M, K in wl.token_stream_ops(cfg, fused_qkv):
         if kind == "gemv":
             total += M * K // 32 * bb + 4 * (M + K)
+        elif kind == "gemv_bias":
+            total += M * K // 32 * bb + 4 * (M + K) + 4 * M
         else:
             total += 2 * M * K // 32 * bb + 8 * K + 4 * M
     return total
@@ -574,6 +593,8 @@ def main():
     ap.add_argument("--inputs", choices=["chained", "independent"], default="independent",
                     help="cfg2/cfg3: each op reads an input of its own (the per-token weight "
                          "stream), or each stage reads the previous stage's output")
+    ap.add_argument("--qkv", choices=["separate", "fused"], default="separate",
+                    help="cfg2/cfg3: q, k, v as three ops, or one fused q|k|v op with a bias")
     ap.add_argument("--layers", type=int, default=0,
                     help="cfg2/cfg3: fewer layers than the model's (smaller cases for profiling)")
     ap.add_argument("--no-other-inputs", dest="other_inputs", action="store_false",
@@ -663,7 +684,7 @@ def main():
         return 0
     ms_step = total_ms / args.steps
     traffic, traffic_src = ncu_traffic(args.config, args.inputs) \
-        if not args.layers and args.launch == "plan" else (None, None)
+        if not args.layers and args.launch == "plan" and args.qkv == "separate" else (None, None)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),

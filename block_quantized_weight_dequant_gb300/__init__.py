@@ -23,6 +23,7 @@ QTYPES = {"q8_0": Q8_0, "q4_0": Q4_0}
 
 __all__ = ["Q8_0", "Q4_0", "BLOCK_BYTES", "BQError", "packed_bytes", "quantize_pack",
            "gemv", "gemv_q8_0", "gemv_q4_0", "gemv_gate_up_silu", "gemv_verify",
+           "gemv_qkv_bias", "concat_packed",
            "device_status", "tree_lanes", "version", "StreamOp", "StreamPlan"]
 
 
@@ -136,6 +137,41 @@ def gemv_gate_up_silu(qtype, Wg, Wu, x, gamma=None, eps=1e-6, y=None):
     return y
 
 
+def concat_packed(mats):
+    """Load-time concatenation of packed matrices with the same K (e.g. the
+    q, k and v projections): a packed matrix is its rows back to back, so the
+    rows are concatenated as they are.  No arithmetic."""
+    if not mats:
+        raise ValueError("no matrices")
+    rb = mats[0].shape[1]
+    for P in mats:
+        _need(P, torch.uint8, "packed matrix")
+        if P.dim() != 2 or P.shape[1] != rb:
+            raise ValueError("packed matrices must share the row size (same K and format)")
+    return torch.cat(list(mats), dim=0)
+
+
+def gemv_qkv_bias(qtype, Wqkv, x, bias=None, y=None):
+    """y = Wqkv x + bias over the concatenated q|k|v rows (concat_packed):
+    the single-row GEMV's dot products, then one fp32 add of the bias."""
+    qt = _qt(qtype)
+    _need(Wqkv, torch.uint8, "Wqkv")
+    _need(x, torch.float32, "x")
+    M, K = _packed_shape(Wqkv, qt)
+    if x.numel() != K:
+        raise ValueError(f"x must have K={K} elements")
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+        if bias.numel() != M:
+            raise ValueError(f"bias must have M={M} elements")
+    if y is None:
+        y = torch.empty(M, dtype=torch.float32, device=Wqkv.device)
+    _need(y, torch.float32, "y")
+    _lib.check(lib.bq_gemv_qkv_bias(qt, _ptr(Wqkv), _ptr(x), _ptr(bias), _ptr(y), M, K,
+                                    _stream(Wqkv)), "gemv_qkv_bias")
+    return y
+
+
 def gemv_verify(qtype, Wq, X, Y=None):
     """Y [R, M] = X [R, K] @ W^T with the weights streamed once; row r is
     bit-identical to gemv(qtype, Wq, X[r])."""
@@ -164,14 +200,15 @@ def device_status(clear=True):
 
 
 class StreamOp:
-    """One op of a per-token stream: a GEMV (``W`` only) or a fused
+    """One op of a per-token stream: a GEMV (``W`` only, optional ``bias``
+    added to its output: the fused q|k|v + bias projection) or a fused
     RMSNorm+gate+up+SiLU (``W`` = gate, ``W_up`` = up, optional ``gamma``).
     ``stage`` orders the ops: ops of one stage run concurrently, and an op may
     read the output ``y`` of an op of an earlier stage as its ``x``."""
 
-    def __init__(self, stage, W, x, y, W_up=None, gamma=None, eps=1e-6):
+    def __init__(self, stage, W, x, y, W_up=None, gamma=None, eps=1e-6, bias=None):
         self.stage, self.W, self.x, self.y = int(stage), W, x, y
-        self.W_up, self.gamma, self.eps = W_up, gamma, float(eps)
+        self.W_up, self.gamma, self.eps, self.bias = W_up, gamma, float(eps), bias
 
 
 class StreamPlan:
@@ -206,6 +243,11 @@ class StreamPlan:
                     a.gamma = op.gamma.data_ptr()
             else:
                 a.kind = _lib.BQ_OP_GEMV
+                if op.bias is not None:
+                    _need(op.bias, torch.float32, "bias")
+                    if op.bias.numel() != M:
+                        raise ValueError(f"op {i}: bias must have M={M} elements")
+                    a.bias = op.bias.data_ptr()
         nstages = len({op.stage for op in ops})
         nbytes = lib.bq_stream_workspace_bytes(len(ops), nstages)
         if nbytes < 0:

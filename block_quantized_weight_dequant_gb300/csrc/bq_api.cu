@@ -165,11 +165,14 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
             (gu && o.gamma && !al(o.gamma, 16)))
             return BQ_ERR_ALIGN;
         if (gu && o.gamma && !(std::isfinite(o.eps) && o.eps >= 0.0f)) return BQ_ERR_SHAPE;
+        if (gu && o.bias) return BQ_ERR_SHAPE;  // gate+up takes no bias
+        if (o.bias && !al(o.bias, 4)) return BQ_ERR_ALIGN;
         ExecOp &e = eo[i];
         std::memset(&e, 0, sizeof e);
         e.W[0] = static_cast<const uint8_t *>(o.W);
         e.W[1] = gu ? static_cast<const uint8_t *>(o.W_up) : nullptr;
         e.y = o.y;
+        e.bias = gu ? nullptr : o.bias;
         e.nmat = gu ? 2 : 1;
         e.M = (int)o.M;
         e.nsc = (int)(o.K / 256);
@@ -207,6 +210,7 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
         int n = 0;
         r[n++] = range(o.x, 4 * o.K);
         if (o.kind == BQ_OP_GATE_UP_SILU && o.gamma) r[n++] = range(o.gamma, 4 * o.K);
+        if (o.kind == BQ_OP_GEMV && o.bias) r[n++] = range(o.bias, 4 * o.M);
         return n;
     };
     auto w_ranges = [&](int i, Range *r) {
@@ -229,11 +233,11 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
         const ExecStage &st = es[s];
         for (int i = st.op_begin; i < st.op_end; ++i) {
             const Range yi = range(ops[i].y, 4 * ops[i].M);
-            Range ri[2];
+            Range ri[3];
             const int ni = in_ranges(i, ri);
             for (int j = 0; j < st.op_end; ++j) {
                 const Range yj = range(ops[j].y, 4 * ops[j].M);
-                Range rj[2];
+                Range rj[3];
                 const int nj = in_ranges(j, rj);
                 bool hit = false;
                 for (int k = 0; k < nj; ++k) hit |= overlap(yi, rj[k]);
@@ -360,6 +364,7 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
         m.gamma = gu ? o.gamma : nullptr;
         m.eps = o.eps;
         m.y = o.y;
+        m.bias = gu ? nullptr : o.bias;
         m.nmat = gu ? 2 : 1;
         m.M = (int)o.M;
         m.K = (int)o.K;
@@ -479,6 +484,7 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     m.x = c.x;
     m.gamma = gu ? c.gamma : nullptr;
     m.y = c.y;
+    m.bias = gu || R > 1 ? nullptr : c.bias;
     m.eps = c.eps;
     m.M = (int)c.M;
     m.K = (int)c.K;
@@ -675,15 +681,17 @@ bq_status run_gemv(const GemvCall &c) {
 }
 
 bq_status gemv_common(int qtype, const void *Wq, const float *x, float *y, int R, int64_t M,
-                      int64_t K, void *stream) {
+                      int64_t K, void *stream, const float *bias = nullptr) {
     if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0) return BQ_ERR_QTYPE;
     if (R < 1 || R > BQ_VERIFY_MAX_ROWS) return BQ_ERR_SHAPE;
     bq_status s = check_shape(M, K);
     if (s != BQ_OK) return s;
     if (M == 0) return BQ_OK;  // empty product: nothing is read or written
     if (!Wq || !x || !y) return BQ_ERR_NULL;
-    if (!aligned_ok(Wq, 16) || !aligned_ok(x, 16) || !aligned_ok(y, 4)) return BQ_ERR_ALIGN;
-    GemvCall c{qtype, bq::MODE_PLAIN, R, Wq, nullptr, x, nullptr, 0.0f, y, M, K, stream};
+    if (!aligned_ok(Wq, 16) || !aligned_ok(x, 16) || !aligned_ok(y, 4) ||
+        (bias && !aligned_ok(bias, 4)))
+        return BQ_ERR_ALIGN;
+    GemvCall c{qtype, bq::MODE_PLAIN, R, Wq, nullptr, x, nullptr, 0.0f, y, M, K, stream, bias};
     return run_gemv(c);
 }
 
@@ -733,6 +741,11 @@ bq_status bq_gemv_q8_0(const void *Wq, const float *x, float *y, int64_t M, int6
 
 bq_status bq_gemv_q4_0(const void *Wq, const float *x, float *y, int64_t M, int64_t K, void *stream) {
     return gemv_common(BQ_Q4_0, Wq, x, y, 1, M, K, stream);
+}
+
+bq_status bq_gemv_qkv_bias(int qtype, const void *Wqkv, const float *x, const float *bias, float *y,
+                           int64_t M, int64_t K, void *stream) {
+    return gemv_common(qtype, Wqkv, x, y, 1, M, K, stream, bias);
 }
 
 bq_status bq_gemv_verify(int qtype, const void *Wq, const float *X, float *Y, int R, int64_t M,

@@ -49,10 +49,11 @@ namespace bq {
 #define BQ_DEVERR_XFULL_WAIT 0x10u    // a warp gave up waiting for a stage's x copies
 #define BQ_DEVERR_XREADY_WAIT 0x20u   // a warp gave up waiting for a stage's normalised x
 
-// one GEMV (or gate+up pair) of the stream; 64 bytes
+// one GEMV (or gate+up pair) of the stream; 80 bytes
 struct ExecOp {
     const uint8_t *W[2];
     float *y;
+    const float *bias;        // GEMV: fp32[M] added to y, or null
     int M, rb;                // rows, packed bytes per row
     int ntiles, tile_base;    // warp tiles; first tile of this op within its stage
     int row_stride, xoff;     // shared-memory bytes per tile row; float offset of x
@@ -60,6 +61,7 @@ struct ExecOp {
     unsigned char G, rpw, nmat, single;  // rpw: rows per tile
     int nsc;
     int rowmode;              // 1: a tile is rpw whole rows, each evaluated by the whole warp
+    int pad[2];               // to a multiple of 16 bytes (see below)
 };
 
 // one distinct input vector of a stage (RMSNorm-ed when gamma is set); 32 bytes
@@ -99,6 +101,13 @@ struct ExecArgs {
 };
 
 constexpr int EXEC_MAX_XBUF = 8;
+
+// The kernel copies the three tables into shared memory back to back with
+// 16-byte vector loads and stores, so every entry must be a multiple of 16
+// bytes: then each table starts 16-byte aligned and is copied whole.
+static_assert(sizeof(ExecOp) % 16 == 0, "ExecOp: a multiple of 16 bytes");
+static_assert(sizeof(ExecX) % 16 == 0, "ExecX: a multiple of 16 bytes");
+static_assert(sizeof(ExecStage) % 16 == 0, "ExecStage: a multiple of 16 bytes");
 
 // launch geometry of a planned executor run (host side)
 struct ExecGeometry {
@@ -437,7 +446,7 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
                     const float v = __shfl_sync(
                         0xffffffffu, row_dot_blockpar<QT>(base + (size_t)r * op.rb, op.nsc, G, xs, lane), 0);
                     if (op.nmat == 1) {
-                        if (lane == 0) op.y[row0 + r] = v;
+                        if (lane == 0) op.y[row0 + r] = op.bias ? __fadd_rn(v, op.bias[row0 + r]) : v;
                     } else if (it.mat == 0) {
                         if (lane == r) p0 = v;
                     } else {
@@ -466,7 +475,7 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
                         const float u = fold_lanes(p1, G);
                         if (rho < rows && l == 0) op.y[row0 + rho] = silu_mul(g, u);
                     } else if (rho < rows && l == 0) {
-                        op.y[row0 + rho] = g;
+                        op.y[row0 + rho] = op.bias ? __fadd_rn(g, op.bias[row0 + rho]) : g;
                     }
                 }
             }

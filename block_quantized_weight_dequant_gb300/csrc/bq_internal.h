@@ -18,6 +18,7 @@ struct GemvCall {
     float *y;
     long long M, K;
     void *stream;
+    const float *bias;  // MODE_PLAIN with R = 1: added to every output row, or null
 };
 
 // generic-kernel geometry (K % 256 != 0).  G fixes the row's summation tree.

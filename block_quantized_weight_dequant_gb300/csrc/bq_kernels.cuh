@@ -30,6 +30,7 @@ struct GenericArgs {
     const float *gamma;
     float eps;
     float *y;
+    const float *bias;  // R = 1 plain: added to y, or null
     int M, K, G;
     long long rb;
 };
@@ -87,7 +88,8 @@ __global__ void __launch_bounds__(GENERIC_WARPS * 32) generic_kernel(const Gener
                 a.y[row] = silu_mul(p[0], p[1]);
             } else {
 #pragma unroll
-                for (int r = 0; r < R; ++r) a.y[(size_t)r * a.M + row] = p[r];
+                for (int r = 0; r < R; ++r)
+                    a.y[(size_t)r * a.M + row] = R == 1 && a.bias ? __fadd_rn(p[r], a.bias[row]) : p[r];
             }
         }
     };
@@ -107,6 +109,7 @@ cudaError_t launch_generic_t(const GemvCall &c, const LaunchPlan &p) {
     a.gamma = c.gamma;
     a.eps = c.eps;
     a.y = c.y;
+    a.bias = c.bias;
     a.M = (int)c.M;
     a.K = (int)c.K;
     a.G = p.G;

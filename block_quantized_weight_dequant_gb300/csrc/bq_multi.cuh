@@ -48,6 +48,7 @@ struct MultiOp {
     const float *x;          // [R][K]
     const float *gamma;      // gate+up RMSNorm gain, or null
     float *y;                // [R][M]
+    const float *bias;       // R = 1 plain GEMV: fp32[M] added to y, or null
     float eps;
     int M, K, rb, nsc;
     int G, rpw;              // lanes per row, rows per tile (NR * 32 / G)
@@ -295,6 +296,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
     for (int op = op0; op <= op_last; ++op) {
         const MultiOp &o = ops[op];
         const float *gamma = o.gamma;
+        const float *bias = o.bias;
         float *y = o.y;
         const int M = o.M, K = o.K, nsc = o.nsc, G = o.G, rpw = o.rpw, KCU = o.KCU;
         const int nchunks = o.nchunks, nmat = o.nmat, tile_base = o.tile_base, ntiles = o.ntiles;
@@ -388,7 +390,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                                                              lane),
                                         0);
                                     if (nmat == 1) {
-                                        if (lane == 0) y[row0 + r] = v;
+                                        if (lane == 0) y[row0 + r] = bias ? __fadd_rn(v, bias[row0 + r]) : v;
                                     } else if (m == 0) {
                                         if (lane == r) p1[0] = v;
                                     } else {
@@ -448,7 +450,8 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                             const float u = fold_lanes(p1[v], G);
                             if (row < rows && l == 0) y[row0 + row] = silu_mul(g, u);
                         } else if (row < rows && l == 0) {
-                            y[(size_t)r * M + row0 + row] = g;
+                            y[(size_t)r * M + row0 + row] =
+                                R == 1 && bias ? __fadd_rn(g, bias[row0 + row]) : g;
                         }
                     }
                 }

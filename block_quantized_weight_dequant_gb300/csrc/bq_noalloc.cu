@@ -31,7 +31,7 @@ constexpr size_t SCRATCH_BYTES = OFF_CNT + al256((size_t)MAX_OPS * sizeof(unsign
 // code this name is only a stand-in for the symbol; the kernel gets the
 // device address fetched by scratch_address().
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SCRATCH_BYTES];
-static_assert(SCRATCH_BYTES == 66 * 1024, "the documented size of the scratch array");
+static_assert(SCRATCH_BYTES == 74 * 1024, "the documented size of the scratch array");
 // the same array holds the multi-op kernel's tables for independent op lists
 constexpr size_t OFF_CT = al256((size_t)MAX_OPS * sizeof(bq::MultiOp));
 static_assert(OFF_CT + (bq::MULTI_MAX_CTAS + 1) * sizeof(int) <= SCRATCH_BYTES,

@@ -21,16 +21,24 @@ launches one kernel per op in stage order; the two give identical bits.
 With ``chained=False`` every op instead reads an input vector of its own (the
 same shapes and weights, no data flowing between ops): the pure per-token
 weight stream, which the executor runs without any grid-wide barrier.
+
+With ``fused_qkv=True`` each layer's q, k and v run as ONE op over their
+rows concatenated at load time (``layer["qkv"]``, see ``concat_packed``)
+with an optional fp32 bias (``layer["qkv_bias"]``): the fused QKV+bias
+projection of the RunIT README (6 dispatches -> 1 per layer on the Qwen
+path).  The op's output holds q, k and v back to back; o reads its q part.
 """
 import torch
 
-from . import StreamOp, StreamPlan, gemv, gemv_gate_up_silu
+from . import StreamOp, StreamPlan, gemv, gemv_gate_up_silu, gemv_qkv_bias
 
 
 class DecodeStream:
-    def __init__(self, qtype, layers, lm_head, eps=1e-6, chained=True):
+    def __init__(self, qtype, layers, lm_head, eps=1e-6, chained=True, fused_qkv=False):
         """layers: list of dicts with packed q, k, v, o, gate, up, down
-        (uint8 [M, row bytes]) and gamma (fp32 [hidden]); lm_head: packed."""
+        (uint8 [M, row bytes]) and gamma (fp32 [hidden]); with fused_qkv,
+        packed qkv (the q, k, v rows concatenated) and optional qkv_bias
+        (fp32) instead of q, k, v; lm_head: packed."""
         from . import _packed_shape, _qt
         self.qtype = _qt(qtype)
         self.eps = eps
@@ -42,7 +50,8 @@ class DecodeStream:
         def rows(P):
             return _packed_shape(P, self.qtype)
 
-        hidden = rows(layers[0]["q"])[1]
+        hidden = rows(layers[0]["qkv" if fused_qkv else "q"])[1]
+        self.fused_qkv = fused_qkv
         self.chained = chained
         # every vector the stream reads from outside lives in one buffer, so a
         # caller fills them with a single copy: x0 (chained), or x0 and one
@@ -68,12 +77,19 @@ class DecodeStream:
         h = self.x0
         st = 0
         for L in layers:
-            bufs = {n: torch.empty(rows(L[n])[0], **f32) for n in ("q", "k", "v", "o", "down")}
+            q_dim = rows(L["o"])[1]  # o reads the attention output, q's width
+            bufs = {n: torch.empty(rows(L[n])[0], **f32) for n in ("o", "down")}
             bufs["ffn"] = torch.empty(rows(L["gate"])[0], **f32)
+            if fused_qkv:
+                bufs["qkv"] = torch.empty(rows(L["qkv"])[0], **f32)
+                bufs["q"] = bufs["qkv"][:q_dim]
+                self.ops.append(StreamOp(st, L["qkv"], h, bufs["qkv"], bias=L.get("qkv_bias")))
+            else:
+                for n in ("q", "k", "v"):
+                    bufs[n] = torch.empty(rows(L[n])[0], **f32)
+                    self.ops.append(StreamOp(st, L[n], h, bufs[n]))
             self.buffers.append(bufs)
-            for n in ("q", "k", "v"):
-                self.ops.append(StreamOp(st, L[n], h, bufs[n]))
-            self.ops.append(StreamOp(st + 1, L["o"], src(bufs["q"], rows(L["o"])[1]), bufs["o"]))
+            self.ops.append(StreamOp(st + 1, L["o"], src(bufs["q"], q_dim), bufs["o"]))
             self.ops.append(StreamOp(st + 2, L["gate"], src(bufs["o"], hidden), bufs["ffn"],
                                      W_up=L["up"], gamma=L["gamma"], eps=eps))
             self.ops.append(StreamOp(st + 3, L["down"], src(bufs["ffn"], rows(L["down"])[1]),
@@ -95,13 +111,15 @@ class DecodeStream:
         return n
 
     def activation_bytes(self):
-        """Algorithmic activation traffic: every op reads x (and gamma) and
-        writes y once."""
+        """Algorithmic activation traffic: every op reads x (and gamma or
+        bias) and writes y once."""
         n = 0
         for op in self.ops:
             n += 4 * (op.x.numel() + op.y.numel())
             if op.gamma is not None:
                 n += 4 * op.gamma.numel()
+            if op.bias is not None:
+                n += 4 * op.bias.numel()
         return n
 
     def plan(self):
@@ -114,7 +132,9 @@ class DecodeStream:
 
     def run_per_op(self):
         for op in self.ops:
-            if op.W_up is None:
+            if op.W_up is None and op.bias is not None:
+                gemv_qkv_bias(self.qtype, op.W, op.x, op.bias, op.y)
+            elif op.W_up is None:
                 gemv(self.qtype, op.W, op.x, op.y)
             else:
                 gemv_gate_up_silu(self.qtype, op.W, op.W_up, op.x, op.gamma, op.eps, op.y)

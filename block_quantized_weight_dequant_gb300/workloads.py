@@ -79,13 +79,18 @@ CFG5 = dict(name="q4_0 verify 17408x5120 + 5120x17408, R=1..6", qtype="q4_0",
             mats=[("a", 17408, 5120), ("b", 5120, 17408)], R=(1, 2, 3, 4, 5, 6))
 
 
-def token_stream_ops(cfg):
-    """Per-token op list in model order: ("gemv", name, M, K) or
-    ("gate_up", name, M, K).  Gate and up share one fused RMSNorm+SiLU op."""
+def token_stream_ops(cfg, fused_qkv=False):
+    """Per-token op list in model order: ("gemv", name, M, K), ("gate_up",
+    name, M, K) or, with fused_qkv, ("gemv_bias", name, M, K) for the q, k, v
+    rows concatenated.  Gate and up share one fused RMSNorm+SiLU op."""
     ops = []
+    mats = {name: (M, K) for name, M, K in cfg["mats"]}
     for layer in range(cfg["layers"]):
+        if fused_qkv:
+            K = mats["q"][1]
+            ops.append(("gemv_bias", f"L{layer}.qkv", mats["q"][0] + mats["k"][0] + mats["v"][0], K))
         for name, M, K in cfg["mats"]:
-            if name == "up":
+            if name == "up" or (fused_qkv and name in ("q", "k", "v")):
                 continue
             if name == "gate":
                 ops.append(("gate_up", f"L{layer}.gate_up", M, K))

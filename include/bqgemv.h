@@ -123,6 +123,18 @@ bq_status bq_gemv_gate_up_silu(int qtype, const void *Wg, const void *Wu, const 
                                const float *gamma, float eps, float *y, int64_t M, int64_t K,
                                void *stream);
 
+/* Fused q|k|v projection with bias: y[m] = sum_k w[m,k] * x[k] + bias[m] for
+ * packed weights Wqkv (M x K) whose rows are the q, k and v projections
+ * concatenated at load time (packed rows concatenate as they are: a packed
+ * matrix is its rows, back to back), fp32 x[K], bias fp32[M] (the q, k and v
+ * biases concatenated the same way) or NULL, fp32 y[M].  The dot product is
+ * the single-row GEMV's, bit for bit; the bias is one fp32 add after it.
+ * (RunIT README kernel table, fused_qkv_bias_q8_0_f32 "Q+K+V+bias in ONE
+ * dispatch", and optimisation table "Fused QKV+bias": 6 dispatches -> 1 per
+ * layer on the Qwen path.)  bias: 4-byte aligned. */
+bq_status bq_gemv_qkv_bias(int qtype, const void *Wqkv, const float *x, const float *bias, float *y,
+                           int64_t M, int64_t K, void *stream);
+
 /* Multi-row verify GEMV: Y[r, m] = sum_k w[m,k] * X[r, k] for r < R,
  * 1 <= R <= BQ_VERIFY_MAX_ROWS, with the weights streamed once for all R rows.
  * X: fp32 [R, K] row-major; Y: fp32 [R, M] row-major.  Row r of Y is
@@ -174,6 +186,8 @@ typedef struct {
     const float *gamma;  /* GATE_UP_SILU: RMSNorm gain fp32[K] or NULL */
     float eps;           /* GATE_UP_SILU with gamma: finite, >= 0 */
     float *y;            /* fp32[M]; must not overlap any input of its own stage */
+    const float *bias;   /* GEMV: fp32[M] added to the output (the fused q|k|v + bias
+                            op), or NULL; GATE_UP_SILU: must be NULL */
 } bq_op;
 
 typedef struct bq_stream_plan bq_stream_plan;
@@ -219,7 +233,7 @@ bq_status bq_stream_plan_destroy(bq_stream_plan *plan);
  * (same validation, same kernel, bit-identical outputs) with the descriptor
  * tables and stage counters kept in one fixed device array inside the
  * library, which every GPU that loads the library holds until the process
- * exits (66 KiB).  The caller still passes the inputs and outputs (in
+ * exits (74 KiB).  The caller still passes the inputs and outputs (in
  * the ops).  It calls no cudaMalloc, cudaFree or other allocating routine.
  *
  *  - At most BQ_NOALLOC_MAX_OPS ops (and as many stages); more returns

@@ -50,6 +50,9 @@ class Oracle:
         lib.bqo_gemv.restype = i32
         lib.bqo_gemv.argtypes = [i32, ctypes.c_void_p, i64, i64, ctypes.c_void_p,
                                  ctypes.c_void_p, ctypes.c_void_p]
+        lib.bqo_gemv_bias.restype = i32
+        lib.bqo_gemv_bias.argtypes = [i32, ctypes.c_void_p, i64, i64, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         lib.bqo_rmsnorm.restype = i32
         lib.bqo_rmsnorm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, i64, ctypes.c_double,
                                     ctypes.c_void_p]
@@ -108,6 +111,21 @@ class Oracle:
         """The same product without S, into a caller-owned fp64 ``y``."""
         return self.lib.bqo_gemv(qtype, Wq.ctypes.data, M, K, x.ctypes.data, y.ctypes.data,
                                  None)
+
+    def gemv_bias(self, qtype, Wq, M, K, x, bias):
+        """Returns (y, S): fp64 y = W x + bias (the fused q|k|v + bias
+        projection) and S = sum_k |w_mk x_k| + |bias_m|."""
+        Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float64)
+        assert x.shape == (K,) and (b is None or b.shape == (M,))
+        y = np.empty(M, dtype=np.float64)
+        S = np.empty(M, dtype=np.float64)
+        if self.lib.bqo_gemv_bias(qtype, Wq.ctypes.data, M, K, x.ctypes.data,
+                                  None if b is None else b.ctypes.data, y.ctypes.data,
+                                  S.ctypes.data):
+            raise ValueError("oracle gemv_bias: bad arguments")
+        return y, S
 
     def rmsnorm(self, x, gamma, eps):
         x = np.ascontiguousarray(x, dtype=np.float64)

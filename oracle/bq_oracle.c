@@ -227,6 +227,22 @@ int bqo_gemv(int qtype, const uint8_t *Wq, int64_t M, int64_t K, const double *x
     return 0;
 }
 
+/* The fused q|k|v + bias projection (RunIT README kernel table,
+ * fused_qkv_bias_q8_0_f32, "Q+K+V+bias in ONE dispatch"), read as the plain
+ * definition: y[m] = sum_k w[m,k] * x[k] + bias[m] over the q, k and v rows
+ * concatenated, in fp64; S[m] = sum_k |w[m,k] * x[k]| + |bias[m]| (S may be
+ * NULL; bias NULL means zeros). */
+int bqo_gemv_bias(int qtype, const uint8_t *Wq, int64_t M, int64_t K, const double *x,
+                  const double *bias, double *y, double *S) {
+    if (bqo_gemv(qtype, Wq, M, K, x, y, S)) return -1;
+    if (bias)
+        for (int64_t m = 0; m < M; ++m) {
+            y[m] += bias[m];
+            if (S) S[m] += fabs(bias[m]);
+        }
+    return 0;
+}
+
 /* xn[k] = x[k] * gamma[k] / sqrt(mean(x^2) + eps); gamma NULL means ones. */
 int bqo_rmsnorm(const double *x, const double *gamma, int64_t K, double eps, double *xn) {
     if (K <= 0) return -1;

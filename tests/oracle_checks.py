@@ -385,8 +385,31 @@ def check_norm_silu(o, rng=None):
     assert np.array_equal(r["Sg"], np.abs(g)) and np.array_equal(r["Su"], np.abs(u))
 
 
+def check_bias(o, rng=None):
+    """The q|k|v + bias projection: with x = 0 the output is the bias exactly
+    (and S = |bias|); with no bias it is the plain GEMV; with power-of-two
+    scales, small-integer x and integer biases every value is an exact dyadic
+    rational, compared with Python's exact arithmetic row by row."""
+    rng = rng or np.random.default_rng(41)
+    for qt in (Q8_0, Q4_0):
+        M, K = 7, 96
+        raw, dsel = _direct_blocks(rng, qt, M, K)
+        bias = rng.integers(-9, 10, size=M).astype(np.float64)
+        y0, S0 = o.gemv_bias(qt, raw, M, K, np.zeros(K), bias)
+        assert np.array_equal(y0, bias) and np.array_equal(S0, np.abs(bias)), "x = 0"
+        x = rng.integers(-2, 3, size=K).astype(np.float64)
+        yb, Sb = o.gemv_bias(qt, raw, M, K, x, None)
+        yg, Sg = o.gemv(qt, raw, M, K, x)
+        assert np.array_equal(yb, yg) and np.array_equal(Sb, Sg), "no bias"
+        y, S = o.gemv_bias(qt, raw, M, K, x, bias)
+        want = _exact_gemv(qt, raw, dsel, M, K, x.astype(np.int64))
+        for m in range(M):
+            assert Fraction(y[m]) == want[m] + Fraction(int(bias[m])), f"row {m}"
+        assert np.array_equal(S, Sg + np.abs(bias)), "S includes |bias|"
+
+
 QUICK_CHECKS = (check_golden, check_fp16_points, check_roundtrip, check_bruteforce,
-                check_all_codes, check_closed_forms, check_norm_silu)
+                check_all_codes, check_closed_forms, check_norm_silu, check_bias)
 
 
 def run_quick(o):

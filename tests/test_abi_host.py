@@ -139,3 +139,30 @@ def test_noalloc_entry_rejects_before_touching_the_device(lib):
     assert lib.bq_stream_run_noalloc(3, ops, 1, None) == _lib.BQ_ERR_QTYPE
     big = (_lib.BqOp * (_lib.BQ_NOALLOC_MAX_OPS + 1))()
     assert lib.bq_stream_run_noalloc(bq.Q4_0, big, len(big), None) == _lib.BQ_ERR_SHAPE
+
+
+def test_qkv_bias_validation(lib):
+    f = lib.bq_gemv_qkv_bias
+    assert f(bq.Q8_0, None, FAKE, FAKE, FAKE, 8, 256, None) == _lib.BQ_ERR_NULL
+    assert f(bq.Q8_0, FAKE, None, FAKE, FAKE, 8, 256, None) == _lib.BQ_ERR_NULL
+    assert f(bq.Q8_0, FAKE, FAKE, FAKE, None, 8, 256, None) == _lib.BQ_ERR_NULL
+    assert f(bq.Q4_0, FAKE, FAKE, ctypes.c_void_p(0x10002), FAKE, 8, 256, None) == \
+        _lib.BQ_ERR_ALIGN
+    assert f(bq.Q4_0, FAKE, FAKE, FAKE, FAKE, 8, 40, None) == _lib.BQ_ERR_SHAPE
+    assert f(6, FAKE, FAKE, FAKE, FAKE, 8, 256, None) == _lib.BQ_ERR_QTYPE
+    assert f(bq.Q8_0, None, None, None, None, 0, 256, None) == _lib.BQ_OK
+
+
+def test_stream_plan_rejects_bias_on_gate_up_and_misaligned_bias(lib):
+    ops = (_lib.BqOp * 1)()
+    o = ops[0]
+    o.kind, o.stage, o.M, o.K = _lib.BQ_OP_GATE_UP_SILU, 0, 64, 256
+    o.W, o.W_up, o.x, o.y, o.eps = 0x10000, 0x20000, 0x30000, 0x40000, 1e-6
+    o.bias = 0x50000
+    plan = ctypes.c_void_p()
+    ws = ctypes.c_void_p(0x100000)
+    assert lib.bq_stream_plan_create(bq.Q8_0, ops, 1, ws, 1 << 20, ctypes.byref(plan)) == \
+        _lib.BQ_ERR_SHAPE
+    o.kind, o.bias = _lib.BQ_OP_GEMV, 0x50002
+    assert lib.bq_stream_plan_create(bq.Q8_0, ops, 1, ws, 1 << 20, ctypes.byref(plan)) == \
+        _lib.BQ_ERR_ALIGN

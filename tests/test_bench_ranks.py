@@ -76,3 +76,24 @@ def test_reference_arm_runs_on_rank_zero_only():
                        timeout=300)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_roofline_entries():
+    """The bench line's roofline object: HBM for streams and decode calls, the
+    FMA pipe for verify with R >= 2 (R + 1 lane-ops per weight)."""
+    import argparse
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    a = argparse.Namespace(config="cfg2", rows=6, steps=10)
+    r = bench.roofline(a, "stream_plan_q8_0", 1, 5000.0, 6778.0, "measured", 123, "x", 1.0)
+    assert r["bound"] == "hbm" and r["frac"] == round(5000.0 / 6778.0, 4)
+    a = argparse.Namespace(config="cfg5", rows=6, steps=10)
+    r = bench.roofline(a, "verify", 14, 500.0, 6778.0, "measured", None, None, 100.0)
+    weights = bench.CFG5_COPIES * (17408 * 5120 + 5120 * 17408)
+    assert r["bound"] == "alu" and r["ops_per_weight"] == 7
+    assert r["achieved"] == pytest.approx(weights * 7 * 10 / 0.1 / 1e9, abs=0.05)
+    assert r["hbm"]["bound"] == "hbm"
+    assert bench.step_bytes_static(argparse.Namespace(config="cfg2", layers=0, qkv="separate")) \
+        == 604_714_496

@@ -208,6 +208,43 @@ def test_gate_up_without_gamma_matches_plain_gemv_bits():
 
 
 # ---------------------------------------------------------------------------
+# fused q|k|v + bias
+# ---------------------------------------------------------------------------
+# (K, q rows, k = v rows): Qwen2.5-0.5B (K = 896 takes the generic kernel),
+# Qwen3-0.6B-like, 7B-like, and a large concatenation (unit-per-lane path)
+QKV = [(896, 896, 128), (1024, 2048, 512), (3584, 3584, 512), (1024, 38000, 1000)]
+
+
+@pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("K,Mq,Mkv", QKV)
+def test_qkv_bias_is_gemv_plus_bias_and_within_bound(qt, K, Mq, Mkv):
+    Ps = [gpu_pack(qt, weights(M, K, seed=21 + i, spread=False))
+          for i, M in enumerate((Mq, Mkv, Mkv))]
+    P = bq.concat_packed(Ps)
+    M = Mq + 2 * Mkv
+    x = xvec(K, seed=21)
+    bias = wl.normal_np(M, 0.5, seed=21, stream=wl.stream_id("qkv_bias", M, K))
+    xc, bc = cuda(x), cuda(bias)
+    y = bq.gemv_qkv_bias(qt, P, xc, bc)
+    # the single-row GEMV's dot products, then one IEEE fp32 add
+    want = bq.gemv(qt, P, xc) + bc
+    assert torch.equal(y.view(torch.int32), want.view(torch.int32))
+    # concatenation changes nothing: each part is its own GEMV plus its bias
+    r0 = 0
+    for Pi in Ps:
+        Mi = Pi.shape[0]
+        yi = bq.gemv_qkv_bias(qt, Pi, xc, bc[r0:r0 + Mi].contiguous())
+        assert torch.equal(yi.view(torch.int32), y[r0:r0 + Mi].view(torch.int32))
+        r0 += Mi
+    y_ref, S = ora().gemv_bias(QT[qt], P.cpu().numpy(), M, K, x.astype(np.float64),
+                               bias.astype(np.float64))
+    assert_gemv_close(y.cpu().numpy(), y_ref, S, f"qkv+bias {qt} K={K}")
+    # no bias: the plain GEMV, bit for bit
+    y0 = bq.gemv_qkv_bias(qt, P, xc, None)
+    assert torch.equal(y0.view(torch.int32), bq.gemv(qt, P, xc).view(torch.int32))
+
+
+# ---------------------------------------------------------------------------
 # multi-row verify
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("qt", ["q4_0", "q8_0"])

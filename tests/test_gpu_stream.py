@@ -17,7 +17,8 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab, seed=0, chained=True):
+def make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab, seed=0, chained=True,
+                fused_qkv=False):
     def packed(M, K, *tag):
         W = wl.normal_torch((M, K), wl.W_STD, seed=seed, stream=wl.stream_id(*tag), device=DEV)
         return bq.quantize_pack(W, qt)
@@ -31,7 +32,13 @@ def make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab, seed=0, chain
             down=packed(hidden, inter, l, "d"),
             gamma=wl.normal_torch(hidden, 0.1, seed=seed, stream=wl.stream_id(l, "gm"),
                                   device=DEV, mean=1.0)))
-    ds = DecodeStream(qt, layers, packed(vocab, hidden, "lm"), chained=chained)
+    if fused_qkv:
+        for l, L in enumerate(layers):
+            L["qkv"] = bq.concat_packed([L.pop("q"), L.pop("k"), L.pop("v")])
+            L["qkv_bias"] = wl.normal_torch(L["qkv"].shape[0], 0.1, seed=seed,
+                                            stream=wl.stream_id(l, "qkv_bias"), device=DEV)
+    ds = DecodeStream(qt, layers, packed(vocab, hidden, "lm"), chained=chained,
+                      fused_qkv=fused_qkv)
     ds.inputs.copy_(wl.normal_torch(ds.inputs.numel(), 1.0, seed=seed, stream=7, device=DEV))
     return ds
 
@@ -153,3 +160,26 @@ def test_plan_rejects_outputs_overlapping_weights_or_own_stage():
         bq.StreamPlan("q8_0", [bq.StreamOp(0, P2, x, y2), bq.StreamOp(0, P, y2, y)])
     # ... which is fine one stage later (the planner inserts a barrier)
     bq.StreamPlan("q8_0", [bq.StreamOp(0, P2, x, y2), bq.StreamOp(1, P, y2, y)])
+
+
+@pytest.mark.parametrize("chained", [True, False], ids=["chained", "independent"])
+@pytest.mark.parametrize("qt,n_layers,hidden,q_dim,kv_dim,inter,vocab", [
+    ("q8_0", 2, 1024, 2048, 512, 3072, 7000),   # Qwen3-0.6B layer shapes
+    ("q4_0", 2, 3584, 3584, 512, 18944, 3000),  # 7B layer shapes
+])
+def test_fused_qkv_bias_plan_matches_launch_per_op_bitwise(qt, n_layers, hidden, q_dim, kv_dim,
+                                                           inter, vocab, chained):
+    """One fused q|k|v + bias op per layer (4 ops per layer): the plan (stream
+    executor or multi-op kernel) and one launch per op agree bit for bit."""
+    ds = make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab, chained=chained,
+                     fused_qkv=True)
+    assert len(ds.ops) == 4 * n_layers + 1
+    ds.run_per_op()
+    want = snapshot(ds)
+    for op in ds.ops:
+        op.y.fill_(float("nan"))
+    ds.run_plan()
+    torch.cuda.synchronize()
+    for i, (op, w) in enumerate(zip(ds.ops, want)):
+        assert torch.equal(op.y.view(torch.int32), w.view(torch.int32)), f"op {i}"
+    assert bq.device_status(clear=True) == 0

@@ -56,6 +56,9 @@ MUTANTS = [
     ("rms_no_gamma", "* (gamma ? gamma[k] : 1.0)", "* 1.0"),
     ("silu_sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
     ("gate_up_swapped", "y[m] = bqo_silu(gm) * um;", "y[m] = bqo_silu(um) * gm;"),
+    ("bias_subtracted", "y[m] += bias[m];", "y[m] -= bias[m];"),
+    ("bias_shifted_row", "y[m] += bias[m];", "y[m] += bias[m > 0 ? m - 1 : 0];"),
+    ("bias_S_signed", "S[m] += fabs(bias[m]);", "S[m] += bias[m];"),
 ]
 
 

@@ -41,6 +41,10 @@ def test_rmsnorm_silu_gate_up():
     checks.check_norm_silu(o())
 
 
+def test_qkv_bias():
+    checks.check_bias(o())
+
+
 def test_packed_bytes_and_bad_args():
     ob = o()
     assert ob.packed_bytes(oracle.Q8_0, 3072, 1024) == 3072 * 32 * 34
