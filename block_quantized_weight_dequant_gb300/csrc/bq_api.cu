@@ -43,6 +43,7 @@ struct Tunables {
     int single_pdl = 1;              // single calls: allow programmatic dependent launch
     int single_rowmode = 4;          // single calls: row mode up to this many unit tiles per SM (0: off)
     int verify_nr = 2;               // verify calls (R > 1): weight rows per lane (1 or 2)
+    int plan_pdl = 0;                // op-list plans: allow programmatic dependent launch
 };
 
 const Tunables &tunables() {
@@ -72,6 +73,7 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "pdl") && val >= 0 && val <= 1) v.single_pdl = val;
             else if (!std::strcmp(tok, "srow") && val >= 0 && val <= 64) v.single_rowmode = val;
             else if (!std::strcmp(tok, "vnr") && (val == 1 || val == 2)) v.verify_nr = val;
+            else if (!std::strcmp(tok, "ppdl") && val >= 0 && val <= 1) v.plan_pdl = val;
         }
         return v;
     }();
@@ -122,11 +124,28 @@ void plan_gemv(const GemvCall &c, LaunchPlan *p) {
 }
 
 // padded shared-memory row stride for `bytes` of units: conflict-free LDS.128
-// when fewer than 8 lanes share a row (see the bank analysis in bq_kernels.cuh)
+// when fewer than 8 lanes share a row (the stream executor's lane order, lane
+// = rho * G + l)
 int padded_stride(int bytes, int G) {
     int s16 = bytes / 16;
     if (G < 8)
         while (s16 % 8 != G % 8) ++s16;
+    return s16 * 16;
+}
+
+// Row stride of the multi-op kernel's slots, whose lane order is lane =
+// l * rg + rho (rg = 32/G rows per tile and matrix row set).  A quarter-warp
+// (8 adjacent lanes) holds min(rg, 8) rows times 8/min(rg, 8) = m units, and
+// lane (rho, l) reads 16-byte chunk rho*S + l*U + k of the slot, U = 17 or 9
+// chunks per unit (both 1 mod 8).  The eight chunks fall in distinct bank
+// groups (chunk mod 8) exactly when S is an odd multiple of m (m < 8); with
+// m = 8 (G = 32, one row per tile) any S does.
+int multi_stride(int bytes, int G) {
+    const int rg = 32 / G;
+    const int m = 8 / std::min(rg, 8);
+    int s16 = bytes / 16;
+    if (m < 8)
+        while (s16 % (2 * m) != m) ++s16;
     return s16 * 16;
 }
 
@@ -378,21 +397,32 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
         maxK = std::max(maxK, m.K);
         // the smallest item: one unit per lane
         const int k1 = std::min(m.nsc, m.G);
-        slot_min = std::max(slot_min, m.rpw * padded_stride(k1 * ub, m.G));
+        slot_min = std::max(slot_min, m.rpw * multi_stride(k1 * ub, m.G));
     }
     if (tiles > (1LL << 30)) return BQ_ERR_SHAPE;
     // shared memory: header | x buffers | nwarps rings of D slots.  Two x
     // buffers (the next op's x copied while this op computes) when they are
-    // small beside the rings.
+    // small beside the rings and cost no warp: the streaming rate follows the
+    // warp count (measured on GB300: 10, 11, 12 warps of the Q8_0 token stream
+    // ran at 4.86, 5.20, 5.32 TB/s), while a CTA meets an op boundary only a
+    // few times per launch.
     const int cap = max_smem_optin();
     const int x_off = MULTI_X_OFF;
     const int x_floats = x_padded_floats(maxK);
-    const int x_buffers = 2 * x_floats * 4 <= t.multi_x2_max ? 2 : 1;
+    auto warps_for = [&](int xb) {
+        const int ro = (x_off + xb * x_floats * 4 + 127) / 128 * 128;
+        const long long b = (long long)cap - ro;
+        if (b < (long long)D * slot_min) return 0;
+        int w = (int)std::min<long long>(multi_max_warps(qtype, 1), b / ((long long)D * slot_min));
+        if (t.multi_warps) w = std::min(w, t.multi_warps);
+        return w;
+    };
+    int x_buffers = 1;
+    if (2 * x_floats * 4 <= t.multi_x2_max && warps_for(2) >= warps_for(1)) x_buffers = 2;
     const int ring_off = (x_off + x_buffers * x_floats * 4 + 127) / 128 * 128;
     const long long budget = (long long)cap - ring_off;
-    if (budget < (long long)D * slot_min) return BQ_ERR_SHAPE;
-    int nwarps = (int)std::min<long long>(multi_max_warps(qtype, 1), budget / ((long long)D * slot_min));
-    if (t.multi_warps) nwarps = std::min(nwarps, t.multi_warps);
+    const int nwarps = warps_for(x_buffers);
+    if (nwarps < 1) return BQ_ERR_SHAPE;
     const int slot_cap = (int)(budget / ((long long)nwarps * D)) / 128 * 128;
     // pass 2: per op, whole rows in a slot when they fit, else the largest
     // chunk of a multiple of G units
@@ -447,15 +477,15 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
 bool multi_chunking(MultiOp &m, int ub, int slot_cap) {
     int KCU = m.nsc, stride = 0, single = 0;
     if ((long long)m.rpw * m.rb <= slot_cap) {
-        single = m.G >= 8 || (m.rb / 16) % 8 == m.G % 8;
-        stride = single ? m.rb : padded_stride(m.rb, m.G);
+        single = multi_stride(m.rb, m.G) == m.rb;
+        stride = single ? m.rb : multi_stride(m.rb, m.G);
         if ((long long)m.rpw * stride > slot_cap) single = 0, stride = 0;
     }
     if (!stride) {
         single = 0;
         for (int k = (m.nsc + m.G - 1) / m.G; k >= 1; --k) {
             KCU = std::min(m.nsc, m.G * k);
-            stride = padded_stride(KCU * ub, m.G);
+            stride = multi_stride(KCU * ub, m.G);
             if ((long long)m.rpw * stride <= slot_cap) break;
         }
         if ((long long)m.rpw * stride > slot_cap) return false;
@@ -528,7 +558,7 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     }
     // warps: enough for the tiles of one CTA per SM, at most what fits
     const int k1 = std::min(m.nsc, m.G);
-    const int slot_min = rowmode ? m.rpw * m.rb : m.rpw * padded_stride(k1 * ub, m.G);
+    const int slot_min = rowmode ? m.rpw * m.rb : m.rpw * multi_stride(k1 * ub, m.G);
     if (budget < (long long)D * slot_min) return false;
     const int fit = (int)std::min<long long>(maxw, budget / ((long long)D * slot_min));
     const int want = (int)std::min<long long>(fit, (m.ntiles + nsms - 1) / nsms);
@@ -542,7 +572,7 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     } else if (PU) {
         // one unit per lane per item, so chunks never straddle a panel
         m.KCU = m.G;
-        m.row_stride = padded_stride(m.G * ub, m.G);
+        m.row_stride = multi_stride(m.G * ub, m.G);
         m.single = 0;
         m.nchunks = (m.nsc + m.G - 1) / m.G;
         if ((long long)m.rpw * m.row_stride > slot_cap) return false;
@@ -864,11 +894,12 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
 bq_status bq_stream_plan_launch(const bq_stream_plan *plan, void *stream) {
     if (!plan) return BQ_ERR_NULL;
     if (plan->multi) {
+        const int pdl = bq::tunables().plan_pdl;
         const int e = plan->qtype == BQ_Q8_0
                           ? bq_internal_multi_launch_q8_0(plan->margs, plan->grid, plan->threads,
-                                                          plan->smem, stream, 0)
+                                                          plan->smem, stream, pdl)
                           : bq_internal_multi_launch_q4_0(plan->margs, plan->grid, plan->threads,
-                                                          plan->smem, stream, 0);
+                                                          plan->smem, stream, pdl);
         return from_cuda(e);
     }
     auto s = static_cast<cudaStream_t>(stream);

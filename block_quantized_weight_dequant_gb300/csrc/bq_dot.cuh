@@ -292,6 +292,7 @@ __device__ __forceinline__ void unit_dot(const uint32_t *const (&w)[NW], int nbk
 // chunks floor(34b/16) .. +2 for Q8_0 (always three chunks) and
 // floor(18b/16) .. +1 for Q4_0 (always two), so a row holds one block's words
 // in registers while every x value read from shared memory serves NR rows.
+// (A chunk shared by two blocks is loaded once: the compiler reuses the load.)
 template <int QT, int NR, int R, int B, class XV>
 __device__ __forceinline__ void rows_block(const uint8_t *const (&up)[NR], const XV &xv,
                                            float (&c)[NR][R]) {
@@ -371,6 +372,15 @@ __device__ __forceinline__ void load_unit_global(uint32_t *w, const uint8_t *p, 
 // fold lane partials of a G-lane group (G a power of two <= 32)
 __device__ __forceinline__ float fold_lanes(float v, int G) {
     for (int o = G >> 1; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+// The same butterfly when virtual lane l of the group sits in hardware lane
+// rho + stride * l (stride a power of two, stride * G <= 32): step o adds the
+// partial of virtual lane l ^ o, exactly as fold_lanes does (fp32 addition is
+// commutative, so every lane of the group ends with the same bits).
+__device__ __forceinline__ float fold_lanes_strided(float v, int G, int stride) {
+    for (int o = G >> 1; o > 0; o >>= 1)
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o * stride));
     return v;
 }
 

@@ -84,20 +84,32 @@ __host__ __device__ constexpr int multi_max_warps(int QT, int R) {
 static_assert(MULTI_MAX_WARPS * 32 <= 1024, "one CTA");
 constexpr int MULTI_MAX_D = 4;
 // shared memory header: mbarriers [0, 512), inline op [512, 768), reduction
-// scratch [768, 1796), abort flag at 2040, x buffers from MULTI_X_OFF
-constexpr int MULTI_X_OFF = 2048;
+// scratch [768, 1796), per-warp issuing state of the current op
+// [MULTI_CUR_OFF, +64 per warp), abort flag at MULTI_ABORT_OFF, x buffers from
+// MULTI_X_OFF
+constexpr int MULTI_CUR_OFF = 1808;
+constexpr int MULTI_ABORT_OFF = MULTI_CUR_OFF + 64 * MULTI_MAX_WARPS;
+constexpr int MULTI_X_OFF = 2944;
+static_assert(MULTI_ABORT_OFF + 4 <= MULTI_X_OFF && MULTI_X_OFF % 128 == 0, "header layout");
 static_assert(sizeof(MultiOp) <= 256, "the inline op fits its header slot");
 
 // One warp's position in its item sequence (tiles t = first, first + nwarps,
-// ...; per tile its matrices, per matrix its K-chunks) together with the
-// fields of its op that issuing needs, read from the table only when the
-// cursor enters a new op.
+// ...; per tile its matrices, per matrix its K-chunks).  The fields of its op
+// that issuing needs sit in a MultiCurOp, read from the op table only when
+// the cursor enters a new op: the warp's own cursor keeps it in shared memory
+// (one 64-byte slot per warp), which holds it out of the registers the dot
+// product needs and lets gate+up items switch matrices without a global read.
 struct MultiCursor {
     int t, op, m, c;
     const uint8_t *W;  // the current matrix (W[m] of the op)
-    int rpw, tile_base, tile_end, M, KCU, rb, nchunks, nmat;
-    int row_stride;    // slot bytes per tile row; negative: rows copied as one block
 };
+struct MultiCurOp {
+    const uint8_t *W[2];
+    int rpw, tile_base, tile_end, M, KCU, rb, nchunks, nmat;
+    int row_stride;  // slot bytes per tile row; negative: rows copied as one block
+    int pad_[3];
+};
+static_assert(sizeof(MultiCurOp) == 64, "one 64-byte slot per warp");
 
 // the op holding tile t, walking forward from op index `op`
 __device__ __forceinline__ int multi_op_of(const MultiOp *ops, int nops, int t, int op) {
@@ -105,18 +117,20 @@ __device__ __forceinline__ int multi_op_of(const MultiOp *ops, int nops, int t, 
     return op;
 }
 
-__device__ __forceinline__ void multi_load_op(const MultiOp *ops, MultiCursor &q) {
+__device__ __forceinline__ void multi_load_op(const MultiOp *ops, MultiCursor &q, MultiCurOp &co) {
     const MultiOp &o = ops[q.op];
     q.W = o.W[0];
-    q.rpw = o.rpw;
-    q.tile_base = o.tile_base;
-    q.tile_end = o.tile_base + o.ntiles;
-    q.M = o.M;
-    q.KCU = o.KCU;
-    q.rb = o.rb;
-    q.nchunks = o.nchunks;
-    q.nmat = o.nmat;
-    q.row_stride = o.single ? -1 : o.row_stride;
+    co.W[0] = o.W[0];
+    co.W[1] = o.W[1];
+    co.rpw = o.rpw;
+    co.tile_base = o.tile_base;
+    co.tile_end = o.tile_base + o.ntiles;
+    co.M = o.M;
+    co.KCU = o.KCU;
+    co.rb = o.rb;
+    co.nchunks = o.nchunks;
+    co.nmat = o.nmat;
+    co.row_stride = o.single ? -1 : o.row_stride;
 }
 
 // the rows and byte range of the item under the cursor
@@ -126,60 +140,72 @@ struct MultiItem {
     uint32_t rowb;
 };
 template <int QT>
-__device__ __forceinline__ MultiItem multi_item(const MultiCursor &q) {
+__device__ __forceinline__ MultiItem multi_item(const MultiCursor &q, const MultiCurOp &co) {
     constexpr int UB = Fmt<QT>::unit_bytes;
-    const int row0 = (q.t - q.tile_base) * q.rpw;
-    const int b0 = q.c * q.KCU * UB;
+    const int row0 = (q.t - co.tile_base) * co.rpw;
+    const int b0 = q.c * co.KCU * UB;
     MultiItem it;
-    it.rows = min(q.rpw, q.M - row0);
-    it.rowb = (uint32_t)min(q.KCU * UB, q.rb - b0);
-    it.src = q.W + (size_t)row0 * q.rb + b0;
+    it.rows = min(co.rpw, co.M - row0);
+    it.rowb = (uint32_t)min(co.KCU * UB, co.rb - b0);
+    it.src = q.W + (size_t)row0 * co.rb + b0;
     return it;
 }
 
 template <int QT>
-__device__ __forceinline__ void multi_issue(const MultiCursor &q, uint8_t *st, uint64_t *bar,
-                                            uint64_t pol, int lane) {
-    const MultiItem it = multi_item<QT>(q);
+__device__ __forceinline__ void multi_issue(const MultiCursor &q, const MultiCurOp &co, uint8_t *st,
+                                            uint64_t *bar, uint64_t pol, int lane) {
+    const MultiItem it = multi_item<QT>(q, co);
+    const int row_stride = co.row_stride, rb = co.rb;
     // the slot's previous contents were read by this warp's generic loads
     __syncwarp();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (lane == 0) mbar_arrive_expect_tx(bar, it.rowb * it.rows);
     __syncwarp();
-    if (q.row_stride < 0) {
+    if (row_stride < 0) {
         if (lane == 0) bulk_g2s(st, it.src, it.rowb * it.rows, bar, pol);
     } else {
         for (int r = lane; r < it.rows; r += 32)
-            bulk_g2s(st + r * q.row_stride, it.src + (size_t)r * q.rb, it.rowb, bar, pol);
+            bulk_g2s(st + r * row_stride, it.src + (size_t)r * rb, it.rowb, bar, pol);
     }
 }
 
 // the same bytes into L2 only (a hint: no completion, no value bound)
 template <int QT>
-__device__ __forceinline__ void multi_prefetch(const MultiCursor &q, int lane) {
-    const MultiItem it = multi_item<QT>(q);
-    if (q.row_stride < 0) {
+__device__ __forceinline__ void multi_prefetch(const MultiCursor &q, const MultiCurOp &co, int lane) {
+    const MultiItem it = multi_item<QT>(q, co);
+    if (co.row_stride < 0) {
         if (lane == 0) bulk_prefetch_l2(it.src, it.rowb * it.rows);
     } else {
-        for (int r = lane; r < it.rows; r += 32) bulk_prefetch_l2(it.src + (size_t)r * q.rb, it.rowb);
+        for (int r = lane; r < it.rows; r += 32) bulk_prefetch_l2(it.src + (size_t)r * co.rb, it.rowb);
     }
 }
 
 __device__ __forceinline__ void multi_advance(const MultiOp *ops, int nops, int nwarps,
-                                              MultiCursor &q) {
-    if (++q.c < q.nchunks) return;
+                                              MultiCursor &q, MultiCurOp &co) {
+    if (++q.c < co.nchunks) return;
     q.c = 0;
-    if (++q.m < q.nmat) {
-        q.W = ops[q.op].W[q.m];
+    if (++q.m < co.nmat) {
+        q.W = co.W[1];  // matrix 0 -> 1 (nmat is 1 or 2)
         return;
     }
     q.m = 0;
     q.t += nwarps;
-    if (q.t >= q.tile_end && q.op + 1 < nops) {
+    if (q.t >= co.tile_end && q.op + 1 < nops) {
         q.op = multi_op_of(ops, nops, q.t, q.op);
-        multi_load_op(ops, q);
-    } else if (q.nmat > 1) {
-        q.W = ops[q.op].W[0];
+        multi_load_op(ops, q, co);
+    } else if (co.nmat > 1) {
+        q.W = co.W[0];
+    }
+}
+
+// bounded mbarrier wait that also gives up once another warp of the CTA has
+// set the abort flag; the flag is read only when the data has not landed yet
+__device__ __forceinline__ bool multi_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (*abort_flag || globaltimer() - t0 > BQ_WAIT_LIMIT_NS) return false;
     }
 }
 
@@ -201,9 +227,13 @@ __device__ __forceinline__ void multi_stage_x(const MultiOp &o, int R, int k0, i
 }
 
 // NR: weight rows per lane; R: input rows.  A tile is NR * 32/G rows; lane
-// (rho, l) of a warp takes rows rho, rho + 32/G, ... of the tile and units
-// l, l + G, ... of each, so every x value it reads from shared memory serves
-// NR weight rows.  NR = 0 is row mode (R = 1): a tile is rpw whole rows, each
+// rho + (32/G) l of a warp takes rows rho, rho + 32/G, ... of the tile and
+// units l, l + G, ... of each, so every x value it reads from shared memory
+// serves NR weight rows.  The lanes that read the same x chunk (same l) are
+// adjacent: a 16-byte shared-memory load whose lane quads each read one
+// address takes half the cycles of one whose quads read four (measured on
+// GB300), and the row stride of the slots keeps the weight reads of every
+// quarter-warp on distinct bank groups (host planning).  NR = 0 is row mode (R = 1): a tile is rpw whole rows, each
 // evaluated block-parallel by the whole warp (row_dot_blockpar: the same tree
 // with one block per lane), for calls too small to keep every lane busy.
 template <int QT, int NR, int R>
@@ -213,7 +243,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [nwarps][D]
     MultiOp *op_inline = reinterpret_cast<MultiOp *>(smem + 512);
     float *red = reinterpret_cast<float *>(smem + 768);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 2040);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MULTI_ABORT_OFF);
     constexpr int UB = Fmt<QT>::unit_bytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nthr = blockDim.x;
@@ -255,17 +285,20 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
     }
     const int op_last = multi_op_of(ops, nops, t_end - 1, op0);
 
+    MultiCurOp &co = reinterpret_cast<MultiCurOp *>(smem + MULTI_CUR_OFF)[warp];
     MultiCursor q;
     q.t = t_begin + warp;
     q.m = q.c = 0;
     q.op = multi_op_of(ops, nops, q.t, op0);
-    multi_load_op(ops, q);
+    multi_load_op(ops, q, co);
     // this warp's first items into L2 while the kernel before may still run
+    // (a copy of the cursor with its own op state in registers)
     {
         MultiCursor f = q;
+        MultiCurOp fo = co;
         for (int i = 0; i < a.D && f.t < t_end; ++i) {
-            multi_prefetch<QT>(f, lane);
-            multi_advance(ops, nops, a.nwarps, f);
+            multi_prefetch<QT>(f, fo, lane);
+            multi_advance(ops, nops, a.nwarps, f, fo);
         }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -273,8 +306,8 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
     // fill the ring with this warp's first D items
     int issued = 0;
     for (; issued < a.D && q.t < t_end; ++issued) {
-        multi_issue<QT>(q, ring + (size_t)issued * a.slot_bytes, wfull + issued, pol, lane);
-        multi_advance(ops, nops, a.nwarps, q);
+        multi_issue<QT>(q, co, ring + (size_t)issued * a.slot_bytes, wfull + issued, pol, lane);
+        multi_advance(ops, nops, a.nwarps, q, co);
     }
 
     auto sync = []() { __syncthreads(); };
@@ -291,6 +324,8 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
     }
 
     int e = 0, landed = 0;  // items consumed (or skipped after an error); items seen landed
+    int slot = 0;           // e mod D
+    uint32_t par = 0;       // (e / D) mod 2: the phase parity of slot's next completion
     bool ok = true;
     int phase = 0;
     for (int op = op0; op <= op_last; ++op) {
@@ -305,7 +340,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
         const int lo = max(t_begin, tile_base), hi = min(t_end, tile_base + ntiles);
         // this warp's first tile in [lo, hi): (t - t_begin) mod nwarps == warp
         const int t_first = lo + ((warp - (lo - t_begin) % a.nwarps) + a.nwarps) % a.nwarps;
-        const int rho = lane / G, l = lane & (G - 1), rg = 32 / G;
+        const int rg = 32 / G, rho = lane & (rg - 1), l = lane / rg;
         constexpr int NRA = NR ? NR : 1;
         float p0[NRA][R], p1[NRA];
         for (int pn = 0; pn < np; ++pn, ++phase) {
@@ -360,16 +395,13 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
                     if (m >= nmat) break;
-                    for (int c = c_lo; c < c_hi; ++c, ++e) {
-                        const int slot = e % a.D;
+                    for (int c = c_lo; c < c_hi;
+                         ++c, ++e, slot = slot + 1 == a.D ? 0 : slot + 1, par ^= slot == 0) {
                         if (ok) {
-                            if (*abort_flag) {
-                                ok = false;
-                            } else if (!__all_sync(0xffffffffu,
-                                                   mbar_wait_bounded(wfull + slot, (e / a.D) & 1))) {
+                            if (!__all_sync(0xffffffffu, multi_wait(wfull + slot, par, abort_flag))) {
                                 if (lane == 0) {
+                                    if (!*abort_flag) atomicOr(status, BQ_DEVERR_FULL_WAIT);
                                     *abort_flag = 1;
-                                    atomicOr(status, BQ_DEVERR_FULL_WAIT);
                                 }
                                 ok = false;
                             } else {
@@ -399,9 +431,9 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                                     }
                                 }
                                 if (q.t < t_end) {
-                                    multi_issue<QT>(q, ring + (size_t)slot * a.slot_bytes,
+                                    multi_issue<QT>(q, co, ring + (size_t)slot * a.slot_bytes,
                                                     wfull + slot, pol, lane);
-                                    multi_advance(ops, nops, a.nwarps, q);
+                                    multi_advance(ops, nops, a.nwarps, q, co);
                                     ++issued;
                                 }
                                 continue;
@@ -432,9 +464,9 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                         }
                         // refill the slot just read with the item D places ahead
                         if (q.t < t_end) {
-                            multi_issue<QT>(q, ring + (size_t)slot * a.slot_bytes, wfull + slot, pol,
+                            multi_issue<QT>(q, co, ring + (size_t)slot * a.slot_bytes, wfull + slot, pol,
                                             lane);
-                            multi_advance(ops, nops, a.nwarps, q);
+                            multi_advance(ops, nops, a.nwarps, q, co);
                             ++issued;
                         }
                     }
@@ -445,9 +477,9 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                     const int row = rho + v * rg;
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        const float g = fold_lanes(p0[v][r], G);
+                        const float g = fold_lanes_strided(p0[v][r], G, rg);
                         if (nmat == 2) {
-                            const float u = fold_lanes(p1[v], G);
+                            const float u = fold_lanes_strided(p1[v], G, rg);
                             if (row < rows && l == 0) y[row0 + row] = silu_mul(g, u);
                         } else if (row < rows && l == 0) {
                             y[(size_t)r * M + row0 + row] =
