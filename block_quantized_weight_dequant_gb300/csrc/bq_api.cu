@@ -133,20 +133,73 @@ int padded_stride(int bytes, int G) {
     return s16 * 16;
 }
 
-// Row stride of the multi-op kernel's slots, whose lane order is lane =
-// l * rg + rho (rg = 32/G rows per tile and matrix row set).  A quarter-warp
-// (8 adjacent lanes) holds min(rg, 8) rows times 8/min(rg, 8) = m units, and
-// lane (rho, l) reads 16-byte chunk rho*S + l*U + k of the slot, U = 17 or 9
-// chunks per unit (both 1 mod 8).  The eight chunks fall in distinct bank
-// groups (chunk mod 8) exactly when S is an odd multiple of m (m < 8); with
-// m = 8 (G = 32, one row per tile) any S does.
-int multi_stride(int bytes, int G) {
-    const int rg = 32 / G;
-    const int m = 8 / std::min(rg, 8);
-    int s16 = bytes / 16;
-    if (m < 8)
-        while (s16 % (2 * m) != m) ++s16;
-    return s16 * 16;
+// Lane order of the multi-op kernel (see bq_multi.cuh): bit b of `umask` set
+// means bit b of the lane index is a bit of the lane's unit column l (the
+// set bits, low to high, are l's bits); the other lane bits give the row rho.
+// Two conditions, both for 16-byte shared-memory loads on GB300:
+//  - x reads: the lanes of one unit column read the same x chunk, and a load
+//    takes 2 cycles when every lane quad reads at most two distinct chunks
+//    (4 when a quad reads four), so at most one of lane bits 0, 1 is a unit bit;
+//  - weight reads: lane (rho, l) reads chunk rho*S + l*U + k of the slot (S the
+//    row stride and U the unit, in 16-byte chunks); the 8 lanes of each
+//    quarter-warp must hit 8 distinct bank groups (chunk mod 8).
+static int pext5(int v, int m) {
+    int r = 0, k = 0;
+    for (int b = 0; b < 5; ++b)
+        if (m >> b & 1) r |= (v >> b & 1) << k++;
+    return r;
+}
+static bool lane_order_ok(int m, int G, int S, int U) {
+    int ub = 0;
+    while ((1 << ub) < G) ++ub;
+    if (__builtin_popcount((unsigned)m) != ub) return false;
+    for (int q = 0; q < 4; ++q) {
+        int seen = 0;
+        for (int ln = 8 * q; ln < 8 * q + 8; ++ln)
+            seen |= 1 << ((pext5(ln, ~m & 31) * S + pext5(ln, m) * U) % 8);
+        if (seen != 0xFF) return false;
+    }
+    for (int q = 0; q < 8; ++q) {
+        int ls = 0;
+        for (int ln = 4 * q; ln < 4 * q + 4; ++ln) ls |= 1 << pext5(ln, m);
+        if (__builtin_popcount((unsigned)ls) > 2) return false;
+    }
+    return true;
+}
+// Choose the slot row stride S >= S0 (chunks) and a lane order for G unit
+// columns that meets both conditions: S = S0 only when `pad` is false.  The
+// candidates put rows in lane bits 0..2 (S odd), row/unit/row (S = 2 mod 4)
+// or row/unit/unit (S = 4 mod 8).  Q4_0 (`rows_low`) has the single order with
+// the row in the low lane bits, which its kernel instance computes by shifts.
+// False when none fits.
+bool lane_order(int G, int S0, int U, bool pad, int *S, int *umask, bool rows_low) {
+    int ub = 0;
+    while ((1 << ub) < G) ++ub;
+    const int rb = 5 - ub;
+    int cand[3], nc = 0;
+    if (rows_low) {
+        cand[nc++] = ((G - 1) << rb) & 31;
+    } else {
+        if (rb >= 3) cand[nc++] = ((G - 1) << rb) & 31;
+        if (ub >= 1 && rb >= 2) cand[nc++] = 0x2 | (((1 << (ub - 1)) - 1) << 3);
+        if (ub >= 2 && rb >= 1) cand[nc++] = (G - 1) << 1;
+    }
+    for (int s = S0; s < S0 + (pad ? 8 : 1); ++s)
+        for (int i = 0; i < nc; ++i)
+            if (lane_order_ok(cand[i], G, s, U)) {
+                *S = s;
+                *umask = cand[i];
+                return true;
+            }
+    return false;
+}
+// The same, falling back (one row per tile, G = 32) to the unit column in the
+// low lane bits: every quarter-warp then reads 8 units of one row, which is
+// conflict-free for any S, and x loads take 4 cycles.
+void lane_order_any(int G, int S0, int U, int *S, int *umask, bool rows_low) {
+    if (lane_order(G, S0, U, true, S, umask, rows_low)) return;
+    *S = S0;
+    *umask = G - 1;
 }
 
 namespace {
@@ -397,7 +450,9 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
         maxK = std::max(maxK, m.K);
         // the smallest item: one unit per lane
         const int k1 = std::min(m.nsc, m.G);
-        slot_min = std::max(slot_min, m.rpw * multi_stride(k1 * ub, m.G));
+        int S1 = 0, um = 0;
+        lane_order_any(m.G, k1 * ub / 16, ub / 16, &S1, &um, qtype == BQ_Q4_0);
+        slot_min = std::max(slot_min, m.rpw * S1 * 16);
     }
     if (tiles > (1LL << 30)) return BQ_ERR_SHAPE;
     // shared memory: header | x buffers | nwarps rings of D slots.  Two x
@@ -473,26 +528,39 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
 }
 
 // One warp-tile item layout for op m: whole rows in a slot of slot_cap bytes
-// when they fit, else chunks of a multiple of G units (bank-padded rows).
+// when they fit (copied as one block when their natural stride admits a lane
+// order), else chunks of a multiple of G units with a padded row stride.
 bool multi_chunking(MultiOp &m, int ub, int slot_cap) {
-    int KCU = m.nsc, stride = 0, single = 0;
+    const int U = ub / 16;
+    const bool q4 = ub == 8 * 18;  // Q4_0: rows in the low lane bits
+    int KCU = m.nsc, S = 0, umask = 0, single = 0;
     if ((long long)m.rpw * m.rb <= slot_cap) {
-        single = multi_stride(m.rb, m.G) == m.rb;
-        stride = single ? m.rb : multi_stride(m.rb, m.G);
-        if ((long long)m.rpw * stride > slot_cap) single = 0, stride = 0;
+        // one copy per item; else padded rows (one copy per row); else, with
+        // G >= 8, one copy in the fallback order (conflict-free for any
+        // stride; for Q4_0 only where it is the rows-low order, G = 32)
+        int Sp = 0, up = 0;
+        if (lane_order(m.G, m.rb / 16, U, false, &Sp, &up, q4)) {
+            S = Sp, umask = up, single = 1;
+        } else if (lane_order(m.G, m.rb / 16, U, true, &Sp, &up, q4) &&
+                   (long long)m.rpw * Sp * 16 <= slot_cap) {
+            S = Sp, umask = up, single = 0;
+        } else if (q4 ? m.G == 32 : m.G >= 8) {
+            S = m.rb / 16, umask = m.G - 1, single = 1;
+        }
     }
-    if (!stride) {
+    if (!S) {
         single = 0;
         for (int k = (m.nsc + m.G - 1) / m.G; k >= 1; --k) {
             KCU = std::min(m.nsc, m.G * k);
-            stride = multi_stride(KCU * ub, m.G);
-            if ((long long)m.rpw * stride <= slot_cap) break;
+            lane_order_any(m.G, KCU * U, U, &S, &umask, q4);
+            if ((long long)m.rpw * S * 16 <= slot_cap) break;
         }
-        if ((long long)m.rpw * stride > slot_cap) return false;
+        if ((long long)m.rpw * S * 16 > slot_cap) return false;
     }
     m.KCU = KCU;
-    m.row_stride = stride;
+    m.row_stride = S * 16;
     m.single = single;
+    m.umask = umask;
     m.nchunks = (m.nsc + KCU - 1) / KCU;
     return true;
 }
@@ -558,7 +626,9 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     }
     // warps: enough for the tiles of one CTA per SM, at most what fits
     const int k1 = std::min(m.nsc, m.G);
-    const int slot_min = rowmode ? m.rpw * m.rb : m.rpw * multi_stride(k1 * ub, m.G);
+    int S1 = 0, um1 = 0;
+    lane_order_any(m.G, k1 * ub / 16, ub / 16, &S1, &um1, c.qtype == BQ_Q4_0);
+    const int slot_min = rowmode ? m.rpw * m.rb : m.rpw * S1 * 16;
     if (budget < (long long)D * slot_min) return false;
     const int fit = (int)std::min<long long>(maxw, budget / ((long long)D * slot_min));
     const int want = (int)std::min<long long>(fit, (m.ntiles + nsms - 1) / nsms);
@@ -572,7 +642,10 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     } else if (PU) {
         // one unit per lane per item, so chunks never straddle a panel
         m.KCU = m.G;
-        m.row_stride = multi_stride(m.G * ub, m.G);
+        int S = 0, um = 0;
+        lane_order_any(m.G, m.G * ub / 16, ub / 16, &S, &um, c.qtype == BQ_Q4_0);
+        m.row_stride = S * 16;
+        m.umask = um;
         m.single = 0;
         m.nchunks = (m.nsc + m.G - 1) / m.G;
         if ((long long)m.rpw * m.row_stride > slot_cap) return false;

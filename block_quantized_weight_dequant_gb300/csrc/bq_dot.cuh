@@ -374,16 +374,6 @@ __device__ __forceinline__ float fold_lanes(float v, int G) {
     for (int o = G >> 1; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
-// The same butterfly when virtual lane l of the group sits in hardware lane
-// rho + stride * l (stride a power of two, stride * G <= 32): step o adds the
-// partial of virtual lane l ^ o, exactly as fold_lanes does (fp32 addition is
-// commutative, so every lane of the group ends with the same bits).
-__device__ __forceinline__ float fold_lanes_strided(float v, int G, int stride) {
-    for (int o = G >> 1; o > 0; o >>= 1)
-        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o * stride));
-    return v;
-}
-
 // One block (34 or 18 bytes) at a 2-byte-aligned shared-memory address,
 // realigned into words so that the block's scale starts at byte 0.  Reads up
 // to 4 bytes past the block; shared-memory rings keep that slack at their end.

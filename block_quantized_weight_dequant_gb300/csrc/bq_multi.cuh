@@ -56,6 +56,7 @@ struct MultiOp {
     int ntiles, tile_base;   // tiles of this op; its first tile in the whole list
     int row_stride, single;  // slot bytes per tile row; rows copied as one block
     int rowmode;             // 1: a tile is rpw whole rows, each evaluated by the whole warp
+    int umask;               // lane bits that form the unit column l (the rest form the row)
 };
 
 struct MultiArgs {
@@ -209,6 +210,36 @@ __device__ __forceinline__ bool multi_wait(uint64_t *bar, uint32_t parity, volat
     }
 }
 
+// The row fold when virtual lane l of the group sits in hardware lane
+// rho + stride * l (stride a power of two, stride * G <= 32): step o adds the
+// partial of virtual lane l ^ o, exactly as fold_lanes does.
+__device__ __forceinline__ float fold_lanes_strided(float v, int G, int stride) {
+    for (int o = G >> 1; o > 0; o >>= 1)
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o * stride));
+    return v;
+}
+
+// the bits of `lane` selected by `mask`, packed from bit 0 up
+__device__ __forceinline__ int lane_bits(int lane, int mask) {
+    int v = 0, k = 0;
+#pragma unroll
+    for (int b = 0; b < 5; ++b)
+        if (mask >> b & 1) v |= (lane >> b & 1) << k++;
+    return v;
+}
+
+// The row fold of fold_lanes when the G partials of a row sit in the lanes
+// whose unit bits (umask) vary: the butterfly takes the unit bits from the
+// highest to the lowest, i.e. virtual-lane offsets G/2, ..., 1, exactly as
+// fold_lanes does (fp32 addition is commutative, so every lane of the row ends
+// with the same bits).
+__device__ __forceinline__ float fold_unit_lanes(float v, int umask) {
+#pragma unroll
+    for (int b = 4; b >= 0; --b)
+        if (umask >> b & 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 1 << b));
+    return v;
+}
+
 __device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
                  : "memory");
@@ -227,13 +258,14 @@ __device__ __forceinline__ void multi_stage_x(const MultiOp &o, int R, int k0, i
 }
 
 // NR: weight rows per lane; R: input rows.  A tile is NR * 32/G rows; lane
-// rho + (32/G) l of a warp takes rows rho, rho + 32/G, ... of the tile and
-// units l, l + G, ... of each, so every x value it reads from shared memory
-// serves NR weight rows.  The lanes that read the same x chunk (same l) are
-// adjacent: a 16-byte shared-memory load whose lane quads each read one
-// address takes half the cycles of one whose quads read four (measured on
-// GB300), and the row stride of the slots keeps the weight reads of every
-// quarter-warp on distinct bank groups (host planning).  NR = 0 is row mode (R = 1): a tile is rpw whole rows, each
+// (rho, l) of a warp takes rows rho, rho + 32/G, ... of the tile and units
+// l, l + G, ... of each, so every x value it reads from shared memory serves
+// NR weight rows.  Which lane bits form l and which form rho is the op's
+// `umask`, chosen on the host per op: lanes of one unit column read the same
+// x chunk, and a 16-byte shared-memory load whose lane quads read at most two
+// distinct chunks takes half the cycles of one whose quads read four
+// (measured on GB300); the slot's row stride keeps the weight reads of every
+// quarter-warp on distinct bank groups.  NR = 0 is row mode (R = 1): a tile is rpw whole rows, each
 // evaluated block-parallel by the whole warp (row_dot_blockpar: the same tree
 // with one block per lane), for calls too small to keep every lane busy.
 template <int QT, int NR, int R>
@@ -340,7 +372,13 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
         const int lo = max(t_begin, tile_base), hi = min(t_end, tile_base + ntiles);
         // this warp's first tile in [lo, hi): (t - t_begin) mod nwarps == warp
         const int t_first = lo + ((warp - (lo - t_begin) % a.nwarps) + a.nwarps) % a.nwarps;
-        const int rg = 32 / G, rho = lane & (rg - 1), l = lane / rg;
+        // Q4_0 always takes the order with the row in the low lane bits (its
+        // instance runs 16 warps at the 128-register cap, where the general
+        // order measured slower); Q8_0 takes the op's order
+        const int rg = 32 / G;
+        const int umask = QT == QT_Q4_0 ? 0 : o.umask;
+        const int rho = QT == QT_Q4_0 ? lane & (rg - 1) : lane_bits(lane, ~umask & 31);
+        const int l = QT == QT_Q4_0 ? lane / rg : lane_bits(lane, umask);
         constexpr int NRA = NR ? NR : 1;
         float p0[NRA][R], p1[NRA];
         for (int pn = 0; pn < np; ++pn, ++phase) {
@@ -477,9 +515,12 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                     const int row = rho + v * rg;
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        const float g = fold_lanes_strided(p0[v][r], G, rg);
+                        auto fold = [&](float x) {
+                            return QT == QT_Q4_0 ? fold_lanes_strided(x, G, rg) : fold_unit_lanes(x, umask);
+                        };
+                        const float g = fold(p0[v][r]);
                         if (nmat == 2) {
-                            const float u = fold_lanes_strided(p1[v], G, rg);
+                            const float u = fold(p1[v]);
                             if (row < rows && l == 0) y[row0 + row] = silu_mul(g, u);
                         } else if (row < rows && l == 0) {
                             y[(size_t)r * M + row0 + row] =
