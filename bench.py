@@ -212,13 +212,14 @@ def build_token_layers(cfg, dev, seed=0, fused_qkv=False):
 
 
 def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None,
-                       fused_qkv=False):
+                       fused_qkv=False, tune=True):
     """One decode step's GEMV stream (block_quantized_weight_dequant_gb300.decode).
     chained=False (default): every op reads an N(0, 1) input of its own, the
     pure per-token weight stream; chained: every stage reads the previous
     stage's output (113 dependent stages, grid-wide barriers).  mode "plan":
     one launch per step; mode "per_op": one launch per op.  `packed`: layers
-    from build_token_layers, shared between the two input modes."""
+    from build_token_layers, shared between the two input modes.  tune: split
+    the plan's tiles among CTAs by measured time (set-up, untimed)."""
     import torch
     import block_quantized_weight_dequant_gb300 as bq
     from block_quantized_weight_dequant_gb300 import workloads as wl
@@ -232,7 +233,9 @@ def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None
     w = Workload()
     nbytes = ds.weight_bytes() + ds.activation_bytes()
     if mode == "plan":
-        ds.plan()
+        p = ds.plan()
+        if tune and not chained:
+            p.tune()
         w.add(ds.run_plan, f"stream_plan_{qt}", nbytes)
     else:
         for op in ds.ops:
@@ -251,6 +254,9 @@ def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None
     w.y_dev = ds.logits if chained else torch.cat([op.y for op in ds.ops])
     w.stream_obj = ds
     w.desc = token_desc(cfg, mode, chained, fused_qkv)
+    if mode == "plan" and not chained:
+        w.desc["cta_split"] = ("equal measured time (bq_stream_plan_tune, set-up)" if tune
+                               else "equal bytes")
     assert (w.desc["ops_per_step"], w.desc["stages_per_step"], w.desc["weight_bytes_per_step"]) == \
         (len(ds.ops), ds.n_stages, ds.weight_bytes())
     return w
@@ -380,10 +386,10 @@ def build_workload(args, dev):
         fq = args.qkv == "fused"
         packed = build_token_layers(cfg, dev, fused_qkv=fq)
         w = build_token_stream(cfg, dev, mode=args.launch, chained=chained, packed=packed,
-                               fused_qkv=fq)
+                               fused_qkv=fq, tune=args.tune)
         if args.other_inputs:
             w.other = build_token_stream(cfg, dev, mode=args.launch, chained=not chained,
-                                         packed=packed, fused_qkv=fq)
+                                         packed=packed, fused_qkv=fq, tune=args.tune)
         return w
     if args.config == "cfg1":
         c = wl.CFG1
@@ -597,6 +603,9 @@ def main():
                     help="cfg2/cfg3: q, k, v as three ops, or one fused q|k|v op with a bias")
     ap.add_argument("--layers", type=int, default=0,
                     help="cfg2/cfg3: fewer layers than the model's (smaller cases for profiling)")
+    ap.add_argument("--no-tune", dest="tune", action="store_false",
+                    help="cfg2/cfg3 plans: keep the planner's equal-bytes CTA split instead of "
+                         "re-splitting by measured time at set-up")
     ap.add_argument("--no-other-inputs", dest="other_inputs", action="store_false",
                     help="cfg2/cfg3: skip timing the other input mode as a secondary figure")
     args = ap.parse_args()

@@ -268,6 +268,13 @@ class StreamPlan:
         _lib.check(lib.bq_stream_plan_launch(self._handle, _stream(self._ops[0].W)),
                    "stream_plan_launch")
 
+    def tune(self, rounds=3):
+        """Re-split the plan's tiles among CTAs by measured time
+        (bq_stream_plan_tune): runs the plan a few times, overwriting the
+        ops' outputs; synchronous, so call it before graph capture."""
+        _lib.check(lib.bq_stream_plan_tune(self._handle, int(rounds), _stream(self._ops[0].W)),
+                   "stream_plan_tune")
+
     def __del__(self):
         h = getattr(self, "_handle", None)
         if h is not None and h.value:

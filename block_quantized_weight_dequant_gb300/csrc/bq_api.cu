@@ -716,6 +716,7 @@ void fill_multi_args(const MultiGeometry &geo, int n_ops, const MultiOp *ops,
     a->x_buffers = geo.x_buffers;
     a->panel_units = geo.panel_units;
     a->inline_op = 0;
+    a->cta_ns = nullptr;
 }
 
 void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const ExecX *xs,
@@ -749,6 +750,12 @@ struct bq_stream_plan {
     bq::ExecArgs args;
     bq::MultiArgs margs;
     unsigned int *counters;
+    // multi-op plans: host copies of the op table and of the CTA tile split,
+    // the split's device copy, and the per-CTA timing array (plan tuning)
+    bq::MultiOp *mo_host;
+    int *ct_host;
+    int *ct_dev;
+    unsigned long long *cta_ns;
 };
 
 using bq::GemvCall;
@@ -881,7 +888,8 @@ int64_t bq_stream_workspace_bytes(int n_ops, int n_stages) {
                          align256((int64_t)n_stages * sizeof(bq::ExecStage)) +
                          align256((int64_t)n_stages * 4);
     const int64_t multi = align256((int64_t)n_ops * sizeof(bq::MultiOp)) +
-                          align256((int64_t)(bq::MULTI_MAX_CTAS + 1) * 4);
+                          align256((int64_t)(bq::MULTI_MAX_CTAS + 1) * 4) +
+                          align256((int64_t)bq::MULTI_MAX_CTAS * 8);
     return std::max(exec, multi);
 }
 
@@ -920,6 +928,16 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
             auto *p = new (std::nothrow) bq_stream_plan;
             if (!p) return BQ_ERR_CUDA;
             std::memset(p, 0, sizeof *p);
+            p->mo_host = new (std::nothrow) bq::MultiOp[(size_t)n_ops];
+            p->ct_host = new (std::nothrow) int[(size_t)mg.grid + 1];
+            if (!p->mo_host || !p->ct_host) {
+                delete[] p->mo_host;
+                delete[] p->ct_host;
+                delete p;
+                return BQ_ERR_CUDA;
+            }
+            std::memcpy(p->mo_host, mo.data(), (size_t)n_ops * sizeof(bq::MultiOp));
+            std::memcpy(p->ct_host, ct.data(), (size_t)(mg.grid + 1) * sizeof(int));
             p->qtype = qtype;
             p->n_ops = n_ops;
             p->n_stages = n_stages;
@@ -928,8 +946,11 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
             p->grid = mg.grid;
             p->threads = mg.threads;
             p->smem = mg.smem;
-            bq::fill_multi_args(mg, n_ops, reinterpret_cast<const bq::MultiOp *>(ws),
-                                reinterpret_cast<const int *>(ws + off_ct), &p->margs);
+            p->ct_dev = reinterpret_cast<int *>(ws + off_ct);
+            p->cta_ns = reinterpret_cast<unsigned long long *>(
+                ws + off_ct + align256((int64_t)(bq::MULTI_MAX_CTAS + 1) * 4));
+            bq::fill_multi_args(mg, n_ops, reinterpret_cast<const bq::MultiOp *>(ws), p->ct_dev,
+                                &p->margs);
             *plan = p;
             return BQ_OK;
         }
@@ -987,7 +1008,103 @@ bq_status bq_stream_plan_launch(const bq_stream_plan *plan, void *stream) {
 }
 
 bq_status bq_stream_plan_destroy(bq_stream_plan *plan) {
+    if (plan) {
+        delete[] plan->mo_host;
+        delete[] plan->ct_host;
+    }
     delete plan;
+    return BQ_OK;
+}
+
+namespace {
+// packed bytes of tile k of op o (rows of the tile times row bytes, per matrix)
+long long tile_bytes(const bq::MultiOp &o, int k) {
+    return (long long)std::min(o.rpw, o.M - k * o.rpw) * o.rb * o.nmat;
+}
+// Split the tiles of a multi-op plan into `grid` contiguous ranges of equal
+// estimated time: tile t costs its bytes times the measured time per byte of
+// the CTA that ran it in split `ct` (d[c] over the bytes of range c; a CTA
+// that ran nothing takes the mean).  Op boundaries, idle lanes and per-tile
+// work make the time per byte differ between op shapes and between ranges.
+void rebalance(const bq::MultiOp *mo, int n_ops, int grid, const int *ct, const double *d, int *out) {
+    std::vector<double> bytes((size_t)grid, 0.0), dens((size_t)grid, 0.0);
+    auto for_tiles = [&](auto f) {  // f(tile index, owner CTA in ct, tile bytes)
+        int c = 0;
+        long long t = 0;
+        for (int i = 0; i < n_ops; ++i)
+            for (int k = 0; k < mo[i].ntiles; ++k, ++t) {
+                while (c + 1 < grid && t >= ct[c + 1]) ++c;
+                f(t, c, (double)tile_bytes(mo[i], k));
+            }
+    };
+    for_tiles([&](long long, int c, double b) { bytes[(size_t)c] += b; });
+    double tb = 0.0, td = 0.0;
+    for (int c = 0; c < grid; ++c)
+        if (bytes[(size_t)c] > 0 && d[c] > 0) tb += bytes[(size_t)c], td += d[c];
+    const double mean = tb > 0 ? td / tb : 1.0;
+    for (int c = 0; c < grid; ++c)
+        dens[(size_t)c] = bytes[(size_t)c] > 0 && d[c] > 0 ? d[c] / bytes[(size_t)c] : mean;
+    double total = 0.0;
+    for_tiles([&](long long, int c, double b) { total += b * dens[(size_t)c]; });
+    out[0] = 0;
+    int o = 1;
+    double acc = 0.0;
+    long long tiles = 0;
+    for_tiles([&](long long t, int c, double b) {
+        acc += b * dens[(size_t)c];
+        while (o < grid && acc * grid >= total * o) out[o++] = (int)t + 1;
+        tiles = t + 1;
+    });
+    while (o <= grid) out[o++] = (int)tiles;
+}
+}  // namespace
+
+bq_status bq_stream_plan_tune(bq_stream_plan *plan, int rounds, void *stream) {
+    if (!plan) return BQ_ERR_NULL;
+    if (rounds < 1 || rounds > 16) return BQ_ERR_SHAPE;
+    if (!plan->multi) return BQ_OK;  // the executor's stages are balanced by construction
+    auto s = static_cast<cudaStream_t>(stream);
+    const int grid = plan->grid;
+    constexpr int REPS = 3;  // launches averaged per measurement
+    std::vector<unsigned long long> ns((size_t)grid);
+    std::vector<double> d((size_t)grid);
+    std::vector<int> best((size_t)grid + 1), next((size_t)grid + 1);
+    std::memcpy(best.data(), plan->ct_host, (size_t)(grid + 1) * sizeof(int));
+    double best_max = -1.0;
+    bq::MultiArgs a = plan->margs;
+    a.cta_ns = plan->cta_ns;
+    for (int r = 0; r <= rounds; ++r) {
+        std::fill(d.begin(), d.end(), 0.0);
+        for (int k = 0; k < REPS; ++k) {
+            if (cudaMemsetAsync(plan->cta_ns, 0, (size_t)grid * 8, s) != cudaSuccess) return BQ_ERR_CUDA;
+            const int e = plan->qtype == BQ_Q8_0
+                              ? bq_internal_multi_launch_q8_0(a, grid, plan->threads, plan->smem, stream, 0)
+                              : bq_internal_multi_launch_q4_0(a, grid, plan->threads, plan->smem, stream, 0);
+            if (e != 0) return BQ_ERR_CUDA;
+            if (cudaMemcpyAsync(ns.data(), plan->cta_ns, (size_t)grid * 8, cudaMemcpyDeviceToHost, s) !=
+                    cudaSuccess ||
+                cudaStreamSynchronize(s) != cudaSuccess)
+                return BQ_ERR_CUDA;
+            for (int c = 0; c < grid; ++c) d[(size_t)c] += (double)ns[(size_t)c] / REPS;
+        }
+        const double mx = *std::max_element(d.begin(), d.end());
+        if (best_max < 0 || mx < best_max) {
+            best_max = mx;
+            std::memcpy(best.data(), plan->ct_host, (size_t)(grid + 1) * sizeof(int));
+        }
+        if (r == rounds) break;
+        rebalance(plan->mo_host, plan->n_ops, grid, plan->ct_host, d.data(), next.data());
+        std::memcpy(plan->ct_host, next.data(), (size_t)(grid + 1) * sizeof(int));
+        if (cudaMemcpyAsync(plan->ct_dev, plan->ct_host, (size_t)(grid + 1) * sizeof(int),
+                            cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return BQ_ERR_CUDA;
+    }
+    // keep the split whose slowest CTA was fastest
+    std::memcpy(plan->ct_host, best.data(), (size_t)(grid + 1) * sizeof(int));
+    if (cudaMemcpyAsync(plan->ct_dev, plan->ct_host, (size_t)(grid + 1) * sizeof(int),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return BQ_ERR_CUDA;
     return BQ_OK;
 }
 

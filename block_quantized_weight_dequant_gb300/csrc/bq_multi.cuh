@@ -71,6 +71,7 @@ struct MultiArgs {
     int x_buffers;              // 1 or 2
     int panel_units;            // 0: an op's whole x is staged; else units of K per panel
     int inline_op;              // 1: `op` is the only op; CTA c takes tiles [cT/grid, (c+1)T/grid)
+    unsigned long long *cta_ns; // list mode: each CTA's duration in ns (plan tuning), or null
     MultiOp op;
 };
 
@@ -334,6 +335,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
         }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint64_t t_start = a.cta_ns ? globaltimer() : 0;
 
     // fill the ring with this warp's first D items
     int issued = 0;
@@ -542,6 +544,10 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
             if (!mbar_wait_bounded(wfull + i % a.D, (i / a.D) & 1))
                 atomicOr(status, BQ_DEVERR_DRAIN_WAIT);
     asm volatile("cp.async.wait_all;" ::: "memory");  // nor any x copy
+    if (a.cta_ns) {
+        __syncthreads();
+        if (threadIdx.x == 0) a.cta_ns[blockIdx.x] = globaltimer() - t_start;
+    }
 }
 
 }  // namespace bq

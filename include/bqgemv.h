@@ -216,6 +216,27 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
  * the counters). */
 bq_status bq_stream_plan_launch(const bq_stream_plan *plan, void *stream);
 
+/* Re-split a plan of independent ops (one launch of the streaming kernel)
+ * among the GPU's CTAs by measured time, a set-up step.  (The pages have no
+ * counterpart: they dispatch one kernel per GEMV.)  The planner first splits
+ * the ops' tiles into one contiguous range per CTA of equal BYTES, but op
+ * shapes stream at different rates per byte (idle lanes when K/256 is not a
+ * multiple of the tree's lane count, per-tile folds, and the x staging at
+ * every op boundary inside a range), so on GB300 the slowest CTA of a
+ * Qwen3-0.6B-shaped Q8_0 token finished 12% after the median.  This call
+ * runs the plan `rounds` + 1 times 3 launches each, with every CTA recording
+ * its duration into the plan's workspace; after each measurement it charges
+ * every tile its CTA's measured time per byte and re-splits for equal
+ * estimated time.  The split whose slowest CTA was fastest is kept.  Only
+ * the assignment of tiles to CTAs changes: every output row is computed by
+ * the same arithmetic, so outputs are bit-identical before and after.
+ *  - 1 <= rounds <= 16, else BQ_ERR_SHAPE; a plan of dependent stages (the
+ *    executor) returns BQ_OK untouched.
+ *  - The runs read the ops' inputs and overwrite their outputs, on `stream`.
+ *  - Synchronous (it reads the timings back): call it after
+ *    bq_stream_plan_create and before capturing the plan in a CUDA graph. */
+bq_status bq_stream_plan_tune(bq_stream_plan *plan, int rounds, void *stream);
+
 /* Free the host object (the workspace stays the caller's). */
 bq_status bq_stream_plan_destroy(bq_stream_plan *plan);
 

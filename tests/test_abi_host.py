@@ -166,3 +166,10 @@ def test_stream_plan_rejects_bias_on_gate_up_and_misaligned_bias(lib):
     o.kind, o.bias = _lib.BQ_OP_GEMV, 0x50002
     assert lib.bq_stream_plan_create(bq.Q8_0, ops, 1, ws, 1 << 20, ctypes.byref(plan)) == \
         _lib.BQ_ERR_ALIGN
+
+
+def test_stream_plan_tune_validation(lib):
+    """A null plan is rejected before any CUDA call; the round count is
+    checked on a real plan in the GPU tests."""
+    assert lib.bq_stream_plan_tune(None, 3, None) == _lib.BQ_ERR_NULL
+    assert lib.bq_stream_workspace_bytes(169, 113) >= 169 * 64 + (1024 + 1) * 4 + 1024 * 8

@@ -55,6 +55,33 @@ STREAMS = [
 ]
 
 
+@pytest.mark.parametrize("qt,n_layers,hidden,q_dim,kv_dim,inter,vocab", STREAMS)
+def test_tuned_plan_is_bitwise_the_same(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab):
+    """bq_stream_plan_tune moves tiles between CTAs by measured time; every
+    output row keeps its arithmetic, so outputs stay bit-identical to the
+    launch-per-op path, and a plan of dependent stages is left as it is."""
+    ds = make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab, chained=False)
+    ds.run_per_op()
+    want = snapshot(ds)
+    plan = ds.plan()
+    plan.tune(rounds=2)
+    for op in ds.ops:
+        op.y.fill_(float("nan"))
+    ds.run_plan()
+    for i, (g, w) in enumerate(zip(snapshot(ds), want)):
+        assert torch.equal(g.view(torch.int32), w.view(torch.int32)), f"op {i} differs after tune"
+    dc = make_stream(qt, 1, hidden, q_dim, kv_dim, inter, vocab, chained=True)
+    dc.run_per_op()
+    want_c = snapshot(dc)
+    dc.plan().tune(rounds=1)
+    dc.run_plan()
+    for g, w in zip(snapshot(dc), want_c):
+        assert torch.equal(g.view(torch.int32), w.view(torch.int32))
+    with pytest.raises(bq.BQError):
+        plan.tune(rounds=0)
+    assert bq.device_status(clear=True) == 0
+
+
 @pytest.mark.parametrize("chained", [True, False], ids=["chained", "independent"])
 @pytest.mark.parametrize("qt,n_layers,hidden,q_dim,kv_dim,inter,vocab", STREAMS)
 def test_plan_matches_launch_per_op_bitwise(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab,
