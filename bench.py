@@ -55,12 +55,11 @@ FALLBACK_HBM_GBS = 6800.0
 # the traffic is null until it is captured again.
 NCU_TRAFFIC = {
     # (config, inputs): (bytes per launch, sha256 of csrc/ at capture, summary)
-    ("cfg2", "independent"): (607008768, "bc85a9b9b3f546b6b335ccf8cef4145b8c1034a533dbff27faeac6a1b844f2e4",
+    ("cfg2", "independent"): (606825216, "046257b6c87e40bb31c3c38a26412bb5cf13def629671b53615e9360011607de",
                               "profiles/multi_kernel_q8_0_qwen3_0.6b_stream.md"),
     # captured on 2 of the 28 layers (+ LM head) and scaled by algorithmic bytes
-    ("cfg3", "independent"): (4006005897, "bc85a9b9b3f546b6b335ccf8cef4145b8c1034a533dbff27faeac6a1b844f2e4",
+    ("cfg3", "independent"): (4008261622, "046257b6c87e40bb31c3c38a26412bb5cf13def629671b53615e9360011607de",
                               "profiles/multi_kernel_q4_0_7b_stream.md"),
-    ("cfg1", None): (3400192, "bc85a9b9b3f546b6b335ccf8cef4145b8c1034a533dbff27faeac6a1b844f2e4", "profiles/multi_kernel_q8_0_gemv_3072x1024.md"),
 }
 
 

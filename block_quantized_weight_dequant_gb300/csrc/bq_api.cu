@@ -42,7 +42,7 @@ struct Tunables {
     int single_x_max = 128 * 1024;   // single calls: largest staged R x K input (else panels)
     int single_pdl = 1;              // single calls: allow programmatic dependent launch
     int single_rowmode = 4;          // single calls: row mode up to this many unit tiles per SM (0: off)
-    int verify_nr = 2;               // verify calls (R > 1): weight rows per lane (1 or 2)
+    int verify_nr = 0;               // verify calls (R > 1): weight rows per lane (1 or 2; 0: by R)
     int plan_pdl = 0;                // op-list plans: allow programmatic dependent launch
 };
 
@@ -414,7 +414,7 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
     return BQ_OK;
 }
 
-bool multi_chunking(MultiOp &m, int ub, int slot_cap);
+bool multi_chunking(MultiOp &m, int ub, int slot_cap, bool rows_low);
 
 bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo, int *cta_tiles,
                             MultiGeometry *geo) {
@@ -484,7 +484,7 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
     int slot_bytes = 0;
     for (int i = 0; i < n_ops; ++i) {
         MultiOp &m = mo[i];
-        if (!multi_chunking(m, ub, slot_cap)) return BQ_ERR_SHAPE;
+        if (!multi_chunking(m, ub, slot_cap, qtype == BQ_Q4_0)) return BQ_ERR_SHAPE;
         slot_bytes = std::max(slot_bytes, m.rpw * m.row_stride);
     }
     slot_bytes = (slot_bytes + 127) / 128 * 128;
@@ -530,21 +530,21 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
 // One warp-tile item layout for op m: whole rows in a slot of slot_cap bytes
 // when they fit (copied as one block when their natural stride admits a lane
 // order), else chunks of a multiple of G units with a padded row stride.
-bool multi_chunking(MultiOp &m, int ub, int slot_cap) {
+// rows_low: the kernel instance uses the rows-low lane order (Q4_0 decode)
+bool multi_chunking(MultiOp &m, int ub, int slot_cap, bool rows_low) {
     const int U = ub / 16;
-    const bool q4 = ub == 8 * 18;  // Q4_0: rows in the low lane bits
     int KCU = m.nsc, S = 0, umask = 0, single = 0;
     if ((long long)m.rpw * m.rb <= slot_cap) {
         // one copy per item; else padded rows (one copy per row); else, with
         // G >= 8, one copy in the fallback order (conflict-free for any
         // stride; for Q4_0 only where it is the rows-low order, G = 32)
         int Sp = 0, up = 0;
-        if (lane_order(m.G, m.rb / 16, U, false, &Sp, &up, q4)) {
+        if (lane_order(m.G, m.rb / 16, U, false, &Sp, &up, rows_low)) {
             S = Sp, umask = up, single = 1;
-        } else if (lane_order(m.G, m.rb / 16, U, true, &Sp, &up, q4) &&
+        } else if (lane_order(m.G, m.rb / 16, U, true, &Sp, &up, rows_low) &&
                    (long long)m.rpw * Sp * 16 <= slot_cap) {
             S = Sp, umask = up, single = 0;
-        } else if (q4 ? m.G == 32 : m.G >= 8) {
+        } else if (rows_low ? m.G == 32 : m.G >= 8) {
             S = m.rb / 16, umask = m.G - 1, single = 1;
         }
     }
@@ -552,7 +552,7 @@ bool multi_chunking(MultiOp &m, int ub, int slot_cap) {
         single = 0;
         for (int k = (m.nsc + m.G - 1) / m.G; k >= 1; --k) {
             KCU = std::min(m.nsc, m.G * k);
-            lane_order_any(m.G, KCU * U, U, &S, &umask, q4);
+            lane_order_any(m.G, KCU * U, U, &S, &umask, rows_low);
             if ((long long)m.rpw * S * 16 <= slot_cap) break;
         }
         if ((long long)m.rpw * S * 16 > slot_cap) return false;
@@ -570,7 +570,10 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     const int bb = block_bytes(c.qtype), ub = 8 * bb;
     const int D = std::min(t.multi_d, MULTI_MAX_D);
     const int R = c.R;
-    int NR = R > 1 ? t.verify_nr : 1;
+    // verify: two weight rows per lane share each x read up to R = 4; from
+    // R = 5 on the R partial sums per row fill the registers and one row per
+    // lane measured faster on GB300 (R = 6: 687 against 576 GB/s)
+    int NR = R == 1 ? 1 : t.verify_nr ? t.verify_nr : R <= 4 ? 2 : 1;
     const int nsms = num_sms_current();
     const int cap = max_smem_optin();
     if (nsms <= 0 || cap <= 0) return false;
@@ -627,7 +630,7 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     // warps: enough for the tiles of one CTA per SM, at most what fits
     const int k1 = std::min(m.nsc, m.G);
     int S1 = 0, um1 = 0;
-    lane_order_any(m.G, k1 * ub / 16, ub / 16, &S1, &um1, c.qtype == BQ_Q4_0);
+    lane_order_any(m.G, k1 * ub / 16, ub / 16, &S1, &um1, c.qtype == BQ_Q4_0 && R == 1);
     const int slot_min = rowmode ? m.rpw * m.rb : m.rpw * S1 * 16;
     if (budget < (long long)D * slot_min) return false;
     const int fit = (int)std::min<long long>(maxw, budget / ((long long)D * slot_min));
@@ -643,13 +646,13 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
         // one unit per lane per item, so chunks never straddle a panel
         m.KCU = m.G;
         int S = 0, um = 0;
-        lane_order_any(m.G, m.G * ub / 16, ub / 16, &S, &um, c.qtype == BQ_Q4_0);
+        lane_order_any(m.G, m.G * ub / 16, ub / 16, &S, &um, c.qtype == BQ_Q4_0 && R == 1);
         m.row_stride = S * 16;
         m.umask = um;
         m.single = 0;
         m.nchunks = (m.nsc + m.G - 1) / m.G;
         if ((long long)m.rpw * m.row_stride > slot_cap) return false;
-    } else if (!multi_chunking(m, ub, slot_cap)) {
+    } else if (!multi_chunking(m, ub, slot_cap, c.qtype == BQ_Q4_0 && R == 1)) {
         return false;
     }
     const int slot_bytes = (m.rpw * m.row_stride + 127) / 128 * 128;

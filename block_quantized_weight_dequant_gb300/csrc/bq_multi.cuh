@@ -374,13 +374,14 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
         const int lo = max(t_begin, tile_base), hi = min(t_end, tile_base + ntiles);
         // this warp's first tile in [lo, hi): (t - t_begin) mod nwarps == warp
         const int t_first = lo + ((warp - (lo - t_begin) % a.nwarps) + a.nwarps) % a.nwarps;
-        // Q4_0 always takes the order with the row in the low lane bits (its
-        // instance runs 16 warps at the 128-register cap, where the general
-        // order measured slower); Q8_0 takes the op's order
+        // Q4_0 decode (R = 1) always takes the order with the row in the low
+        // lane bits (its instance runs 16 warps at the 128-register cap, where
+        // the general order measured slower); the others take the op's order
+        constexpr bool ROWS_LOW = QT == QT_Q4_0 && R == 1;
         const int rg = 32 / G;
-        const int umask = QT == QT_Q4_0 ? 0 : o.umask;
-        const int rho = QT == QT_Q4_0 ? lane & (rg - 1) : lane_bits(lane, ~umask & 31);
-        const int l = QT == QT_Q4_0 ? lane / rg : lane_bits(lane, umask);
+        const int umask = ROWS_LOW ? 0 : o.umask;
+        const int rho = ROWS_LOW ? lane & (rg - 1) : lane_bits(lane, ~umask & 31);
+        const int l = ROWS_LOW ? lane / rg : lane_bits(lane, umask);
         constexpr int NRA = NR ? NR : 1;
         float p0[NRA][R], p1[NRA];
         for (int pn = 0; pn < np; ++pn, ++phase) {
@@ -518,7 +519,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         auto fold = [&](float x) {
-                            return QT == QT_Q4_0 ? fold_lanes_strided(x, G, rg) : fold_unit_lanes(x, umask);
+                            return ROWS_LOW ? fold_lanes_strided(x, G, rg) : fold_unit_lanes(x, umask);
                         };
                         const float g = fold(p0[v][r]);
                         if (nmat == 2) {
