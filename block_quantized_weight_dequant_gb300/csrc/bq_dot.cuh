@@ -53,14 +53,18 @@ __device__ __forceinline__ float q8_raw(uint32_t word, int pos) {
     const uint32_t flipped = word ^ 0x80808080u;
     return __uint_as_float(__byte_perm(flipped, 0x4B000000u, 0x7540u | (uint32_t)pos));
 }
-// Q4_0: the nibbles of a word are masked into bytes once (low nibbles, or
-// high nibbles shifted down), and the byte at `pos` goes into the low
-// mantissa of 2^23: the float 2^23 + n, from which subtracting 2^23 + 8
-// leaves n - 8 exactly.
-constexpr float Q4_MAGIC = 8388616.0f;  // 2^23 + 8
+// Q4_0: the nibbles of a word are masked in place once (low nibbles, or high
+// nibbles), and the byte at `pos` goes into the low mantissa byte of a magic
+// float.  A low nibble n under 2^23 gives 2^23 + n; a high nibble stays in
+// bits 4..7 (the byte holds 16n) under 2^19, whose mantissa step is 2^-4, so
+// it gives 2^19 + 16n * 2^-4 = 2^19 + n without a shift.  Subtracting
+// 2^23 + 8 or 2^19 + 8 leaves n - 8 exactly.
+constexpr float Q4_MAGIC = 8388616.0f;     // 2^23 + 8
+constexpr float Q4_MAGIC_HI = 524296.0f;   // 2^19 + 8
 __device__ __forceinline__ float q4_raw(uint32_t word, bool high, int pos) {
-    const uint32_t nib = (high ? word >> 4 : word) & 0x0F0F0F0Fu;
-    return __uint_as_float(__byte_perm(nib, 0x4B000000u, 0x7540u | (uint32_t)pos));
+    const uint32_t nib = word & (high ? 0xF0F0F0F0u : 0x0F0F0F0Fu);
+    return __uint_as_float(
+        __byte_perm(nib, high ? 0x49000000u : 0x4B000000u, 0x7540u | (uint32_t)pos));
 }
 
 __device__ __forceinline__ float scale_at(const uint32_t *w, int byte_off) {
@@ -179,7 +183,10 @@ __device__ __forceinline__ void block_sum_at(const uint32_t *const (&w)[NW], con
                                              float (&s)[NW][R], float (&d)[NW]) {
     constexpr float M = QT == QT_Q8_0 ? Q8_MAGIC : Q4_MAGIC;
 #if BQ_F32X2
+    // codes 4t..4t+3 are low nibbles for t < 4 and high nibbles for t >= 4
+    // (Q4_0), so each pair takes one magic
     const float2 mneg = make_float2(-M, -M);
+    const float2 mneg_hi = QT == QT_Q8_0 ? mneg : make_float2(-Q4_MAGIC_HI, -Q4_MAGIC_HI);
     float2 a[NW][R][2];
 #pragma unroll
     for (int v = 0; v < NW; ++v)
@@ -192,12 +199,13 @@ __device__ __forceinline__ void block_sum_at(const uint32_t *const (&w)[NW], con
         for (int r = 0; r < R; ++r) xv[r] = xv_.get(r, B, t);
 #pragma unroll
         for (int v = 0; v < NW; ++v) {
+            const float2 mt = t < 4 ? mneg : mneg_hi;
             const float2 q01 = __fadd2_rn(
                 make_float2(raw_at_byte<QT>(w[v], WB, 4 * t), raw_at_byte<QT>(w[v], WB, 4 * t + 1)),
-                mneg);
+                mt);
             const float2 q23 = __fadd2_rn(
                 make_float2(raw_at_byte<QT>(w[v], WB, 4 * t + 2), raw_at_byte<QT>(w[v], WB, 4 * t + 3)),
-                mneg);
+                mt);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 a[v][r][0] = __ffma2_rn(q01, make_float2(xv[r].x, xv[r].y), a[v][r][0]);
@@ -230,7 +238,8 @@ __device__ __forceinline__ void block_sum_at(const uint32_t *const (&w)[NW], con
         for (int i = 0; i < 4; ++i) {
 #pragma unroll
             for (int v = 0; v < NW; ++v) {
-                const float q = __fsub_rn(raw_at_byte<QT>(w[v], WB, 4 * t + i), M);
+                const float q = __fsub_rn(raw_at_byte<QT>(w[v], WB, 4 * t + i),
+                                          QT == QT_Q4_0 && t >= 4 ? Q4_MAGIC_HI : M);
 #pragma unroll
                 for (int r = 0; r < R; ++r) a[v][r][i] = __fmaf_rn(q, f4(xv[r], i), a[v][r][i]);
             }
