@@ -55,10 +55,10 @@ FALLBACK_HBM_GBS = 6800.0
 # the traffic is null until it is captured again.
 NCU_TRAFFIC = {
     # (config, inputs): (bytes per launch, sha256 of csrc/ at capture, summary)
-    ("cfg2", "independent"): (606825216, "046257b6c87e40bb31c3c38a26412bb5cf13def629671b53615e9360011607de",
+    ("cfg2", "independent"): (607116544, "0529889e32ff431d11523a182e9a3816fced3965ddda50ef196019389a0612e4",
                               "profiles/multi_kernel_q8_0_qwen3_0.6b_stream.md"),
     # captured on 2 of the 28 layers (+ LM head) and scaled by algorithmic bytes
-    ("cfg3", "independent"): (4008261622, "046257b6c87e40bb31c3c38a26412bb5cf13def629671b53615e9360011607de",
+    ("cfg3", "independent"): (4006945782, "0529889e32ff431d11523a182e9a3816fced3965ddda50ef196019389a0612e4",
                               "profiles/multi_kernel_q4_0_7b_stream.md"),
 }
 
