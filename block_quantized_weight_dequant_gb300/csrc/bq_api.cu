@@ -1024,43 +1024,52 @@ namespace {
 long long tile_bytes(const bq::MultiOp &o, int k) {
     return (long long)std::min(o.rpw, o.M - k * o.rpw) * o.rb * o.nmat;
 }
-// Split the tiles of a multi-op plan into `grid` contiguous ranges of equal
-// estimated time: tile t costs its bytes times the measured time per byte of
-// the CTA that ran it in split `ct` (d[c] over the bytes of range c; a CTA
-// that ran nothing takes the mean).  Op boundaries, idle lanes and per-tile
-// work make the time per byte differ between op shapes and between ranges.
-void rebalance(const bq::MultiOp *mo, int n_ops, int grid, const int *ct, const double *d, int *out) {
+// Split n tiles (tile t has tb[t] bytes) into `grid` contiguous ranges of
+// equal estimated time: tile t costs its bytes times the measured time per
+// byte of the CTA that ran it in split `ct` (d[c] over the bytes of range c;
+// a CTA that ran nothing, or has no measurement, takes the mean).  Op
+// boundaries, idle lanes and per-tile work make the time per byte differ
+// between op shapes and between ranges.  out[0] = 0, out[grid] = n.
+void rebalance(const double *tb, long long n, int grid, const int *ct, const double *d, int *out) {
     std::vector<double> bytes((size_t)grid, 0.0), dens((size_t)grid, 0.0);
-    auto for_tiles = [&](auto f) {  // f(tile index, owner CTA in ct, tile bytes)
+    auto owner_walk = [&](auto f) {  // f(tile, owner CTA in ct)
         int c = 0;
-        long long t = 0;
-        for (int i = 0; i < n_ops; ++i)
-            for (int k = 0; k < mo[i].ntiles; ++k, ++t) {
-                while (c + 1 < grid && t >= ct[c + 1]) ++c;
-                f(t, c, (double)tile_bytes(mo[i], k));
-            }
+        for (long long t = 0; t < n; ++t) {
+            while (c + 1 < grid && t >= ct[c + 1]) ++c;
+            f(t, c);
+        }
     };
-    for_tiles([&](long long, int c, double b) { bytes[(size_t)c] += b; });
-    double tb = 0.0, td = 0.0;
+    owner_walk([&](long long t, int c) { bytes[(size_t)c] += tb[t]; });
+    double sb = 0.0, sd = 0.0;
     for (int c = 0; c < grid; ++c)
-        if (bytes[(size_t)c] > 0 && d[c] > 0) tb += bytes[(size_t)c], td += d[c];
-    const double mean = tb > 0 ? td / tb : 1.0;
+        if (bytes[(size_t)c] > 0 && d[c] > 0) sb += bytes[(size_t)c], sd += d[c];
+    const double mean = sb > 0 ? sd / sb : 1.0;
     for (int c = 0; c < grid; ++c)
         dens[(size_t)c] = bytes[(size_t)c] > 0 && d[c] > 0 ? d[c] / bytes[(size_t)c] : mean;
     double total = 0.0;
-    for_tiles([&](long long, int c, double b) { total += b * dens[(size_t)c]; });
+    owner_walk([&](long long t, int c) { total += tb[t] * dens[(size_t)c]; });
     out[0] = 0;
     int o = 1;
     double acc = 0.0;
-    long long tiles = 0;
-    for_tiles([&](long long t, int c, double b) {
-        acc += b * dens[(size_t)c];
-        while (o < grid && acc * grid >= total * o) out[o++] = (int)t + 1;
-        tiles = t + 1;
+    // (a relative slack of 1e-12 closes a range at an exact tie despite the
+    // rounding of the running sum)
+    owner_walk([&](long long t, int c) {
+        acc += tb[t] * dens[(size_t)c];
+        while (o < grid && acc * grid >= total * o * (1.0 - 1e-12)) out[o++] = (int)t + 1;
     });
-    while (o <= grid) out[o++] = (int)tiles;
+    while (o <= grid) out[o++] = (int)n;
 }
 }  // namespace
+
+// Host-logic hooks for the CPU test suite (not declared in include/bqgemv.h):
+// the planner's lane-order search and the time-balanced tile split.
+int bq_internal_lane_order(int G, int S0, int U, int pad, int rows_low, int *S, int *umask) {
+    return bq::lane_order(G, S0, U, pad != 0, S, umask, rows_low != 0) ? 1 : 0;
+}
+void bq_internal_rebalance(const double *tile_bytes, long long n, int grid, const int *ct,
+                           const double *cta_time, int *out) {
+    rebalance(tile_bytes, n, grid, ct, cta_time, out);
+}
 
 bq_status bq_stream_plan_tune(bq_stream_plan *plan, int rounds, void *stream) {
     if (!plan) return BQ_ERR_NULL;
@@ -1076,6 +1085,9 @@ bq_status bq_stream_plan_tune(bq_stream_plan *plan, int rounds, void *stream) {
     double best_max = -1.0;
     bq::MultiArgs a = plan->margs;
     a.cta_ns = plan->cta_ns;
+    std::vector<double> tb;
+    for (int i = 0; i < plan->n_ops; ++i)
+        for (int k = 0; k < plan->mo_host[i].ntiles; ++k) tb.push_back((double)tile_bytes(plan->mo_host[i], k));
     for (int r = 0; r <= rounds; ++r) {
         std::fill(d.begin(), d.end(), 0.0);
         for (int k = 0; k < REPS; ++k) {
@@ -1096,7 +1108,7 @@ bq_status bq_stream_plan_tune(bq_stream_plan *plan, int rounds, void *stream) {
             std::memcpy(best.data(), plan->ct_host, (size_t)(grid + 1) * sizeof(int));
         }
         if (r == rounds) break;
-        rebalance(plan->mo_host, plan->n_ops, grid, plan->ct_host, d.data(), next.data());
+        rebalance(tb.data(), (long long)tb.size(), grid, plan->ct_host, d.data(), next.data());
         std::memcpy(plan->ct_host, next.data(), (size_t)(grid + 1) * sizeof(int));
         if (cudaMemcpyAsync(plan->ct_dev, plan->ct_host, (size_t)(grid + 1) * sizeof(int),
                             cudaMemcpyHostToDevice, s) != cudaSuccess)
