@@ -55,10 +55,10 @@ FALLBACK_HBM_GBS = 6800.0
 # the traffic is null until it is captured again.
 NCU_TRAFFIC = {
     # (config, inputs): (bytes per launch, sha256 of csrc/ at capture, summary)
-    ("cfg2", "independent"): (607116544, "0529889e32ff431d11523a182e9a3816fced3965ddda50ef196019389a0612e4",
+    ("cfg2", "independent"): (607563008, "cebc6e0a91d5f37b4f894efc923f8ebec903e406ee0e36f76a5a928271687770",
                               "profiles/multi_kernel_q8_0_qwen3_0.6b_stream.md"),
     # captured on 2 of the 28 layers (+ LM head) and scaled by algorithmic bytes
-    ("cfg3", "independent"): (4006945782, "0529889e32ff431d11523a182e9a3816fced3965ddda50ef196019389a0612e4",
+    ("cfg3", "independent"): (4008177479, "cebc6e0a91d5f37b4f894efc923f8ebec903e406ee0e36f76a5a928271687770",
                               "profiles/multi_kernel_q4_0_7b_stream.md"),
 }
 
