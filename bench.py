@@ -234,7 +234,8 @@ def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None
     if mode == "plan":
         p = ds.plan()
         if tune and not chained:
-            p.tune()
+            # 10 rounds (33 launches at set-up): measured about 1% faster than 3
+            p.tune(rounds=10)
         w.add(ds.run_plan, f"stream_plan_{qt}", nbytes)
     else:
         for op in ds.ops:
@@ -254,8 +255,8 @@ def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None
     w.stream_obj = ds
     w.desc = token_desc(cfg, mode, chained, fused_qkv)
     if mode == "plan" and not chained:
-        w.desc["cta_split"] = ("equal measured time (bq_stream_plan_tune, set-up)" if tune
-                               else "equal bytes")
+        w.desc["cta_split"] = ("equal measured time (bq_stream_plan_tune, 10 rounds, set-up)"
+                               if tune else "equal bytes")
     assert (w.desc["ops_per_step"], w.desc["stages_per_step"], w.desc["weight_bytes_per_step"]) == \
         (len(ds.ops), ds.n_stages, ds.weight_bytes())
     return w
