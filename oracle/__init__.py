@@ -53,6 +53,9 @@ class Oracle:
         lib.bqo_gemv_bias.restype = i32
         lib.bqo_gemv_bias.argtypes = [i32, ctypes.c_void_p, i64, i64, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        lib.bqo_gemv_f16.restype = i32
+        lib.bqo_gemv_f16.argtypes = [ctypes.c_void_p, i64, i64, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_void_p]
         lib.bqo_rmsnorm.restype = i32
         lib.bqo_rmsnorm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, i64, ctypes.c_double,
                                     ctypes.c_void_p]
@@ -125,6 +128,20 @@ class Oracle:
                                   None if b is None else b.ctypes.data, y.ctypes.data,
                                   S.ctypes.data):
             raise ValueError("oracle gemv_bias: bad arguments")
+        return y, S
+
+    def gemv_f16(self, W_bits, x):
+        """Unquantized fp16 weights (uint16 bits [M, K]): returns (y, S), fp64
+        y = W x and S = sum_k |w_mk x_k|."""
+        W_bits = np.ascontiguousarray(W_bits, dtype=np.uint16)
+        M, K = W_bits.shape
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        assert x.shape == (K,)
+        y = np.empty(M, dtype=np.float64)
+        S = np.empty(M, dtype=np.float64)
+        if self.lib.bqo_gemv_f16(W_bits.ctypes.data, M, K, x.ctypes.data, y.ctypes.data,
+                                 S.ctypes.data):
+            raise ValueError("oracle gemv_f16: bad arguments")
         return y, S
 
     def rmsnorm(self, x, gamma, eps):

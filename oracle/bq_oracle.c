@@ -243,6 +243,27 @@ int bqo_gemv_bias(int qtype, const uint8_t *Wq, int64_t M, int64_t K, const doub
     return 0;
 }
 
+/* The unquantized fp16-weight GEMV ("We Wrote Our Own Inference Engine",
+ * "What actually moved it" #4: a GEMV for the unquantized fp16 matrices;
+ * RunIT README, kernel table, gemv_f16w_f32in_f32out: fp16 weights, fp32 in
+ * and out), read as the plain definition: W is fp16 [M, K] row-major (bits),
+ * y[m] = sum_k w[m,k] * x[k] in fp64, summed in index order; S[m] =
+ * sum_k |w[m,k] * x[k]| (S may be NULL). */
+int bqo_gemv_f16(const uint16_t *W, int64_t M, int64_t K, const double *x, double *y, double *S) {
+    if (M < 0 || K < 0) return -1;
+    for (int64_t m = 0; m < M; ++m) {
+        double acc = 0.0, sacc = 0.0;
+        for (int64_t k = 0; k < K; k++) {
+            double p = bqo_f16_bits_to_f64(W[m * K + k]) * x[k];
+            acc += p;
+            sacc += fabs(p); /* sum of |w x| */
+        }
+        y[m] = acc;
+        if (S) S[m] = sacc;
+    }
+    return 0;
+}
+
 /* xn[k] = x[k] * gamma[k] / sqrt(mean(x^2) + eps); gamma NULL means ones. */
 int bqo_rmsnorm(const double *x, const double *gamma, int64_t K, double eps, double *xn) {
     if (K <= 0) return -1;

@@ -408,8 +408,37 @@ def check_bias(o, rng=None):
         assert np.array_equal(S, Sg + np.abs(bias)), "S includes |bias|"
 
 
+def check_gemv_f16(o, rng=None):
+    """The unquantized fp16-weight GEMV, anchored outside the oracle: weights
+    k/8 (|k| <= 40, exact in fp16) against small-integer x compared with
+    Python's exact arithmetic row by row (y and S); one-hot x = e_k returns
+    column k as numpy's float16 decoder reads it (an independent decoder);
+    the identity returns x; x = 0 returns zeros."""
+    rng = rng or np.random.default_rng(51)
+    M, K = 9, 40
+    ints = rng.integers(-40, 41, size=(M, K))
+    W = (ints / 8.0).astype(np.float16)
+    x = rng.integers(-3, 4, size=K).astype(np.float64)
+    y, S = o.gemv_f16(W.view(np.uint16), x)
+    for m in range(M):
+        terms = [Fraction(int(ints[m, k]), 8) * int(x[k]) for k in range(K)]
+        assert Fraction(y[m]) == sum(terms), f"row {m}"
+        assert Fraction(S[m]) == sum(abs(t) for t in terms), f"S row {m}"
+    Wr = (rng.standard_normal((M, K)) * 0.02).astype(np.float16)
+    for k in (0, 17, K - 1):
+        e = np.zeros(K)
+        e[k] = 1.0
+        y, _ = o.gemv_f16(Wr.view(np.uint16), e)
+        assert np.array_equal(y, Wr[:, k].astype(np.float64)), f"column {k}"
+    xr = rng.standard_normal(K)
+    y, _ = o.gemv_f16(np.eye(K, dtype=np.float16).view(np.uint16), xr)
+    assert np.array_equal(y, xr), "identity"
+    y, S = o.gemv_f16(Wr.view(np.uint16), np.zeros(K))
+    assert not y.any() and not S.any(), "x = 0"
+
+
 QUICK_CHECKS = (check_golden, check_fp16_points, check_roundtrip, check_bruteforce,
-                check_all_codes, check_closed_forms, check_norm_silu, check_bias)
+                check_all_codes, check_closed_forms, check_norm_silu, check_bias, check_gemv_f16)
 
 
 def run_quick(o):

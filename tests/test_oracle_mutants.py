@@ -59,6 +59,10 @@ MUTANTS = [
     ("bias_subtracted", "y[m] += bias[m];", "y[m] -= bias[m];"),
     ("bias_shifted_row", "y[m] += bias[m];", "y[m] += bias[m > 0 ? m - 1 : 0];"),
     ("bias_S_signed", "S[m] += fabs(bias[m]);", "S[m] += bias[m];"),
+    ("f16_gemv_transposed", "bqo_f16_bits_to_f64(W[m * K + k])", "bqo_f16_bits_to_f64(W[k * M + m])"),
+    ("f16_gemv_reversed_x", "(W[m * K + k]) * x[k];", "(W[m * K + k]) * x[K - 1 - k];"),
+    ("f16_gemv_dropped_term", "for (int64_t k = 0; k < K; k++) {", "for (int64_t k = 1; k < K; k++) {"),
+    ("f16_gemv_S_signed", "sacc += fabs(p); /* sum of |w x| */", "sacc += p; /* sum of |w x| */"),
 ]
 
 

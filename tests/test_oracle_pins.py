@@ -45,6 +45,10 @@ def test_qkv_bias():
     checks.check_bias(o())
 
 
+def test_gemv_f16():
+    checks.check_gemv_f16(o())
+
+
 def test_packed_bytes_and_bad_args():
     ob = o()
     assert ob.packed_bytes(oracle.Q8_0, 3072, 1024) == 3072 * 32 * 34
