@@ -55,10 +55,10 @@ FALLBACK_HBM_GBS = 6800.0
 # the traffic is null until it is captured again.
 NCU_TRAFFIC = {
     # (config, inputs): (bytes per launch, sha256 of csrc/ at capture, summary)
-    ("cfg2", "independent"): (607563008, "cebc6e0a91d5f37b4f894efc923f8ebec903e406ee0e36f76a5a928271687770",
+    ("cfg2", "independent"): (606401280, "181342f0394ad88d6287134d732d6745538d55dbd1b2ce5aba8004078b8f718a",
                               "profiles/multi_kernel_q8_0_qwen3_0.6b_stream.md"),
     # captured on 2 of the 28 layers (+ LM head) and scaled by algorithmic bytes
-    ("cfg3", "independent"): (4008177479, "cebc6e0a91d5f37b4f894efc923f8ebec903e406ee0e36f76a5a928271687770",
+    ("cfg3", "independent"): (4004955016, "181342f0394ad88d6287134d732d6745538d55dbd1b2ce5aba8004078b8f718a",
                               "profiles/multi_kernel_q4_0_7b_stream.md"),
 }
 
@@ -278,6 +278,24 @@ def build_rotated_gemv(dev, qt, M, K, copies, seed=0, name="cfg1"):
     return w
 
 
+def build_f16_gemv(dev, seed=0):
+    """One fp16-weight GEMV per step over a 151936 x 1024 matrix (311 MB,
+    larger than L2, so every step reads it from HBM)."""
+    import torch
+    import block_quantized_weight_dequant_gb300 as bq
+    from block_quantized_weight_dequant_gb300 import workloads as wl
+    c = wl.F16_LM
+    M, K = c["M"], c["K"]
+    w = Workload()
+    W = (wl.normal_torch((M, K), 1.0, seed=seed, stream=wl.stream_id("f16", "W"), device=dev) *
+         wl.W_STD).to(torch.float16)
+    w.x_dev = wl.normal_torch(K, 1.0, seed=seed, stream=wl.stream_id("f16", "x"), device=dev)
+    w.y_dev = torch.empty(M, device=dev)
+    w.add(lambda: bq.gemv_f16(W, w.x_dev, w.y_dev), "gemv_f16", 2 * M * K + 4 * (M + K))
+    w.desc = {"workload": c["name"], "M": M, "K": K}
+    return w
+
+
 def build_rotated_gate_up(dev, cfg, seed=0):
     import torch
     import block_quantized_weight_dequant_gb300 as bq
@@ -354,6 +372,9 @@ def workload_desc(args):
     if args.config == "cfg4":
         c = wl.CFG4
         return {"workload": c["name"], "M": c["M"], "K": c["K"], "pairs": c["pairs"]}
+    if args.config == "f16":
+        c = wl.F16_LM
+        return {"workload": c["name"], "M": c["M"], "K": c["K"]}
     return {"workload": wl.CFG5["name"], "R": args.rows, "copies": CFG5_COPIES}
 
 
@@ -372,6 +393,9 @@ def step_bytes_static(args):
     if args.config == "cfg4":
         c = wl.CFG4
         return c["pairs"] * (2 * c["M"] * c["K"] // 32 * 34 + 8 * c["K"] + 4 * c["M"])
+    if args.config == "f16":
+        c = wl.F16_LM
+        return 2 * c["M"] * c["K"] + 4 * (c["M"] + c["K"])
     R = args.rows
     return CFG5_COPIES * sum(M * K // 32 * 18 + 4 * R * (M + K) for _, M, K in wl.CFG5["mats"])
 
@@ -398,6 +422,8 @@ def build_workload(args, dev):
         return build_rotated_gate_up(dev, wl.CFG4)
     if args.config == "cfg5":
         return build_verify(dev, wl.CFG5, args.rows, copies=CFG5_COPIES)
+    if args.config == "f16":
+        return build_f16_gemv(dev)
     raise SystemExit(f"unknown config {args.config}")
 
 
@@ -472,6 +498,19 @@ def oracle_sample(config, budget_s):
         c = wl.CFG4
         qt, mats = oracle.Q8_0, [("g", c["M"], c["K"]), ("u", c["M"], c["K"])]
         desc = "oracle GEMVs of one gate/up pair 3072x1024, repeated"
+    elif config == "f16":
+        M, K = 4096, wl.F16_LM["K"]
+        W = wl.normal_np((M, K), wl.W_STD, seed=0, stream=wl.stream_id("cpu", "f16")).astype(np.float16)
+        x = wl.normal_np(K, 1.0, seed=0, stream=wl.stream_id("cpux", "f16")).astype(np.float64)
+        done = 0
+        t0 = time.perf_counter()
+        while True:
+            o.gemv_f16(W.view(np.uint16), x)
+            done += 2 * M * K + 4 * (M + K)
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return done / dt / 1e9, dt, done, f"oracle fp16-weight GEMV over 4096 rows x {K}, repeated"
     else:
         c = wl.CFG5
         qt, mats = oracle.Q4_0, [(n, M, K) for n, M, K in c["mats"]]
@@ -590,7 +629,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=15)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="cfg2", choices=["cfg1", "cfg2", "cfg3", "cfg4", "cfg5"])
+    ap.add_argument("--config", default="cfg2", choices=["cfg1", "cfg2", "cfg3", "cfg4", "cfg5", "f16"])
     ap.add_argument("--rows", type=int, default=6, help="R for cfg5")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for cpu_baseline (0 disables)")

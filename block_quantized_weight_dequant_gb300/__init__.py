@@ -23,7 +23,7 @@ QTYPES = {"q8_0": Q8_0, "q4_0": Q4_0}
 
 __all__ = ["Q8_0", "Q4_0", "BLOCK_BYTES", "BQError", "packed_bytes", "quantize_pack",
            "gemv", "gemv_q8_0", "gemv_q4_0", "gemv_gate_up_silu", "gemv_verify",
-           "gemv_qkv_bias", "concat_packed",
+           "gemv_qkv_bias", "gemv_f16", "concat_packed",
            "device_status", "tree_lanes", "version", "StreamOp", "StreamPlan"]
 
 
@@ -169,6 +169,25 @@ def gemv_qkv_bias(qtype, Wqkv, x, bias=None, y=None):
     _need(y, torch.float32, "y")
     _lib.check(lib.bq_gemv_qkv_bias(qt, _ptr(Wqkv), _ptr(x), _ptr(bias), _ptr(y), M, K,
                                     _stream(Wqkv)), "gemv_qkv_bias")
+    return y
+
+
+def gemv_f16(W, x, y=None):
+    """y = W x for unquantized fp16 weights W [M, K] (K % 8 == 0), fp32 x and
+    y, on the fixed tree of bq_gemv_f16 (bit-reproducible)."""
+    _need(W, torch.float16, "W")
+    _need(x, torch.float32, "x")
+    if W.dim() != 2:
+        raise ValueError("W must be [M, K]")
+    M, K = W.shape
+    if x.numel() != K:
+        raise ValueError(f"x must have K={K} elements")
+    if y is None:
+        y = torch.empty(M, dtype=torch.float32, device=W.device)
+    _need(y, torch.float32, "y")
+    if y.numel() != M:
+        raise ValueError(f"y must have M={M} elements")
+    _lib.check(lib.bq_gemv_f16(_ptr(W), _ptr(x), _ptr(y), M, K, _stream(W)), "gemv_f16")
     return y
 
 

@@ -861,6 +861,14 @@ bq_status bq_gemv_qkv_bias(int qtype, const void *Wqkv, const float *x, const fl
     return gemv_common(qtype, Wqkv, x, y, 1, M, K, stream, bias);
 }
 
+bq_status bq_gemv_f16(const void *W, const float *x, float *y, int64_t M, int64_t K, void *stream) {
+    if (M < 0 || M > bq::M_MAX || K < 8 || K > bq::K_MAX || K % 8) return BQ_ERR_SHAPE;
+    if (M == 0) return BQ_OK;
+    if (!W || !x || !y) return BQ_ERR_NULL;
+    if (!aligned_ok(W, 16) || !aligned_ok(x, 16) || !aligned_ok(y, 4)) return BQ_ERR_ALIGN;
+    return from_cuda(bq_internal_f16_launch(W, x, y, M, K, stream));
+}
+
 bq_status bq_gemv_verify(int qtype, const void *Wq, const float *X, float *Y, int R, int64_t M,
                          int64_t K, void *stream) {
     return gemv_common(qtype, Wq, X, Y, R, M, K, stream);

@@ -42,6 +42,9 @@ int bq_internal_launch_q4_0(const bq::GemvCall &c, const bq::LaunchPlan &p);
 int bq_internal_status_q8_0(unsigned int *flags, int clear);
 int bq_internal_status_q4_0(unsigned int *flags, int clear);
 int bq_internal_pack(int qtype, const float *W, long long M, long long K, void *Wq, void *stream);
+// the fp16-weight GEMV (bq_f16.cu), arguments validated by the caller
+int bq_internal_f16_launch(const void *W, const float *x, float *y, long long M, long long K,
+                           void *stream);
 
 #include "../../include/bqgemv.h"
 

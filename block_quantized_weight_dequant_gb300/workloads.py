@@ -79,6 +79,11 @@ CFG5 = dict(name="q4_0 verify 17408x5120 + 5120x17408, R=1..6", qtype="q4_0",
             mats=[("a", 17408, 5120), ("b", 5120, 17408)], R=(1, 2, 3, 4, 5, 6))
 
 
+# 6. Unquantized fp16-weight GEMV: a Qwen3-0.6B-shaped LM head kept in fp16
+F16_LM = dict(name="fp16-weight gemv 151936x1024 (qwen3-0.6b-shaped lm head, unquantized)",
+              M=151936, K=1024)
+
+
 def token_stream_ops(cfg, fused_qkv=False):
     """Per-token op list in model order: ("gemv", name, M, K), ("gate_up",
     name, M, K) or, with fused_qkv, ("gemv_bias", name, M, K) for the q, k, v

@@ -135,6 +135,17 @@ bq_status bq_gemv_gate_up_silu(int qtype, const void *Wg, const void *Wu, const 
 bq_status bq_gemv_qkv_bias(int qtype, const void *Wqkv, const float *x, const float *bias, float *y,
                            int64_t M, int64_t K, void *stream);
 
+/* The unquantized fp16-weight GEMV: y[m] = sum_k w[m,k] * x[k] for W fp16
+ * [M, K] row-major (IEEE binary16, little-endian), fp32 x[K], fp32 y[M]; each
+ * product and sum in fp32 on a fixed tree that depends on K alone (runs are
+ * bit-reproducible), within 1e-5 * sum_k |w x| of the exact value.  ("We
+ * Wrote Our Own Inference Engine", "What actually moved it" #4: the GEMV for
+ * the unquantized fp16 matrices; RunIT README kernel table,
+ * gemv_f16w_f32in_f32out.)  Preconditions: 8 <= K <= 2^18 and K % 8 == 0,
+ * M >= 0 (M = 0 does nothing), W and x 16-byte aligned, y 4-byte aligned, y
+ * not overlapping W or x. */
+bq_status bq_gemv_f16(const void *W, const float *x, float *y, int64_t M, int64_t K, void *stream);
+
 /* Multi-row verify GEMV: Y[r, m] = sum_k w[m,k] * X[r, k] for r < R,
  * 1 <= R <= BQ_VERIFY_MAX_ROWS, with the weights streamed once for all R rows.
  * X: fp32 [R, K] row-major; Y: fp32 [R, M] row-major.  Row r of Y is

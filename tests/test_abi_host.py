@@ -173,3 +173,17 @@ def test_stream_plan_tune_validation(lib):
     checked on a real plan in the GPU tests."""
     assert lib.bq_stream_plan_tune(None, 3, None) == _lib.BQ_ERR_NULL
     assert lib.bq_stream_workspace_bytes(169, 113) >= 169 * 64 + (1024 + 1) * 4 + 1024 * 8
+
+
+def test_f16_gemv_validation(lib):
+    f = lib.bq_gemv_f16
+    assert f(None, FAKE, FAKE, 8, 256, None) == _lib.BQ_ERR_NULL
+    assert f(FAKE, None, FAKE, 8, 256, None) == _lib.BQ_ERR_NULL
+    assert f(FAKE, FAKE, None, 8, 256, None) == _lib.BQ_ERR_NULL
+    assert f(ctypes.c_void_p(0x10008), FAKE, FAKE, 8, 256, None) == _lib.BQ_ERR_ALIGN
+    assert f(FAKE, ctypes.c_void_p(0x10004), FAKE, 8, 256, None) == _lib.BQ_ERR_ALIGN
+    assert f(FAKE, FAKE, FAKE, 8, 260, None) == _lib.BQ_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, 8, 0, None) == _lib.BQ_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, 8, (1 << 18) + 8, None) == _lib.BQ_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, -1, 256, None) == _lib.BQ_ERR_SHAPE
+    assert f(None, None, None, 0, 256, None) == _lib.BQ_OK
