@@ -97,3 +97,29 @@ def test_roofline_entries():
     assert r["hbm"]["bound"] == "hbm"
     assert bench.step_bytes_static(argparse.Namespace(config="cfg2", layers=0, qkv="separate")) \
         == 604_714_496
+
+
+@pytest.mark.parametrize("config,rows,want", [
+    # one Q8_0 GEMV 3072x1024: 3,342,336 packed + 4 (M + K) = 3,358,720 B, 96 rotated copies
+    ("cfg1", 6, 96 * 3_358_720),
+    # Qwen3-0.6B-shaped Q8_0 token, gate and up fused (169 ops)
+    ("cfg2", 6, 604_714_496),
+    # 7B-shaped Q4_0 token, gate and up fused: 3,977,035,776 weight + activation bytes
+    ("cfg3", 6, 3_985_629_184),
+    # RMSNorm + gate/up + SiLU 3072x1024: 6,705,152 B per call, 28 rotated pairs
+    ("cfg4", 6, 28 * 6_705_152),
+    # Q4_0 verify 17408x5120 and its transpose: 50,135,040 packed + R * 4 (M + K) B per matrix, 7 copies
+    ("cfg5", 1, 7 * 2 * (50_135_040 + 1 * 90_112)),
+    ("cfg5", 6, 7 * 2 * (50_135_040 + 6 * 90_112)),
+    # fp16 LM head 151936x1024: 2 B per weight + 4 (M + K)
+    ("f16", 6, 2 * 151936 * 1024 + 4 * (151936 + 1024)),
+])
+def test_step_bytes_of_every_configuration(config, rows, want):
+    """The algorithmic bytes behind every GB/s figure and roofline fraction,
+    against per-unit figures derived from the shapes and block sizes."""
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+
+    a = argparse.Namespace(config=config, layers=0, qkv="separate", rows=rows)
+    assert bench.step_bytes_static(a) == want
