@@ -172,9 +172,11 @@ def gemv_qkv_bias(qtype, Wqkv, x, bias=None, y=None):
     return y
 
 
-def gemv_f16(W, x, y=None):
-    """y = W x for unquantized fp16 weights W [M, K] (K % 8 == 0), fp32 x and
-    y, on the fixed tree of bq_gemv_f16 (bit-reproducible)."""
+def gemv_f16(W, x, y=None, out_dtype=torch.float32):
+    """y = W x for unquantized fp16 weights W [M, K] (K % 8 == 0) and fp32 x,
+    on the fixed tree of bq_gemv_f16 (bit-reproducible).  y is fp32, or fp16
+    (out_dtype=torch.float16, or a given fp16 y: bq_gemv_f16_f16out, the fp32
+    result rounded to nearest even)."""
     _need(W, torch.float16, "W")
     _need(x, torch.float32, "x")
     if W.dim() != 2:
@@ -183,11 +185,14 @@ def gemv_f16(W, x, y=None):
     if x.numel() != K:
         raise ValueError(f"x must have K={K} elements")
     if y is None:
-        y = torch.empty(M, dtype=torch.float32, device=W.device)
-    _need(y, torch.float32, "y")
+        y = torch.empty(M, dtype=out_dtype, device=W.device)
+    if not isinstance(y, torch.Tensor) or y.dtype not in (torch.float32, torch.float16):
+        raise TypeError("y must be a torch.float32 or torch.float16 tensor")
+    _need(y, y.dtype, "y")
     if y.numel() != M:
         raise ValueError(f"y must have M={M} elements")
-    _lib.check(lib.bq_gemv_f16(_ptr(W), _ptr(x), _ptr(y), M, K, _stream(W)), "gemv_f16")
+    fn = lib.bq_gemv_f16 if y.dtype == torch.float32 else lib.bq_gemv_f16_f16out
+    _lib.check(fn(_ptr(W), _ptr(x), _ptr(y), M, K, _stream(W)), "gemv_f16")
     return y
 
 

@@ -19,8 +19,7 @@ BQ_OP_GEMV, BQ_OP_GATE_UP_SILU = 0, 1
 # every extern "C" symbol of include/bqgemv.h
 EXPORTS = ("bq_version", "bq_status_str", "bq_packed_bytes", "bq_quantize_pack", "bq_gemv_q8_0",
            "bq_gemv_q4_0", "bq_gemv_gate_up_silu", "bq_gemv_verify", "bq_gemv_qkv_bias",
-           "bq_gemv_f16",
-           "bq_device_status",
+           "bq_gemv_f16", "bq_gemv_f16_f16out", "bq_device_status",
            "bq_tree_lanes", "bq_stream_workspace_bytes", "bq_stream_plan_create",
            "bq_stream_plan_launch", "bq_stream_plan_tune", "bq_stream_plan_destroy",
            "bq_stream_run_noalloc")
@@ -54,6 +53,7 @@ def _declare(lib):
         "bq_gemv_verify": (i32, [i32, vp, vp, vp, i32, i64, i64, vp]),
         "bq_gemv_qkv_bias": (i32, [i32, vp, vp, vp, vp, i64, i64, vp]),
         "bq_gemv_f16": (i32, [vp, vp, vp, i64, i64, vp]),
+        "bq_gemv_f16_f16out": (i32, [vp, vp, vp, i64, i64, vp]),
         "bq_device_status": (i32, [ctypes.POINTER(ctypes.c_uint), i32]),
         "bq_tree_lanes": (i32, [i64]),
         "bq_stream_workspace_bytes": (i64, [i32, i32]),

@@ -146,6 +146,16 @@ bq_status bq_gemv_qkv_bias(int qtype, const void *Wqkv, const float *x, const fl
  * not overlapping W or x. */
 bq_status bq_gemv_f16(const void *W, const float *x, float *y, int64_t M, int64_t K, void *stream);
 
+/* bq_gemv_f16 with an fp16 output: y[m] is bq_gemv_f16's fp32 y[m] rounded
+ * to the nearest binary16 value, ties to even (beyond +-65504 it rounds to
+ * +-inf).  ("We Wrote Our Own Inference Engine", "What actually moved it" #5:
+ * fp16-output GEMVs.)  y: fp16 [M], 2-byte aligned; otherwise the arguments,
+ * preconditions and errors of bq_gemv_f16.  Both calls split K across the
+ * warps of a CTA when M is small; the summation tree, and so every bit of y,
+ * does not depend on that choice. */
+bq_status bq_gemv_f16_f16out(const void *W, const float *x, void *y, int64_t M, int64_t K,
+                             void *stream);
+
 /* Multi-row verify GEMV: Y[r, m] = sum_k w[m,k] * X[r, k] for r < R,
  * 1 <= R <= BQ_VERIFY_MAX_ROWS, with the weights streamed once for all R rows.
  * X: fp32 [R, K] row-major; Y: fp32 [R, M] row-major.  Row r of Y is

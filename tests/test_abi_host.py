@@ -187,3 +187,19 @@ def test_f16_gemv_validation(lib):
     assert f(FAKE, FAKE, FAKE, 8, (1 << 18) + 8, None) == _lib.BQ_ERR_SHAPE
     assert f(FAKE, FAKE, FAKE, -1, 256, None) == _lib.BQ_ERR_SHAPE
     assert f(None, None, None, 0, 256, None) == _lib.BQ_OK
+
+
+def test_f16_gemv_f16out_validation(lib):
+    f = lib.bq_gemv_f16_f16out
+    assert f(None, FAKE, FAKE, 8, 256, None) == _lib.BQ_ERR_NULL
+    assert f(FAKE, None, FAKE, 8, 256, None) == _lib.BQ_ERR_NULL
+    assert f(FAKE, FAKE, None, 8, 256, None) == _lib.BQ_ERR_NULL
+    assert f(ctypes.c_void_p(0x10008), FAKE, FAKE, 8, 256, None) == _lib.BQ_ERR_ALIGN
+    assert f(FAKE, ctypes.c_void_p(0x10004), FAKE, 8, 256, None) == _lib.BQ_ERR_ALIGN
+    assert f(FAKE, FAKE, ctypes.c_void_p(0x10001), 8, 256, None) == _lib.BQ_ERR_ALIGN
+    assert f(FAKE, FAKE, FAKE, 8, 260, None) == _lib.BQ_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, 8, 0, None) == _lib.BQ_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, 8, (1 << 18) + 8, None) == _lib.BQ_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, -1, 256, None) == _lib.BQ_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, 1 << 31, 256, None) == _lib.BQ_ERR_SHAPE
+    assert f(None, None, None, 0, 256, None) == _lib.BQ_OK
