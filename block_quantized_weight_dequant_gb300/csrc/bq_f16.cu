@@ -108,7 +108,12 @@ __device__ __forceinline__ void fold_store(float p, int lane, T *__restrict__ y,
     if (lane == 0) y[row] = to_out(p, y);
 }
 
-// T: float, or __half for the fp16 output
+// T: float, or __half for the fp16 output.  A warp's work is a sequence of
+// batches, each four segments of one row; the loads of the next batch (in
+// this row, or the first of the warp's next row) are issued before the
+// arithmetic of the current one, so a warp keeps loads in flight while it
+// adds, folds and stores.  The arithmetic is lane_group_sum's, in the same
+// order.
 template <typename T>
 __global__ void __launch_bounds__(F16_WARPS * 32)
     f16_gemv_kernel(const __half *__restrict__ W, const float *__restrict__ x, T *__restrict__ y,
@@ -117,14 +122,53 @@ __global__ void __launch_bounds__(F16_WARPS * 32)
     const int nseg = (K + F16_SEG - 1) / F16_SEG;
     // M <= 2^30 (the launcher's row chunks), so row + stride never overflows
     const int stride = gridDim.x * F16_WARPS;
-    for (int row = blockIdx.x * F16_WARPS + (threadIdx.x >> 5); row < M; row += stride) {
+    // the four segments s .. s + 3 of a row (lanes past K, and segments past
+    // the row, load nothing)
+    auto load = [&](uint4(&wv)[4], int row, int s) {
         const __half *wr = W + (size_t)row * K;
-        float p = -0.0f;
-        for (int g0 = 0; g0 < nseg; g0 += F16_GROUP) {
-            const float g = lane_group_sum(wr, x, g0, min(nseg, g0 + F16_GROUP), lane, K);
-            p = g0 == 0 ? g : __fadd_rn(p, g);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = (s + u) * F16_SEG + 8 * lane;
+            wv[u] = e < K ? __ldg(reinterpret_cast<const uint4 *>(wr + e)) : make_uint4(0, 0, 0, 0);
         }
-        fold_store(p, lane, y, row);
+    };
+    int row = blockIdx.x * F16_WARPS + (threadIdx.x >> 5), s = 0;
+    if (row >= M) return;
+    uint4 wv[4];
+    load(wv, row, 0);
+    float p = -0.0f;
+    float2 c0 = make_float2(-0.0f, -0.0f), c1 = c0, c2 = c0, c3 = c0;
+    for (;;) {
+        // the next batch: a group is 16 segments, so batches never straddle one
+        int nrow = row, ns = s + 4;
+        if (ns >= nseg) ns = 0, nrow = row + stride;
+        uint4 nx[4];
+        if (nrow < M) load(nx, nrow, ns);
+        if (s % F16_GROUP == 0) c0 = c1 = c2 = c3 = make_float2(-0.0f, -0.0f);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = (s + u) * F16_SEG + 8 * lane;
+            if (e >= K) continue;
+            const float4 xa = __ldg(reinterpret_cast<const float4 *>(x + e));
+            const float4 xb = __ldg(reinterpret_cast<const float4 *>(x + e + 4));
+            c0 = __ffma2_rn(half2_at(wv[u].x), make_float2(xa.x, xa.y), c0);
+            c1 = __ffma2_rn(half2_at(wv[u].y), make_float2(xa.z, xa.w), c1);
+            c2 = __ffma2_rn(half2_at(wv[u].z), make_float2(xb.x, xb.y), c2);
+            c3 = __ffma2_rn(half2_at(wv[u].w), make_float2(xb.z, xb.w), c3);
+        }
+        if ((s + 4) % F16_GROUP == 0 || s + 4 >= nseg) {
+            const float g = __fadd_rn(__fadd_rn(__fadd_rn(c0.x, c0.y), __fadd_rn(c1.x, c1.y)),
+                                      __fadd_rn(__fadd_rn(c2.x, c2.y), __fadd_rn(c3.x, c3.y)));
+            p = s < F16_GROUP ? g : __fadd_rn(p, g);
+        }
+        if (ns == 0) {
+            fold_store(p, lane, y, row);
+            p = -0.0f;
+        }
+        if (nrow >= M) break;
+        row = nrow, s = ns;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) wv[u] = nx[u];
     }
 }
 
