@@ -10,7 +10,6 @@ given build of the C source, which lets the tests run their pins against
 deliberately broken copies of the source (mutants) as well as the real one.
 """
 import ctypes
-import os
 
 import numpy as np
 
