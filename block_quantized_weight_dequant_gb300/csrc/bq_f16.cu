@@ -236,6 +236,8 @@ int bq_internal_f16_launch(const void *W, const float *x, float *y, long long M,
     return bq::f16_launch(W, x, y, M, K, stream);
 }
 
+// The fp16-output entry point (include/bqgemv.h).  Its checks are those of
+// bq_gemv_f16 in bq_api.cu, with y 2-byte aligned instead of 4.
 extern "C" bq_status bq_gemv_f16_f16out(const void *W, const float *x, void *y, int64_t M,
                                         int64_t K, void *stream) {
     if (M < 0 || M > bq::F16_M_MAX || K < 8 || K > bq::F16_K_MAX || K % 8) return BQ_ERR_SHAPE;
