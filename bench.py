@@ -462,6 +462,22 @@ def time_graph(graph, stream, steps, dist_barrier):
     return start_all.elapsed_time(end_all), per
 
 
+def hold_load(replay, sync, seconds, batch=16):
+    """Replay the step back to back, `batch` replays between host syncs, for
+    at least `seconds` of wall time; returns the number of replays.  Run just
+    before the timed region while nvidia-smi samples, so that the clock
+    samples see the GPU under this step's load, not idle."""
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        for _ in range(batch):
+            replay()
+        sync()
+        n += batch
+        if time.perf_counter() - t0 >= seconds:
+            return n
+
+
 def capture(w, stream, warmup):
     """Run the step once eagerly (module load, kernel attributes), capture it
     in a CUDA graph and replay it `warmup` times."""
@@ -684,9 +700,13 @@ def main():
 
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        held = hold_load(graph.replay, stream.synchronize, 1.0)
     total_ms, per = time_graph(graph, stream, args.steps, barrier)
     clk = clocks.stop()
+    if clk is not None:
+        clk["window"] = (f"100 ms samples over {held} untimed replays of the step (1 s) "
+                         "run just before the timed steps, and over the timed steps")
     other = None
     if getattr(w, "other", None) is not None:
         og = capture(w.other, stream, args.warmup)

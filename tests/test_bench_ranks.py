@@ -123,3 +123,17 @@ def test_step_bytes_of_every_configuration(config, rows, want):
 
     a = argparse.Namespace(config=config, layers=0, qkv="separate", rows=rows)
     assert bench.step_bytes_static(a) == want
+
+
+def test_hold_load_replays_in_synced_batches_for_the_given_time():
+    import time
+    sys.path.insert(0, ROOT)
+    import bench
+
+    calls = []
+    t0 = time.perf_counter()
+    n = bench.hold_load(lambda: calls.append("r"), lambda: calls.append("s"), 0.05, batch=4)
+    assert time.perf_counter() - t0 >= 0.05
+    assert n == calls.count("r") and n % 4 == 0 and n >= 4
+    assert calls.count("s") == n // 4
+    assert calls[:5] == ["r"] * 4 + ["s"] and calls[-1] == "s"
