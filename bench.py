@@ -167,6 +167,7 @@ class Workload:
         self.x_dev = None       # concatenated per-step inputs (device)
         self.y_dev = None       # concatenated per-step outputs (device)
         self.desc = {}
+        self.checks = []        # what the CPU leg compares with the oracle (sampled rows)
 
     def add(self, fn, kind, nbytes):
         self.launches.append(fn)
@@ -182,11 +183,17 @@ class Workload:
             fn()
 
 
+# The seeded generator call behind every packed matrix, by the packed tensor's
+# device address: the CPU leg draws the same fp32 rows again for the oracle.
+WEIGHT_SOURCES = {}
+
+
 def _packed(bq, wl, qt, M, K, seed, tag, dev):
-    import torch
-    W = wl.normal_torch((M, K), wl.W_STD, seed=seed, stream=wl.stream_id(*tag), device=dev)
+    src = dict(shape=(M, K), std=wl.W_STD, seed=seed, stream=wl.stream_id(*tag))
+    W = wl.normal_torch(src["shape"], src["std"], seed=seed, stream=src["stream"], device=dev)
     P = bq.quantize_pack(W, qt)
     del W
+    WEIGHT_SOURCES[P.data_ptr()] = src
     return P
 
 
@@ -264,8 +271,22 @@ def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None
     if mode == "plan" and not chained:
         w.desc["cta_split"] = ("equal measured time (bq_stream_plan_tune, 10 rounds, set-up)"
                                if tune else "equal bytes")
-    assert (w.desc["ops_per_step"], w.desc["stages_per_step"], w.desc["weight_bytes_per_step"]) == \
-        (len(ds.ops), ds.n_stages, ds.weight_bytes())
+    assert (w.desc["ops_per_step"], w.desc["weight_bytes_per_step"]) == \
+        (len(ds.ops), ds.weight_bytes())
+    assert w.desc["stages_per_step"] == (ds.n_stages if chained else 1)
+    if not chained:
+        # every op reads a seeded input: each can be checked against the oracle
+        # (a chained op reads another op's output, which the oracle may not use)
+        for i, op in enumerate(ds.ops):
+            tag = ("cfg-token", cfg["name"], i)
+            if op.W_up is not None:
+                w.checks.append(dict(kind="gate_up", qt=qt, Pg=op.W, Pu=op.W_up, x=op.x,
+                                     gamma=op.gamma, eps=op.eps, y=op.y, tag=tag,
+                                     src_g=WEIGHT_SOURCES.get(op.W.data_ptr()),
+                                     src_u=WEIGHT_SOURCES.get(op.W_up.data_ptr())))
+            else:
+                w.checks.append(dict(kind="gemv", qt=qt, P=op.W, x=op.x, y=op.y, bias=op.bias,
+                                     tag=tag, src=WEIGHT_SOURCES.get(op.W.data_ptr())))
     return w
 
 
@@ -281,6 +302,8 @@ def build_rotated_gemv(dev, qt, M, K, copies, seed=0, name="cfg1"):
         P = _packed(bq, wl, qt, M, K, seed, (name, c), dev)
         x, y = w.x_dev[c * K:(c + 1) * K], w.y_dev[c * M:(c + 1) * M]
         w.add(lambda P=P, x=x, y=y: bq.gemv(qt, P, x, y), f"gemv_{qt}", P.numel() + 4 * (M + K))
+        w.checks.append(dict(kind="gemv", qt=qt, P=P, x=x, y=y, bias=None, tag=(name, c),
+                             src=WEIGHT_SOURCES[P.data_ptr()]))
     w.desc = {"workload": f"{qt} gemv {M}x{K}, {copies} rotated copies", "M": M, "K": K}
     return w
 
@@ -294,11 +317,14 @@ def build_f16_gemv(dev, seed=0):
     c = wl.F16_LM
     M, K = c["M"], c["K"]
     w = Workload()
-    W = (wl.normal_torch((M, K), 1.0, seed=seed, stream=wl.stream_id("f16", "W"), device=dev) *
+    src = dict(shape=(M, K), std=1.0, seed=seed, stream=wl.stream_id("f16", "W"),
+               post_scale=wl.W_STD, dtype=torch.float16)
+    W = (wl.normal_torch((M, K), 1.0, seed=seed, stream=src["stream"], device=dev) *
          wl.W_STD).to(torch.float16)
     w.x_dev = wl.normal_torch(K, 1.0, seed=seed, stream=wl.stream_id("f16", "x"), device=dev)
     w.y_dev = torch.empty(M, device=dev)
     w.add(lambda: bq.gemv_f16(W, w.x_dev, w.y_dev), "gemv_f16", 2 * M * K + 4 * (M + K))
+    w.checks.append(dict(kind="f16", W=W, x=w.x_dev, y=w.y_dev, tag=("f16",), src=src))
     w.desc = {"workload": c["name"], "M": M, "K": K}
     return w
 
@@ -320,6 +346,9 @@ def build_rotated_gate_up(dev, cfg, seed=0):
         w.add(lambda Pg=Pg, Pu=Pu, x=x, g=g, y=y:
               bq.gemv_gate_up_silu(qt, Pg, Pu, x, g, cfg["eps"], y), f"gate_up_silu_{qt}",
               Pg.numel() + Pu.numel() + 8 * K + 4 * M)
+        w.checks.append(dict(kind="gate_up", qt=qt, Pg=Pg, Pu=Pu, x=x, gamma=g, eps=cfg["eps"],
+                             y=y, tag=("cfg4", c), src_g=WEIGHT_SOURCES[Pg.data_ptr()],
+                             src_u=WEIGHT_SOURCES[Pu.data_ptr()]))
     w.desc = {"workload": cfg["name"], "M": M, "K": K, "pairs": n}
     return w
 
@@ -344,8 +373,15 @@ def build_verify(dev, cfg, R, copies=7, seed=0):
             yo += R * M
             w.add(lambda P=P, X=X, Y=Y: bq.gemv_verify(qt, P, X, Y), f"verify_{qt}_R{R}",
                   P.numel() + 4 * R * (M + K))
+            w.checks.append(dict(kind="verify", qt=qt, P=P, X=X, Y=Y, tag=("cfg5", name, c, R),
+                                 src=WEIGHT_SOURCES[P.data_ptr()]))
     w.desc = {"workload": cfg["name"], "R": R, "copies": copies}
     return w
+
+
+def wl_cfg5():
+    from block_quantized_weight_dequant_gb300 import workloads as wl
+    return wl.CFG5
 
 
 def token_desc(cfg, mode, chained, fused_qkv=False):
@@ -355,7 +391,8 @@ def token_desc(cfg, mode, chained, fused_qkv=False):
     wbytes = sum(M * K // 32 * bb for _, M, K in wl.token_weight_shapes(cfg))
     d = {"workload": cfg["name"], "layers": cfg["layers"],
          "ops_per_step": len(wl.token_stream_ops(cfg, fused_qkv)),
-         "stages_per_step": 4 * cfg["layers"] + 1,
+         # dependent stages (grid-wide barriers): none when every op reads an input of its own
+         "stages_per_step": 4 * cfg["layers"] + 1 if chained else 1,
          "weight_bytes_per_step": wbytes, "weight_format": cfg["qtype"], "launch": mode,
          "inputs": "chained (each stage reads the previous stage's output)" if chained
          else "independent (each op reads an N(0,1) input of its own)"}
@@ -498,62 +535,168 @@ def capture(w, stream, warmup):
 
 
 # ---------------------------------------------------------------------------
-# the oracle on the host (cpu_baseline and --impl reference)
+# the CPU leg: the oracle on the host (cpu_baseline, --impl reference) and the
+# sampled-row parity of the timed step.  This is the only part of bench.py
+# that loads the oracle (test infrastructure under oracle/ and tests/).
 # ---------------------------------------------------------------------------
-def oracle_sample(config, budget_s):
-    """Time the oracle's GEMV on host cores over a bounded sample of the
-    workload: the first layer's matrices (cycled) of the token stream, or the
-    single matrix of the GEMV configs.  Returns (GB/s, seconds, bytes, desc)."""
-    import numpy as np
+def _oracle_modules():
+    tests = os.path.join(ROOT, "tests")
+    if tests not in sys.path:
+        sys.path.insert(0, tests)
     import oracle
+    return oracle
+
+
+def oracle_jobs(config, rows=6, layers=0):
+    """One step of the config as the oracle computes it: a list of GEMVs
+    (format, M, K, input rows), the matrices in the step's order (gate and up
+    of a fused op are two GEMVs; a verify call is R GEMVs of one matrix)."""
     from block_quantized_weight_dequant_gb300 import workloads as wl
-    o = oracle.get()
     if config in ("cfg2", "cfg3"):
-        cfg = wl.QWEN3_0_6B if config == "cfg2" else wl.Q7B
-        qt = oracle.Q8_0 if cfg["qtype"] == "q8_0" else oracle.Q4_0
-        mats = [(n, M, K) for n, M, K in cfg["mats"]]
-        desc = f"oracle GEMV over layer-0 matrices of {cfg['name']} ({len(mats)} matrices), cycled"
-    elif config == "cfg1":
+        cfg = dict(wl.QWEN3_0_6B if config == "cfg2" else wl.Q7B)
+        if layers:
+            cfg["layers"] = layers
+        return [(cfg["qtype"], M, K, 1) for _, M, K in wl.token_weight_shapes(cfg)]
+    if config == "cfg1":
         c = wl.CFG1
-        qt, mats = oracle.Q8_0, [("w", c["M"], c["K"])]
-        desc = "oracle GEMV over one 3072x1024 Q8_0 matrix, repeated"
-    elif config == "cfg4":
+        return [(c["qtype"], c["M"], c["K"], 1)] * CFG1_COPIES
+    if config == "cfg4":
         c = wl.CFG4
-        qt, mats = oracle.Q8_0, [("g", c["M"], c["K"]), ("u", c["M"], c["K"])]
-        desc = "oracle GEMVs of one gate/up pair 3072x1024, repeated"
-    elif config == "f16":
-        M, K = 4096, wl.F16_LM["K"]
-        W = wl.normal_np((M, K), wl.W_STD, seed=0, stream=wl.stream_id("cpu", "f16")).astype(np.float16)
-        x = wl.normal_np(K, 1.0, seed=0, stream=wl.stream_id("cpux", "f16")).astype(np.float64)
-        done = 0
-        t0 = time.perf_counter()
-        while True:
-            o.gemv_f16(W.view(np.uint16), x)
-            done += 2 * M * K + 4 * (M + K)
-            if time.perf_counter() - t0 >= budget_s:
-                break
-        dt = time.perf_counter() - t0
-        return done / dt / 1e9, dt, done, f"oracle fp16-weight GEMV over 4096 rows x {K}, repeated"
-    else:
-        c = wl.CFG5
-        qt, mats = oracle.Q4_0, [(n, M, K) for n, M, K in c["mats"]]
-        desc = "oracle GEMV over W_a 17408x5120 and W_b 5120x17408 (one row of X), repeated"
-    packed = []
-    for n, M, K in mats:
-        W = wl.normal_np((M, K), wl.W_STD, seed=0, stream=wl.stream_id("cpu", n))
-        packed.append((o.quantize_pack(qt, W), M, K,
-                       wl.normal_np(K, 1.0, seed=0, stream=wl.stream_id("cpux", n)).astype(np.float64),
-                       np.empty(M, dtype=np.float64)))
+        return [(c["qtype"], c["M"], c["K"], 1)] * (2 * c["pairs"])
+    if config == "f16":
+        return [("f16", wl.F16_LM["M"], wl.F16_LM["K"], 1)]
+    return [(wl.CFG5["qtype"], M, K, rows) for _, M, K in wl.CFG5["mats"]] * CFG5_COPIES
+
+
+def oracle_step_data(jobs, seed=0):
+    """Host inputs for the oracle jobs: packed bytes drawn at random (every
+    block scale a finite fp16 between 2^-9 and 2^-6; the scalar oracle's time
+    does not depend on the values) and N(0, 1) inputs.  Distinct arrays per
+    job, so the host caches hold no more of the step than a real one would."""
+    import numpy as np
+    rng = np.random.default_rng([seed, 0xB0])
+    data = []
+    for fmt, M, K, R in jobs:
+        if fmt == "f16":
+            W = (rng.standard_normal((M, K), dtype=np.float32) * np.float32(0.02)).astype(
+                np.float16).view(np.uint16)
+        else:
+            bb = 34 if fmt == "q8_0" else 18
+            W = np.frombuffer(rng.bytes(M * (K // 32) * bb), dtype=np.uint8).copy()
+            blk = W.reshape(-1, bb)
+            blk[:, 1] = rng.integers(0x18, 0x24, size=blk.shape[0], dtype=np.uint8)
+            W = W.reshape(M, (K // 32) * bb)
+        X = rng.standard_normal((R, K))
+        data.append((fmt, M, K, W, X))
+    return data
+
+
+def oracle_run(o, oracle, data, threads, budget_s, whole_steps):
+    """Run the oracle over the step's jobs in order, on `threads` host threads
+    (rows split among them), until `budget_s` has passed -- in whole steps
+    (at least one) when `whole_steps`, else stopping after any job.  Returns
+    (fraction of steps done, seconds)."""
+    import numpy as np
+    weights = sum(M * K * X.shape[0] for _, M, K, _, X in data)
     done = 0
     t0 = time.perf_counter()
     while True:
-        for P, M, K, x, y in packed:
-            o.gemv_y_only(qt, P, M, K, x, y)
-            done += P.size + 4 * (M + K)
+        for fmt, M, K, W, X in data:
+            for x in X:
+                if fmt == "f16":
+                    o.gemv_f16_parallel(W, x, threads=threads, with_S=False)
+                else:
+                    qt = oracle.Q8_0 if fmt == "q8_0" else oracle.Q4_0
+                    o.gemv_parallel(qt, W, M, K, x, threads=threads, with_S=False)
+                done += M * K
+            if not whole_steps and time.perf_counter() - t0 >= budget_s:
+                return done / weights, time.perf_counter() - t0
         if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return done / dt / 1e9, dt, done, desc
+            return done / weights, time.perf_counter() - t0
+
+
+def oracle_timing(args, budget_s, threads, whole_steps):
+    """The oracle (plain C, fp64, scalar) over the config's step on `threads`
+    host threads; GB/s counts the step's algorithmic bytes.  Returns (GB/s,
+    seconds, bytes, description)."""
+    oracle = _oracle_modules()
+    o = oracle.get()
+    jobs = oracle_jobs(args.config, getattr(args, "rows", 6), getattr(args, "layers", 0))
+    data = oracle_step_data(jobs)
+    frac, dt = oracle_run(o, oracle, data, threads, budget_s, whole_steps)
+    nbytes = frac * step_bytes_static(args)
+    desc = (f"the oracle over the whole step ({len(jobs)} GEMVs: "
+            f"{sum(W.nbytes for _, _, _, W, _ in data) / 1e6:.0f} MB of weights drawn at random "
+            f"with finite scales, N(0,1) inputs) on {threads} host thread(s), rows split among "
+            f"them; {frac:.3g} steps in {dt:.1f} s")
+    return nbytes / dt / 1e9, dt, nbytes, desc
+
+
+def cpu_baseline(args, budget_s):
+    """The oracle single-threaded (a bounded part of the step) and on every
+    host core (whole steps)."""
+    oracle = _oracle_modules()
+    n = oracle.host_cores()
+    g1, dt1, nb1, d1 = oracle_timing(args, budget_s, 1, whole_steps=False)
+    gn, dtn, nbn, dn = oracle_timing(args, budget_s, n, whole_steps=True)
+    out = {"value": round(gn, 4), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": dn,
+           "single_core": {"value": round(g1, 4), "cores": 1, "sample": d1}}
+    if tokens_per_step(args):
+        out["tok_per_s"] = round(gn * 1e9 / step_bytes_static(args), 4)
+        out["single_core"]["tok_per_s"] = round(g1 * 1e9 / step_bytes_static(args), 4)
+    return out
+
+
+def sampled_parity(w, rows_per_matrix):
+    """The timed step's outputs against the oracle on sampled rows of every
+    matrix (tests/sampled_parity.py): the oracle packs the seeded fp32 rows
+    itself (the GPU's packed rows must equal its bytes) and its fp64 product
+    bounds the GPU's output.  Verify rows are also compared bit for bit with
+    the single-row decode GEMV."""
+    import torch
+    _oracle_modules()
+    import sampled_parity as sp
+    import block_quantized_weight_dequant_gb300 as bq
+    res, skipped, decode_differ = [], 0, 0
+    per = rows_per_matrix if callable(rows_per_matrix) else (lambda i: rows_per_matrix)
+    for i, c in enumerate(w.checks):
+        rows_per_matrix = per(i)
+        src = c.get("src")
+        if c["kind"] == "gemv":
+            if src is None:
+                skipped += 1
+                continue
+            idx = sp.sample_rows(c["y"].numel(), rows_per_matrix, *c["tag"])
+            res.append(sp.check_gemv(c["qt"], sp.WeightSource(**src), c["P"], c["x"], c["y"], idx,
+                                     c["bias"]))
+        elif c["kind"] == "gate_up":
+            if c["src_g"] is None or c["src_u"] is None:
+                skipped += 1
+                continue
+            idx = sp.sample_rows(c["y"].numel(), rows_per_matrix, *c["tag"])
+            res.append(sp.check_gate_up(c["qt"], sp.WeightSource(**c["src_g"]),
+                                        sp.WeightSource(**c["src_u"]), c["Pg"], c["Pu"], c["x"],
+                                        c["gamma"], c["eps"], c["y"], idx))
+        elif c["kind"] == "verify":
+            X, Y = c["X"], c["Y"]
+            idx = sp.sample_rows(Y.shape[1], rows_per_matrix, *c["tag"])
+            ii = torch.as_tensor(idx, device=Y.device)
+            for r in range(X.shape[0]):
+                res.append(sp.check_gemv(c["qt"], sp.WeightSource(**src), c["P"], X[r], Y[r], idx))
+                yd = bq.gemv(c["qt"], c["P"], X[r].contiguous())
+                decode_differ += int((Y[r].index_select(0, ii).view(torch.int32) !=
+                                      yd.index_select(0, ii).view(torch.int32)).sum().item())
+        elif c["kind"] == "f16":
+            idx = sp.sample_rows(c["y"].numel(), rows_per_matrix, *c["tag"])
+            res.append(sp.check_f16(sp.WeightSource(**src), c["W"], c["x"], c["y"], idx))
+    out = sp.merge(res)
+    out["skipped_matrices"] = skipped
+    if any(c["kind"] == "verify" for c in w.checks):
+        out["verify_rows_differ_from_decode"] = decode_differ
+        out["pass"] = out["pass"] and decode_differ == 0
+    out["sample"] = (f"{per(0)} rows per matrix and input row (the first, the last and "
+                     "seeded rows; every row of smaller matrices)")
+    return out
 
 
 def token_bytes_cfg(cfg, fused_qkv=False):
@@ -617,30 +760,39 @@ def whole_job_gbs(step_bytes, steps, ms, world):
 
 # ---------------------------------------------------------------------------
 def run_reference(args):
+    """The reference arm: the oracle (the pages publish no runnable code; the
+    oracle is this repository's plain CPU statement of the same products) on
+    every host core, one whole step per timed step."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    oracle = _oracle_modules()
+    o = oracle.get()
+    n = oracle.host_cores()
+    jobs = oracle_jobs(args.config, args.rows, args.layers)
+    data = oracle_step_data(jobs)
     for _ in range(args.warmup):
-        oracle_sample(args.config, 0.0)
-    vals = []
-    t_total = 0.0
+        oracle_run(o, oracle, data, n, 0.0, True)
+    per = []
     for _ in range(args.steps):
-        gbs, dt, nb, desc = oracle_sample(args.config, 0.0)
-        vals.append(gbs)
-        t_total += dt
-    value = statistics.median(vals)
+        frac, dt = oracle_run(o, oracle, data, n, 0.0, True)
+        per.append(dt / frac)
+    t_total = sum(per)
+    value = step_bytes_static(args) * args.steps / t_total / 1e9
+    desc = (f"the oracle over one whole step per timed step ({len(jobs)} GEMVs, weights drawn at "
+            f"random with finite scales, N(0,1) inputs) on {n} host threads, rows split among them")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * t_total / max(1, args.steps), 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic: seeded N(0,0.02) weights packed by the oracle, N(0,1) inputs",
+            "data": "synthetic: random packed weights with finite scales, N(0,1) inputs",
             "config": dict(workload_desc(args), config=args.config, bytes_per_step=step_bytes_static(args),
                            parallelism="replicas1"),
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
-                             "kind": "oracle", "sample": desc + ", one pass per step"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n,
+                             "kind": "oracle", "sample": desc},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
-    if args.config in ("cfg2", "cfg3"):
+    if tokens_per_step(args):
         line["tok_per_s"] = round(value * 1e9 / step_bytes_static(args), 4)
     print(json.dumps(line), flush=True)
     return 0
@@ -655,7 +807,9 @@ def main():
     ap.add_argument("--config", default="cfg2", choices=["cfg1", "cfg2", "cfg3", "cfg4", "cfg5", "f16"])
     ap.add_argument("--rows", type=int, default=6, help="R for cfg5")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
-                    help="seconds of oracle work for cpu_baseline (0 disables)")
+                    help="seconds of oracle work per cpu_baseline leg (0 disables)")
+    ap.add_argument("--parity-rows", type=int, default=16,
+                    help="rows per matrix of the timed step checked against the oracle (0: none)")
     ap.add_argument("--launch", choices=["plan", "per_op"], default="plan",
                     help="cfg2/cfg3: one cooperative launch per token, or one launch per op")
     ap.add_argument("--inputs", choices=["chained", "independent"], default="independent",
@@ -724,26 +878,32 @@ def main():
     assert step_bytes == step_bytes_static(args)
     value = whole_job_gbs(step_bytes, args.steps, total_ms, world)
 
-    # e2e: the same step through the public API with host buffers: H2D of the
-    # step's inputs from pinned memory, the graph, D2H of the step's outputs
+    # e2e: the same step with host buffers: H2D of the step's inputs from
+    # pinned memory, the step, D2H of the step's outputs, every step.  `e2e`
+    # makes the step's calls through the public API (Python binding -> C ABI)
+    # each step, as a user would; `e2e_graph` replays the captured graph.
     x_host = torch.empty(w.x_dev.shape, dtype=w.x_dev.dtype, pin_memory=True)
     x_host.copy_(w.x_dev.cpu())
     y_host = torch.empty(w.y_dev.shape, dtype=w.y_dev.dtype, pin_memory=True)
-    barrier()
-    torch.cuda.synchronize()
-    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e_s.record(stream)
-        for _ in range(args.steps):
-            w.x_dev.copy_(x_host, non_blocking=True)
-            graph.replay()
-            y_host.copy_(w.y_dev, non_blocking=True)
-        e_e.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    e2e_ms = e_s.elapsed_time(e_e)
-    e2e_ms = max_over_ranks(e2e_ms, dev, world)
-    e2e_value = whole_job_gbs(step_bytes, args.steps, e2e_ms, world)
+
+    def e2e_leg(step):
+        barrier()
+        torch.cuda.synchronize()
+        e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e_s.record(stream)
+            for _ in range(args.steps):
+                w.x_dev.copy_(x_host, non_blocking=True)
+                step()
+                y_host.copy_(w.y_dev, non_blocking=True)
+            e_e.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms = max_over_ranks(e_s.elapsed_time(e_e), dev, world)
+        return whole_job_gbs(step_bytes, args.steps, ms, world)
+
+    e2e_value = e2e_leg(w.run)
+    e2e_graph_value = e2e_leg(graph.replay)
 
     # every step is one kernel family (the stream executor for cfg2/cfg3, one
     # GEMV family for the rotated configs), so the dominant kernel's launch
@@ -777,7 +937,10 @@ def main():
         "roofline": roofline(args, dom, n_launch, achieved, peak, peak_kind, traffic, traffic_src,
                              total_ms),
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": y_host.numel() * 4},
+                "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": y_host.numel() * 4,
+                "calls": f"{len(w.launches)} public-API call(s) per step, no graph"},
+        "e2e_graph": {"value": round(e2e_graph_value, 2), "unit": "GB/s",
+                      "calls": "the step's calls captured once in a CUDA graph, replayed"},
         "clocks": clk,
         "gpu_launches": len(w.launches) * args.steps,
     }
@@ -788,12 +951,10 @@ def main():
         ds = w.stream_obj
         n_gemv = sum(2 if op.W_up is not None else 1 for op in ds.ops)
         line["gemvs_per_s"] = round(n_gemv * args.steps / (total_ms * 1e-3), 1)
-    if args.cpu_budget > 0 and world >= 1:
-        gbs, dt, nb, desc = oracle_sample(args.config, args.cpu_budget)
-        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1,
-                                "kind": "oracle", "sample": f"{desc}; {nb/1e6:.0f} MB in {dt:.1f} s"}
-        if tokens_per_step(args):
-            line["cpu_baseline"]["tok_per_s"] = round(gbs * 1e9 / step_bytes, 4)
+    if args.parity_rows > 0:
+        line["parity"] = sampled_parity(w, args.parity_rows)
+    if args.cpu_budget > 0:
+        line["cpu_baseline"] = cpu_baseline(args, args.cpu_budget)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -780,12 +780,18 @@ bq_status run_gemv(const GemvCall &c) {
     if (c.K % 256 == 0) {
         bq::MultiArgs a;
         bq::MultiGeometry g;
-        if (!bq::plan_multi_single(c, &a, &g)) return BQ_ERR_CUDA;
-        const int pdl = bq::tunables().single_pdl;
-        const int e = c.qtype == BQ_Q8_0
-                          ? bq_internal_multi_launch_q8_0(a, g.grid, g.threads, g.smem, c.stream, pdl)
-                          : bq_internal_multi_launch_q4_0(a, g.grid, g.threads, g.smem, c.stream, pdl);
-        return from_cuda(e);
+        if (bq::plan_multi_single(c, &a, &g)) {
+            const int pdl = bq::tunables().single_pdl;
+            const int e = c.qtype == BQ_Q8_0
+                              ? bq_internal_multi_launch_q8_0(a, g.grid, g.threads, g.smem, c.stream, pdl)
+                              : bq_internal_multi_launch_q4_0(a, g.grid, g.threads, g.smem, c.stream, pdl);
+            return from_cuda(e);
+        }
+        // The streaming kernel stages the whole input in shared memory for a
+        // single row and for gate+up (only verify cuts it into K-panels), so
+        // an input beyond the staging limit (K > 32768 fp32) cannot be
+        // planned there: the generic kernel, which reads x through L1 with the
+        // same arithmetic tree, takes the call.
     }
     LaunchPlan p;
     bq::plan_gemv(c, &p);

@@ -44,7 +44,8 @@ __global__ void __launch_bounds__(GENERIC_WARPS * 32) generic_kernel(const Gener
     constexpr int UB = Fmt<QT>::unit_bytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = a.G, rpw = 32 / G;
-    const int row = (blockIdx.x * GENERIC_WARPS + warp) * rpw + lane / G;
+    // 64-bit: M may be up to 2^31 - 1 rows
+    const long long row = ((long long)blockIdx.x * GENERIC_WARPS + warp) * rpw + lane / G;
     const int l = lane & (G - 1);
     const int nb = a.K / 32, nsc = (nb + 7) / 8;
 
@@ -89,7 +90,8 @@ __global__ void __launch_bounds__(GENERIC_WARPS * 32) generic_kernel(const Gener
             } else {
 #pragma unroll
                 for (int r = 0; r < R; ++r)
-                    a.y[(size_t)r * a.M + row] = R == 1 && a.bias ? __fadd_rn(p[r], a.bias[row]) : p[r];
+                    a.y[(size_t)r * a.M + (size_t)row] =
+                        R == 1 && a.bias ? __fadd_rn(p[r], a.bias[row]) : p[r];
             }
         }
     };

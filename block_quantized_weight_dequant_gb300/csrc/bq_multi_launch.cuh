@@ -7,15 +7,13 @@
 #include <cuda_runtime.h>
 
 #include "bq_multi.cuh"
+#include "bq_occupancy.cuh"
 
 namespace bq {
 
 template <int QT, int NR, int R>
 int multi_occupancy_t(int threads, size_t smem, int *occ) {
-    auto kern = multi_kernel<QT, NR, R>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return (int)e;
-    return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kern, threads, smem);
+    return occupancy_cached<multi_kernel<QT, NR, R>>(threads, smem, occ);
 }
 
 // pdl: allow programmatic dependent launch (the kernel waits for its

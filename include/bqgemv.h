@@ -281,14 +281,18 @@ bq_status bq_stream_plan_destroy(bq_stream_plan *plan);
  *  - At most BQ_NOALLOC_MAX_OPS ops (and as many stages); more returns
  *    BQ_ERR_SHAPE without touching the device.
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make
- *    that first call before any stream capture.
- *  - Each call copies the tables from host memory into the array on `stream`
- *    and clears the counters there, then launches.  All calls share the one
- *    array, which keeps the last call's contents: calls that overlap on the
- *    GPU (on different streams, or from different host threads without
- *    ordering) race on it and must be serialised by the caller.  Host-side
- *    staging is serialised internally. */
+ *    (cudaGetSymbolAddress), creates one CUDA event for that device (an
+ *    event holds no device memory) and sets the kernel's shared-memory
+ *    limit; make that first call before any stream capture.
+ *  - Each call copies the tables from static host memory into the array on
+ *    `stream` and clears the counters there, then launches.  All calls share
+ *    the one array, which keeps the last call's contents: calls that overlap
+ *    on the GPU (on different streams, or from different host threads
+ *    without ordering) race on it and must be serialised by the caller.
+ *    Host-side staging is serialised internally: a call first waits on the
+ *    host until the previous call's table copies have run (they read the
+ *    static host tables asynchronously), so back-to-back calls on one stream
+ *    are safe but a call may block until the GPU reaches the previous one. */
 #define BQ_NOALLOC_MAX_OPS 512
 bq_status bq_stream_run_noalloc(int qtype, const bq_op *ops, int n_ops, void *stream);
 

@@ -10,10 +10,26 @@ given build of the C source, which lets the tests run their pins against
 deliberately broken copies of the source (mutants) as well as the real one.
 """
 import ctypes
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
 from . import build as _build
+
+
+def host_cores():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _row_ranges(M, parts):
+    """[r0, r1) row ranges splitting M rows into at most `parts` near-equal pieces."""
+    parts = max(1, min(parts, M))
+    return [(M * i // parts, M * (i + 1) // parts) for i in range(parts)]
 
 Q4_0 = 2
 Q8_0 = 8
@@ -108,6 +124,67 @@ class Oracle:
                              S.ctypes.data):
             raise ValueError("oracle gemv: bad arguments")
         return y, S
+
+    def gemv_parallel(self, qtype, Wq, M, K, x, threads=None, with_S=True):
+        """gemv() with the rows split among `threads` host threads (default:
+        every host core).  Each thread runs the same scalar C routine on its own
+        rows (the call releases the GIL), so every row's value is exactly the
+        single-threaded one."""
+        Wq = np.ascontiguousarray(Wq, dtype=np.uint8).reshape(M, -1)
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        assert x.shape == (K,)
+        y = np.empty(M, dtype=np.float64)
+        S = np.empty(M, dtype=np.float64) if with_S else None
+        rb = Wq.shape[1] if M else 0
+
+        def run(r):
+            r0, r1 = r
+            return self.lib.bqo_gemv(qtype, Wq.ctypes.data + r0 * rb, r1 - r0, K, x.ctypes.data,
+                                     y.ctypes.data + 8 * r0,
+                                     S.ctypes.data + 8 * r0 if with_S else None)
+
+        with ThreadPoolExecutor(threads or host_cores()) as ex:
+            if any(ex.map(run, _row_ranges(M, 4 * (threads or host_cores())))):
+                raise ValueError("oracle gemv: bad arguments")
+        return y, S
+
+    def gemv_f16_parallel(self, W_bits, x, threads=None, with_S=True):
+        """gemv_f16() with the rows split among host threads (same values)."""
+        W_bits = np.ascontiguousarray(W_bits, dtype=np.uint16)
+        M, K = W_bits.shape
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        assert x.shape == (K,)
+        y = np.empty(M, dtype=np.float64)
+        S = np.empty(M, dtype=np.float64) if with_S else None
+
+        def run(r):
+            r0, r1 = r
+            return self.lib.bqo_gemv_f16(W_bits.ctypes.data + 2 * r0 * K, r1 - r0, K,
+                                         x.ctypes.data, y.ctypes.data + 8 * r0,
+                                         S.ctypes.data + 8 * r0 if with_S else None)
+
+        with ThreadPoolExecutor(threads or host_cores()) as ex:
+            if any(ex.map(run, _row_ranges(M, 4 * (threads or host_cores())))):
+                raise ValueError("oracle gemv_f16: bad arguments")
+        return y, S
+
+    def quantize_pack_parallel(self, qtype, W, threads=None):
+        """quantize_pack() with the rows split among host threads; every block
+        is packed by the same scalar routine, so the bytes are identical."""
+        W = np.ascontiguousarray(W, dtype=np.float32)
+        M, K = W.shape
+        out = np.empty((M, (K // 32) * BLOCK_BYTES[qtype]), dtype=np.uint8)
+        rb = out.shape[1]
+
+        def run(r):
+            r0, r1 = r
+            return self.lib.bqo_quantize_pack(qtype, W.ctypes.data + 4 * r0 * K, r1 - r0, K,
+                                              out.ctypes.data + r0 * rb)
+
+        with ThreadPoolExecutor(threads or host_cores()) as ex:
+            if any(ex.map(run, _row_ranges(M, 4 * (threads or host_cores())))):
+                raise ValueError(f"oracle quantize_pack rejected qtype={qtype} shape={W.shape}")
+        return out
 
     def gemv_y_only(self, qtype, Wq, M, K, x, y):
         """The same product without S, into a caller-owned fp64 ``y``."""

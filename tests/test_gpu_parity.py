@@ -262,5 +262,64 @@ def test_verify_rows_memcmp_equal_to_decode(qt, M, K, R):
         assert_gemv_close(Y[r], y_ref, S, f"verify {qt} {M}x{K} R={R} row {r}")
 
 
+# ---------------------------------------------------------------------------
+# K beyond what the streaming kernel stages in shared memory for one input row
+# (32768 fp32): the documented range goes to K = 2^18 for every quantized call
+# ---------------------------------------------------------------------------
+LONG_K = [33024, 65536, 1 << 18]
+
+
+@pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("K", LONG_K)
+def test_long_k_gemv_and_qkv_bias(qt, K):
+    M = 37
+    P = gpu_pack(qt, weights(M, K, seed=31))
+    x = xvec(K, seed=31)
+    y = torch.full((M,), float("nan"), device=DEV)
+    bq.gemv(qt, P, cuda(x), y)
+    Pn = P.cpu().numpy()
+    y_ref, S = ora().gemv(QT[qt], Pn, M, K, x.astype(np.float64))
+    assert_gemv_close(y.cpu().numpy(), y_ref, S, f"{qt} gemv {M}x{K}")
+    bias = wl.normal_np(M, 0.5, seed=31, stream=wl.stream_id("long-k bias", K))
+    yb = bq.gemv_qkv_bias(qt, P, cuda(x), cuda(bias))
+    assert torch.equal(yb.view(torch.int32), (y + cuda(bias)).view(torch.int32))
+    y_ref, S = ora().gemv_bias(QT[qt], Pn, M, K, x.astype(np.float64), bias.astype(np.float64))
+    assert_gemv_close(yb.cpu().numpy(), y_ref, S, f"{qt} qkv_bias {M}x{K}")
+
+
+@pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("K", LONG_K)
+def test_long_k_gate_up_silu(qt, K):
+    M = 21
+    Pg = gpu_pack(qt, weights(M, K, seed=32, spread=False))
+    Pu = gpu_pack(qt, weights(M, K, seed=33, spread=False))
+    x = xvec(K, seed=32)
+    gamma = wl.normal_np(K, 0.1, seed=32, stream=wl.stream_id("gamma", K), mean=1.0)
+    o = ora()
+    for g in (gamma, None):
+        y = bq.gemv_gate_up_silu(qt, Pg, Pu, cuda(x), None if g is None else cuda(g),
+                                 1e-6).cpu().numpy()
+        xn = o.rmsnorm(x, g, 1e-6) if g is not None else x.astype(np.float64)
+        r = o.gate_up_silu(QT[qt], Pg.cpu().numpy(), Pu.cpu().numpy(), M, K, xn)
+        assert_gate_up_close(y, r, f"{qt} gate_up {M}x{K} gamma={g is not None}")
+
+
+@pytest.mark.parametrize("qt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("K", [65536, 1 << 18])
+def test_long_k_verify_memcmp_equal_to_decode(qt, K):
+    M = 19
+    P = gpu_pack(qt, weights(M, K, seed=34))
+    X = xvec(K, seed=34, R=6)
+    Pn = P.cpu().numpy()
+    for R in range(1, 7):
+        Y = bq.gemv_verify(qt, P, cuda(X[:R])).cpu().numpy()
+        for r in range(R):
+            y1 = bq.gemv(qt, P, cuda(X[r])).cpu().numpy()
+            assert Y[r].tobytes() == y1.tobytes(), f"R={R} row {r} differs from decode"
+    for r in range(6):
+        y_ref, S = ora().gemv(QT[qt], Pn, M, K, X[r].astype(np.float64))
+        assert_gemv_close(Y[r], y_ref, S, f"verify {qt} {M}x{K} row {r}")
+
+
 def test_no_device_errors_recorded():
     assert bq.device_status(clear=True) == 0

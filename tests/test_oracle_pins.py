@@ -55,3 +55,27 @@ def test_packed_bytes_and_bad_args():
     assert ob.packed_bytes(oracle.Q4_0, 3584, 18944) == 3584 * 592 * 18
     assert ob.packed_bytes(oracle.Q8_0, 1, 33) == -1
     assert ob.packed_bytes(5, 1, 32) == -1
+
+
+def test_parallel_drivers_give_the_single_threaded_values():
+    """The threaded drivers split rows among host threads and call the same
+    scalar routines, so every value equals the single-threaded oracle's."""
+    import numpy as np
+
+    ob = o()
+    rng = np.random.default_rng(5)
+    for qt in (oracle.Q8_0, oracle.Q4_0):
+        for M, K in ((1, 32), (7, 288), (333, 1024)):
+            W = (rng.standard_normal((M, K)) * 0.02).astype(np.float32)
+            P = ob.quantize_pack(qt, W)
+            for threads in (1, 3, 8):
+                assert np.array_equal(ob.quantize_pack_parallel(qt, W, threads), P)
+                x = rng.standard_normal(K)
+                y, S = ob.gemv(qt, P, M, K, x)
+                yp, Sp = ob.gemv_parallel(qt, P, M, K, x, threads)
+                assert np.array_equal(y, yp) and np.array_equal(S, Sp)
+    Wh = (rng.standard_normal((97, 136)) * 0.02).astype(np.float16).view(np.uint16)
+    x = rng.standard_normal(136)
+    y, S = ob.gemv_f16(Wh, x)
+    yp, Sp = ob.gemv_f16_parallel(Wh, x, 5)
+    assert np.array_equal(y, yp) and np.array_equal(S, Sp)

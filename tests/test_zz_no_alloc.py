@@ -98,3 +98,31 @@ def test_noalloc_rejects_too_many_ops():
         big[i] = arr[0]
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     assert _lib.get().bq_stream_run_noalloc(bq.Q8_0, big, len(big), stream) == _lib.BQ_ERR_SHAPE
+
+
+@pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
+def test_noalloc_back_to_back_different_op_lists(qt):
+    """Two calls with DIFFERENT op lists queued on one stream with no host
+    synchronisation between them: each call's tables are staged in the same
+    static host arrays, so the second call must not refill them before the
+    first call's copies have read them.  Both outputs must equal the workspace
+    plan's bit for bit."""
+    a = chained_stream(qt, seed=21, chained=True)
+    b = chained_stream(qt, seed=22, chained=False)
+    want = []
+    for ds in (a, b):
+        ds.run_plan()
+        torch.cuda.synchronize()
+        want.append([op.y.clone() for op in ds.ops])
+        for op in ds.ops:
+            op.y.fill_(float("nan"))
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    arr_a, arr_b = op_array(a), op_array(b)
+    for _ in range(2):
+        assert _lib.get().bq_stream_run_noalloc(bq.QTYPES[qt], arr_a, len(a.ops), stream) == _lib.BQ_OK
+        assert _lib.get().bq_stream_run_noalloc(bq.QTYPES[qt], arr_b, len(b.ops), stream) == _lib.BQ_OK
+    torch.cuda.synchronize()
+    for name, ds, wnt in (("a", a, want[0]), ("b", b, want[1])):
+        for i, (op, w) in enumerate(zip(ds.ops, wnt)):
+            assert torch.equal(op.y.view(torch.int32), w.view(torch.int32)), f"list {name} op {i}"
+    assert bq.device_status(clear=True) == 0
