@@ -33,7 +33,9 @@ def _row_ranges(M, parts):
 
 Q4_0 = 2
 Q8_0 = 8
-BLOCK_BYTES = {Q8_0: 34, Q4_0: 18}
+Q4_K = 12
+# bytes per 32 weights (a Q4_K super-block is 144 bytes per 256 weights)
+BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q4_K: 18}
 
 _dp = ctypes.POINTER(ctypes.c_double)
 _u8p = ctypes.POINTER(ctypes.c_uint8)
@@ -65,6 +67,9 @@ class Oracle:
         lib.bqo_gemv.restype = i32
         lib.bqo_gemv.argtypes = [i32, ctypes.c_void_p, i64, i64, ctypes.c_void_p,
                                  ctypes.c_void_p, ctypes.c_void_p]
+        lib.bqo_q4_k_split_scale.restype = i32
+        lib.bqo_q4_k_split_scale.argtypes = [ctypes.c_void_p, i64, i64, ctypes.c_void_p,
+                                             ctypes.c_void_p]
         lib.bqo_gemv_bias.restype = i32
         lib.bqo_gemv_bias.argtypes = [i32, ctypes.c_void_p, i64, i64, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
@@ -185,6 +190,35 @@ class Oracle:
             if any(ex.map(run, _row_ranges(M, 4 * (threads or host_cores())))):
                 raise ValueError(f"oracle quantize_pack rejected qtype={qtype} shape={W.shape}")
         return out
+
+    def q4_k_split_scale(self, Wq, M, K, x):
+        """Q4_K rows: SK[m] = sum over sub-blocks of d*sc * sum|q x| +
+        dmin*m * sum|x|, the scale of the GEMV bound for a product evaluated
+        as d*sc * sum(q x) - dmin*m * sum(x) per sub-block (SK >= S)."""
+        Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        assert x.shape == (K,)
+        SK = np.empty(M, dtype=np.float64)
+        if self.lib.bqo_q4_k_split_scale(Wq.ctypes.data, M, K, x.ctypes.data, SK.ctypes.data):
+            raise ValueError("oracle q4_k_split_scale: bad arguments")
+        return SK
+
+    def q4_k_split_scale_parallel(self, Wq, M, K, x, threads=None):
+        """q4_k_split_scale() with the rows split among host threads."""
+        Wq = np.ascontiguousarray(Wq, dtype=np.uint8).reshape(M, -1)
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        SK = np.empty(M, dtype=np.float64)
+        rb = Wq.shape[1] if M else 0
+
+        def run(r):
+            r0, r1 = r
+            return self.lib.bqo_q4_k_split_scale(Wq.ctypes.data + r0 * rb, r1 - r0, K,
+                                                 x.ctypes.data, SK.ctypes.data + 8 * r0)
+
+        with ThreadPoolExecutor(threads or host_cores()) as ex:
+            if any(ex.map(run, _row_ranges(M, 4 * (threads or host_cores())))):
+                raise ValueError("oracle q4_k_split_scale: bad arguments")
+        return SK
 
     def gemv_y_only(self, qtype, Wq, M, K, x, y):
         """The same product without S, into a caller-owned fp64 ``y``."""

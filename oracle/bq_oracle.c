@@ -30,6 +30,26 @@
  *    "round" is round-half-away-from-zero (C roundf); the divisions are fp32
  *    and correctly rounded; w / d divides by the STORED fp16 scale; d == 0
  *    gives q = 0 (Q8_0) or n = 8 (Q4_0).
+ *  - Q4_K (RunIT README kernel table, gemv_q4k_f16 / "gemv_q4k.metal", and
+ *    "Quantization" table, Q4_K_M; EdgeRunner forum summary, 核心特性, the
+ *    K-quant formats).  The pages name the format but do not define it; the
+ *    reading here is the public GGUF Q4_K super-block:
+ *      256 weights in 144 bytes: fp16 d at bytes 0-1, fp16 dmin at bytes 2-3,
+ *      12 bytes s[0..11] holding eight 6-bit sub-block scales sc[j] and mins
+ *      m[j] (j < 4: sc = s[j] & 63, m = s[j+4] & 63; j >= 4: sc = (s[j+4] &
+ *      15) | (s[j-4] >> 6) << 4, m = (s[j+4] >> 4) | (s[j] >> 6) << 4), then
+ *      128 bytes qs: sub-blocks 2g and 2g+1 (32 weights each) share
+ *      qs[32g .. 32g+31], element i of sub-block 2g the low nibble of
+ *      qs[32g+i] and element i of sub-block 2g+1 its high nibble;
+ *      w = d*sc[j]*q - dmin*m[j] for sub-block j.
+ *    The quantizer is not on the pages either; the plainest reading that
+ *    fills this layout, per sub-block j: lo = min(0, min w), hi = max w,
+ *    scale_j = (hi - lo) / 15, min_j = -lo; per super-block d =
+ *    fp16(max_j scale_j / 63), dmin = fp16(max_j min_j / 63); sc[j] =
+ *    clamp(round(scale_j / d), 0, 63), m[j] = clamp(round(min_j / dmin), 0,
+ *    63) (0 when the divisor is 0); q = clamp(round((w + dmin*m[j]) /
+ *    (d*sc[j])), 0, 15) (0 when d*sc[j] is 0).  fp32 arithmetic, correctly
+ *    rounded divisions, round half away from zero, as for Q8_0 / Q4_0.
  *  - RMSNorm and SiLU for the fused gate+up kernel (RunIT README kernel table
  *    rows rms_norm_f32_f32_f32g, silu_mul_f32 and fused_ffn_q4_0_f32 "gate+up+
  *    silu fused"; EdgeRunner "The progression", RMSNorm+GEMV fusion stage):
@@ -42,6 +62,7 @@
 
 #define BQO_Q4_0 2
 #define BQO_Q8_0 8
+#define BQO_Q4_K 12
 
 /* ------------------------------------------------------------------------ */
 /* IEEE-754 binary16 conversion, written from the format definition.        */
@@ -105,6 +126,143 @@ void bqo_f32_to_f16_array(const float *in, uint16_t *out, int64_t n) {
 }
 
 /* ------------------------------------------------------------------------ */
+/* Q4_K super-blocks (the reading in the header comment)                    */
+/* ------------------------------------------------------------------------ */
+
+static float q4k_stored(uint16_t h) { return (float)bqo_f16_bits_to_f64(h); }
+
+static float q4k_round_clamp(float v, float hi) {
+    float r = roundf(v);
+    if (r > hi) r = hi;
+    if (r < 0.0f) r = 0.0f;
+    return r;
+}
+
+/* sub-block j's 6-bit scale and min from the 12 scale bytes */
+static void q4k_scale_min(const uint8_t *s, int j, int *sc, int *mn) {
+    if (j < 4) {
+        *sc = s[j] & 63;
+        *mn = s[j + 4] & 63;
+    } else {
+        *sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+        *mn = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+}
+
+/* One super-block of 256 fp32 weights into 144 bytes. */
+static void pack_superblock_q4_k(const float *w, uint8_t *sb) {
+    float scale[8], mins[8], smax = 0.0f, mmax = 0.0f;
+    for (int j = 0; j < 8; ++j) {
+        float lo = 0.0f, hi = w[32 * j];
+        for (int i = 0; i < 32; ++i) {
+            float v = w[32 * j + i];
+            if (v < lo) lo = v;
+            if (v > hi) hi = v;
+        }
+        scale[j] = (hi - lo) / 15.0f;
+        mins[j] = -lo;
+        if (scale[j] > smax) smax = scale[j];
+        if (mins[j] > mmax) mmax = mins[j];
+    }
+    uint16_t dh = bqo_f32_to_f16_bits(smax / 63.0f);
+    uint16_t mh = bqo_f32_to_f16_bits(mmax / 63.0f);
+    float d = q4k_stored(dh), dmin = q4k_stored(mh);
+    int sc[8], mn[8];
+    for (int j = 0; j < 8; ++j) {
+        sc[j] = d != 0.0f ? (int)q4k_round_clamp(scale[j] / d, 63.0f) : 0;
+        mn[j] = dmin != 0.0f ? (int)q4k_round_clamp(mins[j] / dmin, 63.0f) : 0;
+    }
+    sb[0] = (uint8_t)(dh & 0xFFu);
+    sb[1] = (uint8_t)(dh >> 8);
+    sb[2] = (uint8_t)(mh & 0xFFu);
+    sb[3] = (uint8_t)(mh >> 8);
+    uint8_t *s = sb + 4;
+    for (int j = 0; j < 4; ++j) {
+        s[j] = (uint8_t)(sc[j] | ((sc[j + 4] >> 4) << 6));
+        s[j + 4] = (uint8_t)(mn[j] | ((mn[j + 4] >> 4) << 6));
+        s[j + 8] = (uint8_t)((sc[j + 4] & 15) | ((mn[j + 4] & 15) << 4));
+    }
+    uint8_t *qs = sb + 16;
+    memset(qs, 0, 128);
+    for (int j = 0; j < 8; ++j) {
+        float D = d * (float)sc[j], Mf = dmin * (float)mn[j];
+        for (int i = 0; i < 32; ++i) {
+            int q = D != 0.0f ? (int)q4k_round_clamp((w[32 * j + i] + Mf) / D, 15.0f) : 0;
+            qs[32 * (j / 2) + i] |= (uint8_t)((j & 1) ? q << 4 : q);
+        }
+    }
+}
+
+/* code q (0..15), D = d*sc and Mf = dmin*m (fp64, exact) of element e (0..255) */
+static void q4k_elem(const uint8_t *sb, int e, int *q, double *D, double *Mf) {
+    int j = e / 32, i = e % 32, sc, mn;
+    q4k_scale_min(sb + 4, j, &sc, &mn);
+    int byte = sb[16 + 32 * (j / 2) + i];
+    *q = (j & 1) ? (byte >> 4) : (byte & 0xF);
+    *D = bqo_f16_bits_to_f64((uint16_t)(sb[0] | (sb[1] << 8))) * (double)sc;
+    *Mf = bqo_f16_bits_to_f64((uint16_t)(sb[2] | (sb[3] << 8))) * (double)mn;
+}
+
+static double q4k_weight(const uint8_t *row, int64_t k) {
+    int q;
+    double D, Mf;
+    q4k_elem(row + (k / 256) * 144, (int)(k % 256), &q, &D, &Mf);
+    return D * (double)q - Mf;
+}
+
+static int q4k_pack(const float *W, int64_t M, int64_t K, uint8_t *out) {
+    if (M < 0 || K < 0 || K % 256) return -1;
+    int64_t ns = K / 256;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t b = 0; b < ns; ++b) pack_superblock_q4_k(W + m * K + 256 * b, out + (m * ns + b) * 144);
+    return 0;
+}
+
+static int q4k_dequant(const uint8_t *Wq, int64_t M, int64_t K, double *out) {
+    if (M < 0 || K < 0 || K % 256) return -1;
+    int64_t rb = K / 256 * 144;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) out[m * K + k] = q4k_weight(Wq + m * rb, k);
+    return 0;
+}
+
+static int q4k_gemv(const uint8_t *Wq, int64_t M, int64_t K, const double *x, double *y, double *S) {
+    if (M < 0 || K < 0 || K % 256) return -1;
+    int64_t rb = K / 256 * 144;
+    for (int64_t m = 0; m < M; ++m) {
+        double acc = 0.0, sacc = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = q4k_weight(Wq + m * rb, k) * x[k];
+            acc += p;
+            sacc += fabs(p);
+        }
+        y[m] = acc;
+        if (S) S[m] = sacc;
+    }
+    return 0;
+}
+
+/* The bound's scale for Q4_K rows: SK[m] = sum over sub-blocks j of
+ * (d*sc_j * sum_i |q_i x_i| + dmin*m_j * sum_i |x_i|), the sums of the
+ * magnitudes of the two terms w = d*sc*q - dmin*m splits each weight into
+ * (SK >= sum_k |w x|). */
+int bqo_q4_k_split_scale(const uint8_t *Wq, int64_t M, int64_t K, const double *x, double *SK) {
+    if (M < 0 || K < 0 || K % 256) return -1;
+    int64_t rb = K / 256 * 144;
+    for (int64_t m = 0; m < M; ++m) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            int q;
+            double D, Mf;
+            q4k_elem(Wq + m * rb + (k / 256) * 144, (int)(k % 256), &q, &D, &Mf);
+            acc += D * fabs((double)q * x[k]) + Mf * fabs(x[k]);
+        }
+        SK[m] = acc;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Block formats                                                            */
 /* ------------------------------------------------------------------------ */
 
@@ -115,6 +273,7 @@ int64_t bqo_block_bytes(int qtype) {
 }
 
 int64_t bqo_packed_bytes(int qtype, int64_t M, int64_t K) {
+    if (qtype == BQO_Q4_K) return (M < 0 || K < 0 || K % 256) ? -1 : M * (K / 256) * 144;
     int64_t bb = bqo_block_bytes(qtype);
     if (bb < 0 || M < 0 || K < 0 || K % 32) return -1;
     return M * (K / 32) * bb;
@@ -172,6 +331,7 @@ static void pack_block_q4_0(const float *w, uint8_t *blk) {
 /* W: fp32 [M, K] row-major; out: M rows of K/32 blocks.  Returns 0, or -1 on
  * a bad qtype or shape. */
 int bqo_quantize_pack(int qtype, const float *W, int64_t M, int64_t K, uint8_t *out) {
+    if (qtype == BQO_Q4_K) return q4k_pack(W, M, K, out);
     int64_t bb = bqo_block_bytes(qtype);
     if (bb < 0 || M < 0 || K < 0 || K % 32) return -1;
     int64_t nb = K / 32;
@@ -197,6 +357,7 @@ static double dequant_elem(int qtype, const uint8_t *blk, int j) {
 
 /* Wq: M packed rows -> fp64 [M, K]. */
 int bqo_dequant(int qtype, const uint8_t *Wq, int64_t M, int64_t K, double *out) {
+    if (qtype == BQO_Q4_K) return q4k_dequant(Wq, M, K, out);
     int64_t bb = bqo_block_bytes(qtype);
     if (bb < 0 || M < 0 || K < 0 || K % 32) return -1;
     int64_t nb = K / 32;
@@ -211,6 +372,7 @@ int bqo_dequant(int qtype, const uint8_t *Wq, int64_t M, int64_t K, double *out)
  * and an fp64 RMSNorm output can be fed in. */
 int bqo_gemv(int qtype, const uint8_t *Wq, int64_t M, int64_t K, const double *x,
              double *y, double *S) {
+    if (qtype == BQO_Q4_K) return q4k_gemv(Wq, M, K, x, y, S);
     int64_t bb = bqo_block_bytes(qtype);
     if (bb < 0 || M < 0 || K < 0 || K % 32) return -1;
     int64_t nb = K / 32;

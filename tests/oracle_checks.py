@@ -21,8 +21,8 @@ import oracle as _o
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
-Q8_0, Q4_0 = _o.Q8_0, _o.Q4_0
-QNAMES = {"q8_0": Q8_0, "q4_0": Q4_0}
+Q8_0, Q4_0, Q4_K = _o.Q8_0, _o.Q4_0, _o.Q4_K
+QNAMES = {"q8_0": Q8_0, "q4_0": Q4_0, "q4_k": Q4_K}
 
 
 # --------------------------------------------------------------------------
@@ -47,8 +47,77 @@ def decode_independent(qtype, Wq, M, K):
 
 
 def dequant_independent(qtype, Wq, M, K):
+    if qtype == Q4_K:
+        return q4k_dequant_independent(Wq, M, K)
     d, ints = decode_independent(qtype, Wq, M, K)
     return np.repeat(d, 32, axis=1) * ints
+
+
+# Q4_K, the GGUF super-block as read in the oracle's header: 144 bytes per 256
+# weights, decoded here with array slicing instead of per-element indexing
+def q4k_decode_independent(Wq, M, K):
+    """(d [M, ns], dmin [M, ns], sc [M, ns, 8], mn [M, ns, 8], q [M, ns, 8, 32])"""
+    ns = K // 256
+    sb = np.ascontiguousarray(Wq, dtype=np.uint8).reshape(M, ns, 144)
+    d = sb[..., 0:2].copy().view("<f2")[..., 0].astype(np.float64)
+    dmin = sb[..., 2:4].copy().view("<f2")[..., 0].astype(np.float64)
+    s = sb[..., 4:16].astype(np.int64)
+    sc = np.concatenate([s[..., 0:4] & 63, (s[..., 8:12] & 15) | ((s[..., 0:4] >> 6) << 4)], -1)
+    mn = np.concatenate([s[..., 4:8] & 63, (s[..., 8:12] >> 4) | ((s[..., 4:8] >> 6) << 4)], -1)
+    qs = sb[..., 16:].reshape(M, ns, 4, 32).astype(np.int64)
+    q = np.stack([qs & 15, qs >> 4], axis=3).reshape(M, ns, 8, 32)
+    return d, dmin, sc, mn, q
+
+
+def q4k_dequant_independent(Wq, M, K):
+    d, dmin, sc, mn, q = q4k_decode_independent(Wq, M, K)
+    w = (d[..., None, None] * sc[..., None]) * q - (dmin[..., None] * mn)[..., None]
+    return w.reshape(M, K)
+
+
+def _round_away(v):
+    """C roundf of fp32 values, in fp64 (exact for fp32 inputs)."""
+    v = np.asarray(v, dtype=np.float64)
+    return np.sign(v) * np.floor(np.abs(v) + 0.5)
+
+
+def q4k_quantize_independent(W):
+    """The Q4_K packer's reading, vectorised in numpy fp32 (IEEE, correctly
+    rounded divisions; float16 casts round to nearest even): per sub-block
+    lo = min(0, min w), hi = max w, scale = (hi - lo)/15, min = -lo; d and
+    dmin = fp16(max / 63) (+0 when every term is zero); sc, m, q rounded half
+    away from zero and clamped."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    M, K = W.shape
+    ns = K // 256
+    f32 = np.float32
+    w = W.reshape(M, ns, 8, 32)
+    lo = np.minimum(w.min(-1), f32(0))
+    hi = w.max(-1)
+    scale = (hi - lo) / f32(15)
+    mins = -lo
+    smax = scale.max(-1) + f32(0)  # + 0 turns a -0 into +0
+    mmax = mins.max(-1) + f32(0)
+    dh = (smax / f32(63)).astype(np.float16)
+    mh = (mmax / f32(63)).astype(np.float16)
+    df, mf = dh.astype(f32), mh.astype(f32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        sc = np.where(df[..., None] != 0, np.clip(_round_away(scale / df[..., None]), 0, 63), 0)
+        mn = np.where(mf[..., None] != 0, np.clip(_round_away(mins / mf[..., None]), 0, 63), 0)
+        sc, mn = sc.astype(np.int64), mn.astype(np.int64)
+        D = df[..., None] * sc.astype(f32)
+        Mf = mf[..., None] * mn.astype(f32)
+        v = (w + Mf[..., None]) / D[..., None]
+        q = np.where(D[..., None] != 0, np.clip(_round_away(v), 0, 15), 0).astype(np.int64)
+    out = np.zeros((M, ns, 144), np.uint8)
+    out[..., 0:2] = dh.view(np.uint8).reshape(M, ns, 2)
+    out[..., 2:4] = mh.view(np.uint8).reshape(M, ns, 2)
+    out[..., 4:8] = sc[..., :4] | ((sc[..., 4:] >> 4) << 6)
+    out[..., 8:12] = mn[..., :4] | ((mn[..., 4:] >> 4) << 6)
+    out[..., 12:16] = (sc[..., 4:] & 15) | ((mn[..., 4:] & 15) << 4)
+    qq = q.reshape(M, ns, 4, 2, 32)
+    out[..., 16:] = (qq[:, :, :, 0, :] | (qq[:, :, :, 1, :] << 4)).reshape(M, ns, 128)
+    return out.reshape(M, ns * 144)
 
 
 # --------------------------------------------------------------------------
@@ -77,7 +146,7 @@ def load_golden(name):
     return rec
 
 
-GOLDEN_FILES = ("q8_0_example_a.txt", "q4_0_example_b.txt")
+GOLDEN_FILES = ("q8_0_example_a.txt", "q4_0_example_b.txt", "q4_k_example_c.txt")
 
 
 def check_golden(o):
@@ -437,8 +506,127 @@ def check_gemv_f16(o, rng=None):
     assert not y.any() and not S.any(), "x = 0"
 
 
+# --------------------------------------------------------------------------
+# Q4_K
+# --------------------------------------------------------------------------
+def _q4k_weights(rng, M, K):
+    """Weights that exercise the Q4_K packer: N(0, 0.02) scaled per sub-block
+    by 2^-12..2^4, sub-blocks that are all positive, all negative, all zero,
+    or hold -0.0, and a few ties."""
+    w = rng.standard_normal((M, K)).astype(np.float32) * np.float32(0.02)
+    sub = w.reshape(M, K // 32, 32)
+    sub *= (2.0 ** rng.integers(-12, 5, size=(M, K // 32, 1))).astype(np.float32)
+    kind = rng.integers(0, 8, size=(M, K // 32))
+    sub[kind == 1] = np.abs(sub[kind == 1])
+    sub[kind == 2] = -np.abs(sub[kind == 2])
+    sub[kind == 3] = 0.0
+    sub[kind == 4] = -0.0
+    return np.ascontiguousarray(sub.reshape(M, K))
+
+
+def check_q4k_independent(o, rng=None):
+    """The oracle's Q4_K packing equals the independent numpy statement of
+    the same reading byte for byte, and its dequant equals the independent
+    decoder."""
+    rng = rng or np.random.default_rng(11)
+    for M, K in ((1, 256), (5, 512), (33, 1024), (3, 3584)):
+        W = _q4k_weights(rng, M, K)
+        P = o.quantize_pack(Q4_K, W)
+        want = q4k_quantize_independent(W)
+        bad = np.flatnonzero((P != want).any(axis=1))
+        assert bad.size == 0, f"Q4_K pack {M}x{K}: rows {bad[:5]} differ"
+        assert np.array_equal(o.dequant(Q4_K, P, M, K), q4k_dequant_independent(P, M, K)), \
+            f"Q4_K dequant {M}x{K}"
+    assert o.packed_bytes(Q4_K, 7, 512) == 7 * 2 * 144 and o.packed_bytes(Q4_K, 1, 288) == -1
+
+
+def check_q4k_roundtrip(o, rng=None):
+    """|dequant(pack(w)) - w| <= (d sc)/2 wherever the code is not clamped;
+    a clamped code sits at the end of the range it was clamped to."""
+    rng = rng or np.random.default_rng(12)
+    M, K = 24, 1024
+    W = _q4k_weights(rng, M, K)
+    P = o.quantize_pack(Q4_K, W)
+    d, dmin, sc, mn, q = q4k_decode_independent(P, M, K)
+    D = (d[..., None] * sc)[..., None]
+    Mf = (dmin[..., None] * mn)[..., None]
+    w = W.reshape(M, K // 256, 8, 32).astype(np.float64)
+    v = w + Mf  # the code's target times D
+    err = np.abs(D * q - v)
+    inside = (v >= -0.5 * D) & (v <= 15.5 * D)
+    tol = 0.5 * D * (1 + 1e-6) + 1e-6 * np.abs(v)
+    assert np.all(err[inside & (D > 0)] <= tol[inside & (D > 0)]), "Q4_K round trip"
+    assert np.all(q[(v > 15.5 * D * (1 + 1e-6)) & (D > 0)] == 15), "Q4_K clamp at 15"
+    assert np.all(q[(v < -0.5 * D * (1 + 1e-6)) & (D > 0)] == 0), "Q4_K clamp at 0"
+    # the sub-block scales follow the data: the largest sub-block range takes sc = 63
+    rng_w = w.max(-1) - np.minimum(w.min(-1), 0.0)
+    big = rng_w == rng_w.max(-1, keepdims=True)
+    assert np.all(sc[big & (rng_w > 0)] >= 62), "Q4_K scale of the widest sub-block"
+
+
+Q4K_D = {0x3400: Fraction(1, 4), 0x3800: Fraction(1, 2), 0x3C00: Fraction(1), 0x2C00: Fraction(1, 16)}
+
+
+def _q4k_direct(rng, M, K):
+    """Q4_K bytes built without the packer (numpy bit assembly): d and dmin
+    powers of two, 6-bit scales and mins and 4-bit codes over their full
+    ranges.  Returns the bytes and their exact meaning as Fractions."""
+    ns = K // 256
+    keys = list(Q4K_D)
+    dsel = rng.choice(keys, size=(M, ns))
+    msel = rng.choice(keys, size=(M, ns))
+    sc = rng.integers(0, 64, size=(M, ns, 8))
+    mn = rng.integers(0, 64, size=(M, ns, 8))
+    q = rng.integers(0, 16, size=(M, ns, 8, 32))
+    out = np.zeros((M, ns, 144), np.uint8)
+    out[..., 0], out[..., 1] = dsel & 0xFF, dsel >> 8
+    out[..., 2], out[..., 3] = msel & 0xFF, msel >> 8
+    out[..., 4:8] = sc[..., :4] | ((sc[..., 4:] >> 4) << 6)
+    out[..., 8:12] = mn[..., :4] | ((mn[..., 4:] >> 4) << 6)
+    out[..., 12:16] = (sc[..., 4:] & 15) | ((mn[..., 4:] & 15) << 4)
+    qq = q.reshape(M, ns, 4, 2, 32)
+    out[..., 16:] = (qq[:, :, :, 0, :] | (qq[:, :, :, 1, :] << 4)).reshape(M, ns, 128)
+    return out.reshape(M, ns * 144), dsel, msel, sc, mn, q
+
+
+def check_q4k_bruteforce(o, rng=None):
+    """Exact Q4_K products: power-of-two d and dmin and small-integer x make
+    every product and sum a dyadic rational, computed here with Fractions;
+    y, S = sum|w x| and the split scale SK must equal them exactly."""
+    rng = rng or np.random.default_rng(13)
+    for M, K in ((1, 256), (3, 512), (2, 768)):
+        raw, dsel, msel, sc, mn, q = _q4k_direct(rng, M, K)
+        x = rng.integers(-2, 3, size=K)
+        y, S = o.gemv(Q4_K, raw, M, K, x.astype(np.float64))
+        SK = o.q4_k_split_scale(raw, M, K, x.astype(np.float64))
+        for m in range(M):
+            acc = s_abs = s_split = Fraction(0)
+            for b in range(K // 256):
+                d, dm = Q4K_D[int(dsel[m, b])], Q4K_D[int(msel[m, b])]
+                for j in range(8):
+                    for i in range(32):
+                        xi = int(x[256 * b + 32 * j + i])
+                        wv = d * int(sc[m, b, j]) * int(q[m, b, j, i]) - dm * int(mn[m, b, j])
+                        acc += wv * xi
+                        s_abs += abs(wv * xi)
+                        s_split += d * int(sc[m, b, j]) * abs(int(q[m, b, j, i]) * xi) + \
+                            dm * int(mn[m, b, j]) * abs(xi)
+            assert Fraction(y[m]) == acc, f"Q4_K y {M}x{K} row {m}"
+            assert Fraction(S[m]) == s_abs, f"Q4_K S {M}x{K} row {m}"
+            assert Fraction(SK[m]) == s_split, f"Q4_K SK {M}x{K} row {m}"
+    # one-hot x picks column k of the dequantized matrix exactly
+    raw, *_ = _q4k_direct(rng, 4, 512)
+    deq = q4k_dequant_independent(raw, 4, 512)
+    for k in (0, 31, 32, 255, 256, 300, 511):
+        e = np.zeros(512)
+        e[k] = 1.0
+        y, _ = o.gemv(Q4_K, raw, 4, 512, e)
+        assert np.array_equal(y, deq[:, k]), f"Q4_K one-hot column {k}"
+
+
 QUICK_CHECKS = (check_golden, check_fp16_points, check_roundtrip, check_bruteforce,
-                check_all_codes, check_closed_forms, check_norm_silu, check_bias, check_gemv_f16)
+                check_all_codes, check_closed_forms, check_norm_silu, check_bias, check_gemv_f16,
+                check_q4k_independent, check_q4k_roundtrip, check_q4k_bruteforce)
 
 
 def run_quick(o):

@@ -63,6 +63,26 @@ MUTANTS = [
     ("f16_gemv_reversed_x", "(W[m * K + k]) * x[k];", "(W[m * K + k]) * x[K - 1 - k];"),
     ("f16_gemv_dropped_term", "for (int64_t k = 0; k < K; k++) {", "for (int64_t k = 1; k < K; k++) {"),
     ("f16_gemv_S_signed", "sacc += fabs(p); /* sum of |w x| */", "sacc += p; /* sum of |w x| */"),
+    # Q4_K
+    ("q4k_scale_mask", "*sc = s[j] & 63;", "*sc = s[j] & 31;"),
+    ("q4k_min_high_bits", "*mn = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);",
+     "*mn = (s[j + 4] >> 4) | ((s[j - 4] >> 6) << 4);"),
+    ("q4k_nibble_order", "*q = (j & 1) ? (byte >> 4) : (byte & 0xF);",
+     "*q = (j & 1) ? (byte & 0xF) : (byte >> 4);"),
+    ("q4k_min_sign", "return D * (double)q - Mf;", "return D * (double)q + Mf;"),
+    ("q4k_range_divisor", "scale[j] = (hi - lo) / 15.0f;", "scale[j] = (hi - lo) / 16.0f;"),
+    ("q4k_super_divisor", "uint16_t dh = bqo_f32_to_f16_bits(smax / 63.0f);",
+     "uint16_t dh = bqo_f32_to_f16_bits(smax / 64.0f);"),
+    ("q4k_lo_unclamped", "float lo = 0.0f, hi = w[32 * j];", "float lo = w[32 * j], hi = w[32 * j];"),
+    ("q4k_pair_bytes", "qs[32 * (j / 2) + i] |=", "qs[32 * (j % 4) + i] |="),
+    ("q4k_sc_pack_shift", "s[j] = (uint8_t)(sc[j] | ((sc[j + 4] >> 4) << 6));",
+     "s[j] = (uint8_t)(sc[j] | ((sc[j + 4] >> 3) << 6));"),
+    ("q4k_dmin_bytes", "*Mf = bqo_f16_bits_to_f64((uint16_t)(sb[2] | (sb[3] << 8))) * (double)mn;",
+     "*Mf = bqo_f16_bits_to_f64((uint16_t)(sb[0] | (sb[1] << 8))) * (double)mn;"),
+    ("q4k_code_shift", "(w[32 * j + i] + Mf) / D", "(w[32 * j + i] - Mf) / D"),
+    ("q4k_split_drops_min", "acc += D * fabs((double)q * x[k]) + Mf * fabs(x[k]);",
+     "acc += D * fabs((double)q * x[k]);"),
+    ("q4k_superblock_stride", "out + (m * ns + b) * 144", "out + (b * M + m) * 144"),
 ]
 
 

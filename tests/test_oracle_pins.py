@@ -49,6 +49,18 @@ def test_gemv_f16():
     checks.check_gemv_f16(o())
 
 
+def test_q4_k_packing_against_an_independent_statement():
+    checks.check_q4k_independent(o())
+
+
+def test_q4_k_round_trip():
+    checks.check_q4k_roundtrip(o())
+
+
+def test_q4_k_exact_products():
+    checks.check_q4k_bruteforce(o())
+
+
 def test_packed_bytes_and_bad_args():
     ob = o()
     assert ob.packed_bytes(oracle.Q8_0, 3072, 1024) == 3072 * 32 * 34
