@@ -44,6 +44,14 @@ NOMINAL_HBM_GBS = 8000.0
 CFG1_COPIES = 96   # rotated weight copies: 321 MB per sweep, 2.5x the 129 MB L2
 CFG5_COPIES = 7    # of each verify matrix: 702 MB per sweep
 FALLBACK_HBM_GBS = 6800.0
+# per-token weight streams: cfg2 (Qwen3-0.6B-shaped Q8_0), cfg3 (7B-shaped
+# Q4_0) and cfg3k (the 7B-shaped stream in Q4_K super-blocks)
+TOKEN_CONFIGS = ("cfg2", "cfg3", "cfg3k")
+
+
+def token_cfg(config):
+    from block_quantized_weight_dequant_gb300 import workloads as wl
+    return dict({"cfg2": wl.QWEN3_0_6B, "cfg3": wl.Q7B, "cfg3k": wl.Q7B_K}[config])
 
 
 # ---------------------------------------------------------------------------
@@ -83,7 +91,7 @@ def csrc_digest():
 
 
 def ncu_traffic(config, inputs):
-    e = NCU_TRAFFIC.get((config, inputs if config in ("cfg2", "cfg3") else None))
+    e = NCU_TRAFFIC.get((config, inputs if config in TOKEN_CONFIGS else None))
     if e is None or e[1] != csrc_digest():
         return None, None
     return e[0], e[2]
@@ -404,8 +412,8 @@ def token_desc(cfg, mode, chained, fused_qkv=False):
 def workload_desc(args):
     """The step's config entries, identical in both arms (no GPU needed)."""
     from block_quantized_weight_dequant_gb300 import workloads as wl
-    if args.config in ("cfg2", "cfg3"):
-        cfg = dict(wl.QWEN3_0_6B if args.config == "cfg2" else wl.Q7B)
+    if args.config in TOKEN_CONFIGS:
+        cfg = token_cfg(args.config)
         if args.layers:
             cfg["layers"] = args.layers
         return token_desc(cfg, args.launch, args.inputs == "chained", args.qkv == "fused")
@@ -426,8 +434,8 @@ def step_bytes_static(args):
     """Algorithmic bytes of one step (packed weights + x read + y written
     (+ gamma)), computed from the shapes alone."""
     from block_quantized_weight_dequant_gb300 import workloads as wl
-    if args.config in ("cfg2", "cfg3"):
-        cfg = dict(wl.QWEN3_0_6B if args.config == "cfg2" else wl.Q7B)
+    if args.config in TOKEN_CONFIGS:
+        cfg = token_cfg(args.config)
         if args.layers:
             cfg["layers"] = args.layers
         return token_bytes_cfg(cfg, args.qkv == "fused")
@@ -447,8 +455,8 @@ def step_bytes_static(args):
 def build_workload(args, dev):
     from block_quantized_weight_dequant_gb300 import workloads as wl
     chained = args.inputs == "chained"
-    if args.config in ("cfg2", "cfg3"):
-        cfg = dict(wl.QWEN3_0_6B if args.config == "cfg2" else wl.Q7B)
+    if args.config in TOKEN_CONFIGS:
+        cfg = token_cfg(args.config)
         if args.layers:
             cfg["layers"] = args.layers
         fq = args.qkv == "fused"
@@ -472,7 +480,7 @@ def build_workload(args, dev):
 
 
 def tokens_per_step(args):
-    return 1.0 if args.config in ("cfg2", "cfg3") else None
+    return 1.0 if args.config in TOKEN_CONFIGS else None
 
 
 # ---------------------------------------------------------------------------
@@ -552,8 +560,8 @@ def oracle_jobs(config, rows=6, layers=0):
     (format, M, K, input rows), the matrices in the step's order (gate and up
     of a fused op are two GEMVs; a verify call is R GEMVs of one matrix)."""
     from block_quantized_weight_dequant_gb300 import workloads as wl
-    if config in ("cfg2", "cfg3"):
-        cfg = dict(wl.QWEN3_0_6B if config == "cfg2" else wl.Q7B)
+    if config in TOKEN_CONFIGS:
+        cfg = token_cfg(config)
         if layers:
             cfg["layers"] = layers
         return [(cfg["qtype"], M, K, 1) for _, M, K in wl.token_weight_shapes(cfg)]
@@ -583,8 +591,11 @@ def oracle_step_data(jobs, seed=0):
         else:
             bb = 34 if fmt == "q8_0" else 18
             W = np.frombuffer(rng.bytes(M * (K // 32) * bb), dtype=np.uint8).copy()
-            blk = W.reshape(-1, bb)
-            blk[:, 1] = rng.integers(0x18, 0x24, size=blk.shape[0], dtype=np.uint8)
+            # the high byte of every fp16 scale (Q4_K: d and dmin of each
+            # 144-byte super-block)
+            blk = W.reshape(-1, 144) if fmt == "q4_k" else W.reshape(-1, bb)
+            for at in ((1, 3) if fmt == "q4_k" else (1,)):
+                blk[:, at] = rng.integers(0x18, 0x24, size=blk.shape[0], dtype=np.uint8)
             W = W.reshape(M, (K // 32) * bb)
         X = rng.standard_normal((R, K))
         data.append((fmt, M, K, W, X))
@@ -606,7 +617,7 @@ def oracle_run(o, oracle, data, threads, budget_s, whole_steps):
                 if fmt == "f16":
                     o.gemv_f16_parallel(W, x, threads=threads, with_S=False)
                 else:
-                    qt = oracle.Q8_0 if fmt == "q8_0" else oracle.Q4_0
+                    qt = {"q8_0": oracle.Q8_0, "q4_0": oracle.Q4_0, "q4_k": oracle.Q4_K}[fmt]
                     o.gemv_parallel(qt, W, M, K, x, threads=threads, with_S=False)
                 done += M * K
             if not whole_steps and time.perf_counter() - t0 >= budget_s:
@@ -804,7 +815,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=15)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="cfg2", choices=["cfg1", "cfg2", "cfg3", "cfg4", "cfg5", "f16"])
+    ap.add_argument("--config", default="cfg2",
+                    choices=["cfg1", "cfg2", "cfg3", "cfg3k", "cfg4", "cfg5", "f16"])
     ap.add_argument("--rows", type=int, default=6, help="R for cfg5")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work per cpu_baseline leg (0 disables)")

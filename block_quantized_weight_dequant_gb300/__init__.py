@@ -6,23 +6,26 @@ outputs with PyTorch when the caller passes none, and calls the C ABI on the
 current CUDA stream.  All arithmetic runs in this package's CUDA kernels.
 
 Packed weights are uint8 tensors of shape [M, (K/32) * block_bytes]
-(34 bytes per 32 weights for Q8_0, 18 for Q4_0), so M and K are read from
-the packed tensor's shape.
+(34 bytes per 32 weights for Q8_0, 18 for Q4_0 and for Q4_K, whose 144-byte
+super-blocks hold 256 weights), so M and K are read from the packed tensor's
+shape.
 """
 import ctypes
 
 import torch
 
 from . import _lib
-from ._lib import BQ_Q4_0, BQ_Q8_0, BQ_VERIFY_MAX_ROWS, BQError, lib  # noqa: F401
+from ._lib import BQ_Q4_0, BQ_Q4_K, BQ_Q8_0, BQ_VERIFY_MAX_ROWS, BQError, lib  # noqa: F401
 
 Q8_0 = BQ_Q8_0
 Q4_0 = BQ_Q4_0
-BLOCK_BYTES = {Q8_0: 34, Q4_0: 18}
-QTYPES = {"q8_0": Q8_0, "q4_0": Q4_0}
+Q4_K = BQ_Q4_K
+# packed bytes per 32 weights (a Q4_K super-block is 144 bytes per 256 weights)
+BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q4_K: 18}
+QTYPES = {"q8_0": Q8_0, "q4_0": Q4_0, "q4_k": Q4_K}
 
-__all__ = ["Q8_0", "Q4_0", "BLOCK_BYTES", "BQError", "packed_bytes", "quantize_pack",
-           "gemv", "gemv_q8_0", "gemv_q4_0", "gemv_gate_up_silu", "gemv_verify",
+__all__ = ["Q8_0", "Q4_0", "Q4_K", "BLOCK_BYTES", "BQError", "packed_bytes", "quantize_pack",
+           "gemv", "gemv_q8_0", "gemv_q4_0", "gemv_q4_k", "gemv_gate_up_silu", "gemv_verify",
            "gemv_qkv_bias", "gemv_f16", "concat_packed",
            "device_status", "tree_lanes", "version", "StreamOp", "StreamPlan"]
 
@@ -101,7 +104,7 @@ def gemv(qtype, Wq, x, y=None):
     if y is None:
         y = torch.empty(M, dtype=torch.float32, device=Wq.device)
     _need(y, torch.float32, "y")
-    fn = lib.bq_gemv_q8_0 if qt == Q8_0 else lib.bq_gemv_q4_0
+    fn = {Q8_0: lib.bq_gemv_q8_0, Q4_0: lib.bq_gemv_q4_0, Q4_K: lib.bq_gemv_q4_k}[qt]
     _lib.check(fn(_ptr(Wq), _ptr(x), _ptr(y), M, K, _stream(Wq)), "gemv")
     return y
 
@@ -112,6 +115,10 @@ def gemv_q8_0(Wq, x, y=None):
 
 def gemv_q4_0(Wq, x, y=None):
     return gemv(Q4_0, Wq, x, y)
+
+
+def gemv_q4_k(Wq, x, y=None):
+    return gemv(Q4_K, Wq, x, y)
 
 
 def gemv_gate_up_silu(qtype, Wg, Wu, x, gamma=None, eps=1e-6, y=None):

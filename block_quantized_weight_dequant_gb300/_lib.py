@@ -11,14 +11,14 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libbqgemv.so")
 
 BQ_OK, BQ_ERR_NULL, BQ_ERR_SHAPE, BQ_ERR_ALIGN, BQ_ERR_QTYPE, BQ_ERR_CUDA, BQ_ERR_DEVICE = range(7)
-BQ_Q4_0, BQ_Q8_0 = 2, 8
+BQ_Q4_0, BQ_Q8_0, BQ_Q4_K = 2, 8, 12
 BQ_VERIFY_MAX_ROWS = 6
 
 BQ_OP_GEMV, BQ_OP_GATE_UP_SILU = 0, 1
 
 # every extern "C" symbol of include/bqgemv.h
 EXPORTS = ("bq_version", "bq_status_str", "bq_packed_bytes", "bq_quantize_pack", "bq_gemv_q8_0",
-           "bq_gemv_q4_0", "bq_gemv_gate_up_silu", "bq_gemv_verify", "bq_gemv_qkv_bias",
+           "bq_gemv_q4_0", "bq_gemv_q4_k", "bq_gemv_gate_up_silu", "bq_gemv_verify", "bq_gemv_qkv_bias",
            "bq_gemv_f16", "bq_gemv_f16_f16out", "bq_device_status",
            "bq_tree_lanes", "bq_stream_workspace_bytes", "bq_stream_plan_create",
            "bq_stream_plan_launch", "bq_stream_plan_tune", "bq_stream_plan_destroy",
@@ -49,6 +49,7 @@ def _declare(lib):
         "bq_quantize_pack": (i32, [i32, vp, i64, i64, vp, vp]),
         "bq_gemv_q8_0": (i32, [vp, vp, vp, i64, i64, vp]),
         "bq_gemv_q4_0": (i32, [vp, vp, vp, i64, i64, vp]),
+        "bq_gemv_q4_k": (i32, [vp, vp, vp, i64, i64, vp]),
         "bq_gemv_gate_up_silu": (i32, [i32, vp, vp, vp, vp, fp, vp, i64, i64, vp]),
         "bq_gemv_verify": (i32, [i32, vp, vp, vp, i32, i64, i64, vp]),
         "bq_gemv_qkv_bias": (i32, [i32, vp, vp, vp, vp, i64, i64, vp]),

@@ -105,7 +105,13 @@ int max_smem_optin() {
     return n;
 }
 
-int block_bytes(int qtype) { return qtype == BQ_Q8_0 ? 34 : qtype == BQ_Q4_0 ? 18 : -1; }
+// bytes per 32 weights (a Q4_K super-block is 144 bytes per 256 weights)
+int block_bytes(int qtype) {
+    return qtype == BQ_Q8_0 ? 34 : qtype == BQ_Q4_0 || qtype == BQ_Q4_K ? 18 : -1;
+}
+bool known_qtype(int qtype) { return block_bytes(qtype) > 0; }
+// K granularity of a format: 32 weights per block, 256 per Q4_K super-block
+int k_step(int qtype) { return qtype == BQ_Q4_K ? 256 : 32; }
 
 }  // namespace
 
@@ -264,12 +270,24 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
         for (int j = st.x_begin; j < st.x_end; ++j)
             if (ex[j].x == o.x && ex[j].gamma == g && ex[j].eps == eps && ex[j].K == K) found = j;
         if (found < 0) {
-            ex[n_x] = ExecX{o.x, g, eps, K, stage_x, g ? stage_x + x_padded_floats(K) : -1};
-            stage_x += (g ? 2 : 1) * x_padded_floats(K);
+            ExecX &xd = ex[n_x];
+            std::memset(&xd, 0, sizeof xd);
+            xd.x = o.x;
+            xd.gamma = g;
+            xd.eps = eps;
+            xd.K = K;
+            xd.off = stage_x;
+            stage_x += x_padded_floats(K);
+            xd.goff = g ? stage_x : -1;
+            if (g) stage_x += x_padded_floats(K);
+            // Q4_K: the x's 32-element block sums, 16-byte aligned
+            xd.soff = qtype == BQ_Q4_K ? stage_x : -1;
+            if (qtype == BQ_Q4_K) stage_x += (K / 32 + 3) / 4 * 4;
             found = n_x++;
             st.x_end = n_x;
         }
         e.xoff = ex[found].off;
+        e.soff = ex[found].soff;
         x_area = std::max(x_area, stage_x);
     }
     // ---- memory dependences between ops, from their address ranges ----
@@ -344,8 +362,7 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
     while (xbuf < EXEC_MAX_XBUF && total(nsw, xbuf + 1) <= (size_t)cap) ++xbuf;
     const size_t smem = total(nsw, xbuf);
     int occ = 0;
-    const int err = qtype == BQ_Q8_0 ? bq_internal_exec_occupancy_q8_0(threads, smem, &occ)
-                                     : bq_internal_exec_occupancy_q4_0(threads, smem, &occ);
+    const int err = fmt_exec_occupancy(qtype, threads, smem, &occ);
     if (err != 0 || occ < 1) return BQ_ERR_CUDA;
     const int grid = num_sms_current() * occ;
     const int nwarps = grid * warps;
@@ -463,7 +480,8 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
     // few times per launch.
     const int cap = max_smem_optin();
     const int x_off = MULTI_X_OFF;
-    const int x_floats = x_padded_floats(maxK);
+    const int x_rstride = x_padded_floats(maxK);
+    const int x_floats = x_rstride + multi_sum_floats(qtype, 1, x_rstride);
     auto warps_for = [&](int xb) {
         const int ro = (x_off + xb * x_floats * 4 + 127) / 128 * 128;
         const long long b = (long long)cap - ro;
@@ -492,8 +510,7 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
     if (smem > (size_t)cap) return BQ_ERR_SHAPE;
     const int threads = nwarps * 32;
     int occ = 0;
-    const int err = qtype == BQ_Q8_0 ? bq_internal_multi_occupancy_q8_0(NR, 1, threads, smem, &occ)
-                                     : bq_internal_multi_occupancy_q4_0(NR, 1, threads, smem, &occ);
+    const int err = fmt_multi_occupancy(qtype, NR, 1, threads, smem, &occ);
     if (err != 0 || occ < 1) return BQ_ERR_CUDA;
     const int grid = std::min(MULTI_MAX_CTAS, num_sms_current() * occ);
     // byte-balanced contiguous tile ranges
@@ -520,7 +537,7 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
     geo->smem = smem;
     geo->nr = NR;
     geo->R = 1;
-    geo->x_rstride = x_floats;
+    geo->x_rstride = x_rstride;
     geo->x_floats = x_floats;
     geo->x_buffers = x_buffers;
     geo->panel_units = 0;
@@ -574,6 +591,7 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     // R = 5 on the R partial sums per row fill the registers and one row per
     // lane measured faster on GB300 (R = 6: 687 against 576 GB/s)
     int NR = R == 1 ? 1 : t.verify_nr ? t.verify_nr : R <= 4 ? 2 : 1;
+    if (c.qtype == BQ_Q4_K) NR = 1;  // its verify instances hold one weight row per lane
     const int nsms = num_sms_current();
     const int cap = max_smem_optin();
     if (nsms <= 0 || cap <= 0) return false;
@@ -608,6 +626,7 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
         x_floats = R * x_rstride;
         x_buffers = 2;
     }
+    x_floats += multi_sum_floats(c.qtype, R, x_rstride);
     const int ring_off = (MULTI_X_OFF + x_buffers * x_floats * 4 + 127) / 128 * 128;
     const long long budget = (long long)cap - ring_off;
     const int maxw = multi_max_warps(c.qtype, R);
@@ -661,8 +680,7 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     if (smem > (size_t)cap) return false;
     const int threads = nwarps * 32;
     int occ = 0;
-    const int err = c.qtype == BQ_Q8_0 ? bq_internal_multi_occupancy_q8_0(NR, R, threads, smem, &occ)
-                                       : bq_internal_multi_occupancy_q4_0(NR, R, threads, smem, &occ);
+    const int err = fmt_multi_occupancy(c.qtype, NR, R, threads, smem, &occ);
     if (err != 0 || occ < 1) return false;
     // panel mode: every CTA holds at most nwarps tiles (one per warp); else a
     // CTA's warps take its tiles round-robin, at most one CTA wave
@@ -770,9 +788,10 @@ bool aligned_ok(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t
 
 bq_status from_cuda(int e) { return e == 0 ? BQ_OK : BQ_ERR_CUDA; }
 
-bq_status check_shape(long long M, long long K) {
+bq_status check_shape(int qtype, long long M, long long K) {
     if (M < 0 || M > bq::M_MAX) return BQ_ERR_SHAPE;
-    if (K < 32 || K > bq::K_MAX || K % 32) return BQ_ERR_SHAPE;
+    const int ks = bq::k_step(qtype);
+    if (K < ks || K > bq::K_MAX || K % ks) return BQ_ERR_SHAPE;
     return BQ_OK;
 }
 
@@ -782,9 +801,7 @@ bq_status run_gemv(const GemvCall &c) {
         bq::MultiGeometry g;
         if (bq::plan_multi_single(c, &a, &g)) {
             const int pdl = bq::tunables().single_pdl;
-            const int e = c.qtype == BQ_Q8_0
-                              ? bq_internal_multi_launch_q8_0(a, g.grid, g.threads, g.smem, c.stream, pdl)
-                              : bq_internal_multi_launch_q4_0(a, g.grid, g.threads, g.smem, c.stream, pdl);
+            const int e = bq::fmt_multi_launch(c.qtype, a, g.grid, g.threads, g.smem, c.stream, pdl);
             return from_cuda(e);
         }
         // The streaming kernel stages the whole input in shared memory for a
@@ -795,15 +812,15 @@ bq_status run_gemv(const GemvCall &c) {
     }
     LaunchPlan p;
     bq::plan_gemv(c, &p);
-    const int e = c.qtype == BQ_Q8_0 ? bq_internal_launch_q8_0(c, p) : bq_internal_launch_q4_0(c, p);
+    const int e = bq::fmt_generic_launch(c, p);
     return from_cuda(e);
 }
 
 bq_status gemv_common(int qtype, const void *Wq, const float *x, float *y, int R, int64_t M,
                       int64_t K, void *stream, const float *bias = nullptr) {
-    if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0) return BQ_ERR_QTYPE;
+    if (!bq::known_qtype(qtype)) return BQ_ERR_QTYPE;
     if (R < 1 || R > BQ_VERIFY_MAX_ROWS) return BQ_ERR_SHAPE;
-    bq_status s = check_shape(M, K);
+    bq_status s = check_shape(qtype, M, K);
     if (s != BQ_OK) return s;
     if (M == 0) return BQ_OK;  // empty product: nothing is read or written
     if (!Wq || !x || !y) return BQ_ERR_NULL;
@@ -824,9 +841,9 @@ const char *bq_status_str(int status) {
     switch (status) {
         case BQ_OK: return "ok";
         case BQ_ERR_NULL: return "a required pointer is NULL";
-        case BQ_ERR_SHAPE: return "shape outside the supported range (M >= 0, K % 32 == 0, 32 <= K <= 2^18, 1 <= R <= 6)";
+        case BQ_ERR_SHAPE: return "shape outside the supported range (M >= 0, K % 32 == 0 (Q4_K: K % 256 == 0), 32 <= K <= 2^18, 1 <= R <= 6)";
         case BQ_ERR_ALIGN: return "pointer misaligned (packed weights and fp32 inputs need 16 bytes, outputs 4)";
-        case BQ_ERR_QTYPE: return "unknown quantization type (BQ_Q8_0 = 8, BQ_Q4_0 = 2)";
+        case BQ_ERR_QTYPE: return "unknown quantization type (BQ_Q8_0 = 8, BQ_Q4_0 = 2, BQ_Q4_K = 12)";
         case BQ_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
         case BQ_ERR_DEVICE: return "a kernel recorded a device-side error (bounded wait ran out)";
         default: return "unknown status";
@@ -835,7 +852,7 @@ const char *bq_status_str(int status) {
 
 int64_t bq_packed_bytes(int qtype, int64_t M, int64_t K) {
     const int bb = bq::block_bytes(qtype);
-    if (bb < 0 || M < 0 || K < 0 || K % 32) return -1;
+    if (bb < 0 || M < 0 || K < 0 || K % bq::k_step(qtype)) return -1;
     return M * (K / 32) * bb;
 }
 
@@ -845,8 +862,8 @@ int bq_tree_lanes(int64_t K) {
 }
 
 bq_status bq_quantize_pack(int qtype, const float *W, int64_t M, int64_t K, void *Wq, void *stream) {
-    if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0) return BQ_ERR_QTYPE;
-    bq_status s = check_shape(M, K);
+    if (!bq::known_qtype(qtype)) return BQ_ERR_QTYPE;
+    bq_status s = check_shape(qtype, M, K);
     if (s != BQ_OK) return s;
     if (M == 0) return BQ_OK;
     if (!W || !Wq) return BQ_ERR_NULL;
@@ -860,6 +877,10 @@ bq_status bq_gemv_q8_0(const void *Wq, const float *x, float *y, int64_t M, int6
 
 bq_status bq_gemv_q4_0(const void *Wq, const float *x, float *y, int64_t M, int64_t K, void *stream) {
     return gemv_common(BQ_Q4_0, Wq, x, y, 1, M, K, stream);
+}
+
+bq_status bq_gemv_q4_k(const void *Wq, const float *x, float *y, int64_t M, int64_t K, void *stream) {
+    return gemv_common(BQ_Q4_K, Wq, x, y, 1, M, K, stream);
 }
 
 bq_status bq_gemv_qkv_bias(int qtype, const void *Wqkv, const float *x, const float *bias, float *y,
@@ -883,8 +904,8 @@ bq_status bq_gemv_verify(int qtype, const void *Wq, const float *X, float *Y, in
 bq_status bq_gemv_gate_up_silu(int qtype, const void *Wg, const void *Wu, const float *x,
                                const float *gamma, float eps, float *y, int64_t M, int64_t K,
                                void *stream) {
-    if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0) return BQ_ERR_QTYPE;
-    bq_status s = check_shape(M, K);
+    if (!bq::known_qtype(qtype)) return BQ_ERR_QTYPE;
+    bq_status s = check_shape(qtype, M, K);
     if (s != BQ_OK) return s;
     if (gamma && !(std::isfinite(eps) && eps >= 0.0f)) return BQ_ERR_SHAPE;
     if (M == 0) return BQ_OK;
@@ -914,7 +935,7 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
                                 int64_t workspace_bytes, bq_stream_plan **plan) {
     if (!plan) return BQ_ERR_NULL;
     *plan = nullptr;
-    if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0) return BQ_ERR_QTYPE;
+    if (!bq::known_qtype(qtype)) return BQ_ERR_QTYPE;
     if (!ops || !workspace) return BQ_ERR_NULL;
     if (n_ops < 1) return BQ_ERR_SHAPE;
     if (!aligned_ok(workspace, 256)) return BQ_ERR_ALIGN;
@@ -1006,21 +1027,15 @@ bq_status bq_stream_plan_launch(const bq_stream_plan *plan, void *stream) {
     if (!plan) return BQ_ERR_NULL;
     if (plan->multi) {
         const int pdl = bq::tunables().plan_pdl;
-        const int e = plan->qtype == BQ_Q8_0
-                          ? bq_internal_multi_launch_q8_0(plan->margs, plan->grid, plan->threads,
-                                                          plan->smem, stream, pdl)
-                          : bq_internal_multi_launch_q4_0(plan->margs, plan->grid, plan->threads,
-                                                          plan->smem, stream, pdl);
+        const int e = bq::fmt_multi_launch(plan->qtype, plan->margs, plan->grid, plan->threads,
+                                           plan->smem, stream, pdl);
         return from_cuda(e);
     }
     auto s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(plan->counters, 0, (size_t)plan->n_stages * 4, s) != cudaSuccess)
         return BQ_ERR_CUDA;
-    const int e = plan->qtype == BQ_Q8_0
-                      ? bq_internal_exec_launch_q8_0(plan->args, plan->grid, plan->threads,
-                                                     plan->smem, stream)
-                      : bq_internal_exec_launch_q4_0(plan->args, plan->grid, plan->threads,
-                                                     plan->smem, stream);
+    const int e = bq::fmt_exec_launch(plan->qtype, plan->args, plan->grid, plan->threads,
+                                      plan->smem, stream);
     return from_cuda(e);
 }
 
@@ -1106,9 +1121,8 @@ bq_status bq_stream_plan_tune(bq_stream_plan *plan, int rounds, void *stream) {
         std::fill(d.begin(), d.end(), 0.0);
         for (int k = 0; k < REPS; ++k) {
             if (cudaMemsetAsync(plan->cta_ns, 0, (size_t)grid * 8, s) != cudaSuccess) return BQ_ERR_CUDA;
-            const int e = plan->qtype == BQ_Q8_0
-                              ? bq_internal_multi_launch_q8_0(a, grid, plan->threads, plan->smem, stream, 0)
-                              : bq_internal_multi_launch_q4_0(a, grid, plan->threads, plan->smem, stream, 0);
+            const int e = bq::fmt_multi_launch(plan->qtype, a, grid, plan->threads, plan->smem,
+                                               stream, 0);
             if (e != 0) return BQ_ERR_CUDA;
             if (cudaMemcpyAsync(ns.data(), plan->cta_ns, (size_t)grid * 8, cudaMemcpyDeviceToHost, s) !=
                     cudaSuccess ||
@@ -1140,10 +1154,11 @@ bq_status bq_stream_plan_tune(bq_stream_plan *plan, int rounds, void *stream) {
 bq_status bq_device_status(unsigned int *flags, int clear) {
     if (!flags) return BQ_ERR_NULL;
     if (cudaDeviceSynchronize() != cudaSuccess) return BQ_ERR_CUDA;
-    unsigned int a = 0, b = 0;
+    unsigned int a = 0, b = 0, c = 0;
     if (bq_internal_status_q8_0(&a, clear) != 0) return BQ_ERR_CUDA;
     if (bq_internal_status_q4_0(&b, clear) != 0) return BQ_ERR_CUDA;
-    *flags = a | b;
+    if (bq_internal_status_q4_k(&c, clear) != 0) return BQ_ERR_CUDA;
+    *flags = a | b | c;
     return *flags ? BQ_ERR_DEVICE : BQ_OK;
 }
 

@@ -29,6 +29,7 @@ namespace bq {
 
 constexpr int QT_Q4_0 = 2;
 constexpr int QT_Q8_0 = 8;
+constexpr int QT_Q4_K = 12;
 
 template <int QT> struct Fmt;
 template <> struct Fmt<QT_Q8_0> {
@@ -39,6 +40,13 @@ template <> struct Fmt<QT_Q8_0> {
 template <> struct Fmt<QT_Q4_0> {
     static constexpr int block_bytes = 18;
     static constexpr int unit_bytes = 144;  // 8 blocks = 9 x 16 B
+    static constexpr int unit_words = 36;
+};
+// Q4_K: the unit is one super-block of 256 weights (144 B = 9 x 16 B); its
+// bytes per 32 weights (18) are given as block_bytes for size arithmetic only
+template <> struct Fmt<QT_Q4_K> {
+    static constexpr int block_bytes = 18;
+    static constexpr int unit_bytes = 144;
     static constexpr int unit_words = 36;
 };
 
@@ -89,6 +97,10 @@ __host__ __device__ constexpr int x_pos(int e) { return 4 * x_chunk_pos(e >> 2) 
 struct XSmem {
     const float *base;
     int rstride;  // floats between rows
+    // Q4_K: the staged 32-element block sums of x (xblock_sum), block k of
+    // row r at sums[r * sstride + k]; unused by the other formats
+    const float *sums = nullptr;
+    int sstride = 0;
     // Step t of block B of the view sits at p[t ^ B] + 32 B floats: with
     // c0 = e0 / 4 (a multiple of 8) the chunk of (B, t) is at position
     // c0 + 8B + (t ^ B ^ key), key = (c0 >> 3 ^ c0 >> 6) & 7, when e0 is a
@@ -98,9 +110,13 @@ struct XSmem {
     struct View {
         const float *p[8];
         int rstride;
+        const float *s;
+        int sstride;
         __device__ __forceinline__ float4 get(int r, int B, int t) const {
             return *reinterpret_cast<const float4 *>(p[(t ^ B) & 7] + r * rstride + 32 * B);
         }
+        // the staged sum of block B of the view (Q4_K)
+        __device__ __forceinline__ float bsum(int r, int B) const { return s[r * sstride + B]; }
     };
     __device__ __forceinline__ View at(int e0) const {
         const int c0 = e0 >> 2;
@@ -109,11 +125,30 @@ struct XSmem {
 #pragma unroll
         for (int j = 0; j < 8; ++j) v.p[j] = base + (k0 ^ (4 * j));
         v.rstride = rstride;
+        v.s = sums + (e0 >> 5);
+        v.sstride = sstride;
         return v;
     }
 };
 // floats of shared memory one staged x of K elements takes (K rounded up to 128 B)
 __host__ __device__ constexpr int x_padded_floats(int K) { return (K + 31) / 32 * 32; }
+
+// The sum of the 32 x elements of block B of a view, in a fixed order that
+// every kernel shares: u_i = x[i] + x[4+i] + ... + x[28+i] in order (i = 0..3),
+// then (u_0 + u_1) + (u_2 + u_3).  Q4_K subtracts dmin*m times this sum per
+// sub-block; staged x computes it once per CTA, global x recomputes it inline,
+// and both give the same bits.
+template <class XV>
+__device__ __forceinline__ float xblock_sum(const XV &xv, int r, int B) {
+    float2 u01 = make_float2(-0.0f, -0.0f), u23 = make_float2(-0.0f, -0.0f);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const float4 v = xv.get(r, B, t);
+        u01 = __fadd2_rn(u01, make_float2(v.x, v.y));
+        u23 = __fadd2_rn(u23, make_float2(v.z, v.w));
+    }
+    return __fadd_rn(__fadd_rn(u01.x, u01.y), __fadd_rn(u23.x, u23.y));
+}
 
 // x read from global memory (through L1)
 struct XGlobal {
@@ -125,6 +160,7 @@ struct XGlobal {
         __device__ __forceinline__ float4 get(int r, int B, int t) const {
             return __ldg(reinterpret_cast<const float4 *>(p + (size_t)r * K + 32 * B + 4 * t));
         }
+        __device__ __forceinline__ float bsum(int r, int B) const { return xblock_sum(*this, r, B); }
     };
     __device__ __forceinline__ View at(int e0) const { return View{x + e0, K}; }
 };
@@ -144,6 +180,7 @@ struct XGlobalNorm {
             return make_float4(__fmul_rn(__fmul_rn(v.x, rs), g.x), __fmul_rn(__fmul_rn(v.y, rs), g.y),
                                __fmul_rn(__fmul_rn(v.z, rs), g.z), __fmul_rn(__fmul_rn(v.w, rs), g.w));
         }
+        __device__ __forceinline__ float bsum(int r, int B) const { return xblock_sum(*this, r, B); }
     };
     __device__ __forceinline__ View at(int e0) const { return View{x + e0, gamma + e0, rs}; }
 };
@@ -273,11 +310,176 @@ __device__ __forceinline__ void block_dot(const uint32_t *const (&w)[NW], const 
         for (int r = 0; r < R; ++r) c[v][r] = __fmaf_rn(d[v], s[v][r], c[v][r]);
 }
 
+// ---------------------------------------------------------------------------
+// Q4_K: the unit is one super-block (256 weights, 144 bytes): fp16 d, fp16
+// dmin, 12 bytes of eight 6-bit sub-block scales sc_j and mins m_j, then 128
+// bytes of nibbles, sub-blocks 2g (low nibbles) and 2g+1 (high nibbles)
+// sharing bytes 32g..32g+31; w = d*sc_j*q - dmin*m_j (RunIT README kernel
+// table, gemv_q4k_f16, read with the public GGUF Q4_K layout).  The tree of
+// one unit, per weight set v and input row r:
+//   sub-block j: s_j = (a_0 + a_1) + (a_2 + a_3), a_i the in-order FMA chain
+//                over t = 0..7 of q[4t+i] * x[4t+i]   (q = 0..15, exact)
+//   cq = in-order FMA chain over j of (d*sc_j) * s_j
+//   cm = in-order FMA chain over j of (dmin*m_j) * xblock_sum_j
+//   c  = cq - cm
+// d*sc_j and dmin*m_j are exact in fp32 (an 11-bit by a 6-bit significand),
+// so the dequantization itself adds no rounding; the x block sums are shared
+// by every row.
+// ---------------------------------------------------------------------------
+constexpr float Q4K_MAGIC = 8388608.0f;  // 2^23: low nibble n -> 2^23 + n
+constexpr float Q4K_MAGIC_HI = 524288.0f;  // 2^19: a high nibble 16n -> 2^19 + n
+
+// sub-block scales d*sc_j and offsets dmin*m_j from a super-block's first 16 bytes
+__device__ __forceinline__ void q4k_scales(uint4 h, float (&D)[8], float (&Mn)[8]) {
+    const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFFu)));
+    const float dm = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+    const uint32_t sc_lo = h.y & 0x3F3F3F3Fu, mn_lo = h.z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
+    const uint32_t mn_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        D[k] = __fmul_rn(d, __uint2float_rn((sc_lo >> (8 * k)) & 0xFFu));
+        D[4 + k] = __fmul_rn(d, __uint2float_rn((sc_hi >> (8 * k)) & 0xFFu));
+        Mn[k] = __fmul_rn(dm, __uint2float_rn((mn_lo >> (8 * k)) & 0xFFu));
+        Mn[4 + k] = __fmul_rn(dm, __uint2float_rn((mn_hi >> (8 * k)) & 0xFFu));
+    }
+}
+
+// the scale and offset of sub-block j alone (j may differ between lanes)
+__device__ __forceinline__ void q4k_scale_of(uint4 h, int j, float &D, float &Mn) {
+    const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFFu)));
+    const float dm = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+    const int k = 8 * (j & 3);
+    const uint32_t y = h.y >> k, z = h.z >> k, w = h.w >> k;
+    const uint32_t sc = j < 4 ? (y & 63u) : ((w & 15u) | (((y >> 6) & 3u) << 4));
+    const uint32_t mn = j < 4 ? (z & 63u) : (((w >> 4) & 15u) | (((z >> 6) & 3u) << 4));
+    D = __fmul_rn(d, __uint2float_rn(sc));
+    Mn = __fmul_rn(dm, __uint2float_rn(mn));
+}
+
+// s[v][r] = sum over sub-block j's 32 elements of q * x, its codes in the
+// nibbles (low: hi == 0, high: hi == 1) of the 8 words wq[v][0..7] of its
+// byte pair group; x from block B of the view.  With the packed fp32x2 FMAs
+// each half is an IEEE fp32 fma, so the bits equal the scalar chains'.
+template <int NW, int R, class XV>
+__device__ __forceinline__ void q4k_sub_sum(const uint32_t (&wq)[NW][8], int hi, const XV &xv, int B,
+                                            float (&s)[NW][R]) {
+    const uint32_t mask = hi ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
+    const uint32_t magic = hi ? 0x49000000u : 0x4B000000u;
+    const float m = hi ? Q4K_MAGIC_HI : Q4K_MAGIC;
+    const float2 mneg = make_float2(-m, -m);
+    float2 a[NW][R][2];
+#pragma unroll
+    for (int v = 0; v < NW; ++v)
+#pragma unroll
+        for (int r = 0; r < R; ++r) a[v][r][0] = a[v][r][1] = make_float2(-0.0f, -0.0f);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        float4 xv4[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) xv4[r] = xv.get(r, B, t);
+#pragma unroll
+        for (int v = 0; v < NW; ++v) {
+            const uint32_t nib = wq[v][t] & mask;
+            const float2 q01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(nib, magic, 0x7540u)),
+                                                      __uint_as_float(__byte_perm(nib, magic, 0x7541u))),
+                                          mneg);
+            const float2 q23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(nib, magic, 0x7542u)),
+                                                      __uint_as_float(__byte_perm(nib, magic, 0x7543u))),
+                                          mneg);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                a[v][r][0] = __ffma2_rn(q01, make_float2(xv4[r].x, xv4[r].y), a[v][r][0]);
+                a[v][r][1] = __ffma2_rn(q23, make_float2(xv4[r].z, xv4[r].w), a[v][r][1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < NW; ++v)
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            s[v][r] = __fadd_rn(__fadd_rn(a[v][r][0].x, a[v][r][0].y),
+                                __fadd_rn(a[v][r][1].x, a[v][r][1].y));
+}
+
+// One super-block of NW weight sets against R input rows of the view at e0:
+// header(v) returns weight set v's first 16 bytes, pair(v, g, wq) fills the 8
+// words of its byte pair group g.
+template <int NW, int R, class XV, class Header, class Pair>
+__device__ __forceinline__ void q4k_unit(const XV &xv, Header header, Pair pair, float (&c)[NW][R]) {
+    float D[NW][8], Mn[NW][8], cq[NW][R], cm[NW][R];
+#pragma unroll
+    for (int v = 0; v < NW; ++v) {
+        q4k_scales(header(v), D[v], Mn[v]);
+#pragma unroll
+        for (int r = 0; r < R; ++r) cq[v][r] = cm[v][r] = -0.0f;
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        uint32_t wq[NW][8];
+#pragma unroll
+        for (int v = 0; v < NW; ++v) pair(v, g, wq[v]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float sj[NW][R];
+            q4k_sub_sum<NW, R>(wq, h, xv, 2 * g + h, sj);
+#pragma unroll
+            for (int v = 0; v < NW; ++v)
+#pragma unroll
+                for (int r = 0; r < R; ++r) cq[v][r] = __fmaf_rn(D[v][2 * g + h], sj[v][r], cq[v][r]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float sx = xv.bsum(r, j);
+#pragma unroll
+            for (int v = 0; v < NW; ++v) cm[v][r] = __fmaf_rn(Mn[v][j], sx, cm[v][r]);
+        }
+#pragma unroll
+    for (int v = 0; v < NW; ++v)
+#pragma unroll
+        for (int r = 0; r < R; ++r) c[v][r] = __fsub_rn(cq[v][r], cm[v][r]);
+}
+
+// the unit from words in registers (w[v][0..35], the unit's bytes little-endian)
+template <int NW, int R, class XS>
+__device__ __forceinline__ void q4k_unit_words(const uint32_t *const (&w)[NW], const XS &xs, int e0,
+                                               float (&c)[NW][R]) {
+    q4k_unit<NW, R>(
+        xs.at(e0), [&](int v) { return make_uint4(w[v][0], w[v][1], w[v][2], w[v][3]); },
+        [&](int v, int g, uint32_t (&wq)[8]) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) wq[t] = w[v][4 + 8 * g + t];
+        },
+        c);
+}
+
+// the unit from shared memory (up[v]: the unit's first byte, 16-byte aligned)
+template <int NR, int R, class XS>
+__device__ __forceinline__ void q4k_unit_rows(const uint8_t *const (&up)[NR], const XS &xs, int e0,
+                                              float (&c)[NR][R]) {
+    q4k_unit<NR, R>(
+        xs.at(e0), [&](int v) { return *reinterpret_cast<const uint4 *>(up[v]); },
+        [&](int v, int g, uint32_t (&wq)[8]) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(up[v] + 16 + 32 * g);
+            const uint4 b = *reinterpret_cast<const uint4 *>(up[v] + 32 + 32 * g);
+            wq[0] = a.x, wq[1] = a.y, wq[2] = a.z, wq[3] = a.w;
+            wq[4] = b.x, wq[5] = b.y, wq[6] = b.z, wq[7] = b.w;
+        },
+        c);
+}
+
 // One unit (nbk <= 8 blocks; w[v] holds the unit's bytes little-endian from
 // its start) against x elements from e0.  c[v][r] receives the unit partials.
 template <int QT, int NW, int R, class XS>
 __device__ __forceinline__ void unit_dot(const uint32_t *const (&w)[NW], int nbk, const XS &xs,
                                          int e0, float (&c)[NW][R]) {
+    if constexpr (QT == QT_Q4_K) {
+        q4k_unit_words<NW, R>(w, xs, e0, c);  // a super-block is always whole
+        return;
+    }
 #pragma unroll
     for (int v = 0; v < NW; ++v)
 #pragma unroll
@@ -334,6 +536,10 @@ __device__ __forceinline__ void rows_block(const uint8_t *const (&up)[NR], const
 template <int QT, int NR, int R, class XS>
 __device__ __forceinline__ void unit_dot_rows(const uint8_t *const (&up)[NR], const XS &xs, int e0,
                                               float (&c)[NR][R]) {
+    if constexpr (QT == QT_Q4_K) {
+        q4k_unit_rows<NR, R>(up, xs, e0, c);
+        return;
+    }
 #pragma unroll
     for (int v = 0; v < NR; ++v)
 #pragma unroll
@@ -409,9 +615,50 @@ __device__ __forceinline__ void load_block_realigned(uint32_t *w, const uint8_t 
 // the result (returned in lane 0 after fold_lanes) is bit-identical to the
 // unit-per-lane evaluation; the latency is that of nsc/4 blocks instead of
 // nsc/G units.
+// Q4_K rows block-parallel: lane 8j+b takes sub-block b of unit 4r+j (its
+// scale and offset, its 32 nibbles and its x block sum); the unit's two chains
+// cq and cm run over the 8 lanes in sub-block order with shuffles and
+// c = cq - cm, exactly q4k_unit's tree.
+template <class XS>
+__device__ __forceinline__ float row_dot_blockpar_q4k(const uint8_t *rowp, int nsc, int G,
+                                                      const XS &xs, int lane) {
+    const int j = lane >> 3, b = lane & 7;
+    float p = -0.0f;
+    for (int r4 = 0; r4 < nsc; r4 += 4) {
+        const int u = r4 + j;
+        float s[1][1] = {{0.0f}}, D = 0.0f, Mn = 0.0f, sx = 0.0f;
+        if (u < nsc) {
+            const uint8_t *sb = rowp + u * Fmt<QT_Q4_K>::unit_bytes;
+            q4k_scale_of(*reinterpret_cast<const uint4 *>(sb), b, D, Mn);
+            const uint4 a = *reinterpret_cast<const uint4 *>(sb + 16 + 32 * (b >> 1));
+            const uint4 c = *reinterpret_cast<const uint4 *>(sb + 32 + 32 * (b >> 1));
+            const uint32_t wq[1][8] = {{a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w}};
+            const auto xv = xs.at(256 * u + 32 * b);
+            q4k_sub_sum<1, 1>(wq, b & 1, xv, 0, s);
+            sx = xv.bsum(0, 0);
+        }
+        float cq = -0.0f, cm = -0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int src = (j << 3) + k;
+            cq = __fmaf_rn(__shfl_sync(0xffffffffu, D, src), __shfl_sync(0xffffffffu, s[0][0], src), cq);
+            cm = __fmaf_rn(__shfl_sync(0xffffffffu, Mn, src), __shfl_sync(0xffffffffu, sx, src), cm);
+        }
+        const float c = __fsub_rn(cq, cm);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const float cj = __shfl_sync(0xffffffffu, c, jj << 3);
+            const int uu = r4 + jj;
+            if (uu < nsc && lane < G && (uu & (G - 1)) == lane) p = __fadd_rn(p, cj);
+        }
+    }
+    return fold_lanes(p, G);
+}
+
 template <int QT, class XS>
 __device__ __forceinline__ float row_dot_blockpar(const uint8_t *rowp, int nsc, int G,
                                                   const XS &xs, int lane) {
+    if constexpr (QT == QT_Q4_K) return row_dot_blockpar_q4k(rowp, nsc, G, xs, lane);
     constexpr int UB = Fmt<QT>::unit_bytes, BB = Fmt<QT>::block_bytes;
     const int j = lane >> 3, b = lane & 7;
     float p = -0.0f;

@@ -61,16 +61,19 @@ struct ExecOp {
     unsigned char G, rpw, nmat, single;  // rpw: rows per tile
     int nsc;
     int rowmode;              // 1: a tile is rpw whole rows, each evaluated by the whole warp
-    int pad[2];               // to a multiple of 16 bytes (see below)
+    int soff;                 // Q4_K: float offset of x's block sums in the x area
+    int pad;                  // to a multiple of 16 bytes (see below)
 };
 
-// one distinct input vector of a stage (RMSNorm-ed when gamma is set); 32 bytes
+// one distinct input vector of a stage (RMSNorm-ed when gamma is set); 48 bytes
 struct ExecX {
     const float *x;
     const float *gamma;
     float eps;
     int K, off;  // off: float offset in the x area
     int goff;    // float offset of the gain's staged copy (gamma set), else -1
+    int soff;    // Q4_K: float offset of the 32-element block sums, else -1
+    int pad[3];
 };
 
 // 32 bytes
@@ -151,7 +154,9 @@ __device__ __forceinline__ void exec_load_x(const ExecStage &st, const ExecX *xs
 
 // One warp RMSNorms the stage's inputs that have a gain, in place.  The RMS
 // scale uses the fixed tree of rms_scale() (lane L holds the 256-virtual-lane
-// sums 8L..8L+7), so xn matches the single-op kernels bit for bit.
+// sums 8L..8L+7), so xn matches the single-op kernels bit for bit.  Q4_K:
+// then the 32-element block sums of every input (xblock_sum's order).
+template <int QT>
 __device__ __forceinline__ void exec_norm_x_warp(const ExecStage &st, const ExecX *xs, float *xa,
                                                  int lane) {
     for (int j = st.x_begin; j < st.x_end; ++j) {
@@ -180,6 +185,14 @@ __device__ __forceinline__ void exec_norm_x_warp(const ExecStage &st, const Exec
             const float4 g = *reinterpret_cast<const float4 *>(xa + xd.goff + 4 * c);
             *p = make_float4(__fmul_rn(__fmul_rn(x4.x, rs), g.x), __fmul_rn(__fmul_rn(x4.y, rs), g.y),
                              __fmul_rn(__fmul_rn(x4.z, rs), g.z), __fmul_rn(__fmul_rn(x4.w, rs), g.w));
+        }
+        __syncwarp();
+    }
+    if constexpr (QT == QT_Q4_K) {
+        for (int j = st.x_begin; j < st.x_end; ++j) {
+            const ExecX &xd = xs[j];
+            const XSmem x0{xa + xd.off, 0};
+            for (int b = lane; b < xd.K / 32; b += 32) xa[xd.soff + b] = xblock_sum(x0.at(32 * b), 0, 0);
         }
         __syncwarp();
     }
@@ -398,7 +411,7 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
                 ok = false;
                 break;
             }
-            exec_norm_x_warp(st, T.xs, xbuf(s), lane);
+            exec_norm_x_warp<QT>(st, T.xs, xbuf(s), lane);
             if (lane == 0) mbar_arrive(xready + b);
         }
         const float *xa = xbuf(s);
@@ -437,7 +450,7 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
                 p0 = -0.0f;
                 p1 = -0.0f;
             }
-            const XSmem xs{xa + op.xoff, 0};
+            const XSmem xs{xa + op.xoff, 0, xa + op.soff, 0};
             if (op.rowmode) {
                 // rows of this tile one by one, each by the whole warp; lane r
                 // keeps row r's gate value between the two matrices of gate+up

@@ -39,8 +39,10 @@ void plan_gemv(const GemvCall &c, LaunchPlan *p);
 // per-format generic launchers (one translation unit each) and their device status words
 int bq_internal_launch_q8_0(const bq::GemvCall &c, const bq::LaunchPlan &p);
 int bq_internal_launch_q4_0(const bq::GemvCall &c, const bq::LaunchPlan &p);
+int bq_internal_launch_q4_k(const bq::GemvCall &c, const bq::LaunchPlan &p);
 int bq_internal_status_q8_0(unsigned int *flags, int clear);
 int bq_internal_status_q4_0(unsigned int *flags, int clear);
+int bq_internal_status_q4_k(unsigned int *flags, int clear);
 int bq_internal_pack(int qtype, const float *W, long long M, long long K, void *Wq, void *stream);
 // the fp16-weight GEMV (bq_f16.cu), arguments validated by the caller
 int bq_internal_f16_launch(const void *W, const float *x, float *y, long long M, long long K,
@@ -88,16 +90,45 @@ bool tunables_multi();
 }
 // per-format occupancy and launch of the multi-op kernel instance (nr, R);
 // `pdl` allows programmatic dependent launch (single calls)
-int bq_internal_multi_occupancy_q8_0(int nr, int R, int threads, size_t smem, int *occ);
-int bq_internal_multi_occupancy_q4_0(int nr, int R, int threads, size_t smem, int *occ);
-int bq_internal_multi_launch_q8_0(const bq::MultiArgs &a, int grid, int threads, size_t smem,
-                                  void *stream, int pdl);
-int bq_internal_multi_launch_q4_0(const bq::MultiArgs &a, int grid, int threads, size_t smem,
-                                  void *stream, int pdl);
-// persistent per-token stream executor (bq_exec.cuh), one instantiation per format
-int bq_internal_exec_occupancy_q8_0(int threads, size_t smem, int *occ);
-int bq_internal_exec_occupancy_q4_0(int threads, size_t smem, int *occ);
-int bq_internal_exec_launch_q8_0(const bq::ExecArgs &a, int grid, int threads, size_t smem,
-                                 void *stream);
-int bq_internal_exec_launch_q4_0(const bq::ExecArgs &a, int grid, int threads, size_t smem,
-                                 void *stream);
+#define BQ_FORMAT_DECLS(FMT)                                                                       \
+    int bq_internal_multi_occupancy_##FMT(int nr, int R, int threads, size_t smem, int *occ);      \
+    int bq_internal_multi_launch_##FMT(const bq::MultiArgs &a, int grid, int threads, size_t smem, \
+                                       void *stream, int pdl);                                     \
+    int bq_internal_exec_occupancy_##FMT(int threads, size_t smem, int *occ);                      \
+    int bq_internal_exec_launch_##FMT(const bq::ExecArgs &a, int grid, int threads, size_t smem,   \
+                                      void *stream);
+// (the persistent per-token stream executor is bq_exec.cuh, one instance per format)
+BQ_FORMAT_DECLS(q8_0)
+BQ_FORMAT_DECLS(q4_0)
+BQ_FORMAT_DECLS(q4_k)
+
+// dispatch on the format (qtype already validated: BQ_Q8_0, BQ_Q4_0 or BQ_Q4_K)
+namespace bq {
+inline int fmt_generic_launch(const GemvCall &c, const LaunchPlan &p) {
+    return c.qtype == BQ_Q8_0 ? bq_internal_launch_q8_0(c, p)
+           : c.qtype == BQ_Q4_0 ? bq_internal_launch_q4_0(c, p)
+                                : bq_internal_launch_q4_k(c, p);
+}
+inline int fmt_multi_occupancy(int qt, int nr, int R, int threads, size_t smem, int *occ) {
+    return qt == BQ_Q8_0 ? bq_internal_multi_occupancy_q8_0(nr, R, threads, smem, occ)
+           : qt == BQ_Q4_0 ? bq_internal_multi_occupancy_q4_0(nr, R, threads, smem, occ)
+                           : bq_internal_multi_occupancy_q4_k(nr, R, threads, smem, occ);
+}
+inline int fmt_multi_launch(int qt, const MultiArgs &a, int grid, int threads, size_t smem,
+                            void *stream, int pdl) {
+    return qt == BQ_Q8_0 ? bq_internal_multi_launch_q8_0(a, grid, threads, smem, stream, pdl)
+           : qt == BQ_Q4_0 ? bq_internal_multi_launch_q4_0(a, grid, threads, smem, stream, pdl)
+                           : bq_internal_multi_launch_q4_k(a, grid, threads, smem, stream, pdl);
+}
+inline int fmt_exec_occupancy(int qt, int threads, size_t smem, int *occ) {
+    return qt == BQ_Q8_0 ? bq_internal_exec_occupancy_q8_0(threads, smem, occ)
+           : qt == BQ_Q4_0 ? bq_internal_exec_occupancy_q4_0(threads, smem, occ)
+                           : bq_internal_exec_occupancy_q4_k(threads, smem, occ);
+}
+inline int fmt_exec_launch(int qt, const ExecArgs &a, int grid, int threads, size_t smem,
+                           void *stream) {
+    return qt == BQ_Q8_0 ? bq_internal_exec_launch_q8_0(a, grid, threads, smem, stream)
+           : qt == BQ_Q4_0 ? bq_internal_exec_launch_q4_0(a, grid, threads, smem, stream)
+                           : bq_internal_exec_launch_q4_k(a, grid, threads, smem, stream);
+}
+}  // namespace bq

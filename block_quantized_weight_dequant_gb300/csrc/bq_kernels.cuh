@@ -62,7 +62,23 @@ __global__ void __launch_bounds__(GENERIC_WARPS * 32) generic_kernel(const Gener
             for (int u = l; u < nsc; u += G) {
                 const int nbk = min(8, nb - 8 * u);
                 const size_t off = (size_t)row * a.rb + (size_t)u * UB;
-                if constexpr (MODE == MODE_GATE_UP) {
+                if constexpr (QT == QT_Q4_K) {
+                    // super-blocks are 16-byte aligned: read them in place
+                    // (header, then one byte pair group at a time)
+                    if constexpr (MODE == MODE_GATE_UP) {
+                        const uint8_t *const up[2] = {a.W0 + off, a.W1 + off};
+                        float cc[2][1];
+                        unit_dot_rows<QT, 2, 1>(up, xs, 256 * u, cc);
+                        p[0] = __fadd_rn(p[0], cc[0][0]);
+                        p[1] = __fadd_rn(p[1], cc[1][0]);
+                    } else {
+                        const uint8_t *const up[1] = {a.W0 + off};
+                        float cc[1][R];
+                        unit_dot_rows<QT, 1, R>(up, xs, 256 * u, cc);
+#pragma unroll
+                        for (int r = 0; r < R; ++r) p[r] = __fadd_rn(p[r], cc[0][r]);
+                    }
+                } else if constexpr (MODE == MODE_GATE_UP) {
                     uint32_t wg[Fmt<QT>::unit_words], wu[Fmt<QT>::unit_words];
                     load_unit_global<QT>(wg, a.W0 + off, nbk);
                     load_unit_global<QT>(wu, a.W1 + off, nbk);

@@ -83,6 +83,11 @@ constexpr int MULTI_MAX_WARPS = 16;
 __host__ __device__ constexpr int multi_max_warps(int QT, int R) {
     return R > 1 ? 8 : QT == 8 ? 12 : MULTI_MAX_WARPS;
 }
+// floats after the R input rows of an x buffer that hold the rows' 32-element
+// block sums (Q4_K; none for the other formats), rounded to 128 bytes
+__host__ __device__ constexpr int multi_sum_floats(int QT, int R, int rstride) {
+    return QT == QT_Q4_K ? (R * (rstride / 32) + 31) / 32 * 32 : 0;
+}
 static_assert(MULTI_MAX_WARPS * 32 <= 1024, "one CTA");
 constexpr int MULTI_MAX_D = 4;
 // shared memory header: mbarriers [0, 512), inline op [512, 768), reduction
@@ -417,7 +422,21 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                 }
                 sync();
             }
-            const XSmem xs{xa, a.x_rstride};
+            // Q4_K: the phase's 32-element x block sums, once per CTA, after
+            // the input rows in the buffer (the planner sized it for them)
+            float *xsums = xa + R * a.x_rstride;
+            const int sstride = a.x_rstride / 32;
+            if constexpr (QT == QT_Q4_K) {
+                const int kcount = PU ? min(K - pn * PU * 256, PU * 256) : K;
+                const int nblk = kcount / 32;
+                const XSmem x0{xa, a.x_rstride};
+                for (int i = threadIdx.x; i < R * nblk; i += nthr) {
+                    const int r = i / nblk, b = i - r * nblk;
+                    xsums[r * sstride + b] = xblock_sum(x0.at(32 * b), r, 0);
+                }
+                sync();
+            }
+            const XSmem xs{xa, a.x_rstride, xsums, sstride};
             const int k0u = pn * PU;  // first unit of the panel
             const int c_lo = PU ? k0u / KCU : 0;
             const int c_hi = PU ? min(nchunks, (k0u + PU) / KCU) : nchunks;

@@ -36,7 +36,7 @@ constexpr size_t SCRATCH_BYTES = OFF_CNT + al256((size_t)MAX_OPS * sizeof(unsign
 // code this name is only a stand-in for the symbol; the kernel gets the
 // device address fetched by scratch_address().
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SCRATCH_BYTES];
-static_assert(SCRATCH_BYTES == 74 * 1024, "the documented size of the scratch array");
+static_assert(SCRATCH_BYTES == 82 * 1024, "the documented size of the scratch array");
 // the same array holds the multi-op kernel's tables for independent op lists
 constexpr size_t OFF_CT = al256((size_t)MAX_OPS * sizeof(bq::MultiOp));
 static_assert(OFF_CT + (bq::MULTI_MAX_CTAS + 1) * sizeof(int) <= SCRATCH_BYTES,
@@ -83,7 +83,7 @@ cudaError_t device_setup(int *dev_out) {
 }  // namespace
 
 extern "C" bq_status bq_stream_run_noalloc(int qtype, const bq_op *ops, int n_ops, void *stream) {
-    if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0) return BQ_ERR_QTYPE;
+    if (qtype != BQ_Q8_0 && qtype != BQ_Q4_0 && qtype != BQ_Q4_K) return BQ_ERR_QTYPE;
     if (!ops) return BQ_ERR_NULL;
     if (n_ops < 1 || n_ops > MAX_OPS) return BQ_ERR_SHAPE;
     auto s = static_cast<cudaStream_t>(stream);
@@ -118,9 +118,7 @@ extern "C" bq_status bq_stream_run_noalloc(int qtype, const bq_op *ops, int n_op
         bq::MultiArgs ma;
         bq::fill_multi_args(mg, n_ops, reinterpret_cast<const bq::MultiOp *>(scratch),
                             reinterpret_cast<const int *>(scratch + OFF_CT), &ma);
-        const int e = qtype == BQ_Q8_0
-                          ? bq_internal_multi_launch_q8_0(ma, mg.grid, mg.threads, mg.smem, stream, 0)
-                          : bq_internal_multi_launch_q4_0(ma, mg.grid, mg.threads, mg.smem, stream, 0);
+        const int e = bq::fmt_multi_launch(qtype, ma, mg.grid, mg.threads, mg.smem, stream, 0);
         return e == 0 ? BQ_OK : BQ_ERR_CUDA;
     }
     const bool copied =
@@ -140,8 +138,6 @@ extern "C" bq_status bq_stream_run_noalloc(int qtype, const bq_op *ops, int n_op
                        reinterpret_cast<const bq::ExecX *>(scratch + OFF_X),
                        reinterpret_cast<const bq::ExecStage *>(scratch + OFF_ST),
                        reinterpret_cast<unsigned int *>(scratch + OFF_CNT), &a);
-    const int e = qtype == BQ_Q8_0
-                      ? bq_internal_exec_launch_q8_0(a, geo.grid, geo.threads, geo.smem, stream)
-                      : bq_internal_exec_launch_q4_0(a, geo.grid, geo.threads, geo.smem, stream);
+    const int e = bq::fmt_exec_launch(qtype, a, geo.grid, geo.threads, geo.smem, stream);
     return e == 0 ? BQ_OK : BQ_ERR_CUDA;
 }

@@ -1,4 +1,5 @@
-// bq_pack.cu -- fp32 weights -> packed Q8_0 / Q4_0 blocks on the GPU.
+// bq_pack.cu -- fp32 weights -> packed Q8_0 / Q4_0 blocks and Q4_K
+// super-blocks on the GPU.
 //
 // One warp per 32-weight block: lane j owns weight j.  The scale and codes
 // follow the block definitions exactly, with IEEE fp32 operations only:
@@ -55,9 +56,104 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ W, 
     }
 }
 
+// Q4_K: one warp per super-block of 256 weights, lane L holding element L of
+// each of the 8 sub-blocks.  The reading of the GGUF Q4_K packer (the pages
+// name Q4_K_M without defining it), fp32 IEEE operations only:
+//   sub-block j: lo = min(0, min w), hi = max w, scale_j = (hi - lo) / 15,
+//                min_j = -lo
+//   d = fp16_rne(max_j scale_j / 63), dmin = fp16_rne(max_j min_j / 63), both
+//       +0 when every term is zero
+//   sc_j = clamp(round(scale_j / d), 0, 63), m_j = clamp(round(min_j / dmin), 0, 63)
+//       (0 when the divisor is 0)
+//   q = clamp(round((w + dmin*m_j) / (d*sc_j)), 0, 15)  (0 when d*sc_j is 0)
+// round = half away from zero.  The sign of a zero lo, hi or scale never
+// reaches the bytes: the super-block maxima keep +0 unless a term is positive.
+__global__ void __launch_bounds__(256) pack_q4k_kernel(const float *__restrict__ W, long long M,
+                                                       long long K, uint8_t *__restrict__ out) {
+    const long long ns = K / 256;
+    const long long total = M * ns;
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long sbi = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); sbi < total;
+         sbi += warps) {
+        const long long m = sbi / ns, b = sbi % ns;
+        const float *src = W + m * K + 256 * b;
+        float w[8], scale[8], mins[8];
+        float smax = 0.0f, mmax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            w[j] = src[32 * j + lane];
+            float lo = w[j], hi = w[j];
+            for (int o = 16; o > 0; o >>= 1) {
+                lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+                hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+            }
+            lo = fminf(lo, 0.0f);
+            scale[j] = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+            mins[j] = -lo;
+            if (scale[j] > smax) smax = scale[j];
+            if (mins[j] > mmax) mmax = mins[j];
+        }
+        const __half dh = __float2half_rn(__fdiv_rn(smax, 63.0f));
+        const __half mh = __float2half_rn(__fdiv_rn(mmax, 63.0f));
+        const float d = __half2float(dh), dmin = __half2float(mh);
+        int sc[8], mn[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            sc[j] = d != 0.0f ? (int)fminf(fmaxf(roundf(__fdiv_rn(scale[j], d)), 0.0f), 63.0f) : 0;
+            mn[j] = dmin != 0.0f ? (int)fminf(fmaxf(roundf(__fdiv_rn(mins[j], dmin)), 0.0f), 63.0f) : 0;
+        }
+        uint8_t *dst = out + sbi * 144;
+        if (lane < 16) {
+            // lane k writes header byte k
+            uint32_t v;
+            if (lane < 4) {
+                const unsigned short bits = __half_as_ushort(lane < 2 ? dh : mh);
+                v = (lane & 1) ? bits >> 8 : bits & 0xFFu;
+            } else if (lane < 8) {
+                const int j = lane - 4;
+                v = (uint32_t)(sc[j] | ((sc[j + 4] >> 4) << 6));
+            } else if (lane < 12) {
+                const int j = lane - 8;
+                v = (uint32_t)(mn[j] | ((mn[j + 4] >> 4) << 6));
+            } else {
+                const int j = lane - 12;
+                v = (uint32_t)((sc[j + 4] & 15) | ((mn[j + 4] & 15) << 4));
+            }
+            dst[lane] = (uint8_t)v;
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            int q[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = 2 * g + h;
+                const float D = __fmul_rn(d, (float)sc[j]), Mf = __fmul_rn(dmin, (float)mn[j]);
+                q[h] = D != 0.0f
+                           ? (int)fminf(fmaxf(roundf(__fdiv_rn(__fadd_rn(w[j], Mf), D)), 0.0f), 15.0f)
+                           : 0;
+            }
+            dst[16 + 32 * g + lane] = (uint8_t)(q[0] | (q[1] << 4));
+        }
+    }
+}
+
 }  // namespace
 
 int bq_internal_pack(int qtype, const float *W, long long M, long long K, void *Wq, void *stream) {
+    if (qtype == 12) {
+        const long long sbs = M * (K / 256);
+        if (sbs == 0) return 0;
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return (int)e;
+        long long grid = (sbs + 7) / 8;
+        if (grid > (long long)sms * 16) grid = (long long)sms * 16;
+        pack_q4k_kernel<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+            W, M, K, static_cast<uint8_t *>(Wq));
+        return (int)cudaGetLastError();
+    }
     const long long blocks = M * (K / 32);
     if (blocks == 0) return 0;
     int dev = 0, sms = 0;

@@ -70,6 +70,10 @@ Q7B = dict(name="7b-shaped q4_0 token stream", qtype="q4_0", layers=28, hidden=3
                  ("gate", 18944, 3584), ("up", 18944, 3584), ("down", 3584, 18944)],
            lm_head=(152064, 3584))
 
+# 3k. the same 7B-shaped stream in the Q4_K super-block format (the RunIT
+# README's Q4_K_M row; 0.5625 B per weight like Q4_0)
+Q7B_K = dict(Q7B, name="7b-shaped q4_k token stream", qtype="q4_k")
+
 # 4. RMSNorm input + gate/up + SiLU, Q8_0, 28 rotated pairs
 CFG4 = dict(name="rmsnorm+gate_up_silu q8_0 3072x1024 x28", qtype="q8_0", M=3072, K=1024,
             pairs=28, eps=1e-6, gamma_mean=1.0, gamma_std=0.1)

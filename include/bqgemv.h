@@ -17,8 +17,19 @@
  *            w = d * q.
  *      Q4_0, 18 bytes: fp16 scale d then 16 bytes qs; element j < 16 is the
  *            low nibble of qs[j], element j + 16 the high nibble; w = d*(n-8).
- *  - A packed matrix with M rows and K columns is M rows of K/32 blocks, rows
- *    contiguous with no padding: row m starts at byte m * (K/32) * {34, 18}.
+ *      Q4_K, 144 bytes per 256 weights (a super-block; the RunIT README's
+ *            kernel table names gemv_q4k_f16 and its "Quantization" table
+ *            Q4_K_M; the layout is read from the public GGUF definition):
+ *            fp16 d, fp16 dmin, 12 bytes of eight 6-bit sub-block scales
+ *            sc[j] and mins m[j] (j < 4: sc = s[j] & 63, m = s[j+4] & 63;
+ *            j >= 4: sc = (s[j+4] & 15) | (s[j-4] >> 6) << 4,
+ *            m = (s[j+4] >> 4) | (s[j] >> 6) << 4), then 128 bytes qs where
+ *            element i of sub-block 2g is the low nibble of qs[32g+i] and
+ *            element i of sub-block 2g+1 its high nibble;
+ *            w = d*sc[j]*q - dmin*m[j] for sub-block j (32 weights).
+ *  - A packed matrix with M rows and K columns is M rows of K/32 blocks (Q4_K:
+ *    K/256 super-blocks), rows contiguous with no padding: row m starts at
+ *    byte m * (K/32) * {34, 18, 18} (Q8_0, Q4_0, Q4_K).
  *
  * Conventions for every call below:
  *  - All data pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA memory)
@@ -33,7 +44,8 @@
  *    synchronisation, as with any CUDA library.  No call aborts or throws.
  *  - Outputs are overwritten, never accumulated into.  Inputs and outputs
  *    must not overlap.
- *  - Shapes: 0 <= M <= 2^31 - 1, K a multiple of 32, 32 <= K <= 2^18.
+ *  - Shapes: 0 <= M <= 2^31 - 1, K a multiple of 32 (of 256 for Q4_K),
+ *    32 <= K <= 2^18.
  *    M == 0 is an empty product: after the qtype and shape checks the call
  *    returns BQ_OK without reading or writing anything, so its pointers may
  *    be NULL (an empty PyTorch tensor has a NULL data pointer).  The fast
@@ -66,7 +78,7 @@ typedef enum {
     BQ_ERR_DEVICE = 6  /* a kernel recorded a device-side error (see bq_device_status) */
 } bq_status;
 
-typedef enum { BQ_Q4_0 = 2, BQ_Q8_0 = 8 } bq_qtype;
+typedef enum { BQ_Q4_0 = 2, BQ_Q8_0 = 8, BQ_Q4_K = 12 } bq_qtype;
 
 /* Largest R accepted by bq_gemv_verify (the multi-row verify pass of
  * speculative decoding runs 3-6 rows; "We Wrote Our Own Inference Engine",
@@ -79,9 +91,10 @@ int bq_version(void);
 /* Human-readable text for a bq_status value (never NULL). */
 const char *bq_status_str(int status);
 
-/* Bytes of a packed M x K matrix: M * (K/32) * {34 for Q8_0, 18 for Q4_0}.
- * Returns -1 for an unknown qtype, a negative size or K % 32 != 0.
- * (RunIT README, "Quantization" table: 1.06 / 0.56 bytes per element.) */
+/* Bytes of a packed M x K matrix: M * (K/32) * {34 for Q8_0, 18 for Q4_0 and
+ * Q4_K}.  Returns -1 for an unknown qtype, a negative size or K not a multiple
+ * of 32 (of 256 for Q4_K).  (RunIT README, "Quantization" table: 1.06 / 0.56
+ * bytes per element.) */
 int64_t bq_packed_bytes(int qtype, int64_t M, int64_t K);
 
 /* Quantize fp32 weights W [M, K] (row-major) into packed blocks Wq
@@ -89,8 +102,13 @@ int64_t bq_packed_bytes(int qtype, int64_t M, int64_t K);
  *   Q8_0: d = fp16_rne(max|w| / 127);  q = clamp(round(w / d), -127, 127)
  *   Q4_0: d = fp16_rne(max|w| / 8);    n = clamp(round(w / d) + 8, 0, 15)
  * with fp32 IEEE divisions by the stored scale, round = half away from zero,
- * and d == 0 giving q = 0 / n = 8.  The output bytes are a pure function of
- * the input bits.  This is the load-time conversion the pages do in their
+ * and d == 0 giving q = 0 / n = 8.  Q4_K, per super-block of 256 weights and
+ * per sub-block j of 32: lo = min(0, min w), scale_j = (max w - lo) / 15,
+ * min_j = -lo; d = fp16_rne(max scale_j / 63), dmin = fp16_rne(max min_j / 63);
+ * sc_j = clamp(round(scale_j / d), 0, 63), m_j = clamp(round(min_j / dmin),
+ * 0, 63); q = clamp(round((w + dmin*m_j) / (d*sc_j)), 0, 15) (0 where a
+ * divisor is 0) -- the plainest quantizer that fills the GGUF layout (the
+ * pages give none).  The output bytes are a pure function of the input bits.  This is the load-time conversion the pages do in their
  * converters ("We Wrote Our Own Inference Engine", "The recipe rule"), not
  * part of the per-token path.
  * W: 4-byte aligned; Wq: 16-byte aligned.  NaN/Inf weights are outside the
@@ -109,6 +127,18 @@ bq_status bq_gemv_q8_0(const void *Wq, const float *x, float *y, int64_t M, int6
  * gemv_q4_0_f32in_f32out; "We Wrote Our Own Inference Engine", "What actually
  * moved it" #2, the dedicated 4-bit GEMV.) */
 bq_status bq_gemv_q4_0(const void *Wq, const float *x, float *y, int64_t M, int64_t K,
+                       void *stream);
+
+/* The same for packed Q4_K super-blocks (K % 256 == 0).  Per super-block the
+ * fixed tree is: sub-block sums s_j = sum q*x (q = 0..15) in the order of the
+ * 32-weight blocks of Q8_0/Q4_0, cq = sum_j (d*sc_j)*s_j and cm = sum_j
+ * (dmin*m_j)*X_j in sub-block order (X_j the sum of the sub-block's x in a
+ * fixed order), unit = cq - cm.  |y - exact| <= 1e-5 * SK with SK = sum over
+ * sub-blocks of d*sc_j*sum|q x| + dmin*m_j*sum|x| (>= sum |w x|).  (RunIT
+ * README kernel table, gemv_q4k_f16 / "gemv_q4k.metal"; "Quantization"
+ * table, Q4_K_M.)  bq_gemv_gate_up_silu, bq_gemv_qkv_bias, bq_gemv_verify,
+ * the stream plans and bq_stream_run_noalloc take BQ_Q4_K as well. */
+bq_status bq_gemv_q4_k(const void *Wq, const float *x, float *y, int64_t M, int64_t K,
                        void *stream);
 
 /* Fused feed-forward input stage:
@@ -275,7 +305,7 @@ bq_status bq_stream_plan_destroy(bq_stream_plan *plan);
  * (same validation, same kernel, bit-identical outputs) with the descriptor
  * tables and stage counters kept in one fixed device array inside the
  * library, which every GPU that loads the library holds until the process
- * exits (74 KiB).  The caller still passes the inputs and outputs (in
+ * exits (82 KiB).  The caller still passes the inputs and outputs (in
  * the ops).  It calls no cudaMalloc, cudaFree or other allocating routine.
  *
  *  - At most BQ_NOALLOC_MAX_OPS ops (and as many stages); more returns

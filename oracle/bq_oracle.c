@@ -442,9 +442,8 @@ double bqo_silu(double z) { return z / (1.0 + exp(-z)); }
 int bqo_gate_up_silu(int qtype, const uint8_t *Wg, const uint8_t *Wu, int64_t M, int64_t K,
                      const double *xn, double *y, double *g, double *u, double *Sg,
                      double *Su) {
-    int64_t bb = bqo_block_bytes(qtype);
-    if (bb < 0 || M < 0 || K < 0 || K % 32) return -1;
-    int64_t rb = (K / 32) * bb;
+    int64_t rb = bqo_packed_bytes(qtype, 1, K); /* bytes of one packed row */
+    if (rb < 0 || M < 0) return -1;
     for (int64_t m = 0; m < M; ++m) {
         double gm, um, sg, su;
         bqo_gemv(qtype, Wg + m * rb, 1, K, xn, &gm, &sg);

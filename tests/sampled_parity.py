@@ -18,7 +18,7 @@ import torch
 import oracle
 from tolerance import REL, gate_up_bound
 
-QT = {"q8_0": oracle.Q8_0, "q4_0": oracle.Q4_0}
+QT = {"q8_0": oracle.Q8_0, "q4_0": oracle.Q4_0, "q4_k": oracle.Q4_K}
 
 
 class WeightSource:
@@ -88,6 +88,9 @@ def check_gemv(qt, src, P, x, y, idx, bias=None):
     Pref, bad = oracle_packed_rows(qt, src, P, idx)
     xh = x.detach().reshape(-1).cpu().numpy().astype(np.float64)
     y_ref, S = o.gemv_parallel(QT[qt], Pref, len(idx), xh.size, xh)
+    if qt == "q4_k":
+        # the bound's scale for the kernels' split evaluation d*sc*sum(q x) - dmin*m*sum(x)
+        S = o.q4_k_split_scale_parallel(Pref, len(idx), xh.size, xh)
     if bias is not None:
         b = _take(bias, idx).cpu().numpy().astype(np.float64)
         y_ref, S = y_ref + b, S + np.abs(b)
@@ -109,6 +112,9 @@ def check_gate_up(qt, src_g, src_u, Pg, Pu, x, gamma, eps, y, idx):
     else:
         xn = xh
     r = o.gate_up_silu(QT[qt], Pgr, Pur, len(idx), xh.size, xn)
+    if qt == "q4_k":
+        r["Sg"] = o.q4_k_split_scale_parallel(Pgr, len(idx), xh.size, xn)
+        r["Su"] = o.q4_k_split_scale_parallel(Pur, len(idx), xh.size, xn)
     yg = _take(y.reshape(-1), idx).cpu().numpy().astype(np.float64)
     return _result(len(idx), bg + bu, np.abs(yg - r["y"]), gate_up_bound(r))
 

@@ -106,6 +106,8 @@ def test_roofline_entries():
     ("cfg2", 6, 604_714_496),
     # 7B-shaped Q4_0 token, gate and up fused: 3,977,035,776 weight + activation bytes
     ("cfg3", 6, 3_985_629_184),
+    # the same 7B-shaped token in Q4_K super-blocks (144 B per 256 weights = 18 per 32)
+    ("cfg3k", 6, 3_985_629_184),
     # RMSNorm + gate/up + SiLU 3072x1024: 6,705,152 B per call, 28 rotated pairs
     ("cfg4", 6, 28 * 6_705_152),
     # Q4_0 verify 17408x5120 and its transpose: 50,135,040 packed + R * 4 (M + K) B per matrix, 7 copies

@@ -8,9 +8,9 @@ GEMV bound of the oracle's fp64 product).
 
 - Q8_0 GEMV 3072x1024: every row of the first and the last rotated copy;
 - Qwen3-0.6B-shaped Q8_0 token (28 layers + 151936-row LM head) and the
-  7B-shaped Q4_0 token (28 layers + 152064-row LM head): every row of every
-  layer-0 matrix, and 4096 seeded rows (with the first and the last) of every
-  other matrix;
+  7B-shaped token (28 layers + 152064-row LM head) in Q4_0 and in Q4_K: every
+  row of every layer-0 matrix, and 4096 seeded rows (with the first and the
+  last) of every other matrix;
 - RMSNorm + gate/up + SiLU 3072x1024: every row of the first and last pair;
 - Q4_0 verify 17408x5120 and 5120x17408, R = 1..6: 4096 sampled rows of every
   input row against the oracle, and every output row memcmp-equal to the
@@ -64,7 +64,7 @@ def test_gate_up_silu_3072x1024_every_row():
     assert_parity(p, "cfg4")
 
 
-@pytest.mark.parametrize("config", ["cfg2", "cfg3"])
+@pytest.mark.parametrize("config", ["cfg2", "cfg3", "cfg3k"])
 def test_token_stream_full_size(config):
     """The whole tuned one-launch token stream; every row of layer 0 and 4096
     rows of every other matrix."""

@@ -78,7 +78,7 @@ def test_pack_bit_exact(qt, M, K):
 @pytest.mark.parametrize("name", oc.GOLDEN_FILES)
 def test_pack_and_gemv_golden(name):
     g = oc.load_golden(name)
-    qt = "q8_0" if g["qtype"] == oracle.Q8_0 else "q4_0"
+    qt = {oracle.Q8_0: "q8_0", oracle.Q4_0: "q4_0", oracle.Q4_K: "q4_k"}[g["qtype"]]
     P = gpu_pack(qt, g["w"])
     assert np.array_equal(P.cpu().numpy(), g["packed"])
     y = bq.gemv(qt, P, torch.ones(g["K"], device=DEV)).cpu().numpy()

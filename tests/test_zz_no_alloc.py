@@ -65,7 +65,7 @@ def op_array(ds):
 
 
 @pytest.mark.parametrize("chained", [True, False], ids=["chained", "independent"])
-@pytest.mark.parametrize("qt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("qt", ["q8_0", "q4_0", "q4_k"])
 def test_noalloc_matches_workspace_plan_on_two_calls(qt, chained):
     """chained: the stream executor; independent: the multi-op kernel."""
     ds = chained_stream(qt, chained=chained)
@@ -77,6 +77,8 @@ def test_noalloc_matches_workspace_plan_on_two_calls(qt, chained):
     lm = ds.ops[-1]
     x = lm.x.cpu().numpy().astype(np.float64)
     y_ref, S = oracle.get().gemv(bq.QTYPES[qt], lm.W.cpu().numpy(), lm.y.numel(), x.size, x)
+    if qt == "q4_k":  # the bound's scale for the split super-block evaluation
+        S = oracle.get().q4_k_split_scale(lm.W.cpu().numpy(), lm.y.numel(), x.size, x)
     for call in range(2):
         for op in ds.ops:
             op.y.fill_(float("nan"))
