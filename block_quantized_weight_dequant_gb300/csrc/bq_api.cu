@@ -26,6 +26,10 @@ namespace {
 constexpr long long K_MAX = 1LL << 18;
 constexpr long long M_MAX = (1LL << 31) - 1;
 
+// limit of the kernels' bounded waits (passed with every launch); a hook for
+// the tests can shorten it
+std::atomic<unsigned long long> g_wait_ns{BQ_WAIT_LIMIT_NS};
+
 // launch-geometry defaults; BQ_PLAN="md=3,mw=8,pdl=0"
 // overrides them for tuning sweeps (read once)
 struct Tunables {
@@ -701,6 +705,7 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     a->x_buffers = x_buffers;
     a->panel_units = PU;
     a->inline_op = 1;
+    a->wait_ns = g_wait_ns.load();
     geo->grid = (int)grid;
     geo->threads = threads;
     geo->nwarps = nwarps;
@@ -738,6 +743,7 @@ void fill_multi_args(const MultiGeometry &geo, int n_ops, const MultiOp *ops,
     a->panel_units = geo.panel_units;
     a->inline_op = 0;
     a->cta_ns = nullptr;
+    a->wait_ns = g_wait_ns.load();
 }
 
 void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const ExecX *xs,
@@ -758,6 +764,8 @@ void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const
     a->x_buffers = geo.x_buffers;
     a->ring_off = geo.ring_off;
     a->prefetch = geo.prefetch;
+    a->wait_ns = g_wait_ns.load();
+    a->barrier_extra = 0;
 }
 
 }  // namespace bq
@@ -1089,6 +1097,22 @@ void rebalance(const double *tb, long long n, int grid, const int *ct, const dou
     while (o <= grid) out[o++] = (int)n;
 }
 }  // namespace
+
+// Test hooks (not declared in include/bqgemv.h).  Failure detection: the
+// limit of the kernels' bounded waits for launches planned from now on, and
+// extra arrivals that a plan's stage barriers wait for, so that a test can
+// make a barrier wait run out and read the device error word -- the kernel
+// gives up after the limit and returns; nothing faults or hangs.
+extern "C" void bq_internal_set_wait_limit_ns(unsigned long long ns) {
+    bq::g_wait_ns.store(ns < 1000 ? 1000 : ns);
+}
+extern "C" int bq_internal_plan_barrier_extra(bq_stream_plan *plan, unsigned int extra,
+                                              unsigned long long wait_ns) {
+    if (!plan || plan->multi) return -1;  // only the executor has stage barriers
+    plan->args.barrier_extra = extra;
+    plan->args.wait_ns = wait_ns < 1000 ? 1000 : wait_ns;
+    return 0;
+}
 
 // Host-logic hooks for the CPU test suite (not declared in include/bqgemv.h):
 // the planner's lane-order search and the time-balanced tile split.

@@ -2,9 +2,10 @@
 // mbarriers, 1-D bulk copies (TMA) global -> shared, L2 cache policies, and
 // bounded waits.
 //
-// Every wait here gives up after BQ_WAIT_LIMIT_NS of wall time (read from
-// %globaltimer) and reports failure to the caller, which records a device
-// error bit and unwinds.  Nothing spins forever, traps or asserts.
+// Every wait here gives up after a limit of wall time (read from
+// %globaltimer; the kernels take it as a launch argument, BQ_WAIT_LIMIT_NS by
+// default) and reports failure to the caller, which records a device error
+// bit and unwinds.  Nothing spins forever, traps or asserts.
 #pragma once
 
 #include <cstdint>
@@ -79,13 +80,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false after the limit.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity)) return true;
-        if (globaltimer() - t0 > BQ_WAIT_LIMIT_NS) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
 }
 

@@ -101,6 +101,9 @@ struct ExecArgs {
     int x_buffers;    // x buffers in the ring (1..EXEC_MAX_XBUF)
     int ring_off;     // shared-memory offset of the weight rings
     int prefetch;     // items per warp prefetched into L2 beyond the ring
+    unsigned long long wait_ns;  // limit of every bounded wait
+    unsigned int barrier_extra;  // arrivals a stage barrier waits for beyond the grid's CTAs:
+                                 // 0; a test sets 1 so that the wait runs out
 };
 
 constexpr int EXEC_MAX_XBUF = 8;
@@ -257,12 +260,13 @@ __device__ __forceinline__ bool exec_next_any(const ExecTables &T, ExecItem &it,
 }
 
 // bounded mbarrier wait that also returns (false) once the CTA is aborting
-__device__ __forceinline__ bool exec_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+__device__ __forceinline__ bool exec_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity)) return true;
-        if (*abort_flag || globaltimer() - t0 > BQ_WAIT_LIMIT_NS) return false;
+        if (*abort_flag || globaltimer() - t0 > limit_ns) return false;
     }
 }
 
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
         if (lane == 0) first = atomicAdd(entered + 2 * b + ph, 1) == 0;
         first = __shfl_sync(0xffffffffu, first, 0);
         if (first) {
-            if (!__all_sync(0xffffffffu, exec_wait(xfull + b, ph, abort_flag))) {
+            if (!__all_sync(0xffffffffu, exec_wait(xfull + b, ph, abort_flag, a.wait_ns))) {
                 if (lane == 0) atomicOr(status, BQ_DEVERR_XFULL_WAIT);
                 ok = false;
                 break;
@@ -421,7 +425,7 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
         // so no warp may run ahead to a later phase of a buffer whose earlier
         // phase it has not seen complete.  Waiting here in stage order keeps
         // the warps of a CTA within XB stages of each other.
-        if (!__all_sync(0xffffffffu, exec_wait(xready + b, ph, abort_flag))) {
+        if (!__all_sync(0xffffffffu, exec_wait(xready + b, ph, abort_flag, a.wait_ns))) {
             if (lane == 0) atomicOr(status, BQ_DEVERR_XREADY_WAIT);
             ok = false;
             break;
@@ -434,7 +438,7 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
         while (it.op >= 0) {
             const ExecOp &op = T.ops[it.op];
             const int slot = consumed % a.NSW;
-            if (!__all_sync(0xffffffffu, exec_wait(full + slot, (consumed / a.NSW) & 1, abort_flag))) {
+            if (!__all_sync(0xffffffffu, exec_wait(full + slot, (consumed / a.NSW) & 1, abort_flag, a.wait_ns))) {
                 if (lane == 0) atomicOr(status, BQ_DEVERR_FULL_WAIT);
                 ok = false;
                 break;
@@ -528,9 +532,8 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
                                  : "=r"(n)
                                  : "l"(a.counters + s + 1)
                                  : "memory");
-                    if (n >= gridDim.x) break;
-                    if ((i & 63u) == 63u &&
-                        (*abort_flag || globaltimer() - t0 > BQ_WAIT_LIMIT_NS)) {
+                    if (n >= gridDim.x + a.barrier_extra) break;
+                    if ((i & 63u) == 63u && (*abort_flag || globaltimer() - t0 > a.wait_ns)) {
                         failed = 1;
                         break;
                     }
@@ -555,7 +558,7 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
         if (lane == 0) *abort_flag = 1;
         // no weight copy into this warp's ring may still be in flight at exit
         for (int i = consumed; i < issued; ++i)
-            if (!mbar_wait_bounded(full + i % a.NSW, (i / a.NSW) & 1) && lane == 0)
+            if (!mbar_wait_bounded(full + i % a.NSW, (i / a.NSW) & 1, a.wait_ns) && lane == 0)
                 atomicOr(status, BQ_DEVERR_DRAIN_WAIT);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");  // nor any x copy

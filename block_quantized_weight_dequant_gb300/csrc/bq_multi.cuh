@@ -72,6 +72,7 @@ struct MultiArgs {
     int panel_units;            // 0: an op's whole x is staged; else units of K per panel
     int inline_op;              // 1: `op` is the only op; CTA c takes tiles [cT/grid, (c+1)T/grid)
     unsigned long long *cta_ns; // list mode: each CTA's duration in ns (plan tuning), or null
+    unsigned long long wait_ns; // limit of every bounded wait
     MultiOp op;
 };
 
@@ -207,12 +208,13 @@ __device__ __forceinline__ void multi_advance(const MultiOp *ops, int nops, int 
 
 // bounded mbarrier wait that also gives up once another warp of the CTA has
 // set the abort flag; the flag is read only when the data has not landed yet
-__device__ __forceinline__ bool multi_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+__device__ __forceinline__ bool multi_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                           uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity)) return true;
-        if (*abort_flag || globaltimer() - t0 > BQ_WAIT_LIMIT_NS) return false;
+        if (*abort_flag || globaltimer() - t0 > limit_ns) return false;
     }
 }
 
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                     for (int c = c_lo; c < c_hi;
                          ++c, ++e, slot = slot + 1 == a.D ? 0 : slot + 1, par ^= slot == 0) {
                         if (ok) {
-                            if (!__all_sync(0xffffffffu, multi_wait(wfull + slot, par, abort_flag))) {
+                            if (!__all_sync(0xffffffffu, multi_wait(wfull + slot, par, abort_flag, a.wait_ns))) {
                                 if (lane == 0) {
                                     if (!*abort_flag) atomicOr(status, BQ_DEVERR_FULL_WAIT);
                                     *abort_flag = 1;
@@ -561,7 +563,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
     // after an error: let this warp's copies still in flight land before exit
     if (!ok && lane == 0)
         for (int i = landed; i < issued; ++i)
-            if (!mbar_wait_bounded(wfull + i % a.D, (i / a.D) & 1))
+            if (!mbar_wait_bounded(wfull + i % a.D, (i / a.D) & 1, a.wait_ns))
                 atomicOr(status, BQ_DEVERR_DRAIN_WAIT);
     asm volatile("cp.async.wait_all;" ::: "memory");  // nor any x copy
     if (a.cta_ns) {

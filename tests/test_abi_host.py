@@ -203,3 +203,13 @@ def test_f16_gemv_f16out_validation(lib):
     assert f(FAKE, FAKE, FAKE, -1, 256, None) == _lib.BQ_ERR_SHAPE
     assert f(FAKE, FAKE, FAKE, 1 << 31, 256, None) == _lib.BQ_ERR_SHAPE
     assert f(None, None, None, 0, 256, None) == _lib.BQ_OK
+
+
+def test_failure_detection_hooks_exist_and_reject_no_plan(lib):
+    """The internal hooks a GPU test uses to make a stage barrier's bounded
+    wait run out (not part of the public header)."""
+    hook = lib.bq_internal_plan_barrier_extra
+    hook.argtypes = [ctypes.c_void_p, ctypes.c_uint, ctypes.c_ulonglong]
+    hook.restype = ctypes.c_int
+    assert hook(None, 1, 1_000_000) == -1
+    assert lib.bq_internal_set_wait_limit_ns is not None

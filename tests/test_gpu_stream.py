@@ -2,6 +2,8 @@
 launch-per-op path: every output of every stage bit-identical, on chained
 decode streams where each stage reads the previous stage's output; plus the
 oracle bound on the final outputs and repeat-run determinism."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -210,3 +212,44 @@ def test_fused_qkv_bias_plan_matches_launch_per_op_bitwise(qt, n_layers, hidden,
     for i, (op, w) in enumerate(zip(ds.ops, want)):
         assert torch.equal(op.y.view(torch.int32), w.view(torch.int32)), f"op {i}"
     assert bq.device_status(clear=True) == 0
+
+
+BQ_DEVERR_BARRIER_WAIT = 0x8
+
+
+def test_stage_barrier_wait_runs_out_and_reports():
+    """Failure detection without a fault.  A stage barrier told to wait for one
+    arrival more than the grid's CTAs can never complete; with the bounded
+    waits' limit set to 1 ms for that launch, every CTA gives up, records
+    BQ_DEVERR_BARRIER_WAIT in the device error word and returns (its warps
+    waiting on shared-memory phases see the CTA's abort flag and return too).
+    The host reads the word through bq_device_status; the context stays
+    usable, and the same plan run normally afterwards gives the launch-per-op
+    bits."""
+    from block_quantized_weight_dequant_gb300 import _lib
+    lib = _lib.get()
+    hook = lib.bq_internal_plan_barrier_extra
+    hook.argtypes = [ctypes.c_void_p, ctypes.c_uint, ctypes.c_ulonglong]
+    hook.restype = ctypes.c_int
+    ds = make_stream("q8_0", 2, 512, 512, 128, 1024, 2000, chained=True)
+    ds.run_per_op()
+    want = snapshot(ds)
+    assert bq.device_status(clear=True) == 0
+    plan = ds.plan()
+    assert hook(plan._handle, 1, 1_000_000) == 0
+    plan.launch()
+    flags = ctypes.c_uint(0)
+    assert lib.bq_device_status(ctypes.byref(flags), 1) == _lib.BQ_ERR_DEVICE
+    assert flags.value & BQ_DEVERR_BARRIER_WAIT, hex(flags.value)
+    assert bq.device_status(clear=True) == 0  # cleared
+    # the same plan with its barriers intact
+    assert hook(plan._handle, 0, 2_000_000_000) == 0
+    for op in ds.ops:
+        op.y.fill_(float("nan"))
+    ds.run_plan()
+    for i, (g, w) in enumerate(zip(snapshot(ds), want)):
+        assert torch.equal(g.view(torch.int32), w.view(torch.int32)), f"op {i} differs after"
+    assert bq.device_status(clear=True) == 0
+    # plans of independent ops have no stage barrier to break
+    di = make_stream("q8_0", 1, 512, 512, 128, 1024, 2000, chained=False)
+    assert hook(di.plan()._handle, 1, 1_000_000) == -1
