@@ -48,6 +48,7 @@ struct Tunables {
     int single_rowmode = 4;          // single calls: row mode up to this many unit tiles per SM (0: off)
     int verify_nr = 0;               // verify calls (R > 1): weight rows per lane (1 or 2; 0: by R)
     int plan_pdl = 0;                // op-list plans: allow programmatic dependent launch
+    int tree_waste = 8;              // the tree's lanes G leave at most 1/tree_waste of slots idle
 };
 
 const Tunables &tunables() {
@@ -77,6 +78,7 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "pdl") && val >= 0 && val <= 1) v.single_pdl = val;
             else if (!std::strcmp(tok, "srow") && val >= 0 && val <= 64) v.single_rowmode = val;
             else if (!std::strcmp(tok, "vnr") && (val == 1 || val == 2)) v.verify_nr = val;
+            else if (!std::strcmp(tok, "waste") && val >= 2 && val <= 64) v.tree_waste = val;
             else if (!std::strcmp(tok, "ppdl") && val >= 0 && val <= 1) v.plan_pdl = val;
         }
         return v;
@@ -120,9 +122,10 @@ int k_step(int qtype) { return qtype == BQ_Q4_K ? 256 : 32; }
 }  // namespace
 
 int tree_lanes_for_units(long long nsc) {
+    const int den = tunables().tree_waste;
     for (int G = 32; G > 1; G >>= 1) {
         const long long slots = G * ((nsc + G - 1) / G);
-        if ((slots - nsc) * 8 <= slots) return G;
+        if ((slots - nsc) * den <= slots) return G;
     }
     return 1;
 }
@@ -659,7 +662,7 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     const int fit = (int)std::min<long long>(maxw, budget / ((long long)D * slot_min));
     const int want = (int)std::min<long long>(fit, (m.ntiles + nsms - 1) / nsms);
     int nwarps = std::max(1, want);
-    int slot_cap = (int)(budget / ((long long)nwarps * D)) / 128 * 128;
+    const int slot_cap = (int)(budget / ((long long)nwarps * D)) / 128 * 128;
     if (rowmode) {
         m.KCU = m.nsc;
         m.row_stride = m.rb;
