@@ -37,6 +37,10 @@ struct Tunables {
     int exec_nsw = 0;      // stream executor: slots per warp (0 = as many as fit, <= 4)
     int exec_warps = 8;    // stream executor: warps per CTA
     int exec_rowmode_rows = 4;  // stream executor: row mode up to this many rows per warp (0: off)
+    int exec_rowmode_nsc = 12;  // ... for rows of at most this many units (measured on GB300: the
+                                // chained Q8_0 token, K <= 3072, 657 GB/s in row mode against 591
+                                // without; the chained 7B Q4_0 token, K = 3584 and 18944, 1278
+                                // with unit-per-lane tiles against 1170 in row mode)
     int exec_prefetch = 0;      // stream executor: L2 prefetch distance beyond the ring, in items (measured: no gain)
     int multi = 1;              // independent op lists: multi-op streaming kernel (0: executor)
     int multi_warps = 0;        // multi-op kernel: warps per CTA (0: as many as fit, <= 16)
@@ -68,6 +72,7 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "nsw") && val >= 2 && val <= 8) v.exec_nsw = val;
             else if (!std::strcmp(tok, "ewarps") && val >= 1 && val <= 8) v.exec_warps = val;
             else if (!std::strcmp(tok, "rowmode") && val >= 0 && val <= 32) v.exec_rowmode_rows = val;
+            else if (!std::strcmp(tok, "rownsc") && val >= 1) v.exec_rowmode_nsc = val;
             else if (!std::strcmp(tok, "pf") && val >= 0 && val <= 16) v.exec_prefetch = val;
             else if (!std::strcmp(tok, "multi") && val >= 0 && val <= 1) v.multi = val;
             else if (!std::strcmp(tok, "mw") && val >= 1 && val <= 16) v.multi_warps = val;
@@ -383,7 +388,7 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
             ExecOp &e = eo[i];
             const int G = e.G, nsc = e.nsc, rb = e.rb;
             const int rows_per_warp = (int)((e.M + (long long)nwarps - 1) / nwarps);
-            if (rb <= slot && rows_per_warp <= t.exec_rowmode_rows) {
+            if (rb <= slot && rows_per_warp <= t.exec_rowmode_rows && nsc <= t.exec_rowmode_nsc) {
                 // row mode: a few whole rows per tile, contiguous in memory
                 e.rowmode = 1;
                 e.rpw = (unsigned char)std::max(1, std::min({rows_per_warp, slot / rb, 32}));

@@ -140,19 +140,27 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // through L2, so data written by other CTAs before a stage barrier is seen),
 // then every lane arrives on `xfull` once its copies have landed (the
 // barrier expects 32 arrivals).
+// EXEC_LOAD_ALL: the inputs and gains, then the arrival; EXEC_LOAD_GAINS:
+// only the RMSNorm gains (constant, so they are copied before a stage barrier
+// passes; the arrival after the later EXEC_LOAD_X covers them, as an arrival
+// waits for all of the thread's earlier cp.async); EXEC_LOAD_X: only the
+// inputs, then the arrival.
+constexpr int EXEC_LOAD_ALL = 0, EXEC_LOAD_GAINS = 1, EXEC_LOAD_X = 2;
 __device__ __forceinline__ void exec_load_x(const ExecStage &st, const ExecX *xs, float *xa,
-                                            uint64_t *xfull, int lane) {
+                                            uint64_t *xfull, int lane, int what = EXEC_LOAD_ALL) {
     for (int j = st.x_begin; j < st.x_end; ++j) {
         const ExecX &xd = xs[j];
-        for (int c = lane; c < xd.K / 4; c += 32)
-            cp_async16(xa + xd.off + 4 * x_chunk_pos(c), xd.x + 4 * c);
+        if (what != EXEC_LOAD_GAINS)
+            for (int c = lane; c < xd.K / 4; c += 32)
+                cp_async16(xa + xd.off + 4 * x_chunk_pos(c), xd.x + 4 * c);
         // the gain rides along (linear layout), so the RMSNorm reads it from
         // shared memory instead of waiting on global loads one by one
-        if (xd.goff >= 0)
+        if (xd.goff >= 0 && what != EXEC_LOAD_X)
             for (int c = lane; c < xd.K / 4; c += 32) cp_async16(xa + xd.goff + 4 * c, xd.gamma + 4 * c);
     }
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(xfull))
-                 : "memory");
+    if (what != EXEC_LOAD_GAINS)
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(xfull))
+                     : "memory");
 }
 
 // One warp RMSNorms the stage's inputs that have a gain, in place.  The RMS
@@ -525,6 +533,13 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
                 __threadfence();  // this CTA's y stores (ordered by the done counter)
                 asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.counters + s + 1)
                              : "memory");
+            }
+            __syncwarp();
+            // the gains do not depend on earlier stages: their copies go out
+            // once this CTA has arrived and land while the barrier propagates.
+            // Buffer (s+1) % XB is free: this CTA is done with every stage <= s.
+            exec_load_x(T.stages[s + 1], T.xs, xbuf(s + 1), xfull + (s + 1) % XB, lane, EXEC_LOAD_GAINS);
+            if (lane == 0) {
                 const uint64_t t0 = globaltimer();
                 unsigned int n = 0;
                 for (uint32_t i = 0;; ++i) {
@@ -546,7 +561,7 @@ __global__ void __launch_bounds__(256, 1) exec_kernel(const ExecArgs a, unsigned
                 break;
             }
             // buffer (s+1) % XB is free: its previous stage (s+1-XB <= s) is done
-            exec_load_x(T.stages[s + 1], T.xs, xbuf(s + 1), xfull + (s + 1) % XB, lane);
+            exec_load_x(T.stages[s + 1], T.xs, xbuf(s + 1), xfull + (s + 1) % XB, lane, EXEC_LOAD_X);
         }
         if (XB > 1 && s + XB < a.nstages && !T.stages[s + XB].barrier)
             exec_load_x(T.stages[s + XB], T.xs, xbuf(s + XB), xfull + b, lane);
