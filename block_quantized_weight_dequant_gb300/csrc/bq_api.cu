@@ -53,6 +53,7 @@ struct Tunables {
     int verify_nr = 0;               // verify calls (R > 1): weight rows per lane (1 or 2; 0: by R)
     int plan_pdl = 0;                // op-list plans: allow programmatic dependent launch
     int tree_waste = 8;              // the tree's lanes G leave at most 1/tree_waste of slots idle
+    int verify_wave = 1;             // verify panels: two rows per lane when one needs two waves
 };
 
 const Tunables &tunables() {
@@ -84,6 +85,7 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "srow") && val >= 0 && val <= 64) v.single_rowmode = val;
             else if (!std::strcmp(tok, "vnr") && (val == 1 || val == 2)) v.verify_nr = val;
             else if (!std::strcmp(tok, "waste") && val >= 2 && val <= 64) v.tree_waste = val;
+            else if (!std::strcmp(tok, "vwave") && val >= 0 && val <= 1) v.verify_wave = val;
             else if (!std::strcmp(tok, "ppdl") && val >= 0 && val <= 1) v.plan_pdl = val;
         }
         return v;
@@ -632,6 +634,16 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     int PU = 0, x_floats = R * xpad, x_rstride = xpad, x_buffers = 1;
     if ((long long)R * xpad * 4 > t.single_x_max) {
         if (gu || R == 1) return false;
+        // panel mode gives each warp one tile for the whole call (its R x NR
+        // partial sums stay in registers): with one weight row per lane a
+        // large M can need more warps than one wave of CTAs holds (8 per SM
+        // at these register counts), so take two rows per lane then
+        if (NR == 1 && c.qtype != BQ_Q4_K && t.verify_wave &&
+            (c.M + m.rpw - 1) / m.rpw > (long long)nsms * multi_max_warps(c.qtype, R)) {
+            NR = 2;
+            m.rpw = NR * (32 / m.G);
+            m.ntiles = (int)((c.M + m.rpw - 1) / m.rpw);
+        }
         PU = (int)(t.single_x_max / 2 / ((long long)R * 256 * 4)) / m.G * m.G;
         if (PU < m.G) return false;
         x_rstride = PU * 256;
