@@ -63,11 +63,13 @@ def token_cfg(config):
 # the traffic is null until it is captured again.
 NCU_TRAFFIC = {
     # (config, inputs): (bytes per launch, csrc_digest() at capture, summary)
-    ("cfg2", "independent"): (606401280, "0d7abc2fb55556891b791b28b032858a2e7c3ad56b7f88c6427651bf9fb651a1",
+    ("cfg2", "independent"): (606614272, "8ca57ba8bf5bf1bc1519e6098f1a2de0067ebff73fb9c2f51549dbab64411dc4",
                               "profiles/multi_kernel_q8_0_qwen3_0.6b_stream.md"),
     # captured on 2 of the 28 layers (+ LM head) and scaled by algorithmic bytes
-    ("cfg3", "independent"): (4004955016, "0d7abc2fb55556891b791b28b032858a2e7c3ad56b7f88c6427651bf9fb651a1",
+    ("cfg3", "independent"): (4004951435, "8ca57ba8bf5bf1bc1519e6098f1a2de0067ebff73fb9c2f51549dbab64411dc4",
                               "profiles/multi_kernel_q4_0_7b_stream.md"),
+    ("cfg3k", "independent"): (4007192838, "8ca57ba8bf5bf1bc1519e6098f1a2de0067ebff73fb9c2f51549dbab64411dc4",
+                               "profiles/multi_kernel_q4_k_7b_stream.md"),
 }
 
 
@@ -191,18 +193,21 @@ class Workload:
             fn()
 
 
-# The seeded generator call behind every packed matrix, by the packed tensor's
-# device address: the CPU leg draws the same fp32 rows again for the oracle.
-WEIGHT_SOURCES = {}
-
-
+# The seeded generator call behind a packed matrix travels with the tensor
+# (attribute `bq_source`), so the CPU leg can draw the same fp32 rows again for
+# the oracle.  A tensor made otherwise (the load-time q|k|v concatenation) has
+# none, and its rows are not checked.
 def _packed(bq, wl, qt, M, K, seed, tag, dev):
     src = dict(shape=(M, K), std=wl.W_STD, seed=seed, stream=wl.stream_id(*tag))
     W = wl.normal_torch(src["shape"], src["std"], seed=seed, stream=src["stream"], device=dev)
     P = bq.quantize_pack(W, qt)
     del W
-    WEIGHT_SOURCES[P.data_ptr()] = src
+    P.bq_source = src
     return P
+
+
+def weight_source(P):
+    return getattr(P, "bq_source", None)
 
 
 def build_token_layers(cfg, dev, seed=0, fused_qkv=False):
@@ -273,7 +278,9 @@ def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None
                 w.add(lambda op=op: bq.gemv_gate_up_silu(qt, op.W, op.W_up, op.x, op.gamma,
                                                          op.eps, op.y), f"gate_up_silu_{qt}", nb)
     w.x_dev = ds.inputs
-    w.y_dev = ds.logits if chained else torch.cat([op.y for op in ds.ops])
+    # the step's result read back each e2e step: the logits of a chained
+    # token; every op's output (one buffer) of an independent one
+    w.y_dev = ds.logits if chained else ds.outputs
     w.stream_obj = ds
     w.desc = token_desc(cfg, mode, chained, fused_qkv)
     if mode == "plan" and not chained:
@@ -290,11 +297,11 @@ def build_token_stream(cfg, dev, seed=0, mode="plan", chained=False, packed=None
             if op.W_up is not None:
                 w.checks.append(dict(kind="gate_up", qt=qt, Pg=op.W, Pu=op.W_up, x=op.x,
                                      gamma=op.gamma, eps=op.eps, y=op.y, tag=tag,
-                                     src_g=WEIGHT_SOURCES.get(op.W.data_ptr()),
-                                     src_u=WEIGHT_SOURCES.get(op.W_up.data_ptr())))
+                                     src_g=weight_source(op.W),
+                                     src_u=weight_source(op.W_up)))
             else:
                 w.checks.append(dict(kind="gemv", qt=qt, P=op.W, x=op.x, y=op.y, bias=op.bias,
-                                     tag=tag, src=WEIGHT_SOURCES.get(op.W.data_ptr())))
+                                     tag=tag, src=weight_source(op.W)))
     return w
 
 
@@ -311,7 +318,7 @@ def build_rotated_gemv(dev, qt, M, K, copies, seed=0, name="cfg1"):
         x, y = w.x_dev[c * K:(c + 1) * K], w.y_dev[c * M:(c + 1) * M]
         w.add(lambda P=P, x=x, y=y: bq.gemv(qt, P, x, y), f"gemv_{qt}", P.numel() + 4 * (M + K))
         w.checks.append(dict(kind="gemv", qt=qt, P=P, x=x, y=y, bias=None, tag=(name, c),
-                             src=WEIGHT_SOURCES[P.data_ptr()]))
+                             src=weight_source(P)))
     w.desc = {"workload": f"{qt} gemv {M}x{K}, {copies} rotated copies", "M": M, "K": K}
     return w
 
@@ -355,8 +362,8 @@ def build_rotated_gate_up(dev, cfg, seed=0):
               bq.gemv_gate_up_silu(qt, Pg, Pu, x, g, cfg["eps"], y), f"gate_up_silu_{qt}",
               Pg.numel() + Pu.numel() + 8 * K + 4 * M)
         w.checks.append(dict(kind="gate_up", qt=qt, Pg=Pg, Pu=Pu, x=x, gamma=g, eps=cfg["eps"],
-                             y=y, tag=("cfg4", c), src_g=WEIGHT_SOURCES[Pg.data_ptr()],
-                             src_u=WEIGHT_SOURCES[Pu.data_ptr()]))
+                             y=y, tag=("cfg4", c), src_g=weight_source(Pg),
+                             src_u=weight_source(Pu)))
     w.desc = {"workload": cfg["name"], "M": M, "K": K, "pairs": n}
     return w
 
@@ -382,7 +389,7 @@ def build_verify(dev, cfg, R, copies=7, seed=0):
             w.add(lambda P=P, X=X, Y=Y: bq.gemv_verify(qt, P, X, Y), f"verify_{qt}_R{R}",
                   P.numel() + 4 * R * (M + K))
             w.checks.append(dict(kind="verify", qt=qt, P=P, X=X, Y=Y, tag=("cfg5", name, c, R),
-                                 src=WEIGHT_SOURCES[P.data_ptr()]))
+                                 src=weight_source(P)))
     w.desc = {"workload": cfg["name"], "R": R, "copies": copies}
     return w
 

@@ -62,6 +62,24 @@ class DecodeStream:
                 n_in += rows(L["o"])[1] + hidden + rows(L["down"])[1] + hidden
         self.inputs = torch.zeros(n_in, **f32)
         self.x0 = self.inputs[:hidden]
+        # likewise every op's output is a slice of one buffer, so a caller
+        # reads them all back with a single copy; each slice starts on 16
+        # bytes, as an output that a later stage reads as its x must
+        def pad4(n):
+            return (n + 3) // 4 * 4
+
+        n_out = pad4(rows(lm_head)[0])
+        for L in layers:
+            n_out += sum(pad4(rows(L[n])[0]) for n in (("qkv",) if fused_qkv else ("q", "k", "v")))
+            n_out += pad4(rows(L["o"])[0]) + pad4(rows(L["gate"])[0]) + pad4(rows(L["down"])[0])
+        self.outputs = torch.zeros(n_out, **f32)
+        ocursor = [0]
+
+        def out(n):
+            t = self.outputs[ocursor[0]:ocursor[0] + n]
+            ocursor[0] += pad4(n)
+            return t
+
         self.ops = []
         self.buffers = []
         cursor = [hidden]
@@ -78,16 +96,18 @@ class DecodeStream:
         st = 0
         for L in layers:
             q_dim = rows(L["o"])[1]  # o reads the attention output, q's width
-            bufs = {n: torch.empty(rows(L[n])[0], **f32) for n in ("o", "down")}
-            bufs["ffn"] = torch.empty(rows(L["gate"])[0], **f32)
+            bufs = {}
             if fused_qkv:
-                bufs["qkv"] = torch.empty(rows(L["qkv"])[0], **f32)
+                bufs["qkv"] = out(rows(L["qkv"])[0])
                 bufs["q"] = bufs["qkv"][:q_dim]
                 self.ops.append(StreamOp(st, L["qkv"], h, bufs["qkv"], bias=L.get("qkv_bias")))
             else:
                 for n in ("q", "k", "v"):
-                    bufs[n] = torch.empty(rows(L[n])[0], **f32)
+                    bufs[n] = out(rows(L[n])[0])
                     self.ops.append(StreamOp(st, L[n], h, bufs[n]))
+            bufs["o"] = out(rows(L["o"])[0])
+            bufs["ffn"] = out(rows(L["gate"])[0])
+            bufs["down"] = out(rows(L["down"])[0])
             self.buffers.append(bufs)
             self.ops.append(StreamOp(st + 1, L["o"], src(bufs["q"], q_dim), bufs["o"]))
             self.ops.append(StreamOp(st + 2, L["gate"], src(bufs["o"], hidden), bufs["ffn"],
@@ -96,7 +116,8 @@ class DecodeStream:
                                      bufs["down"]))
             h = src(bufs["down"], hidden)
             st += 4
-        self.logits = torch.empty(rows(lm_head)[0], **f32)
+        self.logits = out(rows(lm_head)[0])
+        assert ocursor[0] == n_out
         self.ops.append(StreamOp(st, lm_head, h, self.logits))
         self._plan = None
 

@@ -41,9 +41,18 @@ class WeightSource:
         return t
 
     def rows(self, idx, device):
-        """The drawn matrix's rows `idx` (numpy) on the host."""
-        i = torch.as_tensor(np.asarray(idx), device=device, dtype=torch.long)
+        """The drawn matrix's rows `idx` (numpy) on the host.  The indices are
+        checked here, on the host: an index past the matrix must never reach
+        a device gather."""
+        idx = np.asarray(idx)
+        if idx.size and (idx.min() < 0 or idx.max() >= self.shape[0]):
+            raise IndexError(f"rows {idx.min()}..{idx.max()} outside a {self.shape} source")
+        i = torch.as_tensor(idx, device=device, dtype=torch.long)
         return self.draw(device).index_select(0, i).cpu().numpy()
+
+    def matches(self, rows, K):
+        """Whether this source drew a rows x K matrix."""
+        return tuple(self.shape[:2]) == (int(rows), int(K))
 
 
 def sample_rows(M, n, *tag, seed=0):
@@ -58,7 +67,15 @@ def sample_rows(M, n, *tag, seed=0):
 
 
 def _take(t, idx):
+    idx = np.asarray(idx)
+    if idx.size and (idx.min() < 0 or idx.max() >= t.shape[0]):
+        raise IndexError(f"rows {idx.min()}..{idx.max()} outside a tensor of {t.shape[0]} rows")
     return t.index_select(0, torch.as_tensor(idx, device=t.device, dtype=torch.long))
+
+
+def _need_source(src, P, K):
+    if not src.matches(P.shape[0], K):
+        raise ValueError(f"weight source {src.shape} does not describe a {P.shape[0]} x {K} matrix")
 
 
 def _result(rows, pack_bad, err, bound, S=None):
@@ -85,6 +102,7 @@ def oracle_packed_rows(qt, src, P, idx):
 def check_gemv(qt, src, P, x, y, idx, bias=None):
     """Rows idx of y = W x (+ bias) against the oracle; P the GPU's packed W."""
     o = oracle.get()
+    _need_source(src, P, x.numel())
     Pref, bad = oracle_packed_rows(qt, src, P, idx)
     xh = x.detach().reshape(-1).cpu().numpy().astype(np.float64)
     y_ref, S = o.gemv_parallel(QT[qt], Pref, len(idx), xh.size, xh)
@@ -104,6 +122,8 @@ def check_gate_up(qt, src_g, src_u, Pg, Pu, x, gamma, eps, y, idx):
     """Rows idx of y = silu(Wg xn) * (Wu xn) against the oracle's fp64
     RMSNorm and gate+up, within the propagated bound of tolerance.py."""
     o = oracle.get()
+    _need_source(src_g, Pg, x.numel())
+    _need_source(src_u, Pu, x.numel())
     Pgr, bg = oracle_packed_rows(qt, src_g, Pg, idx)
     Pur, bu = oracle_packed_rows(qt, src_u, Pu, idx)
     xh = x.detach().reshape(-1).cpu().numpy().astype(np.float64)
@@ -123,6 +143,7 @@ def check_f16(src, W, x, y, idx):
     """Rows idx of the fp16-weight GEMV against the oracle; the weights are
     drawn again and must equal the GPU's copy bit for bit."""
     o = oracle.get()
+    _need_source(src, W, x.numel())
     Wr = src.rows(idx, W.device)
     bad = int((_take(W, idx).cpu().numpy().view(np.uint16) != Wr.view(np.uint16)).any(axis=1).sum())
     xh = x.detach().reshape(-1).cpu().numpy().astype(np.float64)

@@ -62,3 +62,21 @@ def test_wrong_dtypes_are_refused(no_lib):
     with pytest.raises(TypeError):
         bq.gemv_q8_0(torch.zeros(M, 68, dtype=torch.int8), torch.zeros(K))
     assert no_lib.used == []
+
+
+def test_parity_sources_check_rows_and_shapes_on_the_host():
+    """The full-size parity check draws a matrix's fp32 rows again from its
+    seeded source: a row index outside the source, or a source that does not
+    describe the packed matrix, is refused on the host before any gather runs
+    on a device (an out-of-range device gather would fault)."""
+    import sampled_parity as sp
+
+    src = sp.WeightSource((8, 64), 0.02, 0, 5)
+    assert src.rows([0, 7], "cpu").shape == (2, 64)
+    with pytest.raises(IndexError):
+        src.rows([0, 8], "cpu")
+    with pytest.raises(IndexError):
+        sp._take(torch.zeros(4), [4])
+    with pytest.raises(ValueError):
+        sp._need_source(src, torch.zeros((12, 36), dtype=torch.uint8), 64)
+    sp._need_source(src, torch.zeros((8, 36), dtype=torch.uint8), 64)
