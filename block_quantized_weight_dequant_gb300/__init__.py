@@ -243,11 +243,13 @@ class StreamOp:
 
 
 class StreamPlan:
-    """A whole list of StreamOps run by ONE cooperative launch per call
-    (bq_stream_plan_* of include/bqgemv.h).  The descriptor workspace is a
-    torch tensor this object owns; keep the op tensors alive as long as the
-    plan.  ``launch()`` enqueues on the current stream and can be captured in
-    a CUDA graph; creating the plan synchronises, so do it before capture."""
+    """A whole list of StreamOps run per call (bq_stream_plan_* of
+    include/bqgemv.h): independent ops in one launch of the streaming kernel,
+    dependent stages in one launch per stage (``launches``).  The descriptor
+    workspace is a torch tensor this object owns; keep the op tensors alive as
+    long as the plan.  ``launch()`` enqueues on the current stream and can be
+    captured in a CUDA graph; creating the plan synchronises, so do it before
+    capture."""
 
     def __init__(self, qtype, ops):
         qt = _qt(qtype)
@@ -298,6 +300,11 @@ class StreamPlan:
     def launch(self):
         _lib.check(lib.bq_stream_plan_launch(self._handle, _stream(self._ops[0].W)),
                    "stream_plan_launch")
+
+    @property
+    def launches(self):
+        """Kernel launches one ``launch()`` enqueues (bq_stream_plan_launches)."""
+        return int(lib.bq_stream_plan_launches(self._handle))
 
     def tune(self, rounds=3):
         """Re-split the plan's tiles among CTAs by measured time

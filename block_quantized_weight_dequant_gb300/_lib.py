@@ -21,8 +21,8 @@ EXPORTS = ("bq_version", "bq_status_str", "bq_packed_bytes", "bq_quantize_pack",
            "bq_gemv_q4_0", "bq_gemv_q4_k", "bq_gemv_gate_up_silu", "bq_gemv_verify", "bq_gemv_qkv_bias",
            "bq_gemv_f16", "bq_gemv_f16_f16out", "bq_device_status",
            "bq_tree_lanes", "bq_stream_workspace_bytes", "bq_stream_plan_create",
-           "bq_stream_plan_launch", "bq_stream_plan_tune", "bq_stream_plan_destroy",
-           "bq_stream_run_noalloc")
+           "bq_stream_plan_launch", "bq_stream_plan_tune", "bq_stream_plan_launches",
+           "bq_stream_plan_destroy", "bq_stream_run_noalloc")
 BQ_NOALLOC_MAX_OPS = 512
 
 
@@ -62,6 +62,7 @@ def _declare(lib):
                                         ctypes.POINTER(vp)]),
         "bq_stream_plan_launch": (i32, [vp, vp]),
         "bq_stream_plan_tune": (i32, [vp, i32, vp]),
+        "bq_stream_plan_launches": (i32, [vp]),
         "bq_stream_plan_destroy": (i32, [vp]),
         "bq_stream_run_noalloc": (i32, [i32, ctypes.POINTER(BqOp), i32, vp]),
     }

@@ -29,6 +29,10 @@ constexpr long long M_MAX = (1LL << 31) - 1;
 // limit of the kernels' bounded waits (passed with every launch); a hook for
 // the tests can shorten it
 std::atomic<unsigned long long> g_wait_ns{BQ_WAIT_LIMIT_NS};
+// how plans of dependent stages run, for plans created from now on: -1 by
+// the tunable, 0 the cooperative executor, 1 one launch per stage (a hook
+// for the tests, which cover both)
+std::atomic<int> g_plan_kind{-1};
 
 // launch-geometry defaults; BQ_PLAN="md=3,mw=8,pdl=0"
 // overrides them for tuning sweeps (read once)
@@ -52,6 +56,14 @@ struct Tunables {
     int single_rowmode = 4;          // single calls: row mode up to this many unit tiles per SM (0: off)
     int verify_nr = 0;               // verify calls (R > 1): weight rows per lane (1 or 2; 0: by R)
     int plan_pdl = 0;                // op-list plans: allow programmatic dependent launch
+    int plan_early = 1;              // staged plans: stages after the first fill their weight
+                                     // rings before waiting for the stage before (measured on
+                                     // GB300, chained tokens: Qwen3-0.6B-shaped Q8_0 950 ->
+                                     // 1013 GB/s, 7B-shaped Q4_0 2476 -> 2539; with an L2
+                                     // prefetch of the next items as well: 1011 and 2444)
+    int plan_staged = 1;             // dependent op lists: one streaming-kernel launch per stage,
+                                     // chained by programmatic dependent launch (0: the cooperative
+                                     // executor, one launch with grid-wide barriers)
     int tree_waste = 8;              // the tree's lanes G leave at most 1/tree_waste of slots idle
     int verify_wave = 1;             // verify panels: two rows per lane when one needs two waves
 };
@@ -87,6 +99,8 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "waste") && val >= 2 && val <= 64) v.tree_waste = val;
             else if (!std::strcmp(tok, "vwave") && val >= 0 && val <= 1) v.verify_wave = val;
             else if (!std::strcmp(tok, "ppdl") && val >= 0 && val <= 1) v.plan_pdl = val;
+            else if (!std::strcmp(tok, "staged") && val >= 0 && val <= 1) v.plan_staged = val;
+            else if (!std::strcmp(tok, "early") && val >= 0 && val <= 1) v.plan_early = val;
         }
         return v;
     }();
@@ -764,6 +778,7 @@ void fill_multi_args(const MultiGeometry &geo, int n_ops, const MultiOp *ops,
     a->inline_op = 0;
     a->cta_ns = nullptr;
     a->wait_ns = g_wait_ns.load();
+    a->early_ring = 0;
 }
 
 void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const ExecX *xs,
@@ -791,9 +806,21 @@ void fill_exec_args(const ExecGeometry &geo, int n_ops, const ExecOp *ops, const
 }  // namespace bq
 
 // the opaque plan handle of include/bqgemv.h
+namespace bq {
+// one launch of a staged plan: the streaming kernel over one stage's ops
+struct StageLaunch {
+    MultiArgs args;
+    int grid, threads, pdl;
+    size_t smem;
+};
+}  // namespace bq
+
 struct bq_stream_plan {
     int qtype, n_ops, n_stages, device;
     int multi;  // 1: independent ops, multi-op streaming kernel; 0: stream executor
+    // staged plans (dependent stages, multi == 0): one streaming-kernel launch
+    // per stage, in stage order; null for the executor
+    bq::StageLaunch *stages;
     int grid, threads;
     size_t smem;
     bq::ExecArgs args;
@@ -857,6 +884,81 @@ bq_status gemv_common(int qtype, const void *Wq, const float *x, float *y, int R
         return BQ_ERR_ALIGN;
     GemvCall c{qtype, bq::MODE_PLAIN, R, Wq, nullptr, x, nullptr, 0.0f, y, M, K, stream, bias};
     return run_gemv(c);
+}
+
+// A plan of dependent stages as one streaming-kernel launch per stage.  A
+// stage of one op takes the single-call geometry (row mode for small ops, as
+// bq_gemv); a stage of several independent ops takes the op-list geometry,
+// its op table and CTA split in the workspace.  Every launch allows
+// programmatic dependent launch: a stage's kernel starts while the previous
+// stage's kernel drains, prefetches its first weight items into L2, and waits
+// for the previous grid (griddepcontrol.wait) before it reads any input, so
+// an op may read an output of the stage before.  Outputs are bit-identical to
+// the executor's and to one call per op: the same fixed tree everywhere.
+// Returns BQ_ERR_SHAPE when some stage does not fit the streaming kernel.
+bq_status plan_staged(int qtype, const bq_op *ops, int n_ops, const bq::ExecStage *es,
+                      int n_stages, uint8_t *ws, bq_stream_plan **out) {
+    const bq::Tunables &t = bq::tunables();
+    std::vector<bq::StageLaunch> sl((size_t)n_stages);
+    std::vector<bq::MultiOp> mo((size_t)n_ops);
+    std::memset(mo.data(), 0, mo.size() * sizeof(bq::MultiOp));
+    const int64_t off_ct = ((int64_t)n_ops * (int64_t)sizeof(bq::MultiOp) + 255) / 256 * 256;
+    std::vector<int> ct;  // the CTA splits of the list-mode stages, back to back
+    std::vector<int> ct_stage((size_t)bq::MULTI_MAX_CTAS + 1);
+    auto *mo_dev = reinterpret_cast<const bq::MultiOp *>(ws);
+    auto *ct_dev = reinterpret_cast<int *>(ws + off_ct);
+    for (int s = 0; s < n_stages; ++s) {
+        const int b = es[s].op_begin, n = es[s].op_end - es[s].op_begin;
+        bq::StageLaunch &l = sl[(size_t)s];
+        l.pdl = t.single_pdl;
+        const int early = s > 0 && t.plan_early;
+        if (n == 1) {
+            const bq_op &o = ops[b];
+            const bool gu = o.kind == BQ_OP_GATE_UP_SILU;
+            GemvCall c{qtype, gu ? bq::MODE_GATE_UP : bq::MODE_PLAIN, 1, o.W,
+                       gu ? o.W_up : nullptr, o.x, gu ? o.gamma : nullptr, o.eps, o.y,
+                       (long long)o.M, (long long)o.K, nullptr, gu ? nullptr : o.bias};
+            bq::MultiGeometry g;
+            if (!bq::plan_multi_single(c, &l.args, &g)) return BQ_ERR_SHAPE;
+            l.args.early_ring = early;
+            l.grid = g.grid;
+            l.threads = g.threads;
+            l.smem = g.smem;
+        } else {
+            bq::MultiGeometry g;
+            const bq_status st = bq::plan_multi_tables(qtype, ops + b, n, mo.data() + b,
+                                                       ct_stage.data(), &g);
+            if (st != BQ_OK) return st == BQ_ERR_CUDA ? st : BQ_ERR_SHAPE;
+            const size_t at = ct.size();
+            ct.insert(ct.end(), ct_stage.begin(), ct_stage.begin() + g.grid + 1);
+            bq::fill_multi_args(g, n, mo_dev + b, ct_dev + at, &l.args);
+            l.args.early_ring = early;
+            l.grid = g.grid;
+            l.threads = g.threads;
+            l.smem = g.smem;
+        }
+    }
+    if (cudaMemcpy(ws, mo.data(), (size_t)n_ops * sizeof(bq::MultiOp), cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
+        (!ct.empty() && cudaMemcpy(ws + off_ct, ct.data(), ct.size() * sizeof(int),
+                                   cudaMemcpyHostToDevice) != cudaSuccess))
+        return BQ_ERR_CUDA;
+    auto *p = new (std::nothrow) bq_stream_plan;
+    if (!p) return BQ_ERR_CUDA;
+    std::memset(p, 0, sizeof *p);
+    p->stages = new (std::nothrow) bq::StageLaunch[(size_t)n_stages];
+    if (!p->stages) {
+        delete p;
+        return BQ_ERR_CUDA;
+    }
+    std::memcpy(p->stages, sl.data(), (size_t)n_stages * sizeof(bq::StageLaunch));
+    p->qtype = qtype;
+    p->n_ops = n_ops;
+    p->n_stages = n_stages;
+    p->multi = 0;
+    cudaGetDevice(&p->device);
+    *out = p;
+    return BQ_OK;
 }
 
 }  // namespace
@@ -956,7 +1058,10 @@ int64_t bq_stream_workspace_bytes(int n_ops, int n_stages) {
     const int64_t multi = align256((int64_t)n_ops * sizeof(bq::MultiOp)) +
                           align256((int64_t)(bq::MULTI_MAX_CTAS + 1) * 4) +
                           align256((int64_t)bq::MULTI_MAX_CTAS * 8);
-    return std::max(exec, multi);
+    // staged: the op table and one CTA split per stage
+    const int64_t staged = align256((int64_t)n_ops * sizeof(bq::MultiOp)) +
+                           align256((int64_t)n_stages * (bq::MULTI_MAX_CTAS + 1) * 4);
+    return std::max({exec, multi, staged});
 }
 
 bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *workspace,
@@ -1022,6 +1127,17 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
         }
         // a list the multi-op kernel cannot hold falls back to the executor
     }
+    const int kind = bq::g_plan_kind.load();
+    if (!independent && (kind >= 0 ? kind == 1 : bq::tunables().plan_staged != 0)) {
+        bq_stream_plan *p = nullptr;
+        const bq_status ss = plan_staged(qtype, ops, n_ops, es.data(), n_stages, ws, &p);
+        if (ss == BQ_OK) {
+            *plan = p;
+            return BQ_OK;
+        }
+        if (ss == BQ_ERR_CUDA) return ss;
+        // a stage the streaming kernel cannot hold: the executor runs the list
+    }
     const int64_t off_x = align256((int64_t)n_ops * sizeof(bq::ExecOp));
     const int64_t off_st = off_x + align256((int64_t)n_ops * sizeof(bq::ExecX));
     const int64_t off_cnt = off_st + align256((int64_t)n_stages * sizeof(bq::ExecStage));
@@ -1053,6 +1169,15 @@ bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *wo
 
 bq_status bq_stream_plan_launch(const bq_stream_plan *plan, void *stream) {
     if (!plan) return BQ_ERR_NULL;
+    if (plan->stages) {
+        for (int s = 0; s < plan->n_stages; ++s) {
+            const bq::StageLaunch &l = plan->stages[s];
+            const int e = bq::fmt_multi_launch(plan->qtype, l.args, l.grid, l.threads, l.smem,
+                                               stream, l.pdl);
+            if (e != 0) return BQ_ERR_CUDA;
+        }
+        return BQ_OK;
+    }
     if (plan->multi) {
         const int pdl = bq::tunables().plan_pdl;
         const int e = bq::fmt_multi_launch(plan->qtype, plan->margs, plan->grid, plan->threads,
@@ -1071,6 +1196,7 @@ bq_status bq_stream_plan_destroy(bq_stream_plan *plan) {
     if (plan) {
         delete[] plan->mo_host;
         delete[] plan->ct_host;
+        delete[] plan->stages;
     }
     delete plan;
     return BQ_OK;
@@ -1126,9 +1252,14 @@ void rebalance(const double *tb, long long n, int grid, const int *ct, const dou
 extern "C" void bq_internal_set_wait_limit_ns(unsigned long long ns) {
     bq::g_wait_ns.store(ns < 1000 ? 1000 : ns);
 }
+// how plans of dependent stages created from now on run: -1 by the
+// BQ_PLAN tunable, 0 the cooperative executor, 1 one launch per stage
+extern "C" void bq_internal_set_plan_kind(int kind) {
+    bq::g_plan_kind.store(kind < 0 ? -1 : kind > 0 ? 1 : 0);
+}
 extern "C" int bq_internal_plan_barrier_extra(bq_stream_plan *plan, unsigned int extra,
                                               unsigned long long wait_ns) {
-    if (!plan || plan->multi) return -1;  // only the executor has stage barriers
+    if (!plan || plan->multi || plan->stages) return -1;  // only the executor has stage barriers
     plan->args.barrier_extra = extra;
     plan->args.wait_ns = wait_ns < 1000 ? 1000 : wait_ns;
     return 0;
@@ -1144,10 +1275,15 @@ void bq_internal_rebalance(const double *tile_bytes, long long n, int grid, cons
     rebalance(tile_bytes, n, grid, ct, cta_time, out);
 }
 
+int bq_stream_plan_launches(const bq_stream_plan *plan) {
+    if (!plan) return -1;
+    return plan->stages ? plan->n_stages : 1;
+}
+
 bq_status bq_stream_plan_tune(bq_stream_plan *plan, int rounds, void *stream) {
     if (!plan) return BQ_ERR_NULL;
     if (rounds < 1 || rounds > 16) return BQ_ERR_SHAPE;
-    if (!plan->multi) return BQ_OK;  // the executor's stages are balanced by construction
+    if (!plan->multi) return BQ_OK;  // dependent stages: left as planned
     auto s = static_cast<cudaStream_t>(stream);
     const int grid = plan->grid;
     constexpr int REPS = 3;  // launches averaged per measurement

@@ -29,7 +29,11 @@
 // its first weight items into L2, and only then waits for the kernel before it
 // in the stream (griddepcontrol.wait) before reading any input.  A prefetch is
 // a hint that binds no value, so this is safe even if the kernel before wrote
-// the weights.
+// the weights.  A stage of a staged plan after the first knows the kernel
+// before it (the plan's previous stage, which writes no weights: the planner
+// rejects outputs overlapping weights), so it copies its first weight items
+// into its ring before the wait (early_ring) and computes as soon as its
+// input is staged.
 //
 // Arithmetic is bq_dot.cuh's fixed tree: every output is bit-identical to the
 // single-op kernels and across R.
@@ -73,6 +77,10 @@ struct MultiArgs {
     int inline_op;              // 1: `op` is the only op; CTA c takes tiles [cT/grid, (c+1)T/grid)
     unsigned long long *cta_ns; // list mode: each CTA's duration in ns (plan tuning), or null
     unsigned long long wait_ns; // limit of every bounded wait
+    int early_ring;             // 1: fill the weight rings before waiting for the kernel
+                                // before (it is known to write no weights: an earlier
+                                // stage of the same plan); 0: only prefetch the first
+                                // items into L2 before the wait
     MultiOp op;
 };
 
@@ -331,9 +339,20 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
     q.m = q.c = 0;
     q.op = multi_op_of(ops, nops, q.t, op0);
     multi_load_op(ops, q, co);
-    // this warp's first items into L2 while the kernel before may still run
-    // (a copy of the cursor with its own op state in registers)
-    {
+    // fill the ring with this warp's first D items: before the wait when the
+    // kernel before writes no weights, else after it
+    int issued = 0;
+    auto fill_ring = [&]() {
+        for (; issued < a.D && q.t < t_end; ++issued) {
+            multi_issue<QT>(q, co, ring + (size_t)issued * a.slot_bytes, wfull + issued, pol, lane);
+            multi_advance(ops, nops, a.nwarps, q, co);
+        }
+    };
+    if (a.early_ring) {
+        fill_ring();
+    } else {
+        // this warp's first items into L2 while the kernel before may still
+        // run (a copy of the cursor with its own op state in registers)
         MultiCursor f = q;
         MultiCurOp fo = co;
         for (int i = 0; i < a.D && f.t < t_end; ++i) {
@@ -343,13 +362,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t t_start = a.cta_ns ? globaltimer() : 0;
-
-    // fill the ring with this warp's first D items
-    int issued = 0;
-    for (; issued < a.D && q.t < t_end; ++issued) {
-        multi_issue<QT>(q, co, ring + (size_t)issued * a.slot_bytes, wfull + issued, pol, lane);
-        multi_advance(ops, nops, a.nwarps, q, co);
-    }
+    fill_ring();
 
     auto sync = []() { __syncthreads(); };
     auto xbuf = [&](int i) {

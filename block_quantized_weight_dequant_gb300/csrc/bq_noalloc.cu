@@ -6,8 +6,10 @@
 // one file-scope device array of fixed size, which every GPU that loads the
 // library holds until the process exits.  Nothing is allocated per call: the
 // host side plans into static arrays, copies the tables into the device array
-// on the caller's stream, clears the counters, and launches the same kernel
-// the workspace path launches.
+// on the caller's stream, clears the counters, and launches: the multi-op
+// streaming kernel for independent ops, as the workspace path does, and the
+// cooperative executor for dependent stages (the workspace path runs those as
+// one launch per stage, whose per-stage tables would not fit the array).
 //
 // The copies read the static host arrays asynchronously: CUDA does not promise
 // that a copy from pageable memory has read its source when cudaMemcpyAsync

@@ -15,12 +15,14 @@ down -> ... -> lm_head):
 Attention itself, residual adds and the other norms are outside this stream
 (they are not weight streaming).  Every op reads the previous stage's output,
 so the stages are truly dependent, as in decode.  ``run_plan()`` runs the
-whole stream in one cooperative launch (bq_stream_plan_*); ``run_per_op()``
+stream through a plan (bq_stream_plan_*): one streaming-kernel launch per
+stage, each waiting for the stage before (programmatic dependent launch; the
+cooperative executor in one launch is the alternative); ``run_per_op()``
 launches one kernel per op in stage order; the two give identical bits.
 
 With ``chained=False`` every op instead reads an input vector of its own (the
 same shapes and weights, no data flowing between ops): the pure per-token
-weight stream, which the executor runs without any grid-wide barrier.
+weight stream, which a plan runs as ONE launch of the streaming kernel.
 
 With ``fused_qkv=True`` each layer's q, k and v run as ONE op over their
 rows concatenated at load time (``layer["qkv"]``, see ``concat_packed``)

@@ -210,19 +210,28 @@ bq_status bq_device_status(unsigned int *flags, int clear);
 int bq_tree_lanes(int64_t K);
 
 /* ------------------------------------------------------------------------
- * Per-token stream executor.
+ * Per-token stream plans.
  *
  * A decode step is a chain of dependent GEMV stages (per layer q|k|v, o,
  * gate+up, down, then the LM head).  The pages run it as one command buffer
  * per token because dispatch cost dominates small GEMVs (EdgeRunner blog
  * post, "What worked" #1; "We Wrote Our Own Inference Engine", 770 dispatches
- * per token).  A plan runs a whole list of GEMV ops in ONE cooperative
- * launch: ops of one stage run concurrently; a grid-wide barrier separates
- * stages, so an op may read an output written by an earlier stage.  Weights
- * never depend on earlier stages, so each warp streams the next stage's
- * weights into shared memory while it waits at the barrier.  Every output is
- * bit-identical to the single-op call (bq_gemv_q8_0 / _q4_0 /
- * bq_gemv_gate_up_silu) on the same inputs.
+ * per token).  A plan is that token's launch schedule, made once:
+ *  - a list of independent ops (no op reads another's output) runs as ONE
+ *    launch of the streaming kernel;
+ *  - a list of dependent stages runs as one launch of the streaming kernel
+ *    per stage, each allowed to start while the stage before drains
+ *    (programmatic dependent launch): it fills its shared-memory weight ring
+ *    first (the plan's stages write no weights), then waits for the stage
+ *    before and reads its input, so an op may read an output written by an
+ *    earlier stage.  Captured in a CUDA graph, the whole token is one graph
+ *    launch: the command buffer of the pages.
+ *  - the cooperative executor (one launch, grid-wide barriers between
+ *    stages) runs a dependent list whose stages the streaming kernel cannot
+ *    hold, and backs bq_stream_run_noalloc.
+ * Every output is bit-identical to the single-op call (bq_gemv_q8_0 /
+ * _q4_0 / _q4_k / bq_gemv_qkv_bias / bq_gemv_gate_up_silu) on the same
+ * inputs, whichever way the plan runs.
  * ------------------------------------------------------------------------ */
 typedef enum { BQ_OP_GEMV = 0, BQ_OP_GATE_UP_SILU = 1 } bq_op_kind;
 
@@ -244,7 +253,7 @@ typedef struct {
 typedef struct bq_stream_plan bq_stream_plan;
 
 /* Device workspace a plan of n_ops ops in n_stages stages needs (descriptor
- * tables and one barrier counter per stage); -1 for bad counts.  Besides the
+ * tables, per-stage CTA splits, barrier counters); -1 for bad counts.  Besides the
  * shape rules of bq_op, the distinct inputs of one stage (ops sharing an x and
  * its norm count once) must fit the executor's shared-memory x area together
  * with two ring slots per warp: about 150 KB of fp32 x per stage;
@@ -261,10 +270,12 @@ int64_t bq_stream_workspace_bytes(int n_ops, int n_stages);
 bq_status bq_stream_plan_create(int qtype, const bq_op *ops, int n_ops, void *workspace,
                                 int64_t workspace_bytes, bq_stream_plan **plan);
 
-/* Enqueue one run of the plan on `stream`: a memset of the stage counters and
- * one cooperative kernel launch; no host synchronisation, capturable in a
- * CUDA graph.  Two runs of one plan must not overlap on the GPU (they share
- * the counters). */
+/* Enqueue one run of the plan on `stream`: one kernel launch (independent
+ * ops), one per stage (dependent stages), or, for the executor, a memset of
+ * its stage counters and one cooperative launch (bq_stream_plan_launches
+ * says how many kernels); no host synchronisation, capturable in a CUDA
+ * graph.  Two runs of one plan must not overlap on the GPU (an executor run
+ * shares the counters, a staged run its stages' outputs). */
 bq_status bq_stream_plan_launch(const bq_stream_plan *plan, void *stream);
 
 /* Re-split a plan of independent ops (one launch of the streaming kernel)
@@ -281,12 +292,17 @@ bq_status bq_stream_plan_launch(const bq_stream_plan *plan, void *stream);
  * estimated time.  The split whose slowest CTA was fastest is kept.  Only
  * the assignment of tiles to CTAs changes: every output row is computed by
  * the same arithmetic, so outputs are bit-identical before and after.
- *  - 1 <= rounds <= 16, else BQ_ERR_SHAPE; a plan of dependent stages (the
- *    executor) returns BQ_OK untouched.
+ *  - 1 <= rounds <= 16, else BQ_ERR_SHAPE; a plan of dependent stages
+ *    returns BQ_OK untouched.
  *  - The runs read the ops' inputs and overwrite their outputs, on `stream`.
  *  - Synchronous (it reads the timings back): call it after
  *    bq_stream_plan_create and before capturing the plan in a CUDA graph. */
 bq_status bq_stream_plan_tune(bq_stream_plan *plan, int rounds, void *stream);
+
+/* Kernel launches one bq_stream_plan_launch enqueues: 1 for a list of
+ * independent ops or a list run by the cooperative executor, the number of
+ * stages for a staged plan; -1 for NULL. */
+int bq_stream_plan_launches(const bq_stream_plan *plan);
 
 /* Free the host object (the workspace stays the caller's). */
 bq_status bq_stream_plan_destroy(bq_stream_plan *plan);
@@ -302,7 +318,8 @@ bq_status bq_stream_plan_destroy(bq_stream_plan *plan);
  * forbids raw cudaMalloc beside it; or a latency-critical path that cannot
  * afford cudaMalloc/cudaFree, which can synchronise the device.  For them
  * this call runs the same ops as bq_stream_plan_create + bq_stream_plan_launch
- * (same validation, same kernel, bit-identical outputs) with the descriptor
+ * (same validation, bit-identical outputs; a list of dependent stages runs
+ * on the cooperative executor in one launch) with the descriptor
  * tables and stage counters kept in one fixed device array inside the
  * library, which every GPU that loads the library holds until the process
  * exits (82 KiB).  The caller still passes the inputs and outputs (in

@@ -1,7 +1,10 @@
-"""The per-token stream executor (one cooperative launch) against the
-launch-per-op path: every output of every stage bit-identical, on chained
-decode streams where each stage reads the previous stage's output; plus the
-oracle bound on the final outputs and repeat-run determinism."""
+"""Stream plans against the launch-per-op path: every output of every stage
+bit-identical, on chained decode streams where each stage reads the previous
+stage's output (run as one streaming-kernel launch per stage, or by the
+cooperative executor in one launch), and on independent streams (one launch
+of the streaming kernel); plus the oracle bound on the final outputs and
+repeat-run determinism."""
+import contextlib
 import ctypes
 
 import numpy as np
@@ -49,6 +52,22 @@ def snapshot(ds):
     return [op.y.clone() for op in ds.ops]
 
 
+@contextlib.contextmanager
+def plan_kind(kind):
+    """Plans of dependent stages created inside run as `kind`: "staged" (one
+    launch per stage), "executor" (one cooperative launch) or None (the
+    library's default); a test hook outside the public header."""
+    from block_quantized_weight_dequant_gb300 import _lib
+    f = _lib.get().bq_internal_set_plan_kind
+    f.argtypes = [ctypes.c_int]
+    f.restype = None
+    f({"staged": 1, "executor": 0, None: -1}[kind])
+    try:
+        yield
+    finally:
+        f(-1)
+
+
 STREAMS = [
     ("q8_0", 3, 512, 512, 128, 1024, 3000),      # G = 4 and 8, whole rows per slot
     ("q8_0", 2, 1024, 2048, 512, 3072, 20000),   # Qwen3-0.6B layer shapes, chunked down
@@ -84,17 +103,23 @@ def test_tuned_plan_is_bitwise_the_same(qt, n_layers, hidden, q_dim, kv_dim, int
     assert bq.device_status(clear=True) == 0
 
 
-@pytest.mark.parametrize("chained", [True, False], ids=["chained", "independent"])
+@pytest.mark.parametrize("mode", ["staged", "executor", "independent"])
 @pytest.mark.parametrize("qt,n_layers,hidden,q_dim,kv_dim,inter,vocab", STREAMS)
 def test_plan_matches_launch_per_op_bitwise(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab,
-                                            chained):
-    """chained: the stream executor with grid-wide stage barriers; independent:
-    the multi-op streaming kernel (the planner finds no dependence)."""
+                                            mode):
+    """staged: chained stages, one streaming-kernel launch per stage (the
+    default); executor: chained stages in one cooperative launch with
+    grid-wide barriers; independent: one launch of the multi-op streaming
+    kernel (the planner finds no dependence)."""
+    chained = mode != "independent"
     ds = make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab, chained=chained)
     ds.run_per_op()
     want = snapshot(ds)
     for op in ds.ops:
         op.y.fill_(float("nan"))
+    with plan_kind(mode if chained else None):
+        ds.plan()
+    assert ds.plan().launches == (ds.n_stages if mode == "staged" else 1)
     ds.run_plan()
     got = snapshot(ds)
     for i, (g, w) in enumerate(zip(got, want)):
@@ -117,11 +142,13 @@ def test_plan_final_output_within_oracle_bound():
     assert_gemv_close(lm.y.cpu().numpy(), y_ref, S, "plan lm_head")
 
 
-def test_plan_in_cuda_graph():
+@pytest.mark.parametrize("kind", ["staged", "executor"])
+def test_plan_in_cuda_graph(kind):
     ds = make_stream("q8_0", 2, 512, 512, 128, 1024, 2000)
     ds.run_per_op()
     want = snapshot(ds)
-    ds.plan()  # created before capture (it synchronises)
+    with plan_kind(kind):
+        ds.plan()  # created before capture (it synchronises)
     s = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
@@ -191,15 +218,17 @@ def test_plan_rejects_outputs_overlapping_weights_or_own_stage():
     bq.StreamPlan("q8_0", [bq.StreamOp(0, P2, x, y2), bq.StreamOp(1, P, y2, y)])
 
 
-@pytest.mark.parametrize("chained", [True, False], ids=["chained", "independent"])
+@pytest.mark.parametrize("mode", ["staged", "executor", "independent"])
 @pytest.mark.parametrize("qt,n_layers,hidden,q_dim,kv_dim,inter,vocab", [
     ("q8_0", 2, 1024, 2048, 512, 3072, 7000),   # Qwen3-0.6B layer shapes
     ("q4_0", 2, 3584, 3584, 512, 18944, 3000),  # 7B layer shapes
 ])
 def test_fused_qkv_bias_plan_matches_launch_per_op_bitwise(qt, n_layers, hidden, q_dim, kv_dim,
-                                                           inter, vocab, chained):
-    """One fused q|k|v + bias op per layer (4 ops per layer): the plan (stream
-    executor or multi-op kernel) and one launch per op agree bit for bit."""
+                                                           inter, vocab, mode):
+    """One fused q|k|v + bias op per layer (4 ops per layer): the plan (one
+    launch per stage, the stream executor, or the multi-op kernel) and one
+    launch per op agree bit for bit."""
+    chained = mode != "independent"
     ds = make_stream(qt, n_layers, hidden, q_dim, kv_dim, inter, vocab, chained=chained,
                      fused_qkv=True)
     assert len(ds.ops) == 4 * n_layers + 1
@@ -207,6 +236,8 @@ def test_fused_qkv_bias_plan_matches_launch_per_op_bitwise(qt, n_layers, hidden,
     want = snapshot(ds)
     for op in ds.ops:
         op.y.fill_(float("nan"))
+    with plan_kind(mode if chained else None):
+        ds.plan()
     ds.run_plan()
     torch.cuda.synchronize()
     for i, (op, w) in enumerate(zip(ds.ops, want)):
@@ -235,7 +266,8 @@ def test_stage_barrier_wait_runs_out_and_reports():
     ds.run_per_op()
     want = snapshot(ds)
     assert bq.device_status(clear=True) == 0
-    plan = ds.plan()
+    with plan_kind("executor"):
+        plan = ds.plan()
     assert hook(plan._handle, 1, 1_000_000) == 0
     plan.launch()
     flags = ctypes.c_uint(0)
@@ -250,6 +282,9 @@ def test_stage_barrier_wait_runs_out_and_reports():
     for i, (g, w) in enumerate(zip(snapshot(ds), want)):
         assert torch.equal(g.view(torch.int32), w.view(torch.int32)), f"op {i} differs after"
     assert bq.device_status(clear=True) == 0
-    # plans of independent ops have no stage barrier to break
+    # plans of independent ops, and staged plans, have no stage barrier to break
     di = make_stream("q8_0", 1, 512, 512, 128, 1024, 2000, chained=False)
     assert hook(di.plan()._handle, 1, 1_000_000) == -1
+    dst = make_stream("q8_0", 1, 512, 512, 128, 1024, 2000, chained=True)
+    with plan_kind("staged"):
+        assert hook(dst.plan()._handle, 1, 1_000_000) == -1
