@@ -29,11 +29,14 @@
 // its first weight items into L2, and only then waits for the kernel before it
 // in the stream (griddepcontrol.wait) before reading any input.  A prefetch is
 // a hint that binds no value, so this is safe even if the kernel before wrote
-// the weights.  A stage of a staged plan after the first knows the kernel
-// before it (the plan's previous stage, which writes no weights: the planner
-// rejects outputs overlapping weights), so it copies its first weight items
-// into its ring before the wait (early_ring) and computes as soon as its
-// input is staged.
+// the weights.  But only this kernel lets its dependents start early, and it
+// writes nothing but its outputs (and the error word): any other kernel
+// before it completes before it starts.  So single calls, whose contract
+// excludes packed weights written by an earlier GEMV call, and the stages of
+// a staged plan after the first (the planner rejects outputs overlapping
+// weights) copy their first weight items into the ring before the wait
+// (early_ring) and compute as soon as their input is staged; the first
+// stage of a plan falls under the single calls' contract.
 //
 // Arithmetic is bq_dot.cuh's fixed tree: every output is bit-identical to the
 // single-op kernels and across R.

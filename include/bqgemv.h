@@ -38,6 +38,15 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  Every call only enqueues work and returns; results are ready
  *    when the stream reaches that point.
+ *  - Back-to-back GEMV calls on one stream overlap: a call may start while
+ *    the GEMV call before it (of this library) drains, and copy its packed
+ *    weights into shared memory then; it reads its inputs and writes its
+ *    outputs only after that call has completed.  So the packed weights of a
+ *    call must not be written by an earlier GEMV call of this library on the
+ *    stream (those calls write only their outputs: the one thing excluded is
+ *    an output buffer reused as a later call's packed weights).  Any other
+ *    work before a call, bq_quantize_pack and foreign kernels included,
+ *    completes before the call starts.
  *  - Arguments are validated on the host before anything is launched; a bad
  *    argument returns an error status and enqueues nothing.  Launch failures
  *    return BQ_ERR_CUDA.  Faults inside a kernel surface at the caller's next
