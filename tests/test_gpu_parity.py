@@ -262,6 +262,29 @@ def test_verify_rows_memcmp_equal_to_decode(qt, M, K, R):
         assert_gemv_close(Y[r], y_ref, S, f"verify {qt} {M}x{K} R={R} row {r}")
 
 
+@pytest.mark.parametrize("qt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("R", [2, 3, 5])
+def test_panel_verify_several_tiles_per_warp(qt, R):
+    """An R x K input over the staging limit (128 KB of fp32) is cut into
+    K-panels; with more tiles than the GPU holds warps, a warp walks several
+    tiles through each panel and parks their partial sums in shared memory
+    between panels.  Every row stays memcmp-equal to decode; sampled rows are
+    within the oracle bound."""
+    M, K = 10000, 17408
+    P = gpu_pack(qt, weights(M, K, seed=35, spread=False))
+    X = xvec(K, seed=35, R=R)
+    Y = bq.gemv_verify(qt, P, cuda(X)).cpu().numpy()
+    Pn = P.cpu().numpy()
+    rng = np.random.default_rng([35, R])
+    idx = np.unique(np.r_[0, M - 1, rng.choice(M, 30, replace=False)])
+    Ps = np.ascontiguousarray(Pn[idx])
+    for r in range(R):
+        y1 = bq.gemv(qt, P, cuda(X[r])).cpu().numpy()
+        assert Y[r].tobytes() == y1.tobytes(), f"row {r} differs from decode"
+        y_ref, S = ora().gemv(QT[qt], Ps, len(idx), K, X[r].astype(np.float64))
+        assert_gemv_close(Y[r][idx], y_ref, S, f"panel verify {qt} {M}x{K} R={R} row {r}")
+
+
 # ---------------------------------------------------------------------------
 # K beyond what the streaming kernel stages in shared memory for one input row
 # (32768 fp32): the documented range goes to K = 2^18 for every quantized call
