@@ -58,7 +58,10 @@ struct Tunables {
                                      // starts its dependents early, and it writes no weights;
                                      // measured on GB300: 3072x1024 Q8_0 GEMV 781 -> 827 GB/s,
                                      // gate+up 962 -> 1015, verify R = 1 2481 -> 2557)
-    int single_rowmode = 4;          // single calls: row mode up to this many unit tiles per SM (0: off)
+    int single_rowmode = 2;          // single calls: row mode up to this many unit tiles per SM (0: off;
+                                     // measured on GB300 with the early ring fill: 3072x1024 Q8_0
+                                     // GEMV 824 GB/s at 4, 947 at 2 or less; chained Qwen3-0.6B
+                                     // token 1014 at 4 or 2, 999 at 1 or 0)
     int verify_nr = 0;               // verify calls (R > 1): weight rows per lane (1 or 2; 0: by R)
     int plan_pdl = 0;                // op-list plans: allow programmatic dependent launch
     int plan_early = 1;              // staged plans: stages after the first fill their weight
