@@ -674,6 +674,7 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
         x_buffers = 2;
     }
     x_floats += multi_sum_floats(c.qtype, R, x_rstride);
+    if (m.gamma) x_floats += x_rstride;  // gate+up (R = 1, whole K): room for the staged gain
     const int ring_off = (MULTI_X_OFF + x_buffers * x_floats * 4 + 127) / 128 * 128;
     const long long budget = (long long)cap - ring_off;
     const int maxw = multi_max_warps(c.qtype, R);
@@ -747,6 +748,7 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
     a->x_floats = x_floats;
     a->x_buffers = x_buffers;
     a->panel_units = PU;
+    a->gain_staged = m.gamma != nullptr;
     a->inline_op = 1;
     a->wait_ns = g_wait_ns.load();
     a->early_ring = t.single_early;
@@ -785,6 +787,7 @@ void fill_multi_args(const MultiGeometry &geo, int n_ops, const MultiOp *ops,
     a->x_floats = geo.x_floats;
     a->x_buffers = geo.x_buffers;
     a->panel_units = geo.panel_units;
+    a->gain_staged = 0;
     a->inline_op = 0;
     a->cta_ns = nullptr;
     a->wait_ns = g_wait_ns.load();

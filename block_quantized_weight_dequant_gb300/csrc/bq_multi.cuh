@@ -77,6 +77,8 @@ struct MultiArgs {
     int x_floats;               // floats per x buffer
     int x_buffers;              // 1 or 2
     int panel_units;            // 0: an op's whole x is staged; else units of K per panel
+    int gain_staged;            // 1: the buffers have room for the op's RMSNorm gain, which
+                                // is staged with x (single gate+up calls); 0: read from L2
     int inline_op;              // 1: `op` is the only op; CTA c takes tiles [cT/grid, (c+1)T/grid)
     unsigned long long *cta_ns; // list mode: each CTA's duration in ns (plan tuning), or null
     unsigned long long wait_ns; // limit of every bounded wait
@@ -99,6 +101,12 @@ __host__ __device__ constexpr int multi_max_warps(int QT, int R) {
 // block sums (Q4_K; none for the other formats), rounded to 128 bytes
 __host__ __device__ constexpr int multi_sum_floats(int QT, int R, int rstride) {
     return QT == QT_Q4_K ? (R * (rstride / 32) + 31) / 32 * 32 : 0;
+}
+// float offset in an x buffer of the staged RMSNorm gain (R = 1 gate+up: a
+// plain copy after the input row and its block sums, when the planner sized
+// the buffer for it)
+__host__ __device__ constexpr int multi_gain_off(int QT, int R, int rstride) {
+    return R * rstride + multi_sum_floats(QT, R, rstride);
 }
 static_assert(MULTI_MAX_WARPS * 32 <= 1024, "one CTA");
 constexpr int MULTI_MAX_D = 4;
@@ -265,14 +273,18 @@ __device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc) {
 }
 
 // All threads: start the copies of elements [k0, k1) of every input row into
-// an x buffer (permuted chunk layout of XSmem, relative to k0), one group.
+// an x buffer (permuted chunk layout of XSmem, relative to k0), and of the
+// op's RMSNorm gain (plain layout at goff), in one group: both fetches are in
+// flight together.
 __device__ __forceinline__ void multi_stage_x(const MultiOp &o, int R, int k0, int k1, float *dst,
-                                              int rstride, int tid, int nthr) {
+                                              int rstride, int goff, int tid, int nthr) {
     const int n4 = (k1 - k0) >> 2;
     for (int i = tid; i < R * n4; i += nthr) {
         const int r = i / n4, c = i - r * n4;
         cp_async_16(dst + r * rstride + 4 * x_chunk_pos(c), o.x + (size_t)r * o.K + k0 + 4 * c);
     }
+    if (o.gamma && goff >= 0)  // gate+up: R = 1, whole K
+        for (int c = tid; c < n4; c += nthr) cp_async_16(dst + goff + 4 * c, o.gamma + 4 * c);
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
@@ -371,13 +383,16 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
     auto xbuf = [&](int i) {
         return reinterpret_cast<float *>(smem + a.x_off) + (size_t)(i % a.x_buffers) * a.x_floats;
     };
+    // the staged gain's offset in an x buffer (-1: not staged)
+    const int goff = a.gain_staged ? multi_gain_off(QT, R, a.x_rstride) : -1;
     // panel mode exists only in the verify instances (R > 1)
     const int PU = R > 1 ? a.panel_units : 0;
     auto n_panels = [&](const MultiOp &o) { return PU ? (o.nsc + PU - 1) / PU : 1; };
     // x phase i = (op, panel); the first phase's copies start now
     {
         const MultiOp &o = ops[op0];
-        multi_stage_x(o, R, 0, PU ? min(o.K, PU * 256) : o.K, xbuf(0), a.x_rstride, threadIdx.x, nthr);
+        multi_stage_x(o, R, 0, PU ? min(o.K, PU * 256) : o.K, xbuf(0), a.x_rstride, goff, threadIdx.x,
+                      nthr);
     }
 
     int e = 0, landed = 0;  // items consumed (or skipped after an error); items seen landed
@@ -424,7 +439,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                 const MultiOp &n = ops[nop];
                 const int k0 = npn * PU * 256;
                 const int k1 = PU ? min(n.K, k0 + PU * 256) : n.K;
-                multi_stage_x(n, R, k0, k1, dst, a.x_rstride, threadIdx.x, nthr);
+                multi_stage_x(n, R, k0, k1, dst, a.x_rstride, goff, threadIdx.x, nthr);
             };
             if (has_next && a.x_buffers == 2) stage_next(xbuf(phase + 1));
             if (gamma) {
@@ -434,7 +449,8 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                 for (int c = threadIdx.x; c < K / 4; c += nthr) {
                     float4 *p = reinterpret_cast<float4 *>(xa + 4 * x_chunk_pos(c));
                     const float4 v = *p;
-                    const float4 g = __ldg(reinterpret_cast<const float4 *>(gamma) + c);
+                    const float4 g = goff >= 0 ? reinterpret_cast<const float4 *>(xa + goff)[c]
+                                               : __ldg(reinterpret_cast<const float4 *>(gamma) + c);
                     *p = make_float4(__fmul_rn(__fmul_rn(v.x, rs), g.x), __fmul_rn(__fmul_rn(v.y, rs), g.y),
                                      __fmul_rn(__fmul_rn(v.z, rs), g.z), __fmul_rn(__fmul_rn(v.w, rs), g.w));
                 }
