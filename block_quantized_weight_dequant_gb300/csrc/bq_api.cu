@@ -74,6 +74,8 @@ struct Tunables {
                                      // executor, one launch with grid-wide barriers)
     int tree_waste = 8;              // the tree's lanes G leave at most 1/tree_waste of slots idle
     int verify_wave = 1;             // verify panels: two rows per lane when one needs two waves
+    int split_by_op = 1;             // op lists with at most half as many ops as CTAs: CTAs of
+                                     // each op's own (no CTA meets an op boundary)
 };
 
 const Tunables &tunables() {
@@ -107,6 +109,7 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "vnr") && (val == 1 || val == 2)) v.verify_nr = val;
             else if (!std::strcmp(tok, "waste") && val >= 2 && val <= 64) v.tree_waste = val;
             else if (!std::strcmp(tok, "vwave") && val >= 0 && val <= 1) v.verify_wave = val;
+            else if (!std::strcmp(tok, "opsplit") && val >= 0 && val <= 1) v.split_by_op = val;
             else if (!std::strcmp(tok, "ppdl") && val >= 0 && val <= 1) v.plan_pdl = val;
             else if (!std::strcmp(tok, "staged") && val >= 0 && val <= 1) v.plan_staged = val;
             else if (!std::strcmp(tok, "early") && val >= 0 && val <= 1) v.plan_early = val;
@@ -470,6 +473,51 @@ bq_status plan_exec_tables(int qtype, const bq_op *ops, int n_ops, ExecOp *eo, E
 
 bool multi_chunking(MultiOp &m, int ub, int slot_cap, bool rows_low);
 
+// CTA split of a list of n <= grid ops in which every op has CTAs of its own:
+// op i gets k_i >= 1 CTAs, the grid shared by bytes (largest remainder), and
+// its tiles (ntiles[i], the ops' tiles concatenated in order) split evenly
+// among them.  out[c] is CTA c's first tile, out[grid] the total.
+void split_by_op(const long long *bytes, const int *ntiles, int n, int grid, int *out) {
+    long long total = 0;
+    for (int i = 0; i < n; ++i) total += bytes[i];
+    std::vector<int> k((size_t)n, 1);
+    std::vector<double> rem((size_t)n, 0.0);
+    int used = n;
+    for (int i = 0; i < n; ++i) {
+        const double q = total > 0 ? (double)grid * (double)bytes[i] / (double)total : 0.0;
+        const int f = std::max(1, (int)q);
+        rem[(size_t)i] = q - f;
+        k[(size_t)i] = f;
+        used += f - 1;
+    }
+    // too many (the at-least-one rule): take from the ops with the smallest remainder
+    while (used > grid) {
+        int j = -1;
+        for (int i = 0; i < n; ++i)
+            if (k[(size_t)i] > 1 && (j < 0 || rem[(size_t)i] < rem[(size_t)j])) j = i;
+        if (j < 0) break;
+        --k[(size_t)j];
+        rem[(size_t)j] += 1.0;
+        --used;
+    }
+    // too few: give to the ops with the largest remainder
+    while (used < grid) {
+        int j = 0;
+        for (int i = 1; i < n; ++i)
+            if (rem[(size_t)i] > rem[(size_t)j]) j = i;
+        ++k[(size_t)j];
+        rem[(size_t)j] -= 1.0;
+        ++used;
+    }
+    int c = 0;
+    long long base = 0;
+    for (int i = 0; i < n; ++i) {
+        for (int j = 0; j < k[(size_t)i]; ++j) out[c++] = (int)(base + (long long)ntiles[i] * j / k[(size_t)i]);
+        base += ntiles[i];
+    }
+    while (c <= grid) out[c++] = (int)base;
+}
+
 bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo, int *cta_tiles,
                             MultiGeometry *geo) {
     const Tunables &t = tunables();
@@ -550,20 +598,32 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
     const int err = fmt_multi_occupancy(qtype, NR, 1, threads, smem, &occ);
     if (err != 0 || occ < 1) return BQ_ERR_CUDA;
     const int grid = std::min(MULTI_MAX_CTAS, num_sms_current() * occ);
-    // byte-balanced contiguous tile ranges
-    long long total = 0;
-    for (int i = 0; i < n_ops; ++i)
-        for (int k = 0; k < mo[i].ntiles; ++k)
-            total += (long long)std::min(mo[i].rpw, mo[i].M - k * mo[i].rpw) * mo[i].rb * mo[i].nmat;
-    cta_tiles[0] = 0;
-    int c = 1;
-    long long acc = 0;
-    for (int i = 0; i < n_ops && c < grid; ++i)
-        for (int k = 0; k < mo[i].ntiles && c < grid; ++k) {
-            acc += (long long)std::min(mo[i].rpw, mo[i].M - k * mo[i].rpw) * mo[i].rb * mo[i].nmat;
-            while (c < grid && acc * grid >= total * c) cta_tiles[c++] = mo[i].tile_base + k + 1;
+    if (t.split_by_op && 2LL * n_ops <= grid) {
+        // few ops (a stage's q, k, v): every op gets CTAs of its own, so that no
+        // CTA meets an op boundary (where all its warps wait and x is staged again)
+        std::vector<long long> ob((size_t)n_ops);
+        std::vector<int> ot((size_t)n_ops);
+        for (int i = 0; i < n_ops; ++i) {
+            ob[(size_t)i] = (long long)mo[i].M * mo[i].rb * mo[i].nmat;
+            ot[(size_t)i] = mo[i].ntiles;
         }
-    while (c <= grid) cta_tiles[c++] = (int)tiles;
+        split_by_op(ob.data(), ot.data(), n_ops, grid, cta_tiles);
+    } else {
+        // byte-balanced contiguous tile ranges
+        long long total = 0;
+        for (int i = 0; i < n_ops; ++i)
+            for (int k = 0; k < mo[i].ntiles; ++k)
+                total += (long long)std::min(mo[i].rpw, mo[i].M - k * mo[i].rpw) * mo[i].rb * mo[i].nmat;
+        cta_tiles[0] = 0;
+        int c = 1;
+        long long acc = 0;
+        for (int i = 0; i < n_ops && c < grid; ++i)
+            for (int k = 0; k < mo[i].ntiles && c < grid; ++k) {
+                acc += (long long)std::min(mo[i].rpw, mo[i].M - k * mo[i].rpw) * mo[i].rb * mo[i].nmat;
+                while (c < grid && acc * grid >= total * c) cta_tiles[c++] = mo[i].tile_base + k + 1;
+            }
+        while (c <= grid) cta_tiles[c++] = (int)tiles;
+    }
     geo->grid = grid;
     geo->threads = threads;
     geo->nwarps = nwarps;
@@ -1288,6 +1348,9 @@ int bq_internal_lane_order(int G, int S0, int U, int pad, int rows_low, int *S, 
 void bq_internal_rebalance(const double *tile_bytes, long long n, int grid, const int *ct,
                            const double *cta_time, int *out) {
     rebalance(tile_bytes, n, grid, ct, cta_time, out);
+}
+void bq_internal_split_by_op(const long long *op_bytes, const int *op_tiles, int n, int grid, int *out) {
+    bq::split_by_op(op_bytes, op_tiles, n, grid, out);
 }
 
 int bq_stream_plan_launches(const bq_stream_plan *plan) {

@@ -1,5 +1,6 @@
 """Host logic of the streaming kernel's planner, on the CPU (no GPU needed):
-the per-op lane-order search and the CTA split by measured time.
+the per-op lane-order search, the CTA split by measured time, and the split
+of a short op list in which every op has CTAs of its own.
 
 The lane order decides which lane bits of a warp form the unit column l and
 which the row rho.  Its contract, for 16-byte shared-memory loads on GB300:
@@ -26,6 +27,8 @@ def lib():
                                          ctypes.POINTER(i32)]
     L.bq_internal_rebalance.restype = None
     L.bq_internal_rebalance.argtypes = [vp, ctypes.c_longlong, i32, vp, vp, vp]
+    L.bq_internal_split_by_op.restype = None
+    L.bq_internal_split_by_op.argtypes = [vp, vp, i32, i32, vp]
     return L
 
 
@@ -163,3 +166,41 @@ def test_rebalance_gives_idle_ctas_the_mean_rate(lib):
     cost = owner_cost(tb, ct[[0, 1, 3]], d[[0, 2]])
     per = [cost[out[c]:out[c + 1]].sum() for c in range(3)]
     assert max(per) - min(per) <= 2 * cost.max()
+
+
+def split_by_op(lib, op_bytes, op_tiles, grid):
+    ob = np.asarray(op_bytes, dtype=np.int64)
+    ot = np.asarray(op_tiles, dtype=np.int32)
+    out = np.zeros(grid + 1, dtype=np.int32)
+    lib.bq_internal_split_by_op(ob.ctypes.data, ot.ctypes.data, len(ob), grid, out.ctypes.data)
+    return out
+
+
+@pytest.mark.parametrize("op_bytes,op_tiles,grid", [
+    ([2048, 1024, 1024], [256, 128, 128], 152),      # a layer's q, k, v
+    ([1, 1, 1, 10 ** 9], [4, 4, 4, 3000], 152),      # tiny ops beside a large one
+    ([5, 7], [1, 1], 152),                            # fewer tiles than CTAs
+    ([3] * 76, [9] * 76, 152),                        # half as many ops as CTAs
+    ([1000, 1], [50, 50], 9),
+])
+def test_split_by_op_gives_every_op_its_own_ctas(lib, op_bytes, op_tiles, grid):
+    out = split_by_op(lib, op_bytes, op_tiles, grid)
+    bounds = np.concatenate([[0], np.cumsum(op_tiles)])
+    assert out[0] == 0 and out[-1] == bounds[-1]
+    assert np.all(np.diff(out) >= 0)  # contiguous ranges covering every tile
+    # no CTA range crosses an op boundary, and every op has at least one CTA
+    owner = np.searchsorted(bounds, out[:-1], side="right") - 1
+    for c in range(grid):
+        lo, hi = out[c], out[c + 1]
+        if hi > lo:
+            assert bounds[owner[c]] <= lo and hi <= bounds[owner[c] + 1], (c, lo, hi)
+    ctas = np.bincount(owner[np.diff(out) >= 0], minlength=len(op_tiles))
+    assert np.all(ctas >= 1)
+    assert ctas.sum() == grid
+    # within an op the tiles are split evenly (sizes differ by at most one)
+    for i in range(len(op_tiles)):
+        sizes = np.diff(out)[owner == i]
+        assert sizes.max() - sizes.min() <= 1
+    # CTAs follow the bytes: within one CTA of the proportional share
+    share = grid * np.asarray(op_bytes, dtype=np.float64) / np.sum(op_bytes)
+    assert np.all(np.abs(ctas - np.maximum(1, share)) <= len(op_tiles))
