@@ -63,12 +63,12 @@ def token_cfg(config):
 # the traffic is null until it is captured again.
 NCU_TRAFFIC = {
     # (config, inputs): (bytes per launch, csrc_digest() at capture, summary)
-    ("cfg2", "independent"): (606394624, "096f13b9e6196aef917874f8a0008fe4b67a0678ef43f883e81c0c9bcecd1d03",
+    ("cfg2", "independent"): (606401536, "56fe7810135ffdeb35132c297a024c85df92f8df744e69057eca693dd83f4719",
                               "profiles/multi_kernel_q8_0_qwen3_0.6b_stream.md"),
     # captured on 2 of the 28 layers (+ LM head) and scaled by algorithmic bytes
-    ("cfg3", "independent"): (4006528652, "096f13b9e6196aef917874f8a0008fe4b67a0678ef43f883e81c0c9bcecd1d03",
+    ("cfg3", "independent"): (4006449881, "56fe7810135ffdeb35132c297a024c85df92f8df744e69057eca693dd83f4719",
                               "profiles/multi_kernel_q4_0_7b_stream.md"),
-    ("cfg3k", "independent"): (4007056778, "096f13b9e6196aef917874f8a0008fe4b67a0678ef43f883e81c0c9bcecd1d03",
+    ("cfg3k", "independent"): (4006272645, "56fe7810135ffdeb35132c297a024c85df92f8df744e69057eca693dd83f4719",
                                "profiles/multi_kernel_q4_k_7b_stream.md"),
 }
 
