@@ -74,6 +74,7 @@ struct Tunables {
                                      // executor, one launch with grid-wide barriers)
     int tree_waste = 8;              // the tree's lanes G leave at most 1/tree_waste of slots idle
     int verify_wave = 1;             // verify panels: two rows per lane when one needs two waves
+    int short_lists = 1;             // op lists with few tiles per SM: only the warps they need
     int split_by_op = 1;             // op lists with at most half as many ops as CTAs: CTAs of
                                      // each op's own (no CTA meets an op boundary)
 };
@@ -110,6 +111,7 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "waste") && val >= 2 && val <= 64) v.tree_waste = val;
             else if (!std::strcmp(tok, "vwave") && val >= 0 && val <= 1) v.verify_wave = val;
             else if (!std::strcmp(tok, "opsplit") && val >= 0 && val <= 1) v.split_by_op = val;
+            else if (!std::strcmp(tok, "short") && val >= 0 && val <= 1) v.short_lists = val;
             else if (!std::strcmp(tok, "ppdl") && val >= 0 && val <= 1) v.plan_pdl = val;
             else if (!std::strcmp(tok, "staged") && val >= 0 && val <= 1) v.plan_staged = val;
             else if (!std::strcmp(tok, "early") && val >= 0 && val <= 1) v.plan_early = val;
@@ -579,8 +581,21 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
     if (2 * x_floats * 4 <= t.multi_x2_max && warps_for(2) >= warps_for(1)) x_buffers = 2;
     const int ring_off = (x_off + x_buffers * x_floats * 4 + 127) / 128 * 128;
     const long long budget = (long long)cap - ring_off;
-    const int nwarps = warps_for(x_buffers);
+    int nwarps = warps_for(x_buffers);
     if (nwarps < 1) return BQ_ERR_SHAPE;
+    // A short list (fewer tiles per SM than warps fit): one CTA per SM with the
+    // warps its tiles need, so that the launch leaves shared memory to the next
+    // launch's CTAs (a staged plan's next stage then starts, fills its rings
+    // and waits beside this one instead of after it).
+    const int nsms = num_sms_current();
+    bool short_list = false;
+    if (t.short_lists && nsms > 0) {
+        const long long per_sm = (tiles + nsms - 1) / nsms;
+        if (per_sm < nwarps) {
+            nwarps = (int)std::max<long long>(1, per_sm);
+            short_list = true;
+        }
+    }
     const int slot_cap = (int)(budget / ((long long)nwarps * D)) / 128 * 128;
     // pass 2: per op, whole rows in a slot when they fit, else the largest
     // chunk of a multiple of G units
@@ -597,7 +612,7 @@ bq_status plan_multi_tables(int qtype, const bq_op *ops, int n_ops, MultiOp *mo,
     int occ = 0;
     const int err = fmt_multi_occupancy(qtype, NR, 1, threads, smem, &occ);
     if (err != 0 || occ < 1) return BQ_ERR_CUDA;
-    const int grid = std::min(MULTI_MAX_CTAS, num_sms_current() * occ);
+    const int grid = short_list ? nsms : std::min(MULTI_MAX_CTAS, nsms * occ);
     if (t.split_by_op && 2LL * n_ops <= grid) {
         // few ops (a stage's q, k, v): every op gets CTAs of its own, so that no
         // CTA meets an op boundary (where all its warps wait and x is staged again)
