@@ -53,6 +53,9 @@ struct Tunables {
     int multi_x2_max = 32 * 1024;    // op lists: two x buffers when together at most this
     int single_x_max = 128 * 1024;   // single calls: largest staged R x K input (else panels)
     int single_pdl = 1;              // single calls: allow programmatic dependent launch
+    int gu_pair = 1;                 // single gate+up calls: the paired instance (1: Q8_0, 2: Q8_0
+                                     // and Q4_0, 0: off; measured on GB300, 3072x1024 Q8_0 calls
+                                     // 1039 -> 1160 GB/s)
     int single_early = 1;            // single calls: fill the weight rings before waiting for
                                      // the kernel before (only this library's streaming kernel
                                      // starts its dependents early, and it writes no weights;
@@ -106,6 +109,7 @@ const Tunables &tunables() {
             else if (!std::strcmp(tok, "sx") && val >= 16384) v.single_x_max = val;
             else if (!std::strcmp(tok, "pdl") && val >= 0 && val <= 1) v.single_pdl = val;
             else if (!std::strcmp(tok, "searly") && val >= 0 && val <= 1) v.single_early = val;
+            else if (!std::strcmp(tok, "gupair") && val >= 0 && val <= 2) v.gu_pair = val;
             else if (!std::strcmp(tok, "srow") && val >= 0 && val <= 64) v.single_rowmode = val;
             else if (!std::strcmp(tok, "vnr") && (val == 1 || val == 2)) v.verify_nr = val;
             else if (!std::strcmp(tok, "waste") && val >= 2 && val <= 64) v.tree_waste = val;
@@ -694,10 +698,10 @@ bool multi_chunking(MultiOp &m, int ub, int slot_cap, bool rows_low) {
     return true;
 }
 
-bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
+bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo, bool pair) {
     const Tunables &t = tunables();
     const int bb = block_bytes(c.qtype), ub = 8 * bb;
-    const int D = std::min(t.multi_d, MULTI_MAX_D);
+    int D = std::min(t.multi_d, MULTI_MAX_D);
     const int R = c.R;
     // verify: two weight rows per lane share each x read up to R = 4; from
     // R = 5 on the R partial sums per row fill the registers and one row per
@@ -769,11 +773,20 @@ bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo) {
         m.ntiles = (int)((c.M + rows - 1) / rows);
         NR = 0;
     }
+    // gate+up in unit mode: the paired instance (NR = 3 tag), which takes the
+    // gate and up items of a chunk together, with four ring slots (two pairs)
+    // when they fit
+    if (pair && gu && !rowmode && !PU &&
+        ((t.gu_pair >= 1 && c.qtype == BQ_Q8_0) || (t.gu_pair >= 2 && c.qtype == BQ_Q4_0))) {
+        NR = 3;
+        D = MULTI_MAX_D;
+    }
     // warps: enough for the tiles of one CTA per SM, at most what fits
     const int k1 = std::min(m.nsc, m.G);
     int S1 = 0, um1 = 0;
     lane_order_any(m.G, k1 * ub / 16, ub / 16, &S1, &um1, c.qtype == BQ_Q4_0 && R == 1);
     const int slot_min = rowmode ? m.rpw * m.rb : m.rpw * S1 * 16;
+    if (NR == 3 && budget < (long long)D * slot_min) D = 2;
     if (budget < (long long)D * slot_min) return false;
     const int fit = (int)std::min<long long>(maxw, budget / ((long long)D * slot_min));
     const int want = (int)std::min<long long>(fit, (m.ntiles + nsms - 1) / nsms);
@@ -1009,7 +1022,9 @@ bq_status plan_staged(int qtype, const bq_op *ops, int n_ops, const bq::ExecStag
                        gu ? o.W_up : nullptr, o.x, gu ? o.gamma : nullptr, o.eps, o.y,
                        (long long)o.M, (long long)o.K, nullptr, gu ? nullptr : o.bias};
             bq::MultiGeometry g;
-            if (!bq::plan_multi_single(c, &l.args, &g)) return BQ_ERR_SHAPE;
+            // (a paired gate+up stage measured slower in the chained Qwen3-0.6B-shaped
+            // token: 895 against 1115 GB/s)
+            if (!bq::plan_multi_single(c, &l.args, &g, false)) return BQ_ERR_SHAPE;
             l.args.early_ring = early;
             l.grid = g.grid;
             l.threads = g.threads;

@@ -84,7 +84,9 @@ void fill_multi_args(const MultiGeometry &geo, int n_ops, const MultiOp *ops,
                      const int *cta_tiles, MultiArgs *a);
 // Plan one GEMV, gate+up or verify call (K % 256 == 0) as an inline op of the
 // multi-op kernel; false if it cannot be planned.
-bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo);
+// pair: gate+up calls may take the paired instance (single calls; the stages
+// of a staged plan keep the sequential one, which measured faster there)
+bool plan_multi_single(const GemvCall &c, MultiArgs *a, MultiGeometry *geo, bool pair = true);
 // whether independent op lists use the multi-op kernel (tuning switch)
 bool tunables_multi();
 }

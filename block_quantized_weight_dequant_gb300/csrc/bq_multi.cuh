@@ -207,15 +207,30 @@ __device__ __forceinline__ void multi_prefetch(const MultiCursor &q, const Multi
     }
 }
 
+// The cursor walks a tile matrix by matrix, each matrix chunk by chunk;
+// PAIR (the paired gate+up instance) walks it chunk by chunk, each chunk
+// gate then up, so that the two items of a chunk land in consecutive slots.
+template <bool PAIR>
 __device__ __forceinline__ void multi_advance(const MultiOp *ops, int nops, int nwarps,
                                               MultiCursor &q, MultiCurOp &co) {
-    if (++q.c < co.nchunks) return;
-    q.c = 0;
-    if (++q.m < co.nmat) {
-        q.W = co.W[1];  // matrix 0 -> 1 (nmat is 1 or 2)
-        return;
+    if (PAIR) {
+        if (++q.m < co.nmat) {
+            q.W = co.W[1];
+            return;
+        }
+        q.m = 0;
+        q.W = co.W[0];
+        if (++q.c < co.nchunks) return;
+        q.c = 0;
+    } else {
+        if (++q.c < co.nchunks) return;
+        q.c = 0;
+        if (++q.m < co.nmat) {
+            q.W = co.W[1];  // matrix 0 -> 1 (nmat is 1 or 2)
+            return;
+        }
+        q.m = 0;
     }
-    q.m = 0;
     q.t += nwarps;
     if (q.t >= co.tile_end && q.op + 1 < nops) {
         q.op = multi_op_of(ops, nops, q.t, q.op);
@@ -310,6 +325,10 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
     constexpr int UB = Fmt<QT>::unit_bytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nthr = blockDim.x;
+    // NR = 3 tags the paired gate+up instance: one weight row per lane of each
+    // matrix, the gate and up items of a chunk evaluated in one pass over x
+    constexpr bool PAIR = NR == 3;
+    static_assert(!PAIR || R == 1, "gate+up pairs are single-row");
 
     // dependents may start now; they wait for this grid before reading
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -360,7 +379,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
     auto fill_ring = [&]() {
         for (; issued < a.D && q.t < t_end; ++issued) {
             multi_issue<QT>(q, co, ring + (size_t)issued * a.slot_bytes, wfull + issued, pol, lane);
-            multi_advance(ops, nops, a.nwarps, q, co);
+            multi_advance<PAIR>(ops, nops, a.nwarps, q, co);
         }
     };
     if (a.early_ring) {
@@ -372,7 +391,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
         MultiCurOp fo = co;
         for (int i = 0; i < a.D && f.t < t_end; ++i) {
             multi_prefetch<QT>(f, fo, lane);
-            multi_advance(ops, nops, a.nwarps, f, fo);
+            multi_advance<PAIR>(ops, nops, a.nwarps, f, fo);
         }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -420,7 +439,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
         const int umask = ROWS_LOW ? 0 : o.umask;
         const int rho = ROWS_LOW ? lane & (rg - 1) : lane_bits(lane, ~umask & 31);
         const int l = ROWS_LOW ? lane / rg : lane_bits(lane, umask);
-        constexpr int NRA = NR ? NR : 1;
+        constexpr int NRA = PAIR ? 1 : NR ? NR : 1;
         float p0[NRA][R], p1[NRA];
         for (int pn = 0; pn < np; ++pn, ++phase) {
             // ---- x of this phase: landed, visible to all, and the other buffer free ----
@@ -486,6 +505,57 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                         for (int r = 0; r < R; ++r) p0[v][r] = -0.0f;
                     }
                 }
+                if constexpr (PAIR) {
+                    // chunk c of the gate matrix and of the up matrix, in two
+                    // consecutive slots; one pass over x gives both unit sums
+                    // (each matrix's own tree, as unit_dot_rows promises)
+                    auto wait_item = [&](int s, uint32_t p) {
+                        if (!ok) return;
+                        if (!__all_sync(0xffffffffu, multi_wait(wfull + s, p, abort_flag, a.wait_ns))) {
+                            if (lane == 0) {
+                                if (!*abort_flag) atomicOr(status, BQ_DEVERR_FULL_WAIT);
+                                *abort_flag = 1;
+                            }
+                            ok = false;
+                        } else {
+                            ++landed;
+                        }
+                    };
+                    auto next_slot = [&]() {
+                        ++e;
+                        slot = slot + 1 == a.D ? 0 : slot + 1;
+                        par ^= slot == 0;
+                    };
+                    for (int c = c_lo; c < c_hi; ++c) {
+                        const int sg = slot;
+                        wait_item(slot, par);
+                        next_slot();
+                        const int su = slot;
+                        wait_item(slot, par);
+                        next_slot();
+                        if (!ok) continue;
+                        const int u0 = c * KCU;
+                        const int cnt = min(KCU, nsc - u0);
+                        const uint8_t *stg = ring + (size_t)sg * a.slot_bytes + rho * row_stride;
+                        const uint8_t *stu = ring + (size_t)su * a.slot_bytes + rho * row_stride;
+                        if (rho < rows) {
+                            for (int ul = l; ul < cnt; ul += G) {
+                                const uint8_t *up2[2] = {stg + ul * UB, stu + ul * UB};
+                                float cc[2][1];
+                                unit_dot_rows<QT, 2, 1>(up2, xs, (u0 + ul - k0u) * 256, cc);
+                                p0[0][0] = __fadd_rn(p0[0][0], cc[0][0]);
+                                p1[0] = __fadd_rn(p1[0], cc[1][0]);
+                            }
+                        }
+                        // refill both slots, in the cursor's order
+                        for (int k = 0; k < 2 && q.t < t_end; ++k) {
+                            const int s = k == 0 ? sg : su;
+                            multi_issue<QT>(q, co, ring + (size_t)s * a.slot_bytes, wfull + s, pol, lane);
+                            multi_advance<PAIR>(ops, nops, a.nwarps, q, co);
+                            ++issued;
+                        }
+                    }
+                } else {
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
                     if (m >= nmat) break;
@@ -527,7 +597,7 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                                 if (q.t < t_end) {
                                     multi_issue<QT>(q, co, ring + (size_t)slot * a.slot_bytes,
                                                     wfull + slot, pol, lane);
-                                    multi_advance(ops, nops, a.nwarps, q, co);
+                                    multi_advance<PAIR>(ops, nops, a.nwarps, q, co);
                                     ++issued;
                                 }
                                 continue;
@@ -560,10 +630,11 @@ __global__ void __launch_bounds__(multi_max_warps(QT, R) * 32, 1)
                         if (q.t < t_end) {
                             multi_issue<QT>(q, co, ring + (size_t)slot * a.slot_bytes, wfull + slot, pol,
                                             lane);
-                            multi_advance(ops, nops, a.nwarps, q, co);
+                            multi_advance<PAIR>(ops, nops, a.nwarps, q, co);
                             ++issued;
                         }
                     }
+                }
                 }
                 if (!ok || pn + 1 < np || NR == 0) continue;
 #pragma unroll
