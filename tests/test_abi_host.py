@@ -175,6 +175,23 @@ def test_stream_plan_tune_validation(lib):
     assert lib.bq_stream_workspace_bytes(169, 113) >= 169 * 64 + (1024 + 1) * 4 + 1024 * 8
 
 
+def test_stream_workspace_covers_staged_plans(lib):
+    """A plan of dependent stages runs one launch per stage: the workspace
+    holds the op table and one CTA split (up to 1024 CTAs + 1 entries) per
+    stage, so it grows with the stage count; bad counts are refused."""
+    n_ops = 113
+    small = lib.bq_stream_workspace_bytes(n_ops, 1)
+    for n_stages in (2, 29, 113):
+        need = lib.bq_stream_workspace_bytes(n_ops, n_stages)
+        assert need >= n_stages * (1024 + 1) * 4
+        assert need >= small
+    assert lib.bq_stream_workspace_bytes(4, 5) == -1  # more stages than ops
+    assert lib.bq_stream_workspace_bytes(0, 0) == -1
+    lib.bq_stream_plan_launches.restype = ctypes.c_int
+    lib.bq_stream_plan_launches.argtypes = [ctypes.c_void_p]
+    assert lib.bq_stream_plan_launches(None) == -1
+
+
 def test_f16_gemv_validation(lib):
     f = lib.bq_gemv_f16
     assert f(None, FAKE, FAKE, 8, 256, None) == _lib.BQ_ERR_NULL
