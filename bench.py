@@ -63,12 +63,12 @@ def token_cfg(config):
 # the traffic is null until it is captured again.
 NCU_TRAFFIC = {
     # (config, inputs): (bytes per launch, csrc_digest() at capture, summary)
-    ("cfg2", "independent"): (606543360, "5f4e0f779e8a5528ce30a9dcc987d4488ebe358ca1532629327d2b425f152f81",
+    ("cfg2", "independent"): (606428416, "d73de573e099ed1dd14718d2c225affa8268bb5f2576b7b49fda195b403af08b",
                               "profiles/multi_kernel_q8_0_qwen3_0.6b_stream.md"),
     # captured on 2 of the 28 layers (+ LM head) and scaled by algorithmic bytes
-    ("cfg3", "independent"): (4005119719, "5f4e0f779e8a5528ce30a9dcc987d4488ebe358ca1532629327d2b425f152f81",
+    ("cfg3", "independent"): (4006526862, "d73de573e099ed1dd14718d2c225affa8268bb5f2576b7b49fda195b403af08b",
                               "profiles/multi_kernel_q4_0_7b_stream.md"),
-    ("cfg3k", "independent"): (4006691566, "5f4e0f779e8a5528ce30a9dcc987d4488ebe358ca1532629327d2b425f152f81",
+    ("cfg3k", "independent"): (4006904606, "d73de573e099ed1dd14718d2c225affa8268bb5f2576b7b49fda195b403af08b",
                                "profiles/multi_kernel_q4_k_7b_stream.md"),
 }
 
