@@ -162,6 +162,39 @@ def test_plan_in_cuda_graph(kind):
         assert torch.equal(g_.view(torch.int32), w.view(torch.int32))
 
 
+def test_staged_plan_falls_back_to_the_executor():
+    """A dependent stage whose input exceeds what the streaming kernel stages
+    for one row (K = 34816 fp32, 136 KB, over its 128 KB limit) cannot run as
+    a stage launch; the plan then runs on the cooperative executor in one
+    launch (its Q4_0 rings leave room for that input), with the same bits as
+    one call per op."""
+    qt = "q4_0"
+
+    def packed(M, K, tag):
+        W = wl.normal_torch((M, K), wl.W_STD, seed=3, stream=wl.stream_id("fallback", tag), device=DEV)
+        return bq.quantize_pack(W, qt)
+
+    K0 = 34816
+    W0, W1 = packed(256, K0, 0), packed(80, 256, 1)
+    x = wl.normal_torch(K0, 1.0, seed=3, stream=wl.stream_id("fallback-x"), device=DEV)
+    y0 = torch.empty(256, device=DEV)
+    y1 = torch.empty(80, device=DEV)
+    ops = [bq.StreamOp(0, W0, x, y0), bq.StreamOp(1, W1, y0, y1)]
+    bq.gemv(qt, W0, x, y0)
+    bq.gemv(qt, W1, y0, y1)
+    want = [y0.clone(), y1.clone()]
+    y0.fill_(float("nan"))
+    y1.fill_(float("nan"))
+    with plan_kind("staged"):
+        plan = bq.StreamPlan(qt, ops)
+    assert plan.launches == 1
+    plan.launch()
+    torch.cuda.synchronize()
+    for g, w in zip((y0, y1), want):
+        assert torch.equal(g.view(torch.int32), w.view(torch.int32))
+    assert bq.device_status(clear=True) == 0
+
+
 def test_plan_rejects_bad_ops():
     P = bq.quantize_pack(torch.zeros(64, 512, device=DEV), "q8_0")
     x = torch.zeros(512, device=DEV)
